@@ -1,0 +1,437 @@
+"""Pins for the CPU oracle: hand-built blocks with closed-form values, the
+router's worked example, invariants and brute force on tiny inputs.
+
+Each check is chosen so that a plausible slip in the oracle (a dropped
+term, a wrong sign, a swapped nibble, a transposed operand, a wrong bit
+position) fails at least one of them.  CPU only.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_golden(name):
+    out = {}
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, *vals = line.split()
+        out[key] = vals
+    return out
+
+
+def _fp16_bytes(v):
+    return np.array([v], dtype=np.float16).view(np.uint8)
+
+
+# ---------------------------------------------------------------- Q8_0
+
+def _q8_block(d, qbytes):
+    b = np.zeros(34, dtype=np.uint8)
+    b[0:2] = _fp16_bytes(d)
+    b[2:] = np.asarray(qbytes, dtype=np.uint8)
+    return b
+
+
+def test_q8_0_every_byte_value_sign_extends():
+    # 8 blocks whose quant bytes run through 0..255; d = 1.
+    blocks = np.stack([_q8_block(1.0, np.arange(32 * i, 32 * i + 32)) for i in range(8)])
+    w = O.dequant_q8_0(blocks)
+    expect = np.concatenate([np.arange(0, 128), np.arange(-128, 0)]).astype(np.float64)
+    np.testing.assert_array_equal(w, expect)
+
+
+@pytest.mark.parametrize("d", [0.5, 0.0, -2.0, 1e-3])
+def test_q8_0_scale_multiplies(d):
+    q = np.arange(256).reshape(8, 32)
+    blocks = np.stack([_q8_block(d, q[i]) for i in range(8)])
+    base = np.concatenate([np.arange(0, 128), np.arange(-128, 0)]).astype(np.float64)
+    d16 = float(np.float16(d))
+    np.testing.assert_array_equal(O.dequant_q8_0(blocks), base * d16)
+
+
+def test_q8_0_block_position_and_scale_index():
+    # a single nonzero quant in block b, position i -> only value 32b+i is nonzero,
+    # and it uses block b's own scale.
+    for b in range(3):
+        for i in (0, 7, 31):
+            blocks = np.stack([_q8_block(2.0 ** (k + 1), np.zeros(32)) for k in range(3)])
+            blocks[b, 2 + i] = 5
+            w = O.dequant_q8_0(blocks)
+            nz = np.flatnonzero(w)
+            assert list(nz) == [32 * b + i]
+            assert w[nz[0]] == 5 * 2.0 ** (b + 1)
+
+
+def test_q8_0_round_trip_quantiser():
+    # reference quantiser idea from iron PR #9: scale = fp16(amax/127), q = round(x/scale);
+    # dequant error per element <= scale/2.
+    g = synth.rng(7)
+    x = g.standard_normal((64, 32)) * 0.05
+    blocks = np.zeros((64, 34), dtype=np.uint8)
+    for r in range(64):
+        d = np.float16(np.abs(x[r]).max() / 127)
+        q = np.clip(np.rint(x[r] / float(d)), -127, 127).astype(np.int64)
+        blocks[r] = _q8_block(d, q & 0xFF)
+    w = O.dequant_q8_0(blocks).reshape(64, 32)
+    d = blocks[:, 0:2].copy().view(np.float16)[:, 0].astype(np.float64)
+    assert np.all(np.abs(w - x) <= d[:, None] / 2 * (1 + 1e-9))
+
+
+def test_q8_0_brute_force_bytes():
+    g = synth.rng(11)
+    blocks = synth.q8_0_blocks(g, 3, 64).reshape(-1, 34)
+    w = O.dequant_q8_0(blocks)
+    ref = []
+    for blk in blocks:
+        d = float(np.frombuffer(bytes(blk[0:2]), dtype="<f2")[0])
+        for u in blk[2:]:
+            u = int(u)
+            ref.append((u - 256 if u >= 128 else u) * d)
+    np.testing.assert_array_equal(w, np.array(ref))
+
+
+# ---------------------------------------------------------------- Q2_K
+
+def _q2k_block(d, dmin, scales, qs):
+    b = np.zeros(84, dtype=np.uint8)
+    b[0:16] = np.asarray(scales, dtype=np.uint8)
+    b[16:80] = np.asarray(qs, dtype=np.uint8)
+    b[80:82] = _fp16_bytes(d)
+    b[82:84] = _fp16_bytes(dmin)
+    return b
+
+
+def test_golden_block_layouts():
+    gld = _read_golden("block_layouts.txt")
+    assert int(gld["q2_k_block_bytes"][0]) == synth.Q2_K_BLOCK_BYTES == 84
+    assert int(gld["q2_k_qs_offset"][0]) == 16
+    # a block whose only nonzero quant byte is at offset 16 dequantises to a
+    # nonzero value in sub-block 0 only (the qs base is byte 16).
+    b = _q2k_block(1.0, 0.0, np.full(16, 1), np.zeros(64))
+    b[int(gld["q2_k_qs_offset"][0])] = 1
+    w = O.dequant_q2_k(b[None])
+    assert list(np.flatnonzero(w)) == [0]
+    blocks = synth.q2_k_blocks(synth.rng(0), 2, 512)
+    assert blocks.shape == (2, 2, int(gld["q2_k_block_bytes"][0]))
+    blocks8 = synth.q8_0_blocks(synth.rng(0), 2, 64)
+    assert blocks8.shape == (2, 64 // int(gld["q8_0_values_per_block"][0]), 34)
+
+
+def test_q2_k_scale_nibble_times_q():
+    # d=1, dmin=0, sc_j = j (low nibble), m_j = 15 (high nibble, must be ignored), q = 3.
+    scales = np.arange(16) | (15 << 4)
+    w = O.dequant_q2_k(_q2k_block(1.0, 0.0, scales, np.full(64, 0xFF))[None])
+    np.testing.assert_array_equal(w, 3.0 * (np.arange(256) // 16))
+
+
+def test_q2_k_min_nibble_subtracts():
+    # d=0, dmin=1, m_j = j (high nibble), sc_j = 15 (ignored because d = 0).
+    scales = (np.arange(16) << 4) | 15
+    w = O.dequant_q2_k(_q2k_block(0.0, 1.0, scales, np.full(64, 0xFF))[None])
+    np.testing.assert_array_equal(w, -1.0 * (np.arange(256) // 16))
+
+
+def test_q2_k_each_bit_pair_lands_on_one_value():
+    # one 2-bit quant set to 1 at byte b, bit pair g -> exactly one nonzero value,
+    # at v = 128*(b//32) + 32*g + b%32 (GGUF order).
+    scales = np.full(16, 1)
+    for b in range(64):
+        for g in range(4):
+            qs = np.zeros(64, dtype=np.int64)
+            qs[b] = 1 << (2 * g)
+            w = O.dequant_q2_k(_q2k_block(1.0, 0.0, scales, qs)[None])
+            nz = np.flatnonzero(w)
+            assert list(nz) == [128 * (b // 32) + 32 * g + b % 32], (b, g)
+            assert w[nz[0]] == 1.0
+
+
+def test_q2_k_two_level_mixed_case():
+    # distinct d, dmin, sc, m and q per sub-block: w = (d*sc)*q - dmin*m.
+    d, dmin = 0.25, 0.125
+    sc = np.arange(16) % 16
+    m = (7 * np.arange(16) + 3) % 16
+    scales = sc | (m << 4)
+    qs = np.zeros(64, dtype=np.int64)
+    qv = np.array([(v * 5 + v // 7) % 4 for v in range(256)])
+    for v in range(256):
+        h, g, l = v // 128, (v // 32) % 4, v % 32
+        qs[32 * h + l] |= int(qv[v]) << (2 * g)
+    w = O.dequant_q2_k(_q2k_block(d, dmin, scales, qs)[None])
+    j = np.arange(256) // 16
+    np.testing.assert_array_equal(w, (d * sc[j]) * qv - dmin * m[j])
+
+
+def test_q2_k_multi_block_uses_own_fields():
+    g = synth.rng(3)
+    blocks = synth.q2_k_blocks(g, 2, 768)            # 2 rows x 3 super-blocks
+    w = O.dequant_q2_k(blocks)
+    assert w.shape == (2, 768)
+    for r in range(2):
+        for s in range(3):
+            np.testing.assert_array_equal(w[r, 256 * s:256 * (s + 1)],
+                                          O.dequant_q2_k(blocks[r, s][None]))
+
+
+def test_q2_k_sum_invariant_and_brute_force():
+    g = synth.rng(5)
+    blocks = synth.q2_k_blocks(g, 4, 256).reshape(-1, 84)
+    w = O.dequant_q2_k(blocks).reshape(4, 256)
+    for r, blk in enumerate(blocks):
+        d = float(np.frombuffer(bytes(blk[80:82]), dtype="<f2")[0])
+        dmin = float(np.frombuffer(bytes(blk[82:84]), dtype="<f2")[0])
+        vals = []
+        for v in range(256):
+            byte = int(blk[16 + 32 * (v // 128) + v % 32])
+            q = (byte >> (2 * ((v // 32) % 4))) & 3
+            s = int(blk[v // 16])
+            vals.append((d * (s & 15)) * q - dmin * (s >> 4))
+        np.testing.assert_array_equal(w[r], np.array(vals))
+        total = math.fsum(vals)
+        assert abs(w[r].sum() - total) <= 1e-12 * max(1.0, abs(total))
+
+
+def test_q2_k_config_range_values_are_fp32_exact():
+    # for d, dmin in [1e-3, 1e-2] fp16, every dequantised value is a multiple
+    # of 2^-20 below 2^-1 in magnitude, hence exact in fp32.
+    blocks = synth.q2_k_blocks(synth.rng(9), 64, 4096)
+    w = O.dequant_q2_k(blocks)
+    np.testing.assert_array_equal(w.astype(np.float32).astype(np.float64), w)
+    assert np.all(np.abs(w) < 0.5)
+    np.testing.assert_array_equal(np.round(w * 2.0 ** 20), w * 2.0 ** 20)
+
+
+# ---------------------------------------------------------------- int4
+
+def test_int4_nibble_order_low_first():
+    words = np.array([[0x76543210, 0xFEDCBA98] * 4], dtype=np.uint32)    # 1 row, k=64
+    s = np.array([[1.0]], dtype=np.float16)
+    b = np.array([[0.0]], dtype=np.float16)
+    w = O.dequant_int4(words, s, b)
+    np.testing.assert_array_equal(w[0], np.tile(np.arange(16), 4).astype(np.float64))
+
+
+def test_int4_affine_ends():
+    k = 128
+    words0 = np.zeros((1, k // 8), dtype=np.uint32)
+    words15 = np.full((1, k // 8), 0xFFFFFFFF, dtype=np.uint32)
+    s = np.array([[0.5, 0.25]], dtype=np.float16)
+    b = np.array([[-1.0, 3.0]], dtype=np.float16)
+    w0 = O.dequant_int4(words0, s, b)[0]
+    w15 = O.dequant_int4(words15, s, b)[0]
+    np.testing.assert_array_equal(w0, np.r_[np.full(64, -1.0), np.full(64, 3.0)])
+    np.testing.assert_array_equal(w15, np.r_[np.full(64, 15 * 0.5 - 1.0), np.full(64, 15 * 0.25 + 3.0)])
+
+
+def test_int4_brute_force():
+    wt = synth.int4_weight(synth.rng(4), (3,), 128)
+    w = O.dequant_int4(wt.words, wt.scales, wt.biases)
+    for n in range(3):
+        for k in range(128):
+            q = (int(wt.words[n, k // 8]) >> (4 * (k % 8))) & 15
+            assert w[n, k] == q * float(wt.scales[n, k // 64]) + float(wt.biases[n, k // 64])
+
+
+# ---------------------------------------------------------------- matmul
+
+def test_qmm_brute_force_non_square():
+    g = synth.rng(12)
+    x = synth.fp16_normal(g, (3, 7))
+    w = g.standard_normal((5, 7))
+    y = O.qmm(x, w)
+    assert y.shape == (3, 5)
+    for m in range(3):
+        for n in range(5):
+            ref = math.fsum(float(x[m, k]) * float(w[n, k]) for k in range(7))
+            assert abs(y[m, n] - ref) <= 1e-12 * max(1.0, abs(ref))
+
+
+def test_qmm_brute_force_dequantised_q2_k():
+    g = synth.rng(13)
+    blocks = synth.q2_k_blocks(g, 4, 256)
+    w = O.dequant_q2_k(blocks)
+    x = synth.fp16_normal(g, (2, 256))
+    y = O.qmm(x, w)
+    for m in range(2):
+        for n in range(4):
+            ref = math.fsum(float(x[m, k]) * w[n, k] for k in range(256))
+            assert abs(y[m, n] - ref) <= 1e-12 * max(1.0, abs(ref))
+
+
+# ---------------------------------------------------------------- routing
+
+def test_router_worked_example_from_pages():
+    gld = _read_golden("router_worked_example.txt")
+    logits = np.array([[float(v) for v in gld["logits"]]], dtype=np.float32)
+    k = int(gld["k"][0])
+    ids, wts = O.route(logits, k)
+    assert list(ids[0]) == [int(v) for v in gld["ids"]]
+    np.testing.assert_allclose(wts[0], [float(v) for v in gld["weights"]], rtol=0, atol=1e-15)
+    assert abs(wts.sum() - float(gld["weight_sum"][0])) < 1e-15
+    assert wts[0, 0] > wts[0, 1]          # the larger logit dominates
+    e = math.e
+    np.testing.assert_allclose(wts[0], [e / (1 + e), 1 / (1 + e)], rtol=1e-15)
+
+
+def test_router_brute_force_random_rows():
+    g = synth.rng(21)
+    logits = synth.fp32_normal(g, (50, 16))
+    bias = g.standard_normal(16).astype(np.float32)
+    for use_bias in (False, True):
+        ids, wts = O.route(logits, 4, bias if use_bias else None)
+        for t in range(50):
+            z = [np.float32(logits[t, e]) + (np.float32(bias[e]) if use_bias else np.float32(0))
+                 for e in range(16)]
+            best = sorted(range(16), key=lambda e: (-float(z[e]), e))[:4]
+            assert list(ids[t]) == best
+            ex = [math.exp(float(z[e]) - float(z[best[0]])) for e in best]
+            ref = [v / math.fsum(ex) for v in ex]
+            np.testing.assert_allclose(wts[t], ref, rtol=1e-13)
+            assert abs(wts[t].sum() - 1) < 1e-12
+            assert np.all(np.diff(wts[t]) <= 0)
+
+
+def test_router_full_softmax_renormalised_equals_selected_softmax():
+    g = synth.rng(22)
+    logits = synth.fp32_normal(g, (8, 32))
+    ids, wts = O.route(logits, 6)
+    full = np.exp(logits.astype(np.float64))
+    full /= full.sum(axis=1, keepdims=True)
+    sel = np.take_along_axis(full, ids.astype(np.int64), axis=1)
+    np.testing.assert_allclose(wts, sel / sel.sum(axis=1, keepdims=True), rtol=1e-12)
+
+
+def test_router_ties_go_to_lower_index_and_bias_changes_choice():
+    ids, wts = O.route(np.zeros((1, 8), dtype=np.float32), 3)
+    assert list(ids[0]) == [0, 1, 2]
+    np.testing.assert_allclose(wts[0], [1 / 3] * 3, rtol=1e-15)
+    logits = np.array([[0.0, 1.0, 2.0, 3.0]], dtype=np.float32)
+    bias = np.array([10.0, 0.0, 0.0, -10.0], dtype=np.float32)
+    ids, wts = O.route(logits, 2, bias)
+    assert list(ids[0]) == [0, 2]
+    np.testing.assert_allclose(wts[0], [1 / (1 + math.exp(-8)), math.exp(-8) / (1 + math.exp(-8))],
+                               rtol=1e-13)
+
+
+def test_router_k_equals_one_weight_is_one():
+    ids, wts = O.route(synth.fp32_normal(synth.rng(2), (5, 7)), 1)
+    np.testing.assert_array_equal(wts, np.ones((5, 1)))
+
+
+# ---------------------------------------------------------------- permute
+
+def test_permute_invariants_and_brute_force():
+    g = synth.rng(31)
+    t, k, e = 37, 3, 11
+    ids = np.stack([g.permutation(e)[:k] for _ in range(t)]).astype(np.int32)
+    p = O.permute(ids, e)
+    flat = ids.reshape(-1)
+    assert p["counts"].sum() == t * k
+    assert p["offsets"][0] == 0 and p["offsets"][-1] == t * k
+    assert np.all(np.diff(p["offsets"]) == p["counts"])
+    assert sorted(p["perm"]) == list(range(t * k))
+    np.testing.assert_array_equal(p["inv"][p["perm"]], np.arange(t * k))
+    brute = sorted(range(t * k), key=lambda f: (int(flat[f]), f))
+    assert list(p["perm"]) == brute
+    for x in range(e):
+        seg = p["perm"][p["offsets"][x]:p["offsets"][x + 1]]
+        assert np.all(flat[seg] == x) and np.all(np.diff(seg) > 0)
+    np.testing.assert_array_equal(p["perm_token"] * k + p["perm_slot"], p["perm"])
+
+
+def test_permute_empty_experts_and_single_expert():
+    ids = np.zeros((4, 1), dtype=np.int32) + 2
+    p = O.permute(ids, 5)
+    assert list(p["counts"]) == [0, 0, 4, 0, 0]
+    assert list(p["offsets"]) == [0, 0, 0, 4, 4, 4]
+    assert list(p["perm"]) == [0, 1, 2, 3]
+
+
+# ---------------------------------------------------------------- FFN / MoE
+
+def test_silu_closed_forms():
+    assert O.silu(0.0) == 0.0
+    np.testing.assert_allclose(O.silu(math.log(3.0)), 0.75 * math.log(3.0), rtol=1e-15)
+    x = np.linspace(-6, 6, 25)
+    np.testing.assert_allclose(O.silu(x) - O.silu(-x), x, rtol=1e-13, atol=1e-15)
+    assert abs(O.silu(40.0) - 40.0) < 1e-12 and abs(O.silu(-40.0)) < 1e-15
+
+
+def test_swiglu_ffn_hand_case():
+    # H = I = 1: y = c * silu(a x) * (b x).  a x = ln 3 gives silu = 0.75 ln 3.
+    x = np.array([[2.0]])
+    a = math.log(3.0) / 2.0
+    w_gu = np.array([[a], [1.5]])
+    w_d = np.array([[-4.0]])
+    y = O.swiglu_ffn(x, w_gu, w_d)
+    np.testing.assert_allclose(y, [[-4.0 * 0.75 * math.log(3.0) * 3.0]], rtol=1e-14)
+    # gate rows come first: swapping the halves changes the answer
+    y2 = O.swiglu_ffn(x, w_gu[::-1].copy(), w_d)
+    assert abs(y2[0, 0] - y[0, 0]) > 1e-3
+
+
+def _tiny_moe(seed, t=5, h=4, i=3, e=4, k=2):
+    g = synth.rng(seed)
+    x = synth.fp16_normal(g, (t, h))
+    gu = g.standard_normal((e, 2 * i, h))
+    dd = g.standard_normal((e, h, i))
+    ids, wts = O.route(synth.fp32_normal(g, (t, e)), k)
+    return x, gu, dd, ids, wts
+
+
+def test_moe_brute_force_loops():
+    x, gu, dd, ids, wts = _tiny_moe(41)
+    y = O.moe_ffn(x, ids, wts, lambda e: gu[e], lambda e: dd[e])
+    t, h = x.shape
+    i = gu.shape[1] // 2
+    for tt in range(t):
+        acc = [0.0] * h
+        for j in range(ids.shape[1]):
+            e = int(ids[tt, j])
+            a = [math.fsum(float(x[tt, c]) * gu[e, r, c] for c in range(h)) for r in range(2 * i)]
+            hv = [a[r] / (1 + math.exp(-a[r])) * a[i + r] for r in range(i)]
+            for c in range(h):
+                acc[c] += wts[tt, j] * math.fsum(hv[r] * dd[e, c, r] for r in range(i))
+        np.testing.assert_allclose(y[tt], acc, rtol=1e-12, atol=1e-14)
+
+
+def test_moe_zero_input_gives_zero_and_shared_adds():
+    x, gu, dd, ids, wts = _tiny_moe(42)
+    z = np.zeros_like(x)
+    assert np.all(O.moe_ffn(z, ids, wts, lambda e: gu[e], lambda e: dd[e]) == 0)
+    y0 = O.moe_ffn(x, ids, wts, lambda e: gu[e], lambda e: dd[e])
+    y1 = O.moe_ffn(x, ids, wts, lambda e: gu[e], lambda e: dd[e], shared=(gu[0], dd[0]))
+    np.testing.assert_allclose(y1 - y0, O.swiglu_ffn(x, gu[0], dd[0]), rtol=1e-12, atol=1e-14)
+
+
+def test_moe_single_expert_reduces_to_dense_ffn():
+    x, gu, dd, _, _ = _tiny_moe(43)
+    ids = np.zeros((x.shape[0], 1), dtype=np.int32)
+    wts = np.ones((x.shape[0], 1))
+    np.testing.assert_allclose(O.moe_ffn(x, ids, wts, lambda e: gu[e], lambda e: dd[e]),
+                               O.swiglu_ffn(x, gu[0], dd[0]), rtol=1e-14)
+
+
+def test_moe_expert_slab_selection():
+    # stack 4 experts, route every token to expert 2 only: output equals the
+    # dense FFN of slab 2 (butter PR #10, "stacks 4 experts' weights, picks expert 2").
+    x, gu, dd, _, _ = _tiny_moe(44)
+    ids = np.full((x.shape[0], 1), 2, dtype=np.int32)
+    y = O.moe_ffn(x, ids, np.ones((x.shape[0], 1)), lambda e: gu[e], lambda e: dd[e])
+    np.testing.assert_allclose(y, O.swiglu_ffn(x, gu[2], dd[2]), rtol=1e-14)
+    assert np.abs(y - O.swiglu_ffn(x, gu[1], dd[1])).max() > 1e-3
+
+
+def test_moe_tokens_subset_matches_full():
+    x, gu, dd, ids, wts = _tiny_moe(45)
+    full = O.moe_ffn(x, ids, wts, lambda e: gu[e], lambda e: dd[e])
+    sub = O.moe_ffn_tokens(x, ids, wts, [3, 1], lambda e: gu[e], lambda e: dd[e])
+    np.testing.assert_allclose(sub, full[[3, 1]], rtol=1e-14)
