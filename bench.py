@@ -1,0 +1,502 @@
+#!/usr/bin/env python
+"""Benchmark: block-quantized MoE gather-qmm on GB300.
+
+Step = one MoE layer call over 2048 tokens: Q2_K routed experts (E=256,
+top-6, Zipf(1.1)-skewed router bias, hidden 4096, SwiGLU intermediate
+2048) plus an always-on Q8_0 shared expert of the same shape: route ->
+permute -> grouped gate/up + SwiGLU -> grouped down x gate -> combine.
+
+Prints one JSON line (rank 0).  `value` is prefill tokens/s with inputs
+resident in HBM; `e2e` is the same through the public API with the
+inputs copied from pinned host memory and the output read back every
+step.  `secondary` holds the other workloads: decode MoE steps (unique
+expert weight GB/s), the int4 MoE prefill, dense qmm and the standalone
+dequant kernels.
+
+`--impl reference` times the CPU oracle (test infrastructure) on a bounded
+sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+import synth  # noqa: E402
+
+MAIN = synth.MOE_Q2K
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["bq", "reference"], default="bq")
+    ap.add_argument("--decode-steps", type=int, default=200)
+    ap.add_argument("--no-secondary", action="store_true", help="only the main step (faster)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- dist
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if _has_cuda() else "gloo")
+    return world, rank, local
+
+
+def _has_cuda():
+    import torch
+    return torch.cuda.is_available()
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class Clocks:
+    """Samples nvidia-smi during a timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- device setup
+def upload(a, dtype=None):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.cuda()
+
+
+def qweight(bq, fmt, w, n_mats, n, k, swiglu=False):
+    import torch
+    q = bq.QWeight(bq.FMT_BY_NAME[fmt], n_mats, n, k, swiglu)
+    if fmt == "q8_0":
+        src = upload(np.asarray(w).reshape(-1))
+        bq.repack_q8_0(src, q)
+    elif fmt == "q2_k":
+        src = upload(np.asarray(w).reshape(-1))
+        bq.repack_q2_k(src, q)
+    else:
+        bq.repack_int4(upload(w.words.reshape(-1).view(np.int32)), upload(w.scales.reshape(-1).view(np.int16)),
+                       upload(w.biases.reshape(-1).view(np.int16)), q)
+    torch.cuda.synchronize()
+    return q
+
+
+def build_layer(bq, case, weights):
+    w_gu, w_d, s_gu, s_d, _ = weights
+    gu = qweight(bq, case.fmt, w_gu, case.experts, 2 * case.inter, case.hidden, True)
+    dn = qweight(bq, case.fmt, w_d, case.experts, case.hidden, case.inter)
+    sg = sd = None
+    if s_gu is not None:
+        sg = qweight(bq, "q8_0", s_gu, 1, 2 * case.inter, case.hidden, True)
+        sd = qweight(bq, "q8_0", s_d, 1, case.hidden, case.inter)
+    return bq.MoELayer(case.t, case.hidden, case.inter, case.experts, case.topk, gu, dn, sg, sd)
+
+
+class L2Flush:
+    def __init__(self):
+        import torch
+        l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+        self.buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
+
+    def __call__(self):
+        self.buf.zero_()
+
+
+def time_steps(fn, k, flush, stage_events=None):
+    """Runs fn() k times, flushing L2 before each, timing each call with CUDA
+    events on the current stream.  Returns (per-step ms list, per-stage ms
+    lists)."""
+    import torch
+    st = torch.cuda.current_stream()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(k)]
+    stage_ms = {}
+    stage_pairs = {}
+    for sid in (stage_events or []):
+        stage_pairs[sid] = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                            for _ in range(k)]
+        for a, b in stage_pairs[sid]:   # materialise the event handles
+            a.record(st)
+            b.record(st)
+    torch.cuda.synchronize()
+    import block_quantized_moe_gather_gb300 as bq
+    for i in range(k):
+        flush()
+        for sid, pairs in stage_pairs.items():
+            bq.set_stage_events(sid, pairs[i][0], pairs[i][1])
+        starts[i].record(st)
+        fn()
+        ends[i].record(st)
+    torch.cuda.synchronize()
+    for sid in stage_pairs:
+        bq.set_stage_events(sid, None, None)
+        stage_ms[sid] = [a.elapsed_time(b) for a, b in stage_pairs[sid]]
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], stage_ms
+
+
+# ----------------------------------------------------------------------------- main arm
+def run_main(args, world, rank, local):
+    import torch
+    import block_quantized_moe_gather_gb300 as bq
+    torch.cuda.set_device(local)
+    pk, pk_src = peaks()
+    case = MAIN
+    weights = synth.moe_weights(case)
+    layer = build_layer(bq, case, weights)
+    xh, logits_h = synth.moe_activations(case)
+    bias_h = weights[4]
+    x = upload(xh.view(np.uint16)).view(torch.float16)
+    logits = upload(logits_h)
+    bias = upload(bias_h)
+    y = torch.empty((case.t, case.hidden), dtype=torch.float32, device="cuda")
+    ws = torch.empty(layer.workspace_bytes(), dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
+
+    def step():
+        bq.moe_gather_qmm(layer, x, logits, bias, y, ws)
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    assert bq.device_status() == bq.DEV_OK
+
+    barrier(world)
+    torch.cuda.synchronize()
+    n0 = bq.launch_count()
+    with Clocks(local) as clk:
+        step_ms, stage_ms = time_steps(step, args.steps, flush, stage_events=[1, 2, 3])
+    n_launch = bq.launch_count() - n0
+    torch.cuda.synchronize()
+    barrier(world)
+    total_ms = max_over_ranks(world, sum(step_ms))
+    ms_per_step = total_ms / args.steps
+    value = world * case.t * args.steps / (total_ms / 1e3)
+
+    # dominant kernel: the routed gate/up grouped GEMM (+ SwiGLU epilogue)
+    pairs = case.t * case.topk
+    gu_flops = 2.0 * pairs * 2 * case.inter * case.hidden
+    gu_ms = statistics.mean(stage_ms[1])
+    peak_tf = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    achieved_tf = gu_flops / (gu_ms / 1e3) / 1e12
+    roofline = {"kernel": "gate_up grouped GEMM + SwiGLU (stage timing)", "bound": "tensor",
+                "achieved": round(achieved_tf, 2), "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": round(achieved_tf / peak_tf, 4), "traffic": None,
+                "peak_source": f"{pk_src} bf16 sustained (fp16 operands, same tensor rate)",
+                "stage_ms": {"gate_up": round(gu_ms, 4), "down": round(statistics.mean(stage_ms[2]), 4),
+                             "shared": round(statistics.mean(stage_ms[3]), 4)}}
+
+    # end to end through the public API with host buffers
+    xp = torch.from_numpy(xh.view(np.uint16)).view(torch.float16).pin_memory()
+    lp = torch.from_numpy(np.ascontiguousarray(logits_h)).pin_memory()
+    yp = torch.empty((case.t, case.hidden), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        x.copy_(xp, non_blocking=True)
+        logits.copy_(lp, non_blocking=True)
+        bq.moe_gather_qmm(layer, x, logits, bias, y, ws)
+        yp.copy_(y, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    e2e_ms, _ = time_steps(e2e_step, args.steps, flush)
+    e2e_total = max_over_ranks(world, sum(e2e_ms))
+    e2e = {"value": round(world * case.t * args.steps / (e2e_total / 1e3), 1), "unit": "tok/s",
+           "h2d_bytes_per_step": int(xp.numel() * 2 + lp.numel() * 4),
+           "d2h_bytes_per_step": int(yp.numel() * 4)}
+
+    secondary = {}
+    if not args.no_secondary:
+        secondary = run_secondary(args, bq, flush, pk)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(case, weights, xh, logits_h, bias_h, budget_s=20.0)
+
+    if rank == 0:
+        line = {
+            "metric": "MoE gather-qmm prefill tok/s (2048 tok); decode qgemv weight GB/s vs HBM",
+            "value": round(value, 1), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": case.name, "tokens": case.t, "hidden": case.hidden, "inter": case.inter,
+                       "experts": case.experts, "topk": case.topk, "expert_format": "Q2_K",
+                       "shared_expert": "Q8_0", "router_bias": "Zipf(1.1)",
+                       "l2": "flushed (2x L2 write) before every timed step; steps timed individually",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": int(n_launch), "clocks": clk.summary(), "secondary": secondary,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_secondary(args, bq, flush, pk):
+    import torch
+    out = {}
+    # decode sweep: C4 shapes (primary reading) and C3 shapes
+    for base in (synth.MOE_Q2K, synth.MOE_INT4):
+        weights = synth.moe_weights(base)
+        layer = build_layer(bq, base, weights)
+        res = {}
+        for b in (1, 2, 4, 8):
+            case = synth.decode_case(base, b)
+            layer.set_tokens(b)
+            xs, ls, uniq = [], [], []
+            for s in range(args.decode_steps):
+                xh, lh = synth.moe_activations(case, synth.decode_step_seed(s))
+                xs.append(xh)
+                ls.append(lh)
+                top = np.argsort(-lh, axis=1, kind="stable")[:, :case.topk]
+                uniq.append(len(np.unique(top)))
+            x_all = upload(np.stack(xs).view(np.uint16)).view(torch.float16)
+            l_all = upload(np.stack(ls))
+            y = torch.empty((b, case.hidden), dtype=torch.float32, device="cuda")
+            ws = torch.empty(layer.workspace_bytes(), dtype=torch.uint8, device="cuda")
+            it = iter(range(10 ** 9))
+
+            def dstep():
+                i = next(it) % args.decode_steps
+                bq.moe_gather_qmm(layer, x_all[i], l_all[i], None, y, ws)
+
+            for _ in range(3):
+                dstep()
+            it = iter(range(10 ** 9))
+            ms, _ = time_steps(dstep, args.decode_steps, flush)
+            eb = synth.expert_weight_bytes(case)
+            shared_b = 3 * case.hidden * case.inter * synth.bytes_per_weight("q8_0") if case.shared_fmt else 0
+            tot_bytes = sum(u * eb + shared_b for u in uniq)
+            gbs = tot_bytes / (sum(ms) / 1e3) / 1e9
+            res[f"B{b}"] = {"GB_s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
+                            "us_per_step": round(1e3 * statistics.mean(ms), 2),
+                            "unique_experts_mean": round(statistics.mean(uniq), 2),
+                            "tok_s": round(b * len(ms) / (sum(ms) / 1e3), 1)}
+        out[f"decode_{base.fmt}"] = res
+        if base.fmt == "int4":
+            layer.set_tokens(base.t)
+            xh, lh = synth.moe_activations(base)
+            x = upload(xh.view(np.uint16)).view(torch.float16)
+            lg = upload(lh)
+            y = torch.empty((base.t, base.hidden), dtype=torch.float32, device="cuda")
+            ws = torch.empty(layer.workspace_bytes(), dtype=torch.uint8, device="cuda")
+            for _ in range(3):
+                bq.moe_gather_qmm(layer, x, lg, None, y, ws)
+            ms, stg = time_steps(lambda: bq.moe_gather_qmm(layer, x, lg, None, y, ws), max(5, args.steps // 2),
+                                 flush, stage_events=[1])
+            fl = synth.moe_flops(base)
+            gu = 2.0 * base.t * base.topk * 2 * base.inter * base.hidden
+            out["prefill_int4"] = {"workload": base.name, "tok_s": round(base.t / (statistics.mean(ms) / 1e3), 1),
+                                   "ms": round(statistics.mean(ms), 4),
+                                   "tflops": round(fl / (statistics.mean(ms) / 1e3) / 1e12, 2),
+                                   "gate_up_tflops": round(gu / (statistics.mean(stg[1]) / 1e3) / 1e12, 2)}
+        del layer
+        torch.cuda.empty_cache()
+    # dense qmm and dequant
+    dense = {}
+    for case in [synth.DENSE_Q8_0_M32] + synth.dense_sweep():
+        xh, w = synth.dense_inputs(case)
+        q = qweight(bq, case.fmt, w, 1, case.n, case.k)
+        x = upload(xh.view(np.uint16)).view(torch.float16)
+        y = torch.empty((case.m, case.n), dtype=torch.float32, device="cuda")
+        for _ in range(3):
+            bq.qmm(x, q, y)
+        ms, _ = time_steps(lambda: bq.qmm(x, q, y), 20, flush)
+        t = statistics.median(ms) / 1e3
+        wb = case.n * case.k * synth.bytes_per_weight(case.fmt)
+        rec = {"us": round(t * 1e6, 2), "weight_GB_s": round(wb / t / 1e9, 1),
+               "tflops": round(2.0 * case.m * case.n * case.k / t / 1e12, 3)}
+        if case.m <= 32:
+            rec["frac_hbm"] = round(wb / t / 1e9 / pk["hbm_gbs"], 4)
+        dense[case.name] = rec
+        if case.m == 1:
+            nb = w.size // (34 if case.fmt == "q8_0" else 84)
+            flat = upload(np.asarray(w).reshape(-1))
+            o = torch.empty(nb * (32 if case.fmt == "q8_0" else 256), dtype=torch.float32, device="cuda")
+            fn = bq.gguf_dequant_q8_0 if case.fmt == "q8_0" else bq.gguf_dequant_q2_k
+            for _ in range(3):
+                fn(flat, o)
+            ms, _ = time_steps(lambda: fn(flat, o), 20, flush)
+            t = statistics.median(ms) / 1e3
+            byt = flat.numel() + o.numel() * 4
+            dense[f"dequant_{case.fmt}_4096x4096"] = {"us": round(t * 1e6, 2), "GB_s": round(byt / t / 1e9, 1),
+                                                       "frac_hbm": round(byt / t / 1e9 / pk["hbm_gbs"], 4)}
+    out["dense"] = dense
+    return out
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(case, weights, xh, logits_h, bias_h, tokens):
+    """The oracle (as it stands) on a sample of token rows of the workload."""
+    import oracle as O
+    w_gu, w_d, s_gu, s_d, _ = weights
+    ids, wts = O.route(logits_h, case.topk, bias_h)
+
+    def deq(w):
+        return O.dequant_q2_k(w) if case.fmt == "q2_k" else O.dequant_int4(w.words, w.scales, w.biases)
+
+    def gu(e):
+        return deq(w_gu[e]).reshape(2 * case.inter, case.hidden)
+
+    def dn(e):
+        return deq(w_d[e]).reshape(case.hidden, case.inter)
+
+    shared = None
+    if s_gu is not None:
+        shared = (O.dequant_q8_0(s_gu).reshape(2 * case.inter, case.hidden),
+                  O.dequant_q8_0(s_d).reshape(case.hidden, case.inter))
+    return O.moe_ffn_tokens(xh, ids, wts, tokens, gu, dn, shared)
+
+
+def _cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
+        return int(n)
+    except Exception:
+        return len(os.sched_getaffinity(0))
+
+
+def cpu_baseline(case, weights, xh, logits_h, bias_h, budget_s=20.0):
+    g = synth.rng(4242)
+    done, t0, tokens_all = 0, time.perf_counter(), []
+    while time.perf_counter() - t0 < budget_s and done < 64:
+        tok = g.choice(case.t, 2, replace=False)
+        oracle_sample(case, weights, xh, logits_h, bias_h, tok)
+        done += len(tok)
+        tokens_all.extend(int(t) for t in tok)
+    el = time.perf_counter() - t0
+    return {"value": round(done / el, 3), "unit": "tok/s", "cores": _cores(), "kind": "oracle",
+            "sample": f"{done} token rows of {case.name} (2 per call, each call dequantises the experts "
+                      f"its tokens route to plus the shared expert, fp64), {el:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    case = MAIN
+    weights = synth.moe_weights(case)
+    xh, logits_h = synth.moe_activations(case)
+    bias_h = weights[4]
+    g = synth.rng(777)
+    for _ in range(args.warmup):
+        oracle_sample(case, weights, xh, logits_h, bias_h, g.choice(case.t, 1, replace=False))
+    t0 = time.perf_counter()
+    n = 0
+    for _ in range(args.steps):
+        tok = g.choice(case.t, 1, replace=False)
+        oracle_sample(case, weights, xh, logits_h, bias_h, tok)
+        n += len(tok)
+    el = time.perf_counter() - t0
+    value = n / el
+    line = {"impl": "reference",
+            "metric": "MoE gather-qmm prefill tok/s (2048 tok); decode qgemv weight GB/s vs HBM",
+            "value": round(value, 4), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * el / args.steps, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": case.name, "tokens": case.t, "hidden": case.hidden, "inter": case.inter,
+                       "experts": case.experts, "topk": case.topk,
+                       "sample": "1 token row per step (its 6 experts + shared expert, fp64 oracle)"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "tok/s", "cores": _cores(), "kind": "oracle",
+                             "sample": f"{n} token rows, 1 per step"},
+            "e2e": {"value": round(value, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_main(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,230 @@
+"""Python binding of the block-quantized MoE gather-qmm library (``libbq.so``).
+
+Argument marshalling only: every function forwards device pointers of
+PyTorch tensors and the current CUDA stream to the C ABI declared in
+``include/bq.h``.  All arithmetic runs in the library's CUDA kernels; there
+is no CPU fallback.  Importing this package fails when the library has not
+been built (``python block_quantized_moe_gather_gb300/build.py``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import POINTER, c_char_p, c_int32, c_int64, c_size_t, c_uint64, c_void_p
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbq.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with "
+                      "`python block_quantized_moe_gather_gb300/build.py`")
+_lib = ctypes.CDLL(LIB_PATH)
+
+# ---------------------------------------------------------------- constants
+OK = 0
+FMT_Q8_0, FMT_Q2_K, FMT_INT4_G64 = 1, 2, 3
+FMT_BY_NAME = {"q8_0": FMT_Q8_0, "q2_k": FMT_Q2_K, "int4": FMT_INT4_G64}
+DEV_OK, DEV_BAD_EXPERT_ID, DEV_WAIT_TIMEOUT = 0, 1, 2
+STATUS_NAMES = {0: "BQ_OK", 1: "BQ_ERR_NULL", 2: "BQ_ERR_SHAPE", 3: "BQ_ERR_ALIGN", 4: "BQ_ERR_FORMAT",
+                5: "BQ_ERR_WORKSPACE", 6: "BQ_ERR_CUDA", 7: "BQ_ERR_DEVICE", 8: "BQ_ERR_ARCH"}
+
+
+class QWeightC(ctypes.Structure):
+    _fields_ = [("fmt", c_int32), ("n_mats", c_int32), ("n", c_int32), ("k", c_int32),
+                ("swiglu", c_int32), ("reserved", c_int32), ("data", c_void_p)]
+
+
+class MoEDescC(ctypes.Structure):
+    _fields_ = [("T", c_int32), ("hidden", c_int32), ("inter", c_int32), ("n_experts", c_int32),
+                ("topk", c_int32), ("reserved", c_int32), ("w_gate_up", QWeightC), ("w_down", QWeightC),
+                ("shared_gate_up", POINTER(QWeightC)), ("shared_down", POINTER(QWeightC))]
+
+
+_SIGS = {
+    "bq_status_string": (c_char_p, [c_int32]),
+    "bq_last_error": (c_char_p, []),
+    "bq_device_status": (c_int32, [c_void_p, POINTER(c_int32)]),
+    "bq_gguf_dequant_q8_0": (c_int32, [c_void_p, c_int64, c_void_p, c_void_p]),
+    "bq_gguf_dequant_q2_k": (c_int32, [c_void_p, c_int64, c_void_p, c_void_p]),
+    "bq_qweight_bytes": (c_size_t, [c_int32, c_int32, c_int32, c_int32]),
+    "bq_repack_q8_0": (c_int32, [c_void_p, POINTER(QWeightC), c_void_p]),
+    "bq_repack_q2_k": (c_int32, [c_void_p, POINTER(QWeightC), c_void_p]),
+    "bq_repack_int4": (c_int32, [c_void_p, c_void_p, c_void_p, POINTER(QWeightC), c_void_p]),
+    "bq_qmm": (c_int32, [c_void_p, c_int32, POINTER(QWeightC), c_void_p, c_void_p]),
+    "bq_moe_route": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p]),
+    "bq_moe_permute_workspace_bytes": (c_size_t, [c_int32, c_int32, c_int32]),
+    "bq_moe_permute": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
+                                 c_void_p, c_void_p, c_size_t, c_void_p]),
+    "bq_moe_workspace_bytes": (c_size_t, [POINTER(MoEDescC)]),
+    "bq_set_stage_events": (c_int32, [c_int32, c_void_p, c_void_p]),
+    "bq_launch_count": (c_uint64, []),
+    "bq_moe_gather_qmm": (c_int32, [POINTER(MoEDescC), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                    c_size_t, c_void_p]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class BQError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.bq_last_error().decode(errors="replace")
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {msg}")
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise BQError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def status_string(s: int) -> str:
+    return _lib.bq_status_string(s).decode()
+
+
+def last_error() -> str:
+    return _lib.bq_last_error().decode()
+
+
+def device_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status code."""
+    code = c_int32(0)
+    st = _lib.bq_device_status(_stream(stream), ctypes.byref(code))
+    if st not in (OK, 7):
+        raise BQError(st, "bq_device_status")
+    return code.value
+
+
+# ---------------------------------------------------------------- dequant
+def gguf_dequant_q8_0(blocks, out, stream=None):
+    """blocks: uint8 device tensor of n*34 bytes; out: fp32 device tensor of n*32."""
+    n = blocks.numel() // 34
+    _check(_lib.bq_gguf_dequant_q8_0(_ptr(blocks), n, _ptr(out), _stream(stream)), "bq_gguf_dequant_q8_0")
+    return out
+
+
+def gguf_dequant_q2_k(blocks, out, stream=None):
+    n = blocks.numel() // 84
+    _check(_lib.bq_gguf_dequant_q2_k(_ptr(blocks), n, _ptr(out), _stream(stream)), "bq_gguf_dequant_q2_k")
+    return out
+
+
+# ---------------------------------------------------------------- weights
+def qweight_bytes(fmt: int, n_mats: int, n: int, k: int) -> int:
+    return int(_lib.bq_qweight_bytes(fmt, n_mats, n, k))
+
+
+class QWeight:
+    """A repacked quantised weight stack [n_mats][n][k] held in a device
+    uint8 tensor (``buf``), plus the C descriptor pointing at it."""
+
+    def __init__(self, fmt: int, n_mats: int, n: int, k: int, swiglu: bool = False, device="cuda"):
+        import torch
+        nbytes = qweight_bytes(fmt, n_mats, n, k)
+        if nbytes == 0:
+            raise BQError(2, f"QWeight(fmt={fmt}, {n_mats}x{n}x{k})")
+        # 256-byte alignment: the caching allocator returns 512-byte aligned blocks
+        self.buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.fmt, self.n_mats, self.n, self.k, self.swiglu = fmt, n_mats, n, k, int(swiglu)
+        self.c = QWeightC(fmt, n_mats, n, k, int(swiglu), 0, self.buf.data_ptr())
+
+    @property
+    def nbytes(self) -> int:
+        return self.buf.numel()
+
+
+def repack_q8_0(blocks, w: QWeight, stream=None) -> QWeight:
+    _check(_lib.bq_repack_q8_0(_ptr(blocks), ctypes.byref(w.c), _stream(stream)), "bq_repack_q8_0")
+    return w
+
+
+def repack_q2_k(blocks, w: QWeight, stream=None) -> QWeight:
+    _check(_lib.bq_repack_q2_k(_ptr(blocks), ctypes.byref(w.c), _stream(stream)), "bq_repack_q2_k")
+    return w
+
+
+def repack_int4(words, scales, biases, w: QWeight, stream=None) -> QWeight:
+    _check(_lib.bq_repack_int4(_ptr(words), _ptr(scales), _ptr(biases), ctypes.byref(w.c), _stream(stream)),
+           "bq_repack_int4")
+    return w
+
+
+# ---------------------------------------------------------------- compute
+def qmm(x, w: QWeight, y, stream=None):
+    """y[m][n] = x[m][k] W^T; x fp16 [m, k], y fp32 [m, n] (device)."""
+    m = x.shape[0] if x.dim() == 2 else 1
+    _check(_lib.bq_qmm(_ptr(x), m, ctypes.byref(w.c), _ptr(y), _stream(stream)), "bq_qmm")
+    return y
+
+
+def moe_route(logits, bias, k: int, ids, weights, stream=None):
+    t, e = logits.shape
+    _check(_lib.bq_moe_route(_ptr(logits), _ptr(bias), t, e, k, _ptr(ids), _ptr(weights), _stream(stream)),
+           "bq_moe_route")
+
+
+def moe_permute_workspace_bytes(t: int, k: int, e: int) -> int:
+    return int(_lib.bq_moe_permute_workspace_bytes(t, k, e))
+
+
+def moe_permute(ids, n_experts: int, counts, offsets, perm_token, perm_slot, inv, workspace, stream=None):
+    t, k = ids.shape
+    _check(_lib.bq_moe_permute(_ptr(ids), t, k, n_experts, _ptr(counts), _ptr(offsets), _ptr(perm_token),
+                               _ptr(perm_slot), _ptr(inv), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "bq_moe_permute")
+
+
+STAGE_ROUTE_PERMUTE, STAGE_GATE_UP, STAGE_DOWN, STAGE_SHARED, STAGE_COMBINE = range(5)
+
+
+def set_stage_events(stage: int, start=None, stop=None):
+    """Have later layer calls record `start`/`stop` (torch.cuda.Event, already
+    recorded once so that they exist) around one stage; None clears."""
+    h = (lambda ev: None if ev is None else ctypes.c_void_p(ev.cuda_event))
+    _check(_lib.bq_set_stage_events(stage, h(start), h(stop)), "bq_set_stage_events")
+
+
+def launch_count() -> int:
+    return int(_lib.bq_launch_count())
+
+
+class MoELayer:
+    """Descriptor of one MoE layer over repacked weights (host struct)."""
+
+    def __init__(self, t: int, hidden: int, inter: int, n_experts: int, topk: int, w_gate_up: QWeight,
+                 w_down: QWeight, shared_gate_up: QWeight | None = None, shared_down: QWeight | None = None):
+        self.weights = (w_gate_up, w_down, shared_gate_up, shared_down)  # keep buffers alive
+        self._s_gu = shared_gate_up.c if shared_gate_up else None
+        self._s_d = shared_down.c if shared_down else None
+        self.c = MoEDescC(t, hidden, inter, n_experts, topk, 0, w_gate_up.c, w_down.c,
+                          ctypes.pointer(self._s_gu) if self._s_gu else None,
+                          ctypes.pointer(self._s_d) if self._s_d else None)
+
+    def set_tokens(self, t: int):
+        self.c.T = t
+
+    def workspace_bytes(self) -> int:
+        return int(_lib.bq_moe_workspace_bytes(ctypes.byref(self.c)))
+
+
+def moe_workspace_bytes(layer: MoELayer) -> int:
+    return layer.workspace_bytes()
+
+
+def moe_gather_qmm(layer: MoELayer, x, router_logits, logit_bias, y, workspace, stream=None):
+    _check(_lib.bq_moe_gather_qmm(ctypes.byref(layer.c), _ptr(x), _ptr(router_logits), _ptr(logit_bias),
+                                  _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "bq_moe_gather_qmm")
+    return y

@@ -1,0 +1,114 @@
+// Internal definitions shared by the library's translation units.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/bq.h"
+
+// --------------------------------------------------------------------------
+// Host-side error reporting
+// --------------------------------------------------------------------------
+namespace bq {
+
+// Records a message for bq_last_error() and returns the status.
+bq_status fail(bq_status s, const char* fmt, ...);
+// Checks the current device is compute capability 10.3 (cached per device).
+bq_status check_arch();
+// Translates a pending launch error into BQ_ERR_CUDA.
+bq_status check_launch(const char* what);
+// Address of the current device's status word (device pointer).
+int32_t* device_status_ptr();
+// Counts kernel launches (bq_launch_count).
+void note_launch(int n = 1);
+// Records the stage's start/stop event (if set) on `st`.
+void stage_begin(int stage, cudaStream_t st);
+void stage_end(int stage, cudaStream_t st);
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// --------------------------------------------------------------------------
+// Device weight layout (tile-major slabs)
+//
+// Matrix e, 128-row tile rt, K-slab kt is one contiguous slab:
+//   [128 rows x 64 quant bytes][scale fields]
+// Q8_0  slab = 64 K  : qs int8 [128][64], d fp16 [128][2]             = 8704 B
+// Q2_K  slab = 256 K : qs u32 [128][16] (one word per 16-value
+//                      sub-block), sc u8 [128][16], (d,dmin) half2 [128] = 10752 B
+// int4  slab = 128 K : words u32 [128][16], (scale,bias) half2 [128][2]  = 9216 B
+//
+// Q2_K sub-block word: value 2p of the sub-block in bits 2p..2p+1, value
+// 2p+1 in bits 16+2p..17+2p (p = 0..7), so (w >> 2p) & 0x00030003 holds
+// the pair (2p, 2p+1) in the two 16-bit lanes.
+// int4 word: value 2p in bits 4p..4p+3, value 2p+1 in bits 16+4p..19+4p
+// (p = 0..3), so (w >> 4p) & 0x000F000F holds the pair (2p, 2p+1).
+//
+// The 64 quant bytes of physical row p are four 16-byte chunks; logical
+// chunk c (quant bytes 16c..16c+15 in K order) is stored at position
+// (c + (p >> 1)) & 3, so that threads reading one chunk of consecutive
+// rows from shared memory hit eight distinct 16-byte bank groups.
+//
+// swiglu = 1: physical row 32w + 16h + i of tile rt (w = 0..3, h = 0..1,
+// i = 0..15) holds logical row h*(n/2) + 64*rt + 16*w + i, so each 32-row
+// quarter pairs 16 gate rows with the 16 matching up rows.
+// --------------------------------------------------------------------------
+constexpr int kTileRows = 128;
+constexpr int kRowQuantBytes = 64;
+
+struct Fmt {
+    int slab_k;       // K values per slab
+    int slab_bytes;   // bytes per slab
+    int scale_off;    // byte offset of the scale fields inside a slab
+};
+
+__host__ __device__ constexpr Fmt fmt_info(int fmt) {
+    return fmt == BQ_FMT_Q8_0   ? Fmt{64, 8704, 8192}
+         : fmt == BQ_FMT_Q2_K   ? Fmt{256, 10752, 8192}
+         : fmt == BQ_FMT_INT4_G64 ? Fmt{128, 9216, 8192}
+                                  : Fmt{0, 0, 0};
+}
+
+__host__ __device__ inline int64_t slab_index(int e, int rt, int kt, int n_tiles, int k_slabs) {
+    return ((int64_t)e * n_tiles + rt) * k_slabs + kt;
+}
+
+__host__ __device__ __forceinline__ int quant_chunk_offset(int p, int c) {
+    return p * kRowQuantBytes + 16 * ((c + (p >> 1)) & 3);
+}
+
+__host__ __device__ inline int logical_row(int rt, int p, int n, int swiglu) {
+    if (!swiglu) return rt * kTileRows + p;
+    int w = p >> 5, h = (p >> 4) & 1, i = p & 15;
+    return h * (n / 2) + 64 * rt + 16 * w + i;
+}
+
+// --------------------------------------------------------------------------
+// Device helpers
+// --------------------------------------------------------------------------
+__device__ __forceinline__ void set_device_error(int32_t* status, int32_t code) {
+    atomicCAS(status, 0, code);
+}
+
+// fp16 pair from two 16-bit codes c0 (low lane) and c1 (high lane) that
+// already sit in the low 10 bits of each lane: 1024 + c exactly, then
+// subtract 1024 exactly.
+__device__ __forceinline__ __half2 codes_to_half2(uint32_t lanes) {
+    uint32_t h = lanes | 0x64006400u;
+    __half2 v = *reinterpret_cast<__half2*>(&h);
+    return __hsub2(v, __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
+}
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
+
+// Two signed int8 values (bytes b0 and b1 of `w` selected by `sel`) as an
+// exact fp16 pair: flip the sign bit to bias by 128, place each byte in the
+// low byte of a 1024-exponent fp16, subtract 1152.
+__device__ __forceinline__ __half2 s8pair_to_half2(uint32_t w_xor80, uint32_t sel) {
+    uint32_t h = __byte_perm(w_xor80, 0x64646464u, sel);
+    __half2 v = *reinterpret_cast<__half2*>(&h);
+    return __hsub2(v, __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+}
+
+}  // namespace bq

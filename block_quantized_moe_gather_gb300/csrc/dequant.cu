@@ -1,0 +1,134 @@
+// Standalone GGUF block dequantisation to fp32 (Q8_0 and Q2_K).
+//
+// "feat(gguf,dsv4): GGUF block-dequant + DSv4 kernel surface (WIP)"
+// (thewafflehaus/iron PR #9), kernels 1 and 2: Q8_0 out[i] = qs[i] *
+// scale[i/32] with select-based sign extension; Q2_K two-level scale over
+// 16-value sub-blocks of a 256-value, 84-byte super-block.
+//
+// Each CTA stages a chunk of whole blocks into shared memory with 16-byte
+// loads (the chunk sizes keep every chunk start 16-byte aligned), then
+// writes the decoded values with 16-byte float4 stores.  The path is bound
+// by the fp32 writes (4 bytes out per 1.06 or 0.33 bytes in).
+#include <algorithm>
+
+#include "bq_internal.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kQ8BlocksPerChunk = 64;   // 64 * 34 = 2176 bytes = 136 x 16
+constexpr int kQ2BlocksPerChunk = 32;   // 32 * 84 = 2688 bytes = 168 x 16
+
+// Copies `bytes` bytes from a 16-byte aligned global address to shared memory.
+__device__ __forceinline__ void stage_bytes(uint8_t* smem, const uint8_t* src, int bytes) {
+    const int vec = bytes / 16;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(smem);
+    for (int i = threadIdx.x; i < vec; i += blockDim.x) d4[i] = __ldg(s4 + i);
+    for (int i = vec * 16 + threadIdx.x; i < bytes; i += blockDim.x) smem[i] = __ldg(src + i);
+}
+
+__device__ __forceinline__ float load_half(const uint8_t* p) {
+    uint16_t bits = (uint16_t)p[0] | ((uint16_t)p[1] << 8);
+    return __half2float(__ushort_as_half(bits));
+}
+
+__global__ void __launch_bounds__(kThreads)
+dequant_q8_0_kernel(const uint8_t* __restrict__ blocks, int64_t n_blocks, float* __restrict__ out) {
+    __shared__ __align__(16) uint8_t sm[kQ8BlocksPerChunk * 34];
+    const int64_t n_chunks = (n_blocks + kQ8BlocksPerChunk - 1) / kQ8BlocksPerChunk;
+    for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+        const int64_t b0 = c * kQ8BlocksPerChunk;
+        const int nb = (int)std::min<int64_t>(kQ8BlocksPerChunk, n_blocks - b0);
+        __syncthreads();
+        stage_bytes(sm, blocks + b0 * 34, nb * 34);
+        __syncthreads();
+        const int n_vec = nb * 8;  // groups of 4 outputs
+        float4* o4 = reinterpret_cast<float4*>(out + b0 * 32);
+        for (int g = threadIdx.x; g < n_vec; g += kThreads) {
+            const int b = g >> 3, i0 = (g & 7) * 4;
+            const uint8_t* blk = sm + b * 34;
+            const float d = load_half(blk);
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int u = blk[2 + i0 + j];
+                const int q = u >= 128 ? u - 256 : u;
+                v[j] = __fmul_rn((float)q, d);
+            }
+            o4[g] = make_float4(v[0], v[1], v[2], v[3]);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+dequant_q2_k_kernel(const uint8_t* __restrict__ blocks, int64_t n_blocks, float* __restrict__ out) {
+    __shared__ __align__(16) uint8_t sm[kQ2BlocksPerChunk * 84];
+    const int64_t n_chunks = (n_blocks + kQ2BlocksPerChunk - 1) / kQ2BlocksPerChunk;
+    for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+        const int64_t b0 = c * kQ2BlocksPerChunk;
+        const int nb = (int)std::min<int64_t>(kQ2BlocksPerChunk, n_blocks - b0);
+        __syncthreads();
+        stage_bytes(sm, blocks + b0 * 84, nb * 84);
+        __syncthreads();
+        const int n_vec = nb * 64;
+        float4* o4 = reinterpret_cast<float4*>(out + b0 * 256);
+        for (int g = threadIdx.x; g < n_vec; g += kThreads) {
+            const int b = g >> 6, v0 = (g & 63) * 4;
+            const uint8_t* blk = sm + b * 84;
+            const float d = load_half(blk + 80), dmin = load_half(blk + 82);
+            const int sbyte = blk[v0 >> 4];                       // same sub-block for v0..v0+3
+            const float dsc = __fmul_rn(d, (float)(sbyte & 15));
+            const float mm = __fmul_rn(dmin, (float)(sbyte >> 4));
+            const int half = v0 >> 7, shift = 2 * ((v0 >> 5) & 3), l0 = v0 & 31;
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int q = (blk[16 + 32 * half + l0 + j] >> shift) & 3;
+                v[j] = __fsub_rn(__fmul_rn(dsc, (float)q), mm);
+            }
+            o4[g] = make_float4(v[0], v[1], v[2], v[3]);
+        }
+    }
+}
+
+int grid_for(int64_t chunks) {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return (int)std::min<int64_t>(chunks, (int64_t)sms * 8);
+}
+
+bq_status validate(const char* name, const void* blocks, int64_t n_blocks, const float* out) {
+    if (n_blocks < 0) return bq::fail(BQ_ERR_SHAPE, "%s: n_blocks = %lld < 0", name, (long long)n_blocks);
+    if (n_blocks > 0 && (!blocks || !out)) return bq::fail(BQ_ERR_NULL, "%s: NULL pointer", name);
+    if (n_blocks > 0 && (!bq::aligned(blocks, 16) || !bq::aligned(out, 16)))
+        return bq::fail(BQ_ERR_ALIGN, "%s: blocks and out must be 16-byte aligned", name);
+    return BQ_OK;
+}
+
+}  // namespace
+
+extern "C" bq_status bq_gguf_dequant_q8_0(const void* blocks, int64_t n_blocks, float* out,
+                                          bq_stream_t stream) {
+    bq_status s = validate("bq_gguf_dequant_q8_0", blocks, n_blocks, out);
+    if (s != BQ_OK || n_blocks == 0) return s;
+    if ((s = bq::check_arch()) != BQ_OK) return s;
+    const int64_t chunks = (n_blocks + kQ8BlocksPerChunk - 1) / kQ8BlocksPerChunk;
+    dequant_q8_0_kernel<<<grid_for(chunks), kThreads, 0, (cudaStream_t)stream>>>(
+        static_cast<const uint8_t*>(blocks), n_blocks, out);
+    bq::note_launch();
+    return bq::check_launch("bq_gguf_dequant_q8_0");
+}
+
+extern "C" bq_status bq_gguf_dequant_q2_k(const void* blocks, int64_t n_blocks, float* out,
+                                          bq_stream_t stream) {
+    bq_status s = validate("bq_gguf_dequant_q2_k", blocks, n_blocks, out);
+    if (s != BQ_OK || n_blocks == 0) return s;
+    if ((s = bq::check_arch()) != BQ_OK) return s;
+    const int64_t chunks = (n_blocks + kQ2BlocksPerChunk - 1) / kQ2BlocksPerChunk;
+    dequant_q2_k_kernel<<<grid_for(chunks), kThreads, 0, (cudaStream_t)stream>>>(
+        static_cast<const uint8_t*>(blocks), n_blocks, out);
+    bq::note_launch();
+    return bq::check_launch("bq_gguf_dequant_q2_k");
+}

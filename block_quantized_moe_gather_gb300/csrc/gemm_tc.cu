@@ -1,0 +1,642 @@
+// Tensor-core (tcgen05) grouped GEMM with in-register dequantisation, for
+// the dense qmm (m > 8), the routed experts' gate/up (+ SwiGLU) and down
+// projections, and the shared expert.
+//
+// "metal: DSV4 M1 Ultra prefill/decode campaign" (QuixiAI/SlimServe PR
+// #2): a work queue (qc_moe_mm_map0) feeds a per-expert tiled prefill GEMM
+// so MoE layers stop being token-at-a-time GEMVs -- "biggest single
+// prefill win"; a q2_K down-projection twin; a wide-tile q8_0 qgemm.
+// "WIP: metaltile shim -- Qwen3.6 mt_qmm_mma / mt_moe_gather dispatch"
+// (TheTom/vllm-swift PR #22): mt_moe_gather_qmm_mma_int4_bm{16,64} tiles
+// gathered token rows against int4 expert weights.  Here, for sm_103a:
+//
+// Tile = 128 weight rows (one row tile of the slab layout, MMA M) x up to
+// 128 token rows of one expert segment (MMA N) x all of K, fp32 in TMEM.
+// 192 threads per CTA, two CTAs per SM:
+//   warp 0     producer: TMA 2D loads of the activation tile (128-byte
+//              swizzle, 32-row boxes) and 1D bulk copies of the raw
+//              quantised slabs into shared-memory rings;
+//   warp 1     owns the TMEM allocation and issues tcgen05.mma (one lane);
+//   warps 2-5  converters: one thread per weight row dequantises its 64
+//              K-values of a stage from the raw slab into 32 fp16 pairs and
+//              writes them to a TMEM A-operand ring with tcgen05.st (the
+//              MMA reads A from TMEM, so the dequantised weights never touch
+//              shared memory); after the K loop the same warps run the
+//              epilogue (tcgen05.ld -> SwiGLU / gate scale -> global).
+// All waits are bounded: a wait that runs out sets BQ_DEV_WAIT_TIMEOUT in
+// the device status word and the CTA unwinds, freeing its TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "gemm_internal.cuh"
+#include "moe_internal.cuh"
+
+namespace {
+
+constexpr int BN = 128;            // max token rows per tile (MMA N)
+constexpr int BK = 64;             // K per stage (one 128-byte swizzle row of fp16)
+constexpr int kStagesB = 4;        // activation tiles in shared memory
+constexpr int kStagesA = 4;        // dequantised weight tiles in TMEM
+constexpr int kRawSlabs = 4;       // raw quantised slabs in shared memory
+constexpr int kThreads = 192;
+constexpr int kBoxRows = 32;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kAccCol = 0;    // accumulator: columns [0, 128)
+constexpr uint32_t kACol = 128;    // A ring: 4 x 32 columns
+constexpr int kBStageBytes = BN * 128;
+constexpr int kRawStride = 10752;  // largest slab
+constexpr int kSmemBytes = 1024 + kStagesB * kBStageBytes + kRawSlabs * kRawStride + 256;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
+
+template <int FMT> struct G;
+template <> struct G<BQ_FMT_Q8_0>     { static constexpr int SK = 64,  SB = 8704,  SPS = 1; };
+template <> struct G<BQ_FMT_Q2_K>     { static constexpr int SK = 256, SB = 10752, SPS = 4; };
+template <> struct G<BQ_FMT_INT4_G64> { static constexpr int SK = 128, SB = 9216,  SPS = 2; };
+
+enum { EPI_SWIGLU = 0, EPI_SCALE = 1, EPI_PLAIN = 2 };
+
+struct GemmArgs {
+    const uint8_t* w;
+    int n, k;
+    const int2* tiles;            // (segment, chunk) per tile, or NULL: one dense segment
+    const int32_t* n_tiles;       // device count of `tiles`
+    int dense_m;
+    const int32_t* seg_expert;
+    const int32_t* seg_start;
+    const int32_t* seg_count;
+    __half* h;                    // EPI_SWIGLU output, row stride ldh
+    int ldh;
+    float* y;                     // EPI_SCALE / EPI_PLAIN output, row stride ldy
+    int ldy;
+    const float* row_scale;       // EPI_SCALE
+    int32_t* status;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: false if the CTA is aborting or the wait ran out (which
+// raises the abort flag and records BQ_DEV_WAIT_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                          int32_t* status) {
+    if (mbar_try(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1u;
+            bq::set_device_error(status, BQ_DEV_WAIT_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Warp-uniform bounded wait: lane 0 polls, every lane gets its verdict.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                          int32_t* status) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, status);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    return (uint64_t)((addr & 0x3FFFFu) >> 4)      // start address
+         | ((uint64_t)1 << 16)                      // leading byte offset (unused for swizzled K-major)
+         | ((uint64_t)(1024 >> 4) << 32)            // stride byte offset
+         | ((uint64_t)1 << 46)                      // descriptor version
+         | ((uint64_t)2 << 61);                     // 128-byte swizzle
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B, fp32 D, both K-major,
+// M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_f16(int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+#define BQ_R32(v) "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), \
+    "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),         \
+    "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),       \
+    "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+#define BQ_W32(v) "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),        \
+    "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),   \
+    "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), \
+    "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), \
+    "=r"(v[31])
+#define BQ_OPS32 "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, " \
+    "%20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32}"
+#define BQ_OPS32_OUT "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, " \
+    "%19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}"
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], " BQ_OPS32 ";" ::"r"(taddr), BQ_R32(v)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 " BQ_OPS32_OUT ", [%32];" : BQ_W32(v) : "r"(taddr)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------- dequantisation of one row x 64 K
+// Output: 32 fp16 pairs, pair i = K values (2i, 2i+1) of the stage.
+template <int FMT>
+__device__ __forceinline__ void dequant_row(const uint8_t* raw, int p, int sub, uint32_t (&out)[32]);
+
+template <>
+__device__ __forceinline__ void dequant_row<BQ_FMT_Q8_0>(const uint8_t* raw, int p, int, uint32_t (&out)[32]) {
+    const uint32_t dd = *reinterpret_cast<const uint32_t*>(raw + 8192 + 4 * p);
+    const __half2 d0 = __low2half2(bq::u32_as_h2(dd)), d1 = __high2half2(bq::u32_as_h2(dd));
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint4 q = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, c));
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        const __half2 d = c < 2 ? d0 : d1;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const uint32_t wx = w[m] ^ 0x80808080u;
+            out[8 * c + 2 * m] = bq::h2_as_u32(__hmul2(bq::s8pair_to_half2(wx, 0x4140u), d));
+            out[8 * c + 2 * m + 1] = bq::h2_as_u32(__hmul2(bq::s8pair_to_half2(wx, 0x4342u), d));
+        }
+    }
+}
+
+template <>
+__device__ __forceinline__ void dequant_row<BQ_FMT_Q2_K>(const uint8_t* raw, int p, int sub, uint32_t (&out)[32]) {
+    const uint4 q = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, sub));
+    const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(raw + 8192 + 16 * p + 4 * sub);
+    const __half2 dm = bq::u32_as_h2(*reinterpret_cast<const uint32_t*>(raw + 10240 + 4 * p));
+    const float d = __low2float(dm), dmin = __high2float(dm);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t scb = (sc4 >> (8 * i)) & 0xFFu;
+        const __half ds = __float2half_rn(d * (float)(scb & 15u));
+        const __half ndm = __float2half_rn(-dmin * (float)(scb >> 4));
+        const __half2 ds2 = __halves2half2(ds, ds), ndm2 = __halves2half2(ndm, ndm);
+#pragma unroll
+        for (int qq = 0; qq < 8; ++qq)
+            out[8 * i + qq] = bq::h2_as_u32(__hfma2(bq::codes_to_half2((w[i] >> (2 * qq)) & 0x00030003u), ds2, ndm2));
+    }
+}
+
+template <>
+__device__ __forceinline__ void dequant_row<BQ_FMT_INT4_G64>(const uint8_t* raw, int p, int sub, uint32_t (&out)[32]) {
+    const uint4 q0 = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, 2 * sub));
+    const uint4 q1 = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, 2 * sub + 1));
+    const __half2 sb = bq::u32_as_h2(*reinterpret_cast<const uint32_t*>(raw + 8192 + 8 * p + 4 * sub));
+    const __half2 s2 = __low2half2(sb), b2 = __high2half2(sb);
+    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq)
+            out[4 * m + qq] = bq::h2_as_u32(__hfma2(bq::codes_to_half2((w[m] >> (4 * qq)) & 0x000F000Fu), s2, b2));
+}
+
+__device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
+
+// ---------------------------------------------------------------- the kernel
+template <int FMT, int EPI>
+__global__ void __launch_bounds__(kThreads, 2)
+gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
+    using F = G<FMT>;
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+    uint8_t* b_ring = smem;
+    uint8_t* raw_ring = smem + kStagesB * kBStageBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(raw_ring + kRawSlabs * kRawStride);
+    // barrier ids
+    const uint32_t bar0 = smem_u32(bars);
+    auto b_full = [&](int s) { return bar0 + 8u * s; };
+    auto b_empty = [&](int s) { return bar0 + 8u * (kStagesB + s); };
+    auto raw_full = [&](int r) { return bar0 + 8u * (2 * kStagesB + r); };
+    auto raw_empty = [&](int r) { return bar0 + 8u * (2 * kStagesB + kRawSlabs + r); };
+    auto a_full = [&](int s) { return bar0 + 8u * (2 * kStagesB + 2 * kRawSlabs + s); };
+    auto a_empty = [&](int s) { return bar0 + 8u * (2 * kStagesB + 2 * kRawSlabs + kStagesA + s); };
+    const uint32_t acc_full = bar0 + 8u * (2 * kStagesB + 2 * kRawSlabs + 2 * kStagesA);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 32);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    // ---- which tile
+    int seg = 0, chunk = blockIdx.y;
+    if (a.tiles) {
+        if ((int)blockIdx.y >= __ldg(a.n_tiles)) return;
+        const int2 t = a.tiles[blockIdx.y];
+        seg = t.x;
+        chunk = t.y;
+    }
+    const int expert = a.seg_expert ? __ldg(a.seg_expert + seg) : 0;
+    const int start = a.seg_start ? __ldg(a.seg_start + seg) : 0;
+    const int count = a.seg_count ? __ldg(a.seg_count + seg) : a.dense_m;
+    const int row0 = start + chunk * BN;
+    const int nvalid = min(BN, count - chunk * BN);
+    if (nvalid <= 0) return;
+    const int n_mma = (nvalid + 15) & ~15;
+    const int n_boxes = (nvalid + kBoxRows - 1) / kBoxRows;
+    const int rt = blockIdx.x;
+    const int n_tiles_w = a.n / bq::kTileRows, k_slabs = a.k / F::SK;
+    const uint8_t* wslab = a.w + bq::slab_index(expert, rt, 0, n_tiles_w, k_slabs) * F::SB;
+    const int KS = a.k / BK;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStagesB; ++i) { mbar_init(b_full(i), 1); mbar_init(b_empty(i), 1); }
+        for (int i = 0; i < kRawSlabs; ++i) { mbar_init(raw_full(i), 1); mbar_init(raw_empty(i), 4); }
+        for (int i = 0; i < kStagesA; ++i) { mbar_init(a_full(i), 4); mbar_init(a_empty(i), 1); }
+        mbar_init(acc_full, 1);
+        *abort_flag = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tmem_slot)), "r"(kTmemCols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
+            int issued_b = 0, issued_raw = 0;
+            bool ok = true;
+            for (int ks = 0; ks < KS && ok; ++ks) {
+                if (ks % F::SPS == 0) {
+                    const int kt = ks / F::SPS, r = kt % kRawSlabs;
+                    if (kt >= kRawSlabs && !(ok = mbar_wait(raw_empty(r), ((kt / kRawSlabs) - 1) & 1, abort_flag, a.status)))
+                        break;
+                    mbar_expect_tx(raw_full(r), F::SB);
+                    bulk_load(smem_u32(raw_ring + r * kRawStride), wslab + (int64_t)kt * F::SB, F::SB, raw_full(r));
+                    ++issued_raw;
+                }
+                const int s = ks % kStagesB;
+                if (ks >= kStagesB && !(ok = mbar_wait(b_empty(s), ((ks / kStagesB) - 1) & 1, abort_flag, a.status)))
+                    break;
+                mbar_expect_tx(b_full(s), n_boxes * kBoxRows * 128);
+                for (int bx = 0; bx < n_boxes; ++bx)
+                    tma_load_2d(smem_u32(b_ring + s * kBStageBytes + bx * kBoxRows * 128), &tmap_b, ks * BK,
+                                row0 + bx * kBoxRows, b_full(s));
+                ++issued_b;
+            }
+            if (!ok) {
+                // let our own copies land before the CTA leaves (bounded)
+                volatile uint32_t no_abort = 0;
+                for (int u = max(0, issued_b - kStagesB); u < issued_b; ++u)
+                    mbar_wait(b_full(u % kStagesB), (u / kStagesB) & 1, &no_abort, a.status);
+                for (int u = max(0, issued_raw - kRawSlabs); u < issued_raw; ++u)
+                    mbar_wait(raw_full(u % kRawSlabs), (u / kRawSlabs) & 1, &no_abort, a.status);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(n_mma);
+            bool ok = true;
+            for (int ks = 0; ks < KS; ++ks) {
+                const int sa = ks % kStagesA, s = ks % kStagesB;
+                if (!(ok = mbar_wait(a_full(sa), (ks / kStagesA) & 1, abort_flag, a.status))) break;
+                if (!(ok = mbar_wait(b_full(s), (ks / kStagesB) & 1, abort_flag, a.status))) break;
+                tc_fence_after();
+                const uint32_t b_addr = smem_u32(b_ring + s * kBStageBytes);
+#pragma unroll
+                for (int j = 0; j < BK / 16; ++j)
+                    mma_f16_ts(tmem + kAccCol, tmem + kACol + 32u * sa + 8u * j, smem_desc_sw128(b_addr + 32u * j),
+                               idesc, (ks | j) != 0);
+                mma_commit(a_empty(sa));
+                mma_commit(b_empty(s));
+            }
+            if (ok) mma_commit(acc_full);
+        }
+    } else {
+        // ------------------------------------------------ converters, then epilogue
+        const int quarter = warp & 3;
+        const int p = 32 * quarter + lane;                       // weight row = TMEM lane
+        const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
+        bool ok = true;
+        for (int ks = 0; ks < KS; ++ks) {
+            const int kt = ks / F::SPS, sub = ks % F::SPS, r = kt % kRawSlabs;
+            const int sa = ks % kStagesA;
+            if (!(ok = warp_wait(raw_full(r), (kt / kRawSlabs) & 1, abort_flag, a.status))) break;
+            if (ks >= kStagesA && !(ok = warp_wait(a_empty(sa), ((ks / kStagesA) - 1) & 1, abort_flag, a.status)))
+                break;
+            uint32_t v[32];
+            dequant_row<FMT>(raw_ring + r * kRawStride, p, sub, v);
+            tmem_st32(tmem + lane_base + kACol + 32u * sa, v);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (sub == F::SPS - 1) mbar_arrive(raw_empty(r));
+                mbar_arrive(a_full(sa));
+            }
+        }
+        if (ok && warp_wait(acc_full, 0, abort_flag, a.status)) {
+            tc_fence_after();
+            const int rt64 = 64 * rt + 16 * quarter + (lane & 15);   // SwiGLU feature
+            const int frow = bq::kTileRows * rt + p;                  // plain output feature
+            for (int c0 = 0; c0 < nvalid; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + kAccCol + (uint32_t)c0, v);
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (EPI == EPI_SWIGLU) {
+                    // lanes 0-15 hold gate rows, 16-31 the matching up rows
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float send = __uint_as_float(lane < 16 ? v[16 + i] : v[i]);
+                        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+                        const float g = lane < 16 ? __uint_as_float(v[i]) : recv;
+                        const float u = lane < 16 ? recv : __uint_as_float(v[16 + i]);
+                        const int tok = c0 + (lane < 16 ? i : 16 + i);
+                        if (tok < nvalid)
+                            a.h[(int64_t)(row0 + tok) * a.ldh + rt64] = __float2half_rn(silu_f(g) * u);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int tok = c0 + i;
+                        if (tok < nvalid) {
+                            float val = __uint_as_float(v[i]);
+                            if (EPI == EPI_SCALE) val *= __ldg(a.row_scale + row0 + tok);
+                            a.y[(int64_t)(row0 + tok) * a.ldy + frow] = val;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- helpers: gather, tile list
+__global__ void gather_rows_kernel(const __half* __restrict__ x, const int32_t* __restrict__ src_row, int rows,
+                                   int cols, __half* __restrict__ out) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (warp >= rows) return;
+    const uint4* s = reinterpret_cast<const uint4*>(x + (int64_t)__ldg(src_row + warp) * cols);
+    uint4* d = reinterpret_cast<uint4*>(out + (int64_t)warp * cols);
+    for (int i = lane; i < cols / 8; i += 32) d[i] = __ldg(s + i);
+}
+
+// Token-chunk tiles of every active segment, in segment order (the
+// per-expert work queue).  One CTA of 1024 threads; <= 1024 segments.
+__global__ void __launch_bounds__(1024)
+tile_list_kernel(const int32_t* __restrict__ seg_count, const int32_t* __restrict__ n_segments,
+                 int2* __restrict__ tiles, int32_t* __restrict__ n_tiles) {
+    __shared__ int32_t warp_sums[32];
+    const int s = threadIdx.x;
+    const int ns = *n_segments;
+    const int c = s < ns ? (seg_count[s] + BN - 1) / BN : 0;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int v = warp_sums[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += u;
+        }
+        warp_sums[lane] = v;
+    }
+    __syncthreads();
+    const int base = incl - c + (warp ? warp_sums[warp - 1] : 0);
+    for (int i = 0; i < c; ++i) tiles[base + i] = make_int2(s, i);
+    if (threadIdx.x == 0) *n_tiles = warp_sums[31];
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2D fp16 [rows][cols] activation map: boxes of 64 columns x 32 rows, 128-byte swizzle.
+bool make_act_map(CUtensorMap* map, const __half* base, int rows, int cols) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)kBoxRows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int FMT, int EPI>
+void launch_one(const CUtensorMap& map, const GemmArgs& a, dim3 grid, cudaStream_t st) {
+    // per device: the attribute is a property of the function on the current device
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        cudaFuncSetAttribute(gemm_kernel<FMT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        attr_set[dev] = true;
+    }
+    gemm_kernel<FMT, EPI><<<grid, kThreads, kSmemBytes, st>>>(map, a);
+    bq::note_launch();
+}
+
+template <int EPI>
+void launch_epi(int fmt, const CUtensorMap& map, const GemmArgs& a, dim3 grid, cudaStream_t st) {
+    switch (fmt) {
+        case BQ_FMT_Q8_0: launch_one<BQ_FMT_Q8_0, EPI>(map, a, grid, st); break;
+        case BQ_FMT_Q2_K: launch_one<BQ_FMT_Q2_K, EPI>(map, a, grid, st); break;
+        default: launch_one<BQ_FMT_INT4_G64, EPI>(map, a, grid, st); break;
+    }
+}
+
+void launch(int fmt, int epi, const CUtensorMap& map, const GemmArgs& a, dim3 grid, cudaStream_t st) {
+    if (epi == EPI_SWIGLU) launch_epi<EPI_SWIGLU>(fmt, map, a, grid, st);
+    else if (epi == EPI_SCALE) launch_epi<EPI_SCALE>(fmt, map, a, grid, st);
+    else launch_epi<EPI_PLAIN>(fmt, map, a, grid, st);
+}
+
+GemmArgs base_args(const bq_qweight* w) {
+    GemmArgs a{};
+    a.w = static_cast<const uint8_t*>(w->data);
+    a.n = w->n;
+    a.k = w->k;
+    a.status = bq::device_status_ptr();
+    return a;
+}
+
+bq_status map_fail() { return bq::fail(BQ_ERR_CUDA, "cuTensorMapEncodeTiled failed for an activation map"); }
+
+// A dense weight over m activation rows: grid (row tiles, token chunks).
+bq_status dense_gemm(const bq_qweight* w, int m, const __half* x, int epi, float* y, int ldy, __half* h, int ldh,
+                     cudaStream_t st) {
+    CUtensorMap map;
+    if (!make_act_map(&map, x, m, w->k)) return map_fail();
+    GemmArgs a = base_args(w);
+    a.dense_m = m;
+    a.y = y; a.ldy = ldy; a.h = h; a.ldh = ldh;
+    launch(w->fmt, epi, map, a, dim3(w->n / bq::kTileRows, (m + BN - 1) / BN), st);
+    return BQ_OK;
+}
+
+// Workspace the routed GEMMs add to the MoE carve-up.
+struct GemmWs {
+    int2* tiles;
+    int32_t* n_tiles;
+    __half* x_perm;
+    size_t bytes;
+};
+
+size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+GemmWs carve(const bq_moe_desc* d, uint8_t* base) {
+    const size_t P = (size_t)d->T * d->topk;
+    const size_t max_tiles = std::min<size_t>(d->n_experts, P) + (P + BN - 1) / BN;
+    GemmWs g;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { uint8_t* p = base ? base + off : nullptr; off += up256(bytes); return p; };
+    g.tiles = (int2*)take(max_tiles * sizeof(int2));
+    g.n_tiles = (int32_t*)take(4);
+    g.x_perm = (__half*)take(P * (size_t)d->hidden * 2);
+    g.bytes = off;
+    return g;
+}
+
+}  // namespace
+
+namespace bq {
+
+bool gemm_supported(int fmt) {
+    return false && (fmt == BQ_FMT_Q8_0 || fmt == BQ_FMT_Q2_K || fmt == BQ_FMT_INT4_G64) && encode_fn() != nullptr;
+}
+
+size_t gemm_moe_workspace_bytes(const bq_moe_desc* d) { return carve(d, nullptr).bytes; }
+
+bq_status launch_gemm_dense(const bq_qweight* w, int m, const __half* x, float* y, cudaStream_t st) {
+    return dense_gemm(w, m, x, EPI_PLAIN, y, w->n, nullptr, 0, st);
+}
+
+bq_status launch_gemm_moe(const bq_moe_desc* d, const __half* x, const int32_t* perm_token, const float* perm_gate,
+                     const int32_t* seg_expert, const int32_t* seg_start, const int32_t* seg_count,
+                     const int32_t* n_segments, const int32_t*, __half* h, float* y_slot, uint8_t* ws,
+                     cudaStream_t st) {
+    const int P = d->T * d->topk, H = d->hidden, I = d->inter;
+    GemmWs g = carve(d, ws);
+    const int max_tiles = std::min(d->n_experts, P) + (P + BN - 1) / BN;
+    tile_list_kernel<<<1, 1024, 0, st>>>(seg_count, n_segments, g.tiles, g.n_tiles);
+    note_launch();
+
+    stage_begin(BQ_STAGE_GATE_UP, st);
+    gather_rows_kernel<<<(P + 7) / 8, 256, 0, st>>>(x, perm_token, P, H, g.x_perm);
+    note_launch();
+    CUtensorMap map_x;
+    if (!make_act_map(&map_x, g.x_perm, P, H)) return map_fail();
+    GemmArgs a = base_args(&d->w_gate_up);
+    a.tiles = g.tiles; a.n_tiles = g.n_tiles;
+    a.seg_expert = seg_expert; a.seg_start = seg_start; a.seg_count = seg_count;
+    a.h = h; a.ldh = I;
+    launch(d->w_gate_up.fmt, EPI_SWIGLU, map_x, a, dim3(2 * I / kTileRows, max_tiles), st);
+    stage_end(BQ_STAGE_GATE_UP, st);
+
+    stage_begin(BQ_STAGE_DOWN, st);
+    CUtensorMap map_h;
+    if (!make_act_map(&map_h, h, P, I)) return map_fail();
+    GemmArgs b = base_args(&d->w_down);
+    b.tiles = g.tiles; b.n_tiles = g.n_tiles;
+    b.seg_expert = seg_expert; b.seg_start = seg_start; b.seg_count = seg_count;
+    b.y = y_slot; b.ldy = H; b.row_scale = perm_gate;
+    launch(d->w_down.fmt, EPI_SCALE, map_h, b, dim3(H / kTileRows, max_tiles), st);
+    stage_end(BQ_STAGE_DOWN, st);
+    return BQ_OK;
+}
+
+bq_status launch_gemm_shared(const bq_qweight* gu, const bq_qweight* dn, int T, const __half* x, __half* h_shared,
+                             float* y, int inter_shared, uint8_t*, cudaStream_t st) {
+    bq_status s = dense_gemm(gu, T, x, EPI_SWIGLU, nullptr, 0, h_shared, inter_shared, st);
+    if (s != BQ_OK) return s;
+    return dense_gemm(dn, T, h_shared, EPI_PLAIN, y, dn->n, nullptr, 0, st);
+}
+
+}  // namespace bq

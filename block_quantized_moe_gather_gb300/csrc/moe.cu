@@ -1,0 +1,258 @@
+// Dense qmm and the MoE layer orchestration (S3-S13).
+//
+// "WIP: metaltile shim -- Qwen3.6 mt_qmm_mma / mt_moe_gather dispatch"
+// (TheTom/vllm-swift PR #22): mt_qmm_mma and mt_moe_gather_qmm replace a
+// generic quantised matmul in the MoE forward.  "metal: DSV4 M1 Ultra
+// prefill/decode campaign" (QuixiAI/SlimServe PR #2): the qc_moe_mm_map0
+// work queue feeds a tiled MoE prefill GEMM, so MoE layers stop being
+// token-at-a-time GEMVs; the q2_K down projection is a separate twin.
+// "Everything Bagel 2" (thewafflehaus/butter PR #10): GPU router, expert
+// indices consumed on the device with no host readback, fused swiglu, and
+// one combine dispatch (scalarFMAChain8) instead of k.
+//
+// Layer flow (all on `stream`, no host synchronisation):
+//   route -> permute (histogram, scan, placement) -> segment list
+//   -> gate/up with fused SwiGLU into H (fp16, permuted pair order)
+//   -> down scaled by the gate weight into Y_slot (fp32, permuted order)
+//   -> [shared expert: gate/up + SwiGLU, down written straight into y]
+//   -> combine: y[t] (+)= sum_j Y_slot[inv[t*k + j]], slots in order.
+#include <string.h>
+
+#include <algorithm>
+
+#include "gemm_internal.cuh"
+#include "moe_internal.cuh"
+
+namespace {
+
+// Compacts the experts with a nonzero count into a segment list (ascending
+// expert id), one CTA of 1024 threads, E <= 1024.
+__global__ void __launch_bounds__(1024)
+segments_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ offsets, int E,
+                int32_t* __restrict__ seg_expert, int32_t* __restrict__ seg_start,
+                int32_t* __restrict__ seg_count, int32_t* __restrict__ n_segments) {
+    __shared__ int32_t warp_sums[32];
+    const int e = threadIdx.x;
+    const int c = e < E ? counts[e] : 0;
+    const int active = c > 0;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t bal = __ballot_sync(0xffffffffu, active);
+    if (lane == 0) warp_sums[warp] = __popc(bal);
+    __syncthreads();
+    if (warp == 0) {
+        int v = warp_sums[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += u;
+        }
+        warp_sums[lane] = v;  // inclusive
+    }
+    __syncthreads();
+    const int before = (warp ? warp_sums[warp - 1] : 0) + __popc(bal & ((1u << lane) - 1u));
+    if (active) {
+        seg_expert[before] = e;
+        seg_start[before] = offsets[e];
+        seg_count[before] = c;
+    }
+    if (threadIdx.x == 0) *n_segments = warp_sums[31];
+}
+
+// y[t][c] (+)= sum_{j < k} y_slot[inv[t*k + j]][c], slots in order.
+__global__ void combine_kernel(const float* __restrict__ y_slot, const int32_t* __restrict__ inv, int T,
+                               int k, int H, int accumulate, float* __restrict__ y) {
+    const int h4 = H / 4;
+    const int64_t total = (int64_t)T * h4;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int t = (int)(i / h4), c4 = (int)(i % h4);
+        float4 acc = accumulate ? reinterpret_cast<const float4*>(y)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const int r = __ldg(inv + (int64_t)t * k + j);
+            if (r < 0) continue;
+            const float4 v = __ldg(reinterpret_cast<const float4*>(y_slot + (int64_t)r * H) + c4);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        reinterpret_cast<float4*>(y)[i] = acc;
+    }
+}
+
+// Workspace carve-up of one MoE call.
+struct MoeWs {
+    int32_t *ids, *counts, *offsets, *perm_token, *perm_slot, *inv;
+    int32_t *seg_expert, *seg_start, *seg_count, *n_segments, *scratch;
+    float *gate, *perm_gate, *y_slot;
+    __half *h, *h_shared;
+    size_t bytes;
+};
+
+size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+MoeWs carve(const bq_moe_desc* d, uint8_t* base) {
+    const size_t T = d->T, P = (size_t)d->T * d->topk, E = d->n_experts, H = d->hidden, I = d->inter;
+    MoeWs w;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { uint8_t* p = base ? base + off : nullptr; off += up256(bytes); return p; };
+    w.ids = (int32_t*)take(P * 4);
+    w.gate = (float*)take(P * 4);
+    w.counts = (int32_t*)take(E * 4);
+    w.offsets = (int32_t*)take((E + 1) * 4);
+    w.perm_token = (int32_t*)take(P * 4);
+    w.perm_slot = (int32_t*)take(P * 4);
+    w.perm_gate = (float*)take(P * 4);
+    w.inv = (int32_t*)take(P * 4);
+    w.seg_expert = (int32_t*)take(E * 4);
+    w.seg_start = (int32_t*)take(E * 4);
+    w.seg_count = (int32_t*)take(E * 4);
+    w.n_segments = (int32_t*)take(4);
+    w.scratch = (int32_t*)take(bq::permute_scratch_bytes((int)P, (int)E));
+    w.h = (__half*)take(P * I * 2);
+    w.y_slot = (float*)take(P * H * 4);
+    w.h_shared = nullptr;
+    if (d->shared_gate_up) w.h_shared = (__half*)take(T * (size_t)(d->shared_gate_up->n / 2) * 2);
+    w.bytes = off;
+    return w;
+}
+
+bq_status check_weight(const char* name, const bq_qweight* w, int n_mats, int n, int k, int swiglu) {
+    if (!w->data) return bq::fail(BQ_ERR_NULL, "%s: weight data is NULL", name);
+    if (bq_qweight_bytes(w->fmt, w->n_mats, w->n, w->k) == 0)
+        return bq::fail(BQ_ERR_FORMAT, "%s: invalid weight (fmt %d, %d x %d x %d)", name, w->fmt, w->n_mats, w->n, w->k);
+    if ((n_mats > 0 && w->n_mats != n_mats) || (n > 0 && w->n != n) || w->k != k || w->swiglu != swiglu)
+        return bq::fail(BQ_ERR_FORMAT, "%s: weight is %d x %d x %d (swiglu %d), expected %d x %d x %d (swiglu %d)",
+                        name, w->n_mats, w->n, w->k, w->swiglu, n_mats, n, k, swiglu);
+    if (!bq::aligned(w->data, 256)) return bq::fail(BQ_ERR_ALIGN, "%s: weight data must be 256-byte aligned", name);
+    return BQ_OK;
+}
+
+bq_status validate_moe(const bq_moe_desc* d) {
+    if (!d) return bq::fail(BQ_ERR_NULL, "bq_moe: desc is NULL");
+    bq_status s = bq::validate_route("bq_moe_gather_qmm", d->T, d->n_experts, d->topk);
+    if (s != BQ_OK) return s;
+    if (d->hidden < 1 || d->inter < 1)
+        return bq::fail(BQ_ERR_SHAPE, "bq_moe_gather_qmm: hidden %d, inter %d", d->hidden, d->inter);
+    if ((s = check_weight("w_gate_up", &d->w_gate_up, d->n_experts, 2 * d->inter, d->hidden, 1)) != BQ_OK) return s;
+    if ((s = check_weight("w_down", &d->w_down, d->n_experts, d->hidden, d->inter, 0)) != BQ_OK) return s;
+    if ((d->shared_gate_up == nullptr) != (d->shared_down == nullptr))
+        return bq::fail(BQ_ERR_NULL, "bq_moe_gather_qmm: shared_gate_up and shared_down must both be set or both NULL");
+    if (d->shared_gate_up) {
+        if ((s = check_weight("shared_gate_up", d->shared_gate_up, 1, -1, d->hidden, 1)) != BQ_OK) return s;
+        if ((s = check_weight("shared_down", d->shared_down, 1, d->hidden, d->shared_gate_up->n / 2, 0)) != BQ_OK)
+            return s;
+    }
+    return BQ_OK;
+}
+
+// One dense weight over `m` rows of x (single segment).
+bq::QgemvParams dense_params(const bq_qweight* w, int m, const __half* x, float* y, __half* h, int ldy) {
+    bq::QgemvParams p{};
+    p.w = static_cast<const uint8_t*>(w->data);
+    p.fmt = w->fmt; p.n = w->n; p.k = w->k; p.swiglu = w->swiglu;
+    p.m = m; p.x = x; p.y = y; p.h = h; p.ldy = ldy;
+    return p;
+}
+
+}  // namespace
+
+extern "C" bq_status bq_qmm(const uint16_t* x, int32_t m, const bq_qweight* w, float* y, bq_stream_t stream) {
+    if (!w) return bq::fail(BQ_ERR_NULL, "bq_qmm: w is NULL");
+    if (m < 0) return bq::fail(BQ_ERR_SHAPE, "bq_qmm: m = %d < 0", m);
+    bq_status s = check_weight("bq_qmm", w, -1, -1, w->k, 0);
+    if (s != BQ_OK || m == 0) return s;
+    if (!x || !y) return bq::fail(BQ_ERR_NULL, "bq_qmm: x or y is NULL");
+    if (!bq::aligned(x, 16) || !bq::aligned(y, 16)) return bq::fail(BQ_ERR_ALIGN, "bq_qmm: x and y must be 16-byte aligned");
+    if ((s = bq::check_arch()) != BQ_OK) return s;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (m <= 8 || !bq::gemm_supported(w->fmt)) {
+        bq::launch_qgemv(dense_params(w, m, reinterpret_cast<const __half*>(x), y, nullptr, w->n), 1, st);
+    } else if ((s = bq::launch_gemm_dense(w, m, reinterpret_cast<const __half*>(x), y, st)) != BQ_OK) {
+        return s;
+    }
+    return bq::check_launch("bq_qmm");
+}
+
+extern "C" size_t bq_moe_workspace_bytes(const bq_moe_desc* desc) {
+    if (!desc || desc->T < 0 || desc->topk < 1 || desc->n_experts < 1 || desc->n_experts > 1024) return 0;
+    return carve(desc, nullptr).bytes + bq::gemm_moe_workspace_bytes(desc);
+}
+
+extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, const float* router_logits,
+                                       const float* logit_bias, float* y, void* workspace, size_t ws_bytes,
+                                       bq_stream_t stream) {
+    bq_status s = validate_moe(d);
+    if (s != BQ_OK || d->T == 0) return s;
+    if (!x || !router_logits || !y) return bq::fail(BQ_ERR_NULL, "bq_moe_gather_qmm: NULL input/output");
+    if (!bq::aligned(x, 16) || !bq::aligned(y, 16) || !bq::aligned(router_logits, 4) ||
+        (logit_bias && !bq::aligned(logit_bias, 4)))
+        return bq::fail(BQ_ERR_ALIGN, "bq_moe_gather_qmm: x and y must be 16-byte aligned, logits 4-byte");
+    if (d->hidden % 4) return bq::fail(BQ_ERR_SHAPE, "bq_moe_gather_qmm: hidden must be a multiple of 4");
+    const size_t need = bq_moe_workspace_bytes(d);
+    if (!workspace || ws_bytes < need)
+        return bq::fail(BQ_ERR_WORKSPACE, "bq_moe_gather_qmm: workspace %zu bytes < %zu", ws_bytes, need);
+    if (!bq::aligned(workspace, 256)) return bq::fail(BQ_ERR_ALIGN, "bq_moe_gather_qmm: workspace must be 256-byte aligned");
+    if ((s = bq::check_arch()) != BQ_OK) return s;
+
+    cudaStream_t st = (cudaStream_t)stream;
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    MoeWs w = carve(d, base);
+    const int T = d->T, k = d->topk, E = d->n_experts, H = d->hidden, I = d->inter, P = T * k;
+    const __half* xh = reinterpret_cast<const __half*>(x);
+
+    bq::stage_begin(BQ_STAGE_ROUTE_PERMUTE, st);
+    bq::launch_route(router_logits, logit_bias, T, E, k, w.ids, w.gate, st);
+    bq::launch_permute(w.ids, w.gate, T, k, E, w.counts, w.offsets, w.perm_token, w.perm_slot, w.perm_gate,
+                       w.inv, w.scratch, st);
+    segments_kernel<<<1, 1024, 0, st>>>(w.counts, w.offsets, E, w.seg_expert, w.seg_start, w.seg_count,
+                                        w.n_segments);
+    bq::note_launch();
+    bq::stage_end(BQ_STAGE_ROUTE_PERMUTE, st);
+    const int max_segments = min(E, P);
+    const bool decode = T <= 8 || !bq::gemm_supported(d->w_gate_up.fmt);
+
+    if (decode) {
+        bq::QgemvParams gu{};
+        gu.w = static_cast<const uint8_t*>(d->w_gate_up.data);
+        gu.fmt = d->w_gate_up.fmt; gu.n = 2 * I; gu.k = H; gu.swiglu = 1;
+        gu.seg_expert = w.seg_expert; gu.seg_start = w.seg_start; gu.seg_count = w.seg_count;
+        gu.n_segments = w.n_segments; gu.src_row = w.perm_token; gu.x = xh; gu.h = w.h;
+        bq::stage_begin(BQ_STAGE_GATE_UP, st);
+        bq::launch_qgemv(gu, max_segments, st);
+        bq::stage_end(BQ_STAGE_GATE_UP, st);
+
+        bq::QgemvParams dn = gu;
+        dn.w = static_cast<const uint8_t*>(d->w_down.data);
+        dn.fmt = d->w_down.fmt; dn.n = H; dn.k = I; dn.swiglu = 0;
+        dn.src_row = nullptr; dn.x = w.h; dn.h = nullptr; dn.y = w.y_slot; dn.ldy = H; dn.row_scale = w.perm_gate;
+        bq::stage_begin(BQ_STAGE_DOWN, st);
+        bq::launch_qgemv(dn, max_segments, st);
+        bq::stage_end(BQ_STAGE_DOWN, st);
+    } else {
+        if ((s = bq::launch_gemm_moe(d, xh, w.perm_token, w.perm_gate, w.seg_expert, w.seg_start, w.seg_count,
+                                     w.n_segments, w.counts, w.h, w.y_slot, base + w.bytes, st)) != BQ_OK)
+            return s;
+    }
+
+    int accumulate = 0;
+    if (d->shared_gate_up) {
+        const int Is = d->shared_gate_up->n / 2;
+        bq::stage_begin(BQ_STAGE_SHARED, st);
+        if (T <= 8 || !bq::gemm_supported(d->shared_gate_up->fmt)) {
+            bq::launch_qgemv(dense_params(d->shared_gate_up, T, xh, nullptr, w.h_shared, 0), 1, st);
+            bq::launch_qgemv(dense_params(d->shared_down, T, w.h_shared, y, nullptr, H), 1, st);
+        } else {
+            if ((s = bq::launch_gemm_shared(d->shared_gate_up, d->shared_down, T, xh, w.h_shared, y, Is,
+                                            base + w.bytes, st)) != BQ_OK)
+                return s;
+        }
+        bq::stage_end(BQ_STAGE_SHARED, st);
+        accumulate = 1;
+    }
+    const int64_t total = (int64_t)T * (H / 4);
+    const int grid = (int)std::min<int64_t>((total + 255) / 256, 152 * 8);
+    bq::stage_begin(BQ_STAGE_COMBINE, st);
+    combine_kernel<<<grid, 256, 0, st>>>(w.y_slot, w.inv, T, k, H, accumulate, y);
+    bq::note_launch();
+    bq::stage_end(BQ_STAGE_COMBINE, st);
+    (void)P;
+    return bq::check_launch("bq_moe_gather_qmm");
+}

@@ -1,0 +1,42 @@
+// Internal launchers shared between the MoE orchestration and the stage
+// entry points.
+#pragma once
+
+#include "bq_internal.cuh"
+
+namespace bq {
+
+// ---- routing / permute (route.cu)
+bq_status validate_route(const char* name, int T, int E, int k);
+void launch_route(const float* logits, const float* bias, int T, int E, int k, int32_t* ids,
+                  float* weights, cudaStream_t st);
+size_t permute_scratch_bytes(int P, int E);
+void launch_permute(const int32_t* ids, const float* gate, int T, int k, int E, int32_t* counts,
+                    int32_t* offsets, int32_t* perm_token, int32_t* perm_slot, float* perm_gate,
+                    int32_t* inv, int32_t* scratch, cudaStream_t st);
+
+// ---- grouped qgemv (qgemv.cu)
+//
+// A segment is a run of consecutive rows [start, start + count) of the
+// activation list that all multiply matrix `expert`.  Segments come either
+// from device arrays (seg_expert / seg_start / seg_count with a device
+// count n_segments) or, when those are NULL, a single segment
+// (expert 0, start 0, count m).
+struct QgemvParams {
+    const uint8_t* w;        // weight slabs
+    int fmt, n, k, swiglu;   // weight geometry (n = rows per matrix)
+    const int32_t* seg_expert;
+    const int32_t* seg_start;
+    const int32_t* seg_count;
+    const int32_t* n_segments;
+    int m;                   // single-segment row count (when seg arrays are NULL)
+    const int32_t* src_row;  // activation row of list row r (NULL: r itself)
+    const __half* x;         // activations [*][k]
+    float* y;                // fp32 output [rows][ldy] (swiglu = 0)
+    __half* h;               // fp16 SwiGLU output [rows][n/2] (swiglu = 1)
+    int ldy;                 // leading dimension of y (elements)
+    const float* row_scale;  // optional per-list-row scale applied to y
+};
+void launch_qgemv(const QgemvParams& p, int max_segments, cudaStream_t st);
+
+}  // namespace bq

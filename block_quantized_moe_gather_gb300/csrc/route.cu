@@ -1,0 +1,257 @@
+// Router top-k (S5) and the expert histogram / exclusive scan / token
+// permutation (S6, S7).
+//
+// "Everything Bagel 2" (thewafflehaus/butter PR #10): moeRouterTopK takes
+// logits [nExperts] to k u32 indices plus k weights that sum to 1, and the
+// indices stay on the device (no host readback per layer).  "metal: DSV4
+// M1 Ultra prefill/decode campaign" (QuixiAI/SlimServe PR #2): router
+// host contract E <= 1024, top-k <= 8; the qc_moe_mm_map0 work queue
+// feeds the per-expert tiled MoE GEMM.
+//
+// Permute design: pairs f = t*k + j are cut into chunks of 256.  (a) each
+// CTA builds its chunk's expert histogram in shared memory with
+// warp-aggregated atomics (one atomic per group of lanes holding the same
+// expert, found with __match_any_sync); (b) one CTA turns the chunk
+// histograms into per-chunk, per-expert base positions (a scan over chunks
+// for each expert, then an exclusive scan over experts); (c) each pair's
+// position is its chunk base plus the number of earlier pairs of the same
+// expert inside its chunk.  Positions therefore depend only on the ids:
+// the permutation is the stable counting sort, bit-identical run to run.
+#include "bq_internal.cuh"
+#include "moe_internal.cuh"
+
+namespace {
+
+constexpr int kChunk = 256;
+
+template <int NPER>
+__global__ void __launch_bounds__(256)
+route_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
+             int32_t* __restrict__ ids, float* __restrict__ weights) {
+    const int lane = threadIdx.x & 31;
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (t >= T) return;
+    const float* row = logits + (int64_t)t * E;
+    float z[NPER];
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) {
+        const int e = lane + 32 * i;
+        z[i] = 0.f;
+        if (e < E) z[i] = bias ? __fadd_rn(__ldg(row + e), __ldg(bias + e)) : __ldg(row + e);
+    }
+    uint32_t taken = 0;
+    float zsel = 0.f, z0 = 0.f, denom = 0.f;
+    int esel = 0;
+    for (int j = 0; j < k; ++j) {
+        // lane-local best among untaken entries; "none" is e = INT_MAX
+        float bz = 0.f;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < NPER; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !(taken >> i & 1u)) {
+                // e ascends within a lane, so ties keep the lower id; a NaN loses to any number
+                const bool better = be == 0x7fffffff || z[i] > bz || (!(bz == bz) && z[i] == z[i]);
+                if (better) { bz = z[i]; be = e; }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float oz = __shfl_xor_sync(0xffffffffu, bz, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+            const bool take = oe != 0x7fffffff &&
+                              (be == 0x7fffffff || oz > bz || (oz == bz && oe < be) ||
+                               (!(bz == bz) && oz == oz));
+            if (take) { bz = oz; be = oe; }
+        }
+        if ((be & 31) == lane && be != 0x7fffffff) taken |= 1u << (be >> 5);
+        if (j == 0) z0 = bz;
+        const float ex = expf(bz - z0);
+        denom += ex;
+        if (lane == j) { zsel = ex; esel = be; }
+    }
+    if (lane < k) {
+        ids[(int64_t)t * k + lane] = esel;
+        weights[(int64_t)t * k + lane] = zsel / denom;
+    }
+}
+
+__global__ void __launch_bounds__(kChunk)
+chunk_hist_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ chunk_hist,
+                  int32_t* status) {
+    extern __shared__ int32_t hist[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const int f = blockIdx.x * kChunk + threadIdx.x;
+    int e = -1;
+    if (f < P) {
+        e = __ldg(ids + f);
+        if (e < 0 || e >= E) {
+            bq::set_device_error(status, BQ_DEV_BAD_EXPERT_ID);
+            e = -1;
+        }
+    }
+    const uint32_t valid = __ballot_sync(0xffffffffu, e >= 0);
+    if (e >= 0) {
+        const uint32_t grp = __match_any_sync(valid, e);
+        if ((threadIdx.x & 31) == __ffs(grp) - 1) atomicAdd(&hist[e], __popc(grp));
+    }
+    __syncthreads();
+    int32_t* out = chunk_hist + (int64_t)blockIdx.x * E;
+    for (int x = threadIdx.x; x < E; x += blockDim.x) out[x] = hist[x];
+}
+
+// One CTA of 1024 threads, E <= 1024: chunk_hist[c][e] becomes the first
+// output position of expert e's pairs from chunk c.
+__global__ void __launch_bounds__(1024)
+scan_kernel(int32_t* __restrict__ chunk_hist, int n_chunks, int E, int32_t* __restrict__ counts,
+            int32_t* __restrict__ offsets) {
+    __shared__ int32_t warp_sums[32];
+    const int e = threadIdx.x;
+    int32_t total = 0;
+    if (e < E) {
+        for (int c = 0; c < n_chunks; ++c) {
+            int32_t* p = chunk_hist + (int64_t)c * E + e;
+            const int32_t v = *p;
+            *p = total;
+            total += v;
+        }
+        counts[e] = total;
+    }
+    // block exclusive scan of `total` over e
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t incl = total;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t s = warp_sums[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, s, off);
+            if (lane >= off) s += v;
+        }
+        warp_sums[lane] = s;  // inclusive
+    }
+    __syncthreads();
+    const int32_t excl = incl - total + (warp ? warp_sums[warp - 1] : 0);
+    if (e < E) {
+        offsets[e] = excl;
+        if (e == E - 1) offsets[E] = excl + total;
+        for (int c = 0; c < n_chunks; ++c) chunk_hist[(int64_t)c * E + e] += excl;
+    }
+}
+
+__global__ void __launch_bounds__(kChunk)
+place_kernel(const int32_t* __restrict__ ids, const float* __restrict__ gate, int P, int k, int E,
+             const int32_t* __restrict__ chunk_base, int32_t* __restrict__ perm_token,
+             int32_t* __restrict__ perm_slot, float* __restrict__ perm_gate, int32_t* __restrict__ inv) {
+    __shared__ int32_t sid[kChunk];
+    const int f0 = blockIdx.x * kChunk;
+    const int f = f0 + threadIdx.x;
+    int e = -1;
+    if (f < P) {
+        e = __ldg(ids + f);
+        if (e < 0 || e >= E) e = -1;
+    }
+    sid[threadIdx.x] = e;
+    __syncthreads();
+    if (f >= P) return;
+    if (e < 0) {
+        inv[f] = -1;
+        return;
+    }
+    int rank = 0;
+    for (int i = 0; i < (int)threadIdx.x; ++i) rank += sid[i] == e;
+    const int r = __ldg(chunk_base + (int64_t)blockIdx.x * E + e) + rank;
+    perm_token[r] = f / k;
+    perm_slot[r] = f % k;
+    if (perm_gate) perm_gate[r] = __ldg(gate + f);
+    inv[f] = r;
+}
+
+}  // namespace
+
+namespace bq {
+
+bq_status validate_route(const char* name, int T, int E, int k) {
+    if (T < 0) return fail(BQ_ERR_SHAPE, "%s: T = %d < 0", name, T);
+    if (E < 1 || E > 1024) return fail(BQ_ERR_SHAPE, "%s: E = %d outside [1, 1024]", name, E);
+    if (k < 1 || k > 8 || k > E) return fail(BQ_ERR_SHAPE, "%s: k = %d outside [1, min(8, E)]", name, k);
+    return BQ_OK;
+}
+
+void launch_route(const float* logits, const float* bias, int T, int E, int k, int32_t* ids,
+                  float* weights, cudaStream_t st) {
+    if (T == 0) return;
+    note_launch();
+    const int grid = (T + 7) / 8;
+    if (E <= 32) route_kernel<1><<<grid, 256, 0, st>>>(logits, bias, T, E, k, ids, weights);
+    else if (E <= 64) route_kernel<2><<<grid, 256, 0, st>>>(logits, bias, T, E, k, ids, weights);
+    else if (E <= 128) route_kernel<4><<<grid, 256, 0, st>>>(logits, bias, T, E, k, ids, weights);
+    else if (E <= 256) route_kernel<8><<<grid, 256, 0, st>>>(logits, bias, T, E, k, ids, weights);
+    else if (E <= 512) route_kernel<16><<<grid, 256, 0, st>>>(logits, bias, T, E, k, ids, weights);
+    else route_kernel<32><<<grid, 256, 0, st>>>(logits, bias, T, E, k, ids, weights);
+}
+
+size_t permute_scratch_bytes(int P, int E) {
+    const size_t n_chunks = (size_t)(P + kChunk - 1) / kChunk;
+    return ((n_chunks * E * sizeof(int32_t)) + 255) & ~(size_t)255;
+}
+
+void launch_permute(const int32_t* ids, const float* gate, int T, int k, int E, int32_t* counts,
+                    int32_t* offsets, int32_t* perm_token, int32_t* perm_slot, float* perm_gate,
+                    int32_t* inv, int32_t* scratch, cudaStream_t st) {
+    const int P = T * k;
+    const int n_chunks = (P + kChunk - 1) / kChunk;
+    note_launch(n_chunks > 0 ? 3 : 1);
+    if (n_chunks > 0)
+        chunk_hist_kernel<<<n_chunks, kChunk, E * sizeof(int32_t), st>>>(ids, P, E, scratch,
+                                                                        device_status_ptr());
+    scan_kernel<<<1, 1024, 0, st>>>(scratch, n_chunks, E, counts, offsets);
+    if (n_chunks > 0)
+        place_kernel<<<n_chunks, kChunk, 0, st>>>(ids, gate, P, k, E, scratch, perm_token, perm_slot,
+                                                 perm_gate, inv);
+}
+
+}  // namespace bq
+
+extern "C" bq_status bq_moe_route(const float* logits, const float* bias, int32_t T, int32_t E,
+                                  int32_t k, int32_t* ids, float* weights, bq_stream_t stream) {
+    bq_status s = bq::validate_route("bq_moe_route", T, E, k);
+    if (s != BQ_OK || T == 0) return s;
+    if (!logits || !ids || !weights) return bq::fail(BQ_ERR_NULL, "bq_moe_route: NULL pointer");
+    if (!bq::aligned(logits, 4) || !bq::aligned(ids, 4) || !bq::aligned(weights, 4) ||
+        (bias && !bq::aligned(bias, 4)))
+        return bq::fail(BQ_ERR_ALIGN, "bq_moe_route: pointers must be 4-byte aligned");
+    if ((s = bq::check_arch()) != BQ_OK) return s;
+    bq::launch_route(logits, bias, T, E, k, ids, weights, (cudaStream_t)stream);
+    return bq::check_launch("bq_moe_route");
+}
+
+extern "C" size_t bq_moe_permute_workspace_bytes(int32_t T, int32_t k, int32_t E) {
+    if (T < 0 || k < 1 || k > 8 || E < 1 || E > 1024) return 0;
+    return bq::permute_scratch_bytes(T * k, E);
+}
+
+extern "C" bq_status bq_moe_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t* counts,
+                                    int32_t* offsets, int32_t* perm_token, int32_t* perm_slot,
+                                    int32_t* inv, void* workspace, size_t workspace_bytes,
+                                    bq_stream_t stream) {
+    bq_status s = bq::validate_route("bq_moe_permute", T, E, k);
+    if (s != BQ_OK) return s;
+    if (!counts || !offsets || (T > 0 && (!ids || !perm_token || !perm_slot || !inv)))
+        return bq::fail(BQ_ERR_NULL, "bq_moe_permute: NULL pointer");
+    const size_t need = bq::permute_scratch_bytes(T * k, E);
+    if (!workspace || workspace_bytes < need)
+        return bq::fail(BQ_ERR_WORKSPACE, "bq_moe_permute: workspace %zu bytes < %zu", workspace_bytes, need);
+    if (!bq::aligned(workspace, 16)) return bq::fail(BQ_ERR_ALIGN, "bq_moe_permute: workspace alignment");
+    if ((s = bq::check_arch()) != BQ_OK) return s;
+    bq::launch_permute(ids, nullptr, T, k, E, counts, offsets, perm_token, perm_slot, nullptr, inv,
+                       static_cast<int32_t*>(workspace), (cudaStream_t)stream);
+    return bq::check_launch("bq_moe_permute");
+}

@@ -1,0 +1,268 @@
+/*
+ * bq.h -- C ABI of the block-quantized MoE gather-qmm library for GB300
+ * (sm_103a).  Plain pointers and sizes only; no C++ or framework types.
+ *
+ * Pages cited below (titles as they appear on each page):
+ *   [iron]      "feat(gguf,dsv4): GGUF block-dequant + DSv4 kernel surface (WIP)",
+ *               thewafflehaus/iron PR #9
+ *   [butter]    "Everything Bagel 2", thewafflehaus/butter PR #10
+ *   [slimserve] "metal: DSV4 M1 Ultra prefill/decode campaign", QuixiAI/SlimServe PR #2
+ *   [vllm]      "WIP: metaltile shim -- Qwen3.6 mt_qmm_mma / mt_moe_gather dispatch",
+ *               TheTom/vllm-swift PR #22
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - Pointers marked "device" must point to device memory the caller
+ *    allocated and owns; the library never allocates or frees in these
+ *    calls and keeps no pointer after a call returns.  Caller-owned
+ *    scratch ("workspace") lets a loop reuse one buffer ([butter], the
+ *    two-pass decode note: scratch buffers are caller-owned so a decode
+ *    loop can amortise them).
+ *  - Every call is asynchronous on `stream` (NULL = the legacy default
+ *    stream) and does no host synchronisation, except bq_device_status.
+ *    Inputs must stay valid until the stream reaches the call.
+ *  - Preconditions are checked on the host before any launch ([butter]:
+ *    wrapper preconditions with a clear message; [slimserve]: host-checked
+ *    TORCH_CHECK contracts).  A failing check returns a status != BQ_OK
+ *    and launches nothing; bq_last_error() then holds a message.
+ *  - Errors found on the device (an expert id out of range, a bounded
+ *    wait that ran out) never trap: the kernel records a code in a
+ *    per-device status word and skips the bad element.  Read and clear it
+ *    with bq_device_status().
+ *  - Pointers must be 16-byte aligned unless stated otherwise.
+ */
+#ifndef BQ_H
+#define BQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st* bq_stream_t;
+
+typedef enum {
+    BQ_OK = 0,
+    BQ_ERR_NULL = 1,       /* a required pointer is NULL                     */
+    BQ_ERR_SHAPE = 2,      /* a size is out of range or not divisible        */
+    BQ_ERR_ALIGN = 3,      /* a pointer is not aligned as required           */
+    BQ_ERR_FORMAT = 4,     /* unknown or mismatched weight format            */
+    BQ_ERR_WORKSPACE = 5,  /* workspace pointer NULL or too small            */
+    BQ_ERR_CUDA = 6,       /* a CUDA runtime call or launch failed           */
+    BQ_ERR_DEVICE = 7,     /* the device status word was set (see below)     */
+    BQ_ERR_ARCH = 8        /* current device is not a compute-capability 10.3 GPU */
+} bq_status;
+
+/* Codes written to the device status word. */
+enum {
+    BQ_DEV_OK = 0,
+    BQ_DEV_BAD_EXPERT_ID = 1,   /* a routed expert id was outside [0, E)        */
+    BQ_DEV_WAIT_TIMEOUT = 2     /* a bounded mbarrier / flag wait ran out       */
+};
+
+typedef enum {
+    BQ_FMT_Q8_0 = 1,      /* GGUF Q8_0: 32-value blocks, fp16 d + 32 int8 ([iron] kernel 1) */
+    BQ_FMT_Q2_K = 2,      /* GGUF Q2_K: 256-value super-blocks of 84 bytes ([iron] kernel 2) */
+    BQ_FMT_INT4_G64 = 3   /* MLX int4 affine, 8 codes per u32, fp16 scale+bias per 64 ([butter]) */
+} bq_format;
+
+/*
+ * A quantised weight resident on the device in the library's tile-major
+ * layout (built by bq_repack_*).  The matrix stack is [n_mats][n][k]:
+ * n_mats experts (1 for a dense weight), n output rows, k input columns;
+ * row r of matrix e computes output feature r.  `data` is one device
+ * buffer of bq_qweight_bytes() bytes, 256-byte aligned, owned by the
+ * caller.  swiglu = 1 marks a fused gate/up weight (rows [0, n/2) gate,
+ * [n/2, n) up) stored in the interleaved order the SwiGLU epilogue reads.
+ *
+ * Layout (informative): for each matrix, 128-row tile and K-slab, one
+ * contiguous slab of bytes holding 64 quant bytes per row followed by the
+ * slab's scale fields.  K-slab width: Q8_0 64, Q2_K 256, int4 128 values.
+ * Bytes per weight equal the on-disk format's (34/32, 84/256, 9/16).
+ */
+typedef struct {
+    int32_t fmt;      /* bq_format */
+    int32_t n_mats;
+    int32_t n;        /* multiple of 128 */
+    int32_t k;        /* multiple of 256 (Q2_K), 128 (int4) or 64 (Q8_0) */
+    int32_t swiglu;   /* 0 or 1 */
+    int32_t reserved;
+    void* data;       /* device */
+} bq_qweight;
+
+/* Human-readable name of a status code (static storage). */
+const char* bq_status_string(bq_status s);
+
+/* Message of the last failing call on this host thread ("" if none). */
+const char* bq_last_error(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word.  *code receives BQ_DEV_OK or the first device error code recorded
+ * since the last read.  Returns BQ_ERR_DEVICE if a code was set.
+ */
+bq_status bq_device_status(bq_stream_t stream, int32_t* code);
+
+/* ------------------------------------------------------------------ S1, S2
+ * Standalone GGUF block dequantisation to fp32 ([iron] kernels 1 and 2).
+ *   Q8_0: out[32b + i] = sext8(qs[i]) * d,  sext8(u) = u >= 128 ? u - 256 : u
+ *   Q2_K: for value v of super-block b, sub-block j = v/16:
+ *         out[256b + v] = (d * sc_j) * q_v - dmin * m_j,
+ *         sc_j = scales[j] & 15, m_j = scales[j] >> 4,
+ *         q_v = (qs[32*(v/128) + v%32] >> 2*((v/32)%4)) & 3
+ * blocks: device, n_blocks on-disk blocks back to back (34 or 84 bytes
+ *         each; Q8_0: d then qs; Q2_K: scales[16], qs[64], d, dmin).
+ * out:    device fp32 [n_blocks * 32] or [n_blocks * 256].
+ * Every product and difference is evaluated in fp32 round-to-nearest with
+ * no contraction, in the order written above.
+ * Errors: BQ_ERR_NULL, BQ_ERR_SHAPE (n_blocks < 0), BQ_ERR_ALIGN, BQ_ERR_CUDA.
+ * n_blocks == 0 is a no-op.
+ */
+bq_status bq_gguf_dequant_q8_0(const void* blocks, int64_t n_blocks, float* out,
+                               bq_stream_t stream);
+bq_status bq_gguf_dequant_q2_k(const void* blocks, int64_t n_blocks, float* out,
+                               bq_stream_t stream);
+
+/* ------------------------------------------------------------------ S0
+ * Load-time repack of on-disk blocks into the device layout ([iron]:
+ * CPU-side decomposition of each block into separate GPU tensors;
+ * [slimserve]: load-time q2_K SoA repack).  Runs on the device.
+ * bq_qweight_bytes: bytes `data` must hold (0 if the shape is invalid).
+ * Sources (device):
+ *   Q8_0: blocks [n_mats][n][k/32] x 34 bytes
+ *   Q2_K: blocks [n_mats][n][k/256] x 84 bytes
+ *   int4: words [n_mats][n][k/8] u32 (value 8w+i in bits 4i..4i+3),
+ *         scales and biases [n_mats][n][k/64] fp16 (passed as uint16 bits)
+ * dst->fmt/n_mats/n/k/swiglu/data must be filled in by the caller.
+ * Errors: BQ_ERR_NULL, BQ_ERR_FORMAT, BQ_ERR_SHAPE, BQ_ERR_ALIGN, BQ_ERR_CUDA.
+ */
+size_t bq_qweight_bytes(int32_t fmt, int32_t n_mats, int32_t n, int32_t k);
+bq_status bq_repack_q8_0(const void* blocks, const bq_qweight* dst, bq_stream_t stream);
+bq_status bq_repack_q2_k(const void* blocks, const bq_qweight* dst, bq_stream_t stream);
+bq_status bq_repack_int4(const uint32_t* words, const uint16_t* scales,
+                         const uint16_t* biases, const bq_qweight* dst,
+                         bq_stream_t stream);
+
+/* ------------------------------------------------------------------ S3, S4
+ * Dense qmm: Y[m][r] = sum_k X[m][k] * W[r][k] with W the dequantised
+ * weight (matrix 0 of w, swiglu must be 0), fp32 accumulation
+ * ([vllm]: mt_qmm_mma, dense activations x 4-bit weights; [butter]:
+ * dequantGemmDynamicM; [slimserve]: qc_mmvq batch 2-8 qgemv and the q8_0
+ * qgemm).  Weights are dequantised in registers to fp16; products are
+ * accumulated in fp32.  m <= 8 runs the split-K qgemv; larger m the
+ * tensor-core (tcgen05) GEMM.
+ * x: device fp16 [m][k] row-major (uint16 bits), k = w->k.
+ * y: device fp32 [m][w->n] row-major.
+ * Errors: BQ_ERR_NULL, BQ_ERR_SHAPE (m < 0), BQ_ERR_FORMAT, BQ_ERR_ALIGN,
+ * BQ_ERR_CUDA.  m == 0 is a no-op.
+ */
+bq_status bq_qmm(const uint16_t* x, int32_t m, const bq_qweight* w, float* y,
+                 bq_stream_t stream);
+
+/* ------------------------------------------------------------------ S5
+ * Router top-k ([butter]: moeRouterTopK, logits -> top-k u32 indices and
+ * weights summing to 1; [slimserve]: router contract E <= 1024, k <= 8).
+ * z[t][e] = logits[t][e] + bias[e] (fp32; bias may be NULL).  ids[t][j]
+ * = the j-th largest z of row t (ties: lower e first); weights[t][j] =
+ * exp(z_j - z_0) / sum_i exp(z_i - z_0) over the k selected (fp32).
+ * logits: device fp32 [T][E]; bias: device fp32 [E] or NULL;
+ * ids: device int32 [T][k]; weights: device fp32 [T][k].
+ * Errors: BQ_ERR_NULL, BQ_ERR_SHAPE (T < 0, E < 1 or > 1024, k < 1 or
+ * > min(8, E)), BQ_ERR_ALIGN (4-byte alignment suffices here), BQ_ERR_CUDA.
+ */
+bq_status bq_moe_route(const float* logits, const float* bias, int32_t T, int32_t E,
+                       int32_t k, int32_t* ids, float* weights, bq_stream_t stream);
+
+/* ------------------------------------------------------------------ S6, S7
+ * Expert histogram, exclusive scan and deterministic token permutation
+ * (the per-expert work queue of [slimserve] qc_moe_mm_map0 and the
+ * gathered layout of [vllm] mt_moe_gather_qmm).  With f = t*k + j:
+ *   counts[e]      = #{f : ids[f] == e}
+ *   offsets[e]     = sum_{e' < e} counts[e'],  offsets[E] = T*k
+ *   perm[r]        = the f listed by (ids[f], f) ascending
+ *   perm_token[r]  = perm[r] / k,  perm_slot[r] = perm[r] % k,  inv[perm[r]] = r
+ * ids: device int32 [T*k]; counts: device int32 [E]; offsets [E+1];
+ * perm_token, perm_slot, inv: device int32 [T*k].  workspace: device,
+ * >= bq_moe_permute_workspace_bytes(T, k, E) bytes.
+ * Out-of-range ids set BQ_DEV_BAD_EXPERT_ID on the device and are
+ * excluded from every output (their perm entries are not written).
+ * Errors: BQ_ERR_NULL, BQ_ERR_SHAPE, BQ_ERR_WORKSPACE, BQ_ERR_ALIGN, BQ_ERR_CUDA.
+ */
+size_t bq_moe_permute_workspace_bytes(int32_t T, int32_t k, int32_t E);
+bq_status bq_moe_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E,
+                         int32_t* counts, int32_t* offsets, int32_t* perm_token,
+                         int32_t* perm_slot, int32_t* inv, void* workspace,
+                         size_t workspace_bytes, bq_stream_t stream);
+
+/* ------------------------------------------------------------------ S5..S13
+ * One MoE layer: route -> permute -> grouped gate/up GEMM with SwiGLU ->
+ * grouped down GEMM scaled by the gate weight -> combine, plus an
+ * optional always-on shared expert added with weight 1.
+ *   y[t] = sum_j g[t][j] * W_d[e_tj] (silu(W_g[e_tj] x_t) * (W_u[e_tj] x_t))
+ *          (+ W_ds (silu(W_gs x_t) * (W_us x_t)))
+ * ([vllm]: mt_moe_gather_qmm_mma_int4_bm{16,64}; [slimserve]: tiled MoE
+ * prefill GEMM and sum-folded q2_K down projection; [butter]: GPU router,
+ * expert-indexed gemv with no host readback, swiglu, scalarFMA combine.)
+ * Token counts up to 8 take the decode path (gather-qgemv); larger ones
+ * the tensor-core grouped GEMM.  Intermediates: gathered activations and
+ * the SwiGLU output are fp16, expert outputs fp32.
+ *
+ * desc: host struct.  w_gate_up: n_mats = E, n = 2*inter, k = hidden,
+ *   swiglu = 1.  w_down: n_mats = E, n = hidden, k = inter, swiglu = 0.
+ *   shared_gate_up / shared_down: NULL, or dense weights (n_mats = 1) of
+ *   the shared expert, with its own intermediate size.
+ * x: device fp16 [T][hidden]; router_logits: device fp32 [T][E];
+ * logit_bias: device fp32 [E] or NULL (added before selection and
+ * weighting); y: device fp32 [T][hidden].
+ * workspace: device, >= bq_moe_workspace_bytes(desc) bytes, 256-aligned.
+ * Errors: as above, plus BQ_ERR_FORMAT if the weights' shapes disagree
+ * with the descriptor.
+ */
+typedef struct {
+    int32_t T;
+    int32_t hidden;
+    int32_t inter;
+    int32_t n_experts;   /* E, 1..1024 */
+    int32_t topk;        /* 1..min(8, E) */
+    int32_t reserved;
+    bq_qweight w_gate_up;
+    bq_qweight w_down;
+    const bq_qweight* shared_gate_up;  /* host pointer or NULL */
+    const bq_qweight* shared_down;     /* host pointer or NULL */
+} bq_moe_desc;
+
+size_t bq_moe_workspace_bytes(const bq_moe_desc* desc);
+bq_status bq_moe_gather_qmm(const bq_moe_desc* desc, const uint16_t* x,
+                            const float* router_logits, const float* logit_bias,
+                            float* y, void* workspace, size_t workspace_bytes,
+                            bq_stream_t stream);
+
+/* ------------------------------------------------------------------ observability
+ * Stage timing: while set, every bq_moe_gather_qmm call on this host thread
+ * records `start` (a cudaEvent_t) on its stream immediately before the
+ * kernels of `stage` and `stop` immediately after them.  Passing NULL
+ * events clears the stage.  Events are owned by the caller.  This exists so
+ * that a benchmark can time one stage of a layer call with CUDA events on
+ * the stream the stage runs on; it adds two event records per stage.
+ * Errors: BQ_ERR_SHAPE (unknown stage).
+ */
+typedef enum {
+    BQ_STAGE_ROUTE_PERMUTE = 0,  /* route, histogram, scan, placement, segment list */
+    BQ_STAGE_GATE_UP = 1,        /* routed gate/up GEMM with SwiGLU (+ activation gather) */
+    BQ_STAGE_DOWN = 2,           /* routed down GEMM scaled by the gate weight */
+    BQ_STAGE_SHARED = 3,         /* shared expert (gate/up + down) */
+    BQ_STAGE_COMBINE = 4,        /* gate-weighted combine */
+    BQ_STAGE_COUNT = 5
+} bq_stage;
+bq_status bq_set_stage_events(int32_t stage, void* start_event, void* stop_event);
+
+/* Number of kernels this library has launched in this process (all threads). */
+uint64_t bq_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BQ_H */

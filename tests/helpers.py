@@ -1,0 +1,125 @@
+"""Shared helpers for the parity tests: upload seeded inputs, build device
+weights through the C ABI, dequantise with the oracle, compare."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle as O
+import synth
+
+# Float tolerance for fp32-accumulated matmuls against the fp64 oracle on the
+# same dequantised weights: relative Frobenius error and max abs error
+# relative to the reference RMS.
+REL_FROB = 2e-3
+MAX_ABS_RMS = 1e-2
+
+
+def assert_close_matmul(got, ref, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    diff = got - ref
+    nref = np.linalg.norm(ref)
+    rel = np.linalg.norm(diff) / max(nref, 1e-300)
+    rms = nref / np.sqrt(max(ref.size, 1))
+    mx = np.abs(diff).max() if diff.size else 0.0
+    assert rel <= REL_FROB, f"{what}: relative Frobenius error {rel:.3e} > {REL_FROB}"
+    assert mx <= MAX_ABS_RMS * rms, f"{what}: max abs error {mx:.3e} > {MAX_ABS_RMS} * rms {rms:.3e}"
+    return rel, mx / max(rms, 1e-300)
+
+
+def dev(a, torch_dtype=None):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if torch_dtype is not None:
+        t = t.view(torch_dtype)
+    return t.cuda()
+
+
+def half_dev(a):
+    import torch
+    return dev(np.ascontiguousarray(a, dtype=np.float16).view(np.uint16), None).view(torch.float16)
+
+
+def make_qweight(bq, fmt: str, w, n_mats: int, n: int, k: int, swiglu: bool = False):
+    """Upload on-disk weights and repack them through the C ABI."""
+    import torch
+    qw = bq.QWeight(bq.FMT_BY_NAME[fmt], n_mats, n, k, swiglu)
+    if fmt == "q8_0":
+        bq.repack_q8_0(dev(np.asarray(w).reshape(-1)), qw)
+    elif fmt == "q2_k":
+        bq.repack_q2_k(dev(np.asarray(w).reshape(-1)), qw)
+    else:
+        bq.repack_int4(dev(w.words.reshape(-1).view(np.int32)),
+                       dev(w.scales.reshape(-1).view(np.int16)),
+                       dev(w.biases.reshape(-1).view(np.int16)), qw)
+    torch.cuda.synchronize()
+    return qw
+
+
+def dequant(fmt: str, w):
+    """Oracle dequantisation of an on-disk weight to fp64 [..., n, k]."""
+    if fmt == "q8_0":
+        return O.dequant_q8_0(np.asarray(w))
+    if fmt == "q2_k":
+        return O.dequant_q2_k(np.asarray(w))
+    return O.dequant_int4(w.words, w.scales, w.biases)
+
+
+def expert_slice(fmt: str, w, e: int):
+    if fmt == "int4":
+        return synth.Int4Weight(w.words[e], w.scales[e], w.biases[e])
+    return w[e]
+
+
+def build_layer(bq, inp: synth.MoEInputs):
+    """Device weights + descriptor for a MoE case."""
+    c = inp.case
+    gu = make_qweight(bq, c.fmt, inp.w_gu, c.experts, 2 * c.inter, c.hidden, swiglu=True)
+    dn = make_qweight(bq, c.fmt, inp.w_d, c.experts, c.hidden, c.inter)
+    s_gu = s_d = None
+    if inp.shared_gu is not None:
+        s_gu = make_qweight(bq, "q8_0", inp.shared_gu, 1, 2 * c.inter, c.hidden, swiglu=True)
+        s_d = make_qweight(bq, "q8_0", inp.shared_d, 1, c.hidden, c.inter)
+    return bq.MoELayer(c.t, c.hidden, c.inter, c.experts, c.topk, gu, dn, s_gu, s_d)
+
+
+def run_moe(bq, layer, inp: synth.MoEInputs):
+    import torch
+    c = inp.case
+    x = half_dev(inp.x)
+    logits = dev(inp.logits)
+    bias = dev(inp.bias) if inp.bias is not None else None
+    y = torch.empty((c.t, c.hidden), dtype=torch.float32, device="cuda")
+    ws = torch.empty(layer.workspace_bytes(), dtype=torch.uint8, device="cuda")
+    bq.moe_gather_qmm(layer, x, logits, bias, y, ws)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def oracle_moe(inp: synth.MoEInputs, tokens=None):
+    """fp64 oracle of the MoE layer (optionally on a subset of tokens)."""
+    c = inp.case
+    ids, wts = O.route(inp.logits, c.topk, inp.bias)
+    cache = {}
+
+    def gu(e):
+        key = ("gu", e)
+        if key not in cache:
+            cache[key] = dequant(c.fmt, expert_slice(c.fmt, inp.w_gu, e)).reshape(2 * c.inter, c.hidden)
+        return cache[key]
+
+    def dn(e):
+        key = ("d", e)
+        if key not in cache:
+            cache[key] = dequant(c.fmt, expert_slice(c.fmt, inp.w_d, e)).reshape(c.hidden, c.inter)
+        return cache[key]
+
+    shared = None
+    if inp.shared_gu is not None:
+        shared = (dequant("q8_0", inp.shared_gu).reshape(2 * c.inter, c.hidden),
+                  dequant("q8_0", inp.shared_d).reshape(c.hidden, c.inter))
+    if tokens is None:
+        return O.moe_ffn(inp.x, ids, wts, gu, dn, shared)
+    return O.moe_ffn_tokens(inp.x, ids, wts, tokens, gu, dn, shared)

@@ -1,0 +1,99 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, it
+exports every function include/bq.h declares, host-only queries give the
+expected sizes, and the product package never imports the oracle."""
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bq.h")
+PKG = os.path.join(ROOT, "block_quantized_moe_gather_gb300")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(bq_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def bq():
+    if not os.path.exists(os.path.join(PKG, "libbq.so")):
+        import __graft_entry__
+        __graft_entry__.build()
+    import block_quantized_moe_gather_gb300 as m
+    return m
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for must in ("bq_gguf_dequant_q8_0", "bq_gguf_dequant_q2_k", "bq_qmm", "bq_moe_gather_qmm",
+                 "bq_moe_route", "bq_moe_permute", "bq_repack_q8_0", "bq_repack_q2_k", "bq_repack_int4"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(bq):
+    lib = ctypes.CDLL(bq.LIB_PATH)
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(bq):
+    for code, name in bq.STATUS_NAMES.items():
+        assert bq.status_string(code).startswith(name)
+
+
+def test_qweight_bytes_match_format_density(bq):
+    # bytes per weight equal the on-disk formats: 34/32, 84/256, 9/16
+    assert bq.qweight_bytes(bq.FMT_Q8_0, 1, 256, 2048) == 256 * 2048 * 34 // 32
+    assert bq.qweight_bytes(bq.FMT_Q2_K, 1, 4096, 4096) == 4096 * 4096 * 84 // 256
+    assert bq.qweight_bytes(bq.FMT_INT4_G64, 128, 1536, 2048) == 128 * 1536 * 2048 * 9 // 16
+    assert bq.qweight_bytes(bq.FMT_Q2_K, 1, 100, 4096) == 0      # n not a multiple of 128
+    assert bq.qweight_bytes(bq.FMT_Q2_K, 1, 128, 200) == 0       # k not a multiple of 256
+    assert bq.qweight_bytes(9, 1, 128, 256) == 0                 # unknown format
+
+
+def test_permute_workspace_query(bq):
+    assert bq.moe_permute_workspace_bytes(2048, 8, 128) >= 64 * 128 * 4
+    assert bq.moe_permute_workspace_bytes(1, 9, 16) == 0          # k > 8
+    assert bq.moe_permute_workspace_bytes(1, 2, 2000) == 0        # E > 1024
+
+
+def test_struct_layout_matches_header(bq):
+    assert ctypes.sizeof(bq.QWeightC) == 32
+    assert bq.MoEDescC.w_gate_up.offset == 24
+    assert ctypes.sizeof(bq.MoEDescC) == 24 + 32 + 32 + 16
+
+
+def test_host_validation_rejects_before_launch(bq):
+    # shape checks run before the device is touched, so they work without a GPU
+    lib = bq._lib
+    assert lib.bq_moe_route(None, None, 4, 2000, 2, None, None, None) == 2        # E > 1024
+    assert lib.bq_moe_route(None, None, 4, 16, 9, None, None, None) == 2          # k > 8
+    assert lib.bq_gguf_dequant_q8_0(None, -1, None, None) == 2
+    assert lib.bq_gguf_dequant_q8_0(None, 5, None, None) == 1
+    assert lib.bq_gguf_dequant_q2_k(ctypes.c_void_p(8), 5, ctypes.c_void_p(16), None) == 3   # misaligned
+    assert "aligned" in bq.last_error()
+
+
+def test_product_never_imports_the_oracle():
+    for dirpath, _, files in os.walk(PKG):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "bq_oracle" not in text, f
+
+
+def test_import_fails_loudly_without_the_library(tmp_path):
+    dst = tmp_path / "block_quantized_moe_gather_gb300"
+    shutil.copytree(PKG, dst, ignore=shutil.ignore_patterns("*.so", "_build", "__pycache__"))
+    r = subprocess.run([sys.executable, "-c", "import block_quantized_moe_gather_gb300"], cwd=tmp_path,
+                       capture_output=True, text=True)
+    assert r.returncode != 0 and "ImportError" in r.stderr

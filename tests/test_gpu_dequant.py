@@ -1,0 +1,77 @@
+"""GPU parity: standalone GGUF dequant kernels against the oracle, bit-exact
+(every value in the tested ranges is exactly representable in fp32, so the
+fp64 oracle value cast to fp32 is the only correct fp32 answer)."""
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+from helpers import dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(lib, fmt, blocks):
+    import torch
+    flat = dev(np.ascontiguousarray(blocks).reshape(-1))
+    nb = flat.numel() // (34 if fmt == "q8_0" else 84)
+    out = torch.full((nb * (32 if fmt == "q8_0" else 256),), float("nan"), dtype=torch.float32, device="cuda")
+    (lib.gguf_dequant_q8_0 if fmt == "q8_0" else lib.gguf_dequant_q2_k)(flat, out)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def _exact(got, ref):
+    ref32 = ref.astype(np.float32)
+    assert np.array_equal(ref32.astype(np.float64), ref), "oracle value not fp32-exact"
+    np.testing.assert_array_equal(got.view(np.uint32), ref32.view(np.uint32))
+
+
+@pytest.mark.parametrize("n_blocks", [1, 63, 64, 65, 1000, 4097])
+def test_q8_0_bit_exact_ragged(lib, n_blocks):
+    blocks = synth.q8_0_blocks(synth.rng(100 + n_blocks), n_blocks, 32).reshape(-1, 34)
+    _exact(_run(lib, "q8_0", blocks), O.dequant_q8_0(blocks))
+
+
+@pytest.mark.parametrize("n_blocks", [1, 31, 32, 33, 777])
+def test_q2_k_bit_exact_ragged(lib, n_blocks):
+    blocks = synth.q2_k_blocks(synth.rng(200 + n_blocks), n_blocks, 256).reshape(-1, 84)
+    _exact(_run(lib, "q2_k", blocks), O.dequant_q2_k(blocks))
+
+
+def test_q8_0_every_byte_and_minus_128(lib):
+    blocks = np.zeros((8, 34), dtype=np.uint8)
+    blocks[:, 0:2] = np.array([1.0], dtype=np.float16).view(np.uint8)
+    blocks[:, 2:] = np.arange(256, dtype=np.uint8).reshape(8, 32)
+    got = _run(lib, "q8_0", blocks)
+    np.testing.assert_array_equal(got, np.concatenate([np.arange(128), np.arange(-128, 0)]).astype(np.float32))
+
+
+def test_q2_k_hand_blocks(lib):
+    b = np.zeros((2, 84), dtype=np.uint8)
+    b[0, 0:16] = np.arange(16) | (15 << 4)
+    b[0, 16:80] = 0xFF
+    b[0, 80:82] = np.array([1.0], dtype=np.float16).view(np.uint8)
+    b[1, 0:16] = (np.arange(16) << 4) | 15
+    b[1, 16:80] = 0xFF
+    b[1, 82:84] = np.array([1.0], dtype=np.float16).view(np.uint8)
+    got = _run(lib, "q2_k", b)
+    j = np.arange(256) // 16
+    np.testing.assert_array_equal(got, np.r_[3.0 * j, -1.0 * j].astype(np.float32))
+
+
+def test_dequant_full_size_weights(lib):
+    # the dense workloads' weights: Q8_0 [256, 2048] and Q2_K [4096, 4096]
+    _, w8 = synth.dense_inputs(synth.DENSE_Q8_0_M32)
+    _exact(_run(lib, "q8_0", w8.reshape(-1, 34)), O.dequant_q8_0(w8.reshape(-1, 34)))
+    case = [c for c in synth.dense_sweep() if c.fmt == "q2_k"][0]
+    _, w2 = synth.dense_inputs(case)
+    _exact(_run(lib, "q2_k", w2.reshape(-1, 84)), O.dequant_q2_k(w2.reshape(-1, 84)))
+
+
+def test_dequant_empty_is_noop(lib):
+    import torch
+    out = torch.zeros(4, device="cuda")
+    lib.gguf_dequant_q8_0(torch.zeros(0, dtype=torch.uint8, device="cuda"), out)
+    torch.cuda.synchronize()
+    assert out.abs().sum().item() == 0

@@ -1,0 +1,112 @@
+"""GPU parity: the full MoE layer (route -> permute -> gate/up + SwiGLU ->
+down x gate -> combine, + shared expert) against the fp64 oracle."""
+import numpy as np
+import pytest
+
+import synth
+from helpers import assert_close_matmul, build_layer, oracle_moe, run_moe
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(name, fmt, t, h, i, e, k, zipf=False, shared=None, seed=7):
+    return synth.MoECase(name, fmt, t, h, i, e, k, zipf, shared, seed)
+
+
+SMALL = [
+    _case("int4_small", "int4", 37, 256, 128, 16, 4),
+    _case("int4_k1", "int4", 19, 256, 128, 8, 1),
+    _case("q2k_zipf_shared", "q2_k", 29, 512, 256, 8, 3, zipf=True, shared="q8_0"),
+    _case("q2k_e1", "q2_k", 21, 256, 256, 1, 1),
+    _case("int4_many_tokens", "int4", 300, 256, 256, 4, 2),
+    _case("q2k_ragged", "q2_k", 131, 256, 256, 12, 6, zipf=True),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: c.name)
+def test_moe_small(lib, case):
+    inp = synth.moe_inputs(case)
+    layer = build_layer(lib, inp)
+    got = run_moe(lib, layer, inp)
+    assert_close_matmul(got, oracle_moe(inp), case.name)
+
+
+@pytest.mark.parametrize("t", [1, 2, 5, 8])
+@pytest.mark.parametrize("base", [_case("dec_int4", "int4", 0, 256, 128, 32, 8),
+                                  _case("dec_q2k", "q2_k", 0, 512, 256, 64, 6, shared="q8_0")],
+                         ids=lambda c: c.name)
+def test_moe_decode_small(lib, base, t):
+    case = synth.dataclasses.replace(base, t=t)
+    inp = synth.moe_inputs(case)
+    layer = build_layer(lib, inp)
+    assert_close_matmul(run_moe(lib, layer, inp), oracle_moe(inp), f"{case.name} t={t}")
+
+
+def test_moe_bit_reproducible(lib):
+    case = SMALL[2]
+    inp = synth.moe_inputs(case)
+    layer = build_layer(lib, inp)
+    a = run_moe(lib, layer, inp)
+    b = run_moe(lib, layer, inp)
+    np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_moe_zero_tokens_is_noop(lib):
+    import torch
+    case = synth.dataclasses.replace(SMALL[0], t=0)
+    inp = synth.moe_inputs(SMALL[0])
+    layer = build_layer(lib, inp)
+    layer.set_tokens(0)
+    y = torch.zeros((1, case.hidden), device="cuda")
+    ws = torch.empty(max(layer.workspace_bytes(), 256), dtype=torch.uint8, device="cuda")
+    lib.moe_gather_qmm(layer, torch.zeros((1, case.hidden), dtype=torch.float16, device="cuda"),
+                       torch.zeros((1, case.experts), device="cuda"), None, y, ws)
+    torch.cuda.synchronize()
+    assert y.abs().sum().item() == 0
+
+
+def test_moe_rejects_small_workspace(lib):
+    import torch
+    inp = synth.moe_inputs(SMALL[0])
+    layer = build_layer(lib, inp)
+    ws = torch.empty(layer.workspace_bytes() - 256, dtype=torch.uint8, device="cuda")
+    y = torch.empty((SMALL[0].t, SMALL[0].hidden), device="cuda")
+    with pytest.raises(lib.BQError, match="WORKSPACE"):
+        lib.moe_gather_qmm(layer, torch.zeros((SMALL[0].t, SMALL[0].hidden), dtype=torch.float16, device="cuda"),
+                           torch.zeros((SMALL[0].t, SMALL[0].experts), device="cuda"), None, y, ws)
+
+
+# ---------------------------------------------------------------- full size
+
+_FULL = {}
+
+
+def _full(lib, base):
+    """Weights (host) and device layer of a full-size case, built once."""
+    if base.name not in _FULL:
+        weights = synth.moe_weights(base)
+        inp = synth.moe_inputs(base, weights)
+        _FULL[base.name] = (weights, build_layer(lib, inp))
+    return _FULL[base.name]
+
+
+@pytest.mark.parametrize("base", [synth.MOE_INT4, synth.MOE_Q2K], ids=lambda c: c.name)
+def test_moe_prefill_full_size_sampled(lib, base):
+    weights, layer = _full(lib, base)
+    inp = synth.moe_inputs(base, weights)
+    layer.set_tokens(base.t)
+    got = run_moe(lib, layer, inp)
+    assert np.all(np.isfinite(got))
+    tokens = synth.rng(99).choice(base.t, 6, replace=False)
+    assert_close_matmul(got[tokens], oracle_moe(inp, tokens), base.name)
+
+
+@pytest.mark.parametrize("batch", [1, 2, 4, 8])
+@pytest.mark.parametrize("base", [synth.MOE_Q2K, synth.MOE_INT4], ids=lambda c: c.name)
+def test_moe_decode_full_shapes(lib, base, batch):
+    weights, layer = _full(lib, base)
+    case = synth.decode_case(base, batch)
+    layer.set_tokens(batch)
+    inp = synth.moe_inputs(case, weights, act_seed=synth.decode_step_seed(batch))
+    inp.bias = None   # decode steps use plain N(0,1) logits
+    assert_close_matmul(run_moe(lib, layer, inp), oracle_moe(inp), case.name)
