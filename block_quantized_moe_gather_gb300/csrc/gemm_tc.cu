@@ -589,7 +589,7 @@ GemmWs carve(const bq_moe_desc* d, uint8_t* base) {
 namespace bq {
 
 bool gemm_supported(int fmt) {
-    return false && (fmt == BQ_FMT_Q8_0 || fmt == BQ_FMT_Q2_K || fmt == BQ_FMT_INT4_G64) && encode_fn() != nullptr;
+    return (fmt == BQ_FMT_Q8_0 || fmt == BQ_FMT_Q2_K || fmt == BQ_FMT_INT4_G64) && encode_fn() != nullptr;
 }
 
 size_t gemm_moe_workspace_bytes(const bq_moe_desc* d) { return carve(d, nullptr).bytes; }
