@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 MAIN = synth.MOE_Q2K
+WORKLOADS = {"q2k": synth.MOE_Q2K, "int4": synth.MOE_INT4}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -42,8 +43,13 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["bq", "reference"], default="bq")
+    ap.add_argument("--workload", choices=["q2k", "int4"], default="q2k",
+                    help="q2k: Q2_K experts + Q8_0 shared (default); int4: int4 experts, E=128, top-8")
     ap.add_argument("--decode-steps", type=int, default=200)
     ap.add_argument("--no-secondary", action="store_true", help="only the main step (faster)")
+    ap.add_argument("--only", choices=["decode", "int4", "dense"], default=None,
+                    help="run one secondary section alone and print it (no main step; for profiling)")
+    ap.add_argument("--dense-case", default=None, help="with --only dense: run just this dense case")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -178,13 +184,23 @@ def build_layer(bq, case, weights):
 
 
 class L2Flush:
+    """Evicts L2 between timed steps: writes a buffer of twice the L2 size,
+    then reads another one, so the timed step starts from a cold L2 that
+    holds no dirty lines (write-backs of a write-only flush would otherwise
+    be charged to the next kernel)."""
+
     def __init__(self):
         import torch
         l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
-        self.buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device="cuda")
+        n = max(2 * l2, 256 << 20)
+        self.wbuf = torch.empty(n, dtype=torch.uint8, device="cuda")
+        self.rbuf = torch.ones(n // 4, dtype=torch.float32, device="cuda")
+        self.sink = torch.empty((), dtype=torch.float32, device="cuda")
 
     def __call__(self):
-        self.buf.zero_()
+        import torch
+        self.wbuf.zero_()
+        torch.sum(self.rbuf, dim=0, out=self.sink)
 
 
 def time_steps(fn, k, flush, stage_events=None):
@@ -220,19 +236,28 @@ def time_steps(fn, k, flush, stage_events=None):
 
 
 # ----------------------------------------------------------------------------- main arm
+def run_only(args, local):
+    import torch
+    import block_quantized_moe_gather_gb300 as bq
+    torch.cuda.set_device(local)
+    pk, _ = peaks()
+    print(json.dumps({"only": args.only, "secondary": run_secondary(args, bq, L2Flush(), pk, (args.only,))}),
+          flush=True)
+
+
 def run_main(args, world, rank, local):
     import torch
     import block_quantized_moe_gather_gb300 as bq
     torch.cuda.set_device(local)
     pk, pk_src = peaks()
-    case = MAIN
+    case = WORKLOADS[args.workload]
     weights = synth.moe_weights(case)
     layer = build_layer(bq, case, weights)
     xh, logits_h = synth.moe_activations(case)
     bias_h = weights[4]
     x = upload(xh.view(np.uint16)).view(torch.float16)
     logits = upload(logits_h)
-    bias = upload(bias_h)
+    bias = upload(bias_h) if bias_h is not None else None
     y = torch.empty((case.t, case.hidden), dtype=torch.float32, device="cuda")
     ws = torch.empty(layer.workspace_bytes(), dtype=torch.uint8, device="cuda")
     flush = L2Flush()
@@ -250,7 +275,7 @@ def run_main(args, world, rank, local):
     torch.cuda.synchronize()
     n0 = bq.launch_count()
     with Clocks(local) as clk:
-        step_ms, stage_ms = time_steps(step, args.steps, flush, stage_events=[1, 2, 3])
+        step_ms, stage_ms = time_steps(step, args.steps, flush, stage_events=[1, 2, 3] if case.shared_fmt else [1, 2])
     n_launch = bq.launch_count() - n0
     torch.cuda.synchronize()
     barrier(world)
@@ -269,7 +294,7 @@ def run_main(args, world, rank, local):
                 "frac": round(achieved_tf / peak_tf, 4), "traffic": None,
                 "peak_source": f"{pk_src} bf16 sustained (fp16 operands, same tensor rate)",
                 "stage_ms": {"gate_up": round(gu_ms, 4), "down": round(statistics.mean(stage_ms[2]), 4),
-                             "shared": round(statistics.mean(stage_ms[3]), 4)}}
+                             "shared": round(statistics.mean(stage_ms[3]), 4) if 3 in stage_ms else None}}
 
     # end to end through the public API with host buffers
     xp = torch.from_numpy(xh.view(np.uint16)).view(torch.float16).pin_memory()
@@ -305,9 +330,9 @@ def run_main(args, world, rank, local):
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
             "config": {"workload": case.name, "tokens": case.t, "hidden": case.hidden, "inter": case.inter,
-                       "experts": case.experts, "topk": case.topk, "expert_format": "Q2_K",
-                       "shared_expert": "Q8_0", "router_bias": "Zipf(1.1)",
-                       "l2": "flushed (2x L2 write) before every timed step; steps timed individually",
+                       "experts": case.experts, "topk": case.topk, "expert_format": case.fmt,
+                       "shared_expert": case.shared_fmt, "router_bias": "Zipf(1.1)" if case.zipf_bias else None,
+                       "l2": "flushed before every timed step (2x L2 write, then 2x L2 read); steps timed individually",
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": int(n_launch), "clocks": clk.summary(), "secondary": secondary,
@@ -315,15 +340,17 @@ def run_main(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def run_secondary(args, bq, flush, pk):
+def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "dense")):
     import torch
     out = {}
     # decode sweep: C4 shapes (primary reading) and C3 shapes
     for base in (synth.MOE_Q2K, synth.MOE_INT4):
+        if "decode" not in sections and not (base.fmt == "int4" and "int4" in sections):
+            continue
         weights = synth.moe_weights(base)
         layer = build_layer(bq, base, weights)
         res = {}
-        for b in (1, 2, 4, 8):
+        for b in ((1, 2, 4, 8) if "decode" in sections else ()):
             case = synth.decode_case(base, b)
             layer.set_tokens(b)
             xs, ls, uniq = [], [], []
@@ -355,8 +382,9 @@ def run_secondary(args, bq, flush, pk):
                             "us_per_step": round(1e3 * statistics.mean(ms), 2),
                             "unique_experts_mean": round(statistics.mean(uniq), 2),
                             "tok_s": round(b * len(ms) / (sum(ms) / 1e3), 1)}
-        out[f"decode_{base.fmt}"] = res
-        if base.fmt == "int4":
+        if res:
+            out[f"decode_{base.fmt}"] = res
+        if base.fmt == "int4" and "int4" in sections:
             layer.set_tokens(base.t)
             xh, lh = synth.moe_activations(base)
             x = upload(xh.view(np.uint16)).view(torch.float16)
@@ -375,9 +403,13 @@ def run_secondary(args, bq, flush, pk):
                                    "gate_up_tflops": round(gu / (statistics.mean(stg[1]) / 1e3) / 1e12, 2)}
         del layer
         torch.cuda.empty_cache()
+    if "dense" not in sections:
+        return out
     # dense qmm and dequant
     dense = {}
     for case in [synth.DENSE_Q8_0_M32] + synth.dense_sweep():
+        if args.dense_case and case.name != args.dense_case:
+            continue
         xh, w = synth.dense_inputs(case)
         q = qweight(bq, case.fmt, w, 1, case.n, case.k)
         x = upload(xh.view(np.uint16)).view(torch.float16)
@@ -491,6 +523,8 @@ def main():
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
+    elif args.only:
+        run_only(args, local)
     else:
         run_main(args, world, rank, local)
     if world > 1:

@@ -11,15 +11,16 @@
 // gathered token rows against int4 expert weights.  Here, for sm_103a:
 //
 // Tile = 128 weight rows (one row tile of the slab layout, MMA M) x up to
-// 128 token rows of one expert segment (MMA N) x all of K, fp32 in TMEM.
-// 192 threads per CTA, two CTAs per SM:
+// 192 token rows of one expert segment (MMA N) x all of K, fp32 in TMEM.
+// A segment of c tokens is cut into ceil(c/192) chunks of near-equal size.
+// 320 threads per CTA, two CTAs per SM:
 //   warp 0     producer: TMA 2D loads of the activation tile (128-byte
 //              swizzle, 32-row boxes) and 1D bulk copies of the raw
 //              quantised slabs into shared-memory rings;
 //   warp 1     owns the TMEM allocation and issues tcgen05.mma (one lane);
-//   warps 2-5  converters: one thread per weight row dequantises its 64
-//              K-values of a stage from the raw slab into 32 fp16 pairs and
-//              writes them to a TMEM A-operand ring with tcgen05.st (the
+//   warps 2-9  converters: two threads per weight row each dequantise 32
+//              K-values of a stage from the raw slab into 16 fp16 pairs and
+//              write them to a TMEM A-operand ring with tcgen05.st (the
 //              MMA reads A from TMEM, so the dequantised weights never touch
 //              shared memory); after the K loop the same warps run the
 //              epilogue (tcgen05.ld -> SwiGLU / gate scale -> global).
@@ -35,19 +36,20 @@
 
 namespace {
 
-constexpr int BN = 128;            // max token rows per tile (MMA N)
+constexpr int BN = 192;            // max token rows per tile (MMA N)
 constexpr int BK = 64;             // K per stage (one 128-byte swizzle row of fp16)
-constexpr int kStagesB = 4;        // activation tiles in shared memory
-constexpr int kStagesA = 4;        // dequantised weight tiles in TMEM
-constexpr int kRawSlabs = 4;       // raw quantised slabs in shared memory
-constexpr int kThreads = 192;
+constexpr int kStagesB = 3;        // activation tiles in shared memory
+constexpr int kStagesA = 2;        // dequantised weight tiles in TMEM
+constexpr int kRawSlabs = 3;       // raw quantised slabs in shared memory
+constexpr int kConvWarps = 8;      // two per TMEM lane quarter, each half a stage
+constexpr int kThreads = 32 * (2 + kConvWarps);
 constexpr int kBoxRows = 32;
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kAccCol = 0;    // accumulator: columns [0, 128)
-constexpr uint32_t kACol = 128;    // A ring: 4 x 32 columns
+constexpr uint32_t kAccCol = 0;    // accumulator: columns [0, 192)
+constexpr uint32_t kACol = 192;    // A ring: 2 x 32 columns
 constexpr int kBStageBytes = BN * 128;
 constexpr int kRawStride = 10752;  // largest slab
-constexpr int kSmemBytes = 1024 + kStagesB * kBStageBytes + kRawSlabs * kRawStride + 256;
+constexpr int kSmemBytes = 1024 + kStagesB * kBStageBytes + kRawSlabs * kRawStride + 512;  // + barriers, TMEM slot
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
 
 template <int FMT> struct G;
@@ -60,7 +62,7 @@ enum { EPI_SWIGLU = 0, EPI_SCALE = 1, EPI_PLAIN = 2 };
 struct GemmArgs {
     const uint8_t* w;
     int n, k;
-    const int2* tiles;            // (segment, chunk) per tile, or NULL: one dense segment
+    const int4* tiles;            // (segment, row offset, rows, -) per tile, or NULL: one dense segment
     const int32_t* n_tiles;       // device count of `tiles`
     int dense_m;
     const int32_t* seg_expert;
@@ -196,25 +198,37 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
                  : "memory");
 }
 
+#define BQ_R16(v) "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), \
+    "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+                 ::"r"(taddr), BQ_R16(v) : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 " BQ_OPS32_OUT ", [%32];" : BQ_W32(v) : "r"(taddr)
                  : "memory");
 }
 
-// ---------------------------------------------------------------- dequantisation of one row x 64 K
-// Output: 32 fp16 pairs, pair i = K values (2i, 2i+1) of the stage.
+// ---------------------------------------------------------------- dequantisation of one row x 32 K
+// Output: 16 fp16 pairs, pair i = K values (32h + 2i, 32h + 2i + 1) of the
+// stage, h = the converter's half.
 template <int FMT>
-__device__ __forceinline__ void dequant_row(const uint8_t* raw, int p, int sub, uint32_t (&out)[32]);
+__device__ __forceinline__ void dequant_half(const uint8_t* raw, int p, int sub, int h, uint32_t (&out)[16]);
 
 template <>
-__device__ __forceinline__ void dequant_row<BQ_FMT_Q8_0>(const uint8_t* raw, int p, int, uint32_t (&out)[32]) {
-    const uint32_t dd = *reinterpret_cast<const uint32_t*>(raw + 8192 + 4 * p);
-    const __half2 d0 = __low2half2(bq::u32_as_h2(dd)), d1 = __high2half2(bq::u32_as_h2(dd));
+__device__ __forceinline__ void dequant_half<BQ_FMT_Q8_0>(const uint8_t* raw, int p, int, int h,
+                                                          uint32_t (&out)[16]) {
+    // half h of the 64-value slab is exactly Q8_0 block h
+    const uint16_t db = *reinterpret_cast<const uint16_t*>(raw + 8192 + 4 * p + 2 * h);
+    const __half d1 = __ushort_as_half(db);
+    const __half2 d = __halves2half2(d1, d1);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const uint4 q = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, c));
+    for (int c = 0; c < 2; ++c) {
+        const uint4 q = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, 2 * h + c));
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-        const __half2 d = c < 2 ? d0 : d1;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
             const uint32_t wx = w[m] ^ 0x80808080u;
@@ -225,15 +239,17 @@ __device__ __forceinline__ void dequant_row<BQ_FMT_Q8_0>(const uint8_t* raw, int
 }
 
 template <>
-__device__ __forceinline__ void dequant_row<BQ_FMT_Q2_K>(const uint8_t* raw, int p, int sub, uint32_t (&out)[32]) {
-    const uint4 q = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, sub));
-    const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(raw + 8192 + 16 * p + 4 * sub);
+__device__ __forceinline__ void dequant_half<BQ_FMT_Q2_K>(const uint8_t* raw, int p, int sub, int h,
+                                                          uint32_t (&out)[16]) {
+    // stage `sub` of the super-block = sub-blocks 4sub..4sub+3; half h = two of them
+    const uint2 q = *reinterpret_cast<const uint2*>(raw + bq::quant_chunk_offset(p, sub) + 8 * h);
+    const uint32_t sc2 = *reinterpret_cast<const uint16_t*>(raw + 8192 + 16 * p + 4 * sub + 2 * h);
     const __half2 dm = bq::u32_as_h2(*reinterpret_cast<const uint32_t*>(raw + 10240 + 4 * p));
     const float d = __low2float(dm), dmin = __high2float(dm);
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    const uint32_t w[2] = {q.x, q.y};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t scb = (sc4 >> (8 * i)) & 0xFFu;
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t scb = (sc2 >> (8 * i)) & 0xFFu;
         const __half ds = __float2half_rn(d * (float)(scb & 15u));
         const __half ndm = __float2half_rn(-dmin * (float)(scb >> 4));
         const __half2 ds2 = __halves2half2(ds, ds), ndm2 = __halves2half2(ndm, ndm);
@@ -244,14 +260,15 @@ __device__ __forceinline__ void dequant_row<BQ_FMT_Q2_K>(const uint8_t* raw, int
 }
 
 template <>
-__device__ __forceinline__ void dequant_row<BQ_FMT_INT4_G64>(const uint8_t* raw, int p, int sub, uint32_t (&out)[32]) {
-    const uint4 q0 = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, 2 * sub));
-    const uint4 q1 = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, 2 * sub + 1));
+__device__ __forceinline__ void dequant_half<BQ_FMT_INT4_G64>(const uint8_t* raw, int p, int sub, int h,
+                                                              uint32_t (&out)[16]) {
+    // stage `sub` = K group `sub` of the 128-value slab; half h = chunk 2sub + h
+    const uint4 q = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, 2 * sub + h));
     const __half2 sb = bq::u32_as_h2(*reinterpret_cast<const uint32_t*>(raw + 8192 + 8 * p + 4 * sub));
     const __half2 s2 = __low2half2(sb), b2 = __high2half2(sb);
-    const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int m = 0; m < 8; ++m)
+    for (int m = 0; m < 4; ++m)
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq)
             out[4 * m + qq] = bq::h2_as_u32(__hfma2(bq::codes_to_half2((w[m] >> (4 * qq)) & 0x000F000Fu), s2, b2));
@@ -281,19 +298,22 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 32);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
-    // ---- which tile
-    int seg = 0, chunk = blockIdx.y;
+    // ---- which tile: segment, first row, row count
+    int seg = 0, roff, nvalid;
     if (a.tiles) {
         if ((int)blockIdx.y >= __ldg(a.n_tiles)) return;
-        const int2 t = a.tiles[blockIdx.y];
+        const int4 t = a.tiles[blockIdx.y];
         seg = t.x;
-        chunk = t.y;
+        roff = t.y;
+        nvalid = t.z;
+    } else {
+        const int chunks = (a.dense_m + BN - 1) / BN, size = (a.dense_m + chunks - 1) / chunks;
+        roff = blockIdx.y * size;
+        nvalid = min(size, a.dense_m - roff);
     }
     const int expert = a.seg_expert ? __ldg(a.seg_expert + seg) : 0;
     const int start = a.seg_start ? __ldg(a.seg_start + seg) : 0;
-    const int count = a.seg_count ? __ldg(a.seg_count + seg) : a.dense_m;
-    const int row0 = start + chunk * BN;
-    const int nvalid = min(BN, count - chunk * BN);
+    const int row0 = start + roff;
     if (nvalid <= 0) return;
     const int n_mma = (nvalid + 15) & ~15;
     const int n_boxes = (nvalid + kBoxRows - 1) / kBoxRows;
@@ -305,8 +325,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStagesB; ++i) { mbar_init(b_full(i), 1); mbar_init(b_empty(i), 1); }
-        for (int i = 0; i < kRawSlabs; ++i) { mbar_init(raw_full(i), 1); mbar_init(raw_empty(i), 4); }
-        for (int i = 0; i < kStagesA; ++i) { mbar_init(a_full(i), 4); mbar_init(a_empty(i), 1); }
+        for (int i = 0; i < kRawSlabs; ++i) { mbar_init(raw_full(i), 1); mbar_init(raw_empty(i), kConvWarps); }
+        for (int i = 0; i < kStagesA; ++i) { mbar_init(a_full(i), kConvWarps); mbar_init(a_empty(i), 1); }
         mbar_init(acc_full, 1);
         *abort_flag = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -376,7 +396,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
         }
     } else {
         // ------------------------------------------------ converters, then epilogue
-        const int quarter = warp & 3;
+        const int quarter = warp & 3, half = (warp - 2) >> 2;
         const int p = 32 * quarter + lane;                       // weight row = TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
         bool ok = true;
@@ -386,9 +406,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
             if (!(ok = warp_wait(raw_full(r), (kt / kRawSlabs) & 1, abort_flag, a.status))) break;
             if (ks >= kStagesA && !(ok = warp_wait(a_empty(sa), ((ks / kStagesA) - 1) & 1, abort_flag, a.status)))
                 break;
-            uint32_t v[32];
-            dequant_row<FMT>(raw_ring + r * kRawStride, p, sub, v);
-            tmem_st32(tmem + lane_base + kACol + 32u * sa, v);
+            uint32_t v[16];
+            dequant_half<FMT>(raw_ring + r * kRawStride, p, sub, half, v);
+            tmem_st16(tmem + lane_base + kACol + 32u * sa + 16u * half, v);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
             __syncwarp();
@@ -401,7 +421,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
             tc_fence_after();
             const int rt64 = 64 * rt + 16 * quarter + (lane & 15);   // SwiGLU feature
             const int frow = bq::kTileRows * rt + p;                  // plain output feature
-            for (int c0 = 0; c0 < nvalid; c0 += 32) {
+            // the two warps of a lane quarter take alternate 32-column chunks
+            for (int c0 = 32 * half; c0 < nvalid; c0 += 64) {
                 uint32_t v[32];
                 tmem_ld32(tmem + lane_base + kAccCol + (uint32_t)c0, v);
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -451,14 +472,16 @@ __global__ void gather_rows_kernel(const __half* __restrict__ x, const int32_t* 
 }
 
 // Token-chunk tiles of every active segment, in segment order (the
-// per-expert work queue).  One CTA of 1024 threads; <= 1024 segments.
+// per-expert work queue): a segment of c rows becomes ceil(c/BN) chunks of
+// near-equal size.  One CTA of 1024 threads; <= 1024 segments.
 __global__ void __launch_bounds__(1024)
 tile_list_kernel(const int32_t* __restrict__ seg_count, const int32_t* __restrict__ n_segments,
-                 int2* __restrict__ tiles, int32_t* __restrict__ n_tiles) {
+                 int4* __restrict__ tiles, int32_t* __restrict__ n_tiles) {
     __shared__ int32_t warp_sums[32];
     const int s = threadIdx.x;
     const int ns = *n_segments;
-    const int c = s < ns ? (seg_count[s] + BN - 1) / BN : 0;
+    const int cnt = s < ns ? seg_count[s] : 0;
+    const int c = (cnt + BN - 1) / BN;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = c;
 #pragma unroll
@@ -479,7 +502,8 @@ tile_list_kernel(const int32_t* __restrict__ seg_count, const int32_t* __restric
     }
     __syncthreads();
     const int base = incl - c + (warp ? warp_sums[warp - 1] : 0);
-    for (int i = 0; i < c; ++i) tiles[base + i] = make_int2(s, i);
+    const int size = c ? (cnt + c - 1) / c : 0;
+    for (int i = 0; i < c; ++i) tiles[base + i] = make_int4(s, i * size, min(size, cnt - i * size), 0);
     if (threadIdx.x == 0) *n_tiles = warp_sums[31];
 }
 
@@ -563,7 +587,7 @@ bq_status dense_gemm(const bq_qweight* w, int m, const __half* x, int epi, float
 
 // Workspace the routed GEMMs add to the MoE carve-up.
 struct GemmWs {
-    int2* tiles;
+    int4* tiles;
     int32_t* n_tiles;
     __half* x_perm;
     size_t bytes;
@@ -577,7 +601,7 @@ GemmWs carve(const bq_moe_desc* d, uint8_t* base) {
     GemmWs g;
     size_t off = 0;
     auto take = [&](size_t bytes) { uint8_t* p = base ? base + off : nullptr; off += up256(bytes); return p; };
-    g.tiles = (int2*)take(max_tiles * sizeof(int2));
+    g.tiles = (int4*)take(max_tiles * sizeof(int4));
     g.n_tiles = (int32_t*)take(4);
     g.x_perm = (__half*)take(P * (size_t)d->hidden * 2);
     g.bytes = off;

@@ -76,8 +76,9 @@ route_kernel(const float* __restrict__ logits, const float* __restrict__ bias, i
     }
 }
 
+// chunk_hist is stored expert-major: chunk_hist[e * n_chunks + c].
 __global__ void __launch_bounds__(kChunk)
-chunk_hist_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __restrict__ chunk_hist,
+chunk_hist_kernel(const int32_t* __restrict__ ids, int P, int E, int n_chunks, int32_t* __restrict__ chunk_hist,
                   int32_t* status) {
     extern __shared__ int32_t hist[];
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
@@ -97,29 +98,39 @@ chunk_hist_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* __rest
         if ((threadIdx.x & 31) == __ffs(grp) - 1) atomicAdd(&hist[e], __popc(grp));
     }
     __syncthreads();
-    int32_t* out = chunk_hist + (int64_t)blockIdx.x * E;
-    for (int x = threadIdx.x; x < E; x += blockDim.x) out[x] = hist[x];
+    for (int x = threadIdx.x; x < E; x += blockDim.x) chunk_hist[(int64_t)x * n_chunks + blockIdx.x] = hist[x];
 }
 
-// One CTA of 1024 threads, E <= 1024: chunk_hist[c][e] becomes the first
-// output position of expert e's pairs from chunk c.
+// One CTA of 1024 threads, E <= 1024.  Warp w scans the chunk counts of
+// experts w, w+32, ... with shuffles; then one block scan over experts.
+// chunk_hist[e][c] becomes the first output position of expert e's pairs
+// from chunk c.
 __global__ void __launch_bounds__(1024)
 scan_kernel(int32_t* __restrict__ chunk_hist, int n_chunks, int E, int32_t* __restrict__ counts,
             int32_t* __restrict__ offsets) {
+    __shared__ int32_t cnt[1024];
     __shared__ int32_t warp_sums[32];
-    const int e = threadIdx.x;
-    int32_t total = 0;
-    if (e < E) {
-        for (int c = 0; c < n_chunks; ++c) {
-            int32_t* p = chunk_hist + (int64_t)c * E + e;
-            const int32_t v = *p;
-            *p = total;
-            total += v;
-        }
-        counts[e] = total;
-    }
-    // block exclusive scan of `total` over e
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int e = warp; e < E; e += 32) {
+        int32_t* row = chunk_hist + (int64_t)e * n_chunks;
+        int32_t total = 0;
+        for (int c0 = 0; c0 < n_chunks; c0 += 32) {
+            const int c = c0 + lane;
+            const int32_t v = c < n_chunks ? row[c] : 0;
+            int32_t incl = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int32_t u = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += u;
+            }
+            if (c < n_chunks) row[c] = total + incl - v;
+            total += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) cnt[e] = total;
+    }
+    __syncthreads();
+    const int e = threadIdx.x;
+    const int32_t total = e < E ? cnt[e] : 0;
     int32_t incl = total;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -129,20 +140,26 @@ scan_kernel(int32_t* __restrict__ chunk_hist, int n_chunks, int E, int32_t* __re
     if (lane == 31) warp_sums[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        int32_t s = warp_sums[lane];
+        int32_t v = warp_sums[lane];
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int32_t v = __shfl_up_sync(0xffffffffu, s, off);
-            if (lane >= off) s += v;
+            const int32_t u = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += u;
         }
-        warp_sums[lane] = s;  // inclusive
+        warp_sums[lane] = v;  // inclusive
     }
     __syncthreads();
     const int32_t excl = incl - total + (warp ? warp_sums[warp - 1] : 0);
     if (e < E) {
+        counts[e] = total;
         offsets[e] = excl;
         if (e == E - 1) offsets[E] = excl + total;
-        for (int c = 0; c < n_chunks; ++c) chunk_hist[(int64_t)c * E + e] += excl;
+        cnt[e] = excl;
+    }
+    __syncthreads();
+    for (int x = warp; x < E; x += 32) {
+        const int32_t base = cnt[x];
+        for (int c = lane; c < n_chunks; c += 32) chunk_hist[(int64_t)x * n_chunks + c] += base;
     }
 }
 
@@ -167,7 +184,7 @@ place_kernel(const int32_t* __restrict__ ids, const float* __restrict__ gate, in
     }
     int rank = 0;
     for (int i = 0; i < (int)threadIdx.x; ++i) rank += sid[i] == e;
-    const int r = __ldg(chunk_base + (int64_t)blockIdx.x * E + e) + rank;
+    const int r = __ldg(chunk_base + (int64_t)e * gridDim.x + blockIdx.x) + rank;
     perm_token[r] = f / k;
     perm_slot[r] = f % k;
     if (perm_gate) perm_gate[r] = __ldg(gate + f);
@@ -210,7 +227,7 @@ void launch_permute(const int32_t* ids, const float* gate, int T, int k, int E, 
     const int n_chunks = (P + kChunk - 1) / kChunk;
     note_launch(n_chunks > 0 ? 3 : 1);
     if (n_chunks > 0)
-        chunk_hist_kernel<<<n_chunks, kChunk, E * sizeof(int32_t), st>>>(ids, P, E, scratch,
+        chunk_hist_kernel<<<n_chunks, kChunk, E * sizeof(int32_t), st>>>(ids, P, E, n_chunks, scratch,
                                                                         device_status_ptr());
     scan_kernel<<<1, 1024, 0, st>>>(scratch, n_chunks, E, counts, offsets);
     if (n_chunks > 0)
