@@ -35,8 +35,13 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 //   [128 rows x 64 quant bytes][scale fields]
 // Q8_0  slab = 64 K  : qs int8 [128][64], d fp16 [128][2]             = 8704 B
 // Q2_K  slab = 256 K : qs u32 [128][16] (one word per 16-value
-//                      sub-block), sc u8 [128][16], (d,dmin) half2 [128] = 10752 B
-// int4  slab = 128 K : words u32 [128][16], (scale,bias) half2 [128][2]  = 9216 B
+//                      sub-block), sc u8 [4][128][4] (scale bytes of
+//                      sub-blocks 4s..4s+3 of row p at s*512 + 4p),
+//                      (d,dmin) half2 [128]                          = 10752 B
+// int4  slab = 128 K : words u32 [128][16], (scale,bias) half2 [2][128]
+//                      (group g of row p at g*512 + 4p)              = 9216 B
+// Scale fields are stored group-major so that threads reading one group
+// of consecutive rows read consecutive words (no bank conflicts).
 //
 // Q2_K sub-block word: value 2p of the sub-block in bits 2p..2p+1, value
 // 2p+1 in bits 16+2p..17+2p (p = 0..7), so (w >> 2p) & 0x00030003 holds

@@ -11,17 +11,22 @@
 // gathered token rows against int4 expert weights.  Here, for sm_103a:
 //
 // Tile = 128 weight rows (one row tile of the slab layout, MMA M) x up to
-// 192 token rows of one expert segment (MMA N) x all of K, fp32 in TMEM.
-// A segment of c tokens is cut into ceil(c/192) chunks of near-equal size.
-// 320 threads per CTA, two CTAs per SM:
-//   warp 0     producer: TMA 2D loads of the activation tile (128-byte
-//              swizzle, 32-row boxes) and 1D bulk copies of the raw
-//              quantised slabs into shared-memory rings;
-//   warp 1     owns the TMEM allocation and issues tcgen05.mma (one lane);
-//   warps 2-9  converters: two threads per weight row each dequantise 32
+// 160 token rows of one expert segment (MMA N) x all of K, fp32 in TMEM.
+// A segment of c tokens is cut into ceil(c/160) chunks of near-equal size.
+// 352 threads per CTA, two CTAs per SM:
+//   warp 0     activation producer: TMA 2D loads of 32-row boxes (128-byte
+//              swizzle) into a ring of 15 boxes, i.e. 15 stages for tiles of
+//              up to 32 tokens down to 3 stages for 160;
+//   warp 1     owns the TMEM allocation and issues tcgen05.mma (one lane;
+//              its loop is kept lean because a single issuing thread's
+//              scalar work per stage bounds the tensor-core rate);
+//   warp 2     weight producer: 1D bulk copies of raw quantised slabs, up to
+//              three slabs ahead, independent of the activation ring;
+//   warps 3-10 converters: two threads per weight row each dequantise 32
 //              K-values of a stage from the raw slab into 16 fp16 pairs and
-//              write them to a TMEM A-operand ring with tcgen05.st (the
-//              MMA reads A from TMEM, so the dequantised weights never touch
+//              write them to a TMEM A-operand ring with tcgen05.st (the ring
+//              takes the 256 - accumulator columns, 3 to 7 stages; the MMA
+//              reads A from TMEM, so the dequantised weights never touch
 //              shared memory); after the K loop the same warps run the
 //              epilogue (tcgen05.ld -> SwiGLU / gate scale -> global).
 // All waits are bounded: a wait that runs out sets BQ_DEV_WAIT_TIMEOUT in
@@ -36,20 +41,21 @@
 
 namespace {
 
-constexpr int BN = 192;            // max token rows per tile (MMA N)
+constexpr int BN = 160;            // max token rows per tile (MMA N)
 constexpr int BK = 64;             // K per stage (one 128-byte swizzle row of fp16)
-constexpr int kStagesB = 3;        // activation tiles in shared memory
-constexpr int kStagesA = 2;        // dequantised weight tiles in TMEM
+constexpr int kBoxRows = 32;       // activation rows per TMA box (4 KB)
+constexpr int kBBoxes = 15;        // activation ring capacity in boxes: 15 stages of 32 rows .. 3 of 160
+constexpr int kMaxStagesB = kBBoxes;
+constexpr int kMaxStagesA = 7;     // TMEM A ring: whatever the accumulator leaves of 256 columns
 constexpr int kRawSlabs = 3;       // raw quantised slabs in shared memory
 constexpr int kConvWarps = 8;      // two per TMEM lane quarter, each half a stage
-constexpr int kThreads = 32 * (2 + kConvWarps);
-constexpr int kBoxRows = 32;
+constexpr int kFirstConvWarp = 3;  // warp 0: activation producer, 1: MMA, 2: weight producer
+constexpr int kThreads = 32 * (kFirstConvWarp + kConvWarps);
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kAccCol = 0;    // accumulator: columns [0, 192)
-constexpr uint32_t kACol = 192;    // A ring: 2 x 32 columns
-constexpr int kBStageBytes = BN * 128;
+constexpr int kBoxBytes = kBoxRows * 128;
 constexpr int kRawStride = 10752;  // largest slab
-constexpr int kSmemBytes = 1024 + kStagesB * kBStageBytes + kRawSlabs * kRawStride + 512;  // + barriers, TMEM slot
+constexpr int kNumBars = 2 * kMaxStagesB + 2 * kRawSlabs + 2 * kMaxStagesA + 1;
+constexpr int kSmemBytes = 1024 + kBBoxes * kBoxBytes + kRawSlabs * kRawStride + 8 * kNumBars + 64;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
 
 template <int FMT> struct G;
@@ -243,7 +249,7 @@ __device__ __forceinline__ void dequant_half<BQ_FMT_Q2_K>(const uint8_t* raw, in
                                                           uint32_t (&out)[16]) {
     // stage `sub` of the super-block = sub-blocks 4sub..4sub+3; half h = two of them
     const uint2 q = *reinterpret_cast<const uint2*>(raw + bq::quant_chunk_offset(p, sub) + 8 * h);
-    const uint32_t sc2 = *reinterpret_cast<const uint16_t*>(raw + 8192 + 16 * p + 4 * sub + 2 * h);
+    const uint32_t sc2 = *reinterpret_cast<const uint16_t*>(raw + 8192 + 512 * sub + 4 * p + 2 * h);
     const __half2 dm = bq::u32_as_h2(*reinterpret_cast<const uint32_t*>(raw + 10240 + 4 * p));
     const float d = __low2float(dm), dmin = __high2float(dm);
     const uint32_t w[2] = {q.x, q.y};
@@ -264,7 +270,7 @@ __device__ __forceinline__ void dequant_half<BQ_FMT_INT4_G64>(const uint8_t* raw
                                                               uint32_t (&out)[16]) {
     // stage `sub` = K group `sub` of the 128-value slab; half h = chunk 2sub + h
     const uint4 q = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, 2 * sub + h));
-    const __half2 sb = bq::u32_as_h2(*reinterpret_cast<const uint32_t*>(raw + 8192 + 8 * p + 4 * sub));
+    const __half2 sb = bq::u32_as_h2(*reinterpret_cast<const uint32_t*>(raw + 8192 + 512 * sub + 4 * p));
     const __half2 s2 = __low2half2(sb), b2 = __high2half2(sb);
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -284,18 +290,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
     uint8_t* b_ring = smem;
-    uint8_t* raw_ring = smem + kStagesB * kBStageBytes;
+    uint8_t* raw_ring = smem + kBBoxes * kBoxBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(raw_ring + kRawSlabs * kRawStride);
-    // barrier ids
     const uint32_t bar0 = smem_u32(bars);
     auto b_full = [&](int s) { return bar0 + 8u * s; };
-    auto b_empty = [&](int s) { return bar0 + 8u * (kStagesB + s); };
-    auto raw_full = [&](int r) { return bar0 + 8u * (2 * kStagesB + r); };
-    auto raw_empty = [&](int r) { return bar0 + 8u * (2 * kStagesB + kRawSlabs + r); };
-    auto a_full = [&](int s) { return bar0 + 8u * (2 * kStagesB + 2 * kRawSlabs + s); };
-    auto a_empty = [&](int s) { return bar0 + 8u * (2 * kStagesB + 2 * kRawSlabs + kStagesA + s); };
-    const uint32_t acc_full = bar0 + 8u * (2 * kStagesB + 2 * kRawSlabs + 2 * kStagesA);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 32);
+    auto b_empty = [&](int s) { return bar0 + 8u * (kMaxStagesB + s); };
+    auto raw_full = [&](int r) { return bar0 + 8u * (2 * kMaxStagesB + r); };
+    auto raw_empty = [&](int r) { return bar0 + 8u * (2 * kMaxStagesB + kRawSlabs + r); };
+    auto a_full = [&](int s) { return bar0 + 8u * (2 * kMaxStagesB + 2 * kRawSlabs + s); };
+    auto a_empty = [&](int s) { return bar0 + 8u * (2 * kMaxStagesB + 2 * kRawSlabs + kMaxStagesA + s); };
+    const uint32_t acc_full = bar0 + 8u * (kNumBars - 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     // ---- which tile: segment, first row, row count
@@ -317,6 +322,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
     if (nvalid <= 0) return;
     const int n_mma = (nvalid + 15) & ~15;
     const int n_boxes = (nvalid + kBoxRows - 1) / kBoxRows;
+    // ring depths for this tile
+    const int stages_b = min(kMaxStagesB, kBBoxes / n_boxes);
+    const uint32_t acc_cols = (uint32_t)((n_mma + 31) & ~31);
+    const int stages_a = min(kMaxStagesA, (int)((kTmemCols - acc_cols) / 32));
     const int rt = blockIdx.x;
     const int n_tiles_w = a.n / bq::kTileRows, k_slabs = a.k / F::SK;
     const uint8_t* wslab = a.w + bq::slab_index(expert, rt, 0, n_tiles_w, k_slabs) * F::SB;
@@ -324,9 +333,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStagesB; ++i) { mbar_init(b_full(i), 1); mbar_init(b_empty(i), 1); }
+        for (int i = 0; i < kMaxStagesB; ++i) { mbar_init(b_full(i), 1); mbar_init(b_empty(i), 1); }
         for (int i = 0; i < kRawSlabs; ++i) { mbar_init(raw_full(i), 1); mbar_init(raw_empty(i), kConvWarps); }
-        for (int i = 0; i < kStagesA; ++i) { mbar_init(a_full(i), kConvWarps); mbar_init(a_empty(i), 1); }
+        for (int i = 0; i < kMaxStagesA; ++i) { mbar_init(a_full(i), kConvWarps); mbar_init(a_empty(i), 1); }
         mbar_init(acc_full, 1);
         *abort_flag = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -340,81 +349,103 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const uint32_t a_col0 = acc_cols;   // A ring starts after the accumulator
 
     if (warp == 0) {
-        // ------------------------------------------------ producer
+        // ------------------------------------------------ activation producer
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
-            int issued_b = 0, issued_raw = 0;
+            int issued = 0, s = 0;
+            uint32_t ph = 0;   // parity of the current pass over the ring
             bool ok = true;
-            for (int ks = 0; ks < KS && ok; ++ks) {
-                if (ks % F::SPS == 0) {
-                    const int kt = ks / F::SPS, r = kt % kRawSlabs;
-                    if (kt >= kRawSlabs && !(ok = mbar_wait(raw_empty(r), ((kt / kRawSlabs) - 1) & 1, abort_flag, a.status)))
-                        break;
-                    mbar_expect_tx(raw_full(r), F::SB);
-                    bulk_load(smem_u32(raw_ring + r * kRawStride), wslab + (int64_t)kt * F::SB, F::SB, raw_full(r));
-                    ++issued_raw;
-                }
-                const int s = ks % kStagesB;
-                if (ks >= kStagesB && !(ok = mbar_wait(b_empty(s), ((ks / kStagesB) - 1) & 1, abort_flag, a.status)))
-                    break;
-                mbar_expect_tx(b_full(s), n_boxes * kBoxRows * 128);
+            const uint32_t stage_bytes = n_boxes * kBoxBytes;
+            for (int ks = 0; ks < KS; ++ks) {
+                if (ks >= stages_b && !(ok = mbar_wait(b_empty(s), ph ^ 1u, abort_flag, a.status))) break;
+                mbar_expect_tx(b_full(s), stage_bytes);
+                const uint32_t dst = smem_u32(b_ring) + s * stage_bytes;
                 for (int bx = 0; bx < n_boxes; ++bx)
-                    tma_load_2d(smem_u32(b_ring + s * kBStageBytes + bx * kBoxRows * 128), &tmap_b, ks * BK,
-                                row0 + bx * kBoxRows, b_full(s));
-                ++issued_b;
+                    tma_load_2d(dst + bx * kBoxBytes, &tmap_b, ks * BK, row0 + bx * kBoxRows, b_full(s));
+                ++issued;
+                if (++s == stages_b) { s = 0; ph ^= 1u; }
+            }
+            if (!ok) {   // let our own copies land before the CTA leaves (bounded)
+                volatile uint32_t no_abort = 0;
+                for (int u = max(0, issued - stages_b); u < issued; ++u)
+                    mbar_wait(b_full(u % stages_b), (u / stages_b) & 1, &no_abort, a.status);
+            }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------ weight producer
+        if (lane == 0) {
+            int issued = 0, r = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int kt = 0; kt < k_slabs; ++kt) {
+                if (kt >= kRawSlabs && !(ok = mbar_wait(raw_empty(r), ph ^ 1u, abort_flag, a.status))) break;
+                mbar_expect_tx(raw_full(r), F::SB);
+                bulk_load(smem_u32(raw_ring + r * kRawStride), wslab + (int64_t)kt * F::SB, F::SB, raw_full(r));
+                ++issued;
+                if (++r == kRawSlabs) { r = 0; ph ^= 1u; }
             }
             if (!ok) {
-                // let our own copies land before the CTA leaves (bounded)
                 volatile uint32_t no_abort = 0;
-                for (int u = max(0, issued_b - kStagesB); u < issued_b; ++u)
-                    mbar_wait(b_full(u % kStagesB), (u / kStagesB) & 1, &no_abort, a.status);
-                for (int u = max(0, issued_raw - kRawSlabs); u < issued_raw; ++u)
+                for (int u = max(0, issued - kRawSlabs); u < issued; ++u)
                     mbar_wait(raw_full(u % kRawSlabs), (u / kRawSlabs) & 1, &no_abort, a.status);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
+        // Kept lean: one lane issues every MMA, so its scalar work per stage
+        // (ring counters, descriptors) directly limits the tensor-core rate.
         if (lane == 0) {
             const uint32_t idesc = idesc_f16(n_mma);
+            const uint64_t b_desc0 = smem_desc_sw128(smem_u32(b_ring));
+            const uint64_t b_step = (uint64_t)((n_boxes * kBoxBytes) >> 4);   // encoded stage stride
+            int sa = 0, sb = 0;
+            uint32_t pa = 0, pb = 0;
+            uint64_t bd = b_desc0;
+            uint32_t at = tmem + a_col0;
             bool ok = true;
             for (int ks = 0; ks < KS; ++ks) {
-                const int sa = ks % kStagesA, s = ks % kStagesB;
-                if (!(ok = mbar_wait(a_full(sa), (ks / kStagesA) & 1, abort_flag, a.status))) break;
-                if (!(ok = mbar_wait(b_full(s), (ks / kStagesB) & 1, abort_flag, a.status))) break;
+                if (!(ok = mbar_wait(a_full(sa), pa, abort_flag, a.status))) break;
+                if (!(ok = mbar_wait(b_full(sb), pb, abort_flag, a.status))) break;
                 tc_fence_after();
-                const uint32_t b_addr = smem_u32(b_ring + s * kBStageBytes);
-#pragma unroll
-                for (int j = 0; j < BK / 16; ++j)
-                    mma_f16_ts(tmem + kAccCol, tmem + kACol + 32u * sa + 8u * j, smem_desc_sw128(b_addr + 32u * j),
-                               idesc, (ks | j) != 0);
+                mma_f16_ts(tmem, at, bd, idesc, ks != 0);
+                mma_f16_ts(tmem, at + 8u, bd + 2u, idesc, 1u);      // +32 bytes along K
+                mma_f16_ts(tmem, at + 16u, bd + 4u, idesc, 1u);
+                mma_f16_ts(tmem, at + 24u, bd + 6u, idesc, 1u);
                 mma_commit(a_empty(sa));
-                mma_commit(b_empty(s));
+                mma_commit(b_empty(sb));
+                if (++sa == stages_a) { sa = 0; pa ^= 1u; at = tmem + a_col0; } else { at += 32u; }
+                if (++sb == stages_b) { sb = 0; pb ^= 1u; bd = b_desc0; } else { bd += b_step; }
             }
             if (ok) mma_commit(acc_full);
         }
     } else {
         // ------------------------------------------------ converters, then epilogue
-        const int quarter = warp & 3, half = (warp - 2) >> 2;
+        const int quarter = warp & 3, half = (warp - kFirstConvWarp) >> 2;
         const int p = 32 * quarter + lane;                       // weight row = TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
         bool ok = true;
+        int sa = 0, r = 0, sub = 0;
+        uint32_t pa = 0, pr = 0;
         for (int ks = 0; ks < KS; ++ks) {
-            const int kt = ks / F::SPS, sub = ks % F::SPS, r = kt % kRawSlabs;
-            const int sa = ks % kStagesA;
-            if (!(ok = warp_wait(raw_full(r), (kt / kRawSlabs) & 1, abort_flag, a.status))) break;
-            if (ks >= kStagesA && !(ok = warp_wait(a_empty(sa), ((ks / kStagesA) - 1) & 1, abort_flag, a.status)))
-                break;
+            if (sub == 0 && !(ok = warp_wait(raw_full(r), pr, abort_flag, a.status))) break;
+            if (ks >= stages_a && !(ok = warp_wait(a_empty(sa), pa ^ 1u, abort_flag, a.status))) break;
             uint32_t v[16];
             dequant_half<FMT>(raw_ring + r * kRawStride, p, sub, half, v);
-            tmem_st16(tmem + lane_base + kACol + 32u * sa + 16u * half, v);
+            tmem_st16(tmem + lane_base + a_col0 + 32u * sa + 16u * half, v);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 if (sub == F::SPS - 1) mbar_arrive(raw_empty(r));
                 mbar_arrive(a_full(sa));
+            }
+            if (++sa == stages_a) { sa = 0; pa ^= 1u; }
+            if (++sub == F::SPS) {
+                sub = 0;
+                if (++r == kRawSlabs) { r = 0; pr ^= 1u; }
             }
         }
         if (ok && warp_wait(acc_full, 0, abort_flag, a.status)) {
@@ -424,7 +455,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
             // the two warps of a lane quarter take alternate 32-column chunks
             for (int c0 = 32 * half; c0 < nvalid; c0 += 64) {
                 uint32_t v[32];
-                tmem_ld32(tmem + lane_base + kAccCol + (uint32_t)c0, v);
+                tmem_ld32(tmem + lane_base + (uint32_t)c0, v);
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
                 if (EPI == EPI_SWIGLU) {
                     // lanes 0-15 hold gate rows, 16-31 the matching up rows

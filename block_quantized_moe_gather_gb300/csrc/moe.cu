@@ -83,6 +83,11 @@ struct MoeWs {
     int32_t *seg_expert, *seg_start, *seg_count, *n_segments, *scratch;
     float *gate, *perm_gate, *y_slot;
     __half *h, *h_shared;
+    // decode (T <= 8) split-K: split factors, partials and counters per GEMV
+    int ks_gu, ks_d, ks_sgu, ks_sd;
+    float *part_gu, *part_d, *part_sgu, *part_sd;
+    int32_t *cnt_gu, *cnt_d, *cnt_sgu, *cnt_sd;
+    int n_counters;
     size_t bytes;
 };
 
@@ -110,6 +115,36 @@ MoeWs carve(const bq_moe_desc* d, uint8_t* base) {
     w.y_slot = (float*)take(P * H * 4);
     w.h_shared = nullptr;
     if (d->shared_gate_up) w.h_shared = (__half*)take(T * (size_t)(d->shared_gate_up->n / 2) * 2);
+    // decode split-K buffers
+    w.ks_gu = w.ks_d = w.ks_sgu = w.ks_sd = 1;
+    w.part_gu = w.part_d = w.part_sgu = w.part_sd = nullptr;
+    w.cnt_gu = w.cnt_d = w.cnt_sgu = w.cnt_sd = nullptr;
+    w.n_counters = 0;
+    if (d->T <= 8) {
+        const int segs = (int)std::min(E, P);
+        const int t_gu = 2 * (int)I / bq::kTileRows, t_d = (int)H / bq::kTileRows;
+        w.ks_gu = bq::qgemv_ksplit(d->w_gate_up.fmt, 2 * (int)I, (int)H, segs, d->T);
+        w.ks_d = bq::qgemv_ksplit(d->w_down.fmt, (int)H, (int)I, segs, d->T);
+        w.part_gu = (float*)take((size_t)segs * t_gu * w.ks_gu * 4096);
+        w.part_d = (float*)take((size_t)segs * t_d * w.ks_d * 4096);
+        int nc = segs * t_gu + segs * t_d;
+        if (d->shared_gate_up) {
+            const int n_s = d->shared_gate_up->n, i_s = n_s / 2;
+            w.ks_sgu = bq::qgemv_ksplit(d->shared_gate_up->fmt, n_s, (int)H, 1, d->T);
+            w.ks_sd = bq::qgemv_ksplit(d->shared_down->fmt, (int)H, i_s, 1, d->T);
+            w.part_sgu = (float*)take((size_t)(n_s / bq::kTileRows) * w.ks_sgu * 4096);
+            w.part_sd = (float*)take((size_t)t_d * w.ks_sd * 4096);
+            nc += n_s / bq::kTileRows + t_d;
+        }
+        int32_t* cnt = (int32_t*)take((size_t)nc * 4);
+        w.n_counters = nc;
+        w.cnt_gu = cnt;
+        w.cnt_d = cnt ? cnt + segs * t_gu : nullptr;
+        if (d->shared_gate_up) {
+            w.cnt_sgu = cnt ? w.cnt_d + segs * t_d : nullptr;
+            w.cnt_sd = cnt ? w.cnt_sgu + d->shared_gate_up->n / bq::kTileRows : nullptr;
+        }
+    }
     w.bytes = off;
     return w;
 }
@@ -144,11 +179,13 @@ bq_status validate_moe(const bq_moe_desc* d) {
 }
 
 // One dense weight over `m` rows of x (single segment).
-bq::QgemvParams dense_params(const bq_qweight* w, int m, const __half* x, float* y, __half* h, int ldy) {
+bq::QgemvParams dense_params(const bq_qweight* w, int m, const __half* x, float* y, __half* h, int ldy,
+                             int ksplit = 1, float* partial = nullptr, int32_t* counters = nullptr) {
     bq::QgemvParams p{};
     p.w = static_cast<const uint8_t*>(w->data);
     p.fmt = w->fmt; p.n = w->n; p.k = w->k; p.swiglu = w->swiglu;
     p.m = m; p.x = x; p.y = y; p.h = h; p.ldy = ldy;
+    p.ksplit = ksplit; p.partial = partial; p.counters = counters;
     return p;
 }
 
@@ -199,12 +236,19 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
     const __half* xh = reinterpret_cast<const __half*>(x);
 
     bq::stage_begin(BQ_STAGE_ROUTE_PERMUTE, st);
-    bq::launch_route(router_logits, logit_bias, T, E, k, w.ids, w.gate, st);
-    bq::launch_permute(w.ids, w.gate, T, k, E, w.counts, w.offsets, w.perm_token, w.perm_slot, w.perm_gate,
-                       w.inv, w.scratch, st);
-    segments_kernel<<<1, 1024, 0, st>>>(w.counts, w.offsets, E, w.seg_expert, w.seg_start, w.seg_count,
-                                        w.n_segments);
-    bq::note_launch();
+    if (bq::route_permute_small_ok(T, k)) {
+        const bq::MoeRouting r{w.ids, w.gate, w.counts, w.offsets, w.perm_token, w.perm_slot, w.perm_gate,
+                               w.inv, w.seg_expert, w.seg_start, w.seg_count, w.n_segments,
+                               w.n_counters ? w.cnt_gu : nullptr, w.n_counters};
+        bq::launch_route_permute_small(router_logits, logit_bias, T, E, k, r, st);
+    } else {
+        bq::launch_route(router_logits, logit_bias, T, E, k, w.ids, w.gate, st);
+        bq::launch_permute(w.ids, w.gate, T, k, E, w.counts, w.offsets, w.perm_token, w.perm_slot, w.perm_gate,
+                           w.inv, w.scratch, st);
+        segments_kernel<<<1, 1024, 0, st>>>(w.counts, w.offsets, E, w.seg_expert, w.seg_start, w.seg_count,
+                                            w.n_segments);
+        bq::note_launch();
+    }
     bq::stage_end(BQ_STAGE_ROUTE_PERMUTE, st);
     const int max_segments = min(E, P);
     const bool decode = T <= 8 || !bq::gemm_supported(d->w_gate_up.fmt);
@@ -215,6 +259,7 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
         gu.fmt = d->w_gate_up.fmt; gu.n = 2 * I; gu.k = H; gu.swiglu = 1;
         gu.seg_expert = w.seg_expert; gu.seg_start = w.seg_start; gu.seg_count = w.seg_count;
         gu.n_segments = w.n_segments; gu.src_row = w.perm_token; gu.x = xh; gu.h = w.h;
+        gu.ksplit = w.ks_gu; gu.partial = w.part_gu; gu.counters = w.cnt_gu;
         bq::stage_begin(BQ_STAGE_GATE_UP, st);
         bq::launch_qgemv(gu, max_segments, st);
         bq::stage_end(BQ_STAGE_GATE_UP, st);
@@ -223,6 +268,7 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
         dn.w = static_cast<const uint8_t*>(d->w_down.data);
         dn.fmt = d->w_down.fmt; dn.n = H; dn.k = I; dn.swiglu = 0;
         dn.src_row = nullptr; dn.x = w.h; dn.h = nullptr; dn.y = w.y_slot; dn.ldy = H; dn.row_scale = w.perm_gate;
+        dn.ksplit = w.ks_d; dn.partial = w.part_d; dn.counters = w.cnt_d;
         bq::stage_begin(BQ_STAGE_DOWN, st);
         bq::launch_qgemv(dn, max_segments, st);
         bq::stage_end(BQ_STAGE_DOWN, st);
@@ -237,8 +283,10 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
         const int Is = d->shared_gate_up->n / 2;
         bq::stage_begin(BQ_STAGE_SHARED, st);
         if (T <= 8 || !bq::gemm_supported(d->shared_gate_up->fmt)) {
-            bq::launch_qgemv(dense_params(d->shared_gate_up, T, xh, nullptr, w.h_shared, 0), 1, st);
-            bq::launch_qgemv(dense_params(d->shared_down, T, w.h_shared, y, nullptr, H), 1, st);
+            bq::launch_qgemv(dense_params(d->shared_gate_up, T, xh, nullptr, w.h_shared, 0, w.ks_sgu, w.part_sgu,
+                                          w.cnt_sgu), 1, st);
+            bq::launch_qgemv(dense_params(d->shared_down, T, w.h_shared, y, nullptr, H, w.ks_sd, w.part_sd,
+                                          w.cnt_sd), 1, st);
         } else {
             if ((s = bq::launch_gemm_shared(d->shared_gate_up, d->shared_down, T, xh, w.h_shared, y, Is,
                                             base + w.bytes, st)) != BQ_OK)

@@ -15,6 +15,28 @@ void launch_permute(const int32_t* ids, const float* gate, int T, int k, int E, 
                     int32_t* offsets, int32_t* perm_token, int32_t* perm_slot, float* perm_gate,
                     int32_t* inv, int32_t* scratch, cudaStream_t st);
 
+// Outputs of the routing front end (device pointers).
+struct MoeRouting {
+    int32_t* ids;         // [T*k]
+    float* gate;          // [T*k]
+    int32_t* counts;      // [E]
+    int32_t* offsets;     // [E+1]
+    int32_t* perm_token;  // [T*k]
+    int32_t* perm_slot;   // [T*k]
+    float* perm_gate;     // [T*k]
+    int32_t* inv;         // [T*k]
+    int32_t* seg_expert;  // [E]
+    int32_t* seg_start;   // [E]
+    int32_t* seg_count;   // [E]
+    int32_t* n_segments;  // [1]
+    int32_t* zero;        // optional: ints to clear (split-K counters), or NULL
+    int n_zero;
+};
+// One-CTA routing front end for small batches (T <= 32, T*k <= 256).
+bool route_permute_small_ok(int T, int k);
+void launch_route_permute_small(const float* logits, const float* bias, int T, int E, int k, const MoeRouting& out,
+                                cudaStream_t st);
+
 // ---- grouped qgemv (qgemv.cu)
 //
 // A segment is a run of consecutive rows [start, start + count) of the
@@ -36,7 +58,17 @@ struct QgemvParams {
     __half* h;               // fp16 SwiGLU output [rows][n/2] (swiglu = 1)
     int ldy;                 // leading dimension of y (elements)
     const float* row_scale;  // optional per-list-row scale applied to y
+    // Split K across `ksplit` CTAs (requires <= 8 rows per segment): each
+    // publishes a [128][8] fp32 partial to `partial` ([segment][tile][split]);
+    // the last CTA of a (segment, tile), counted in `counters`
+    // ([segment][tile], zero on entry, left zero), sums them in split order.
+    int ksplit;
+    float* partial;
+    int32_t* counters;
 };
+constexpr int kMaxKsplit = 16;
+// Split factor that gives the GPU enough CTAs for this shape.
+int qgemv_ksplit(int fmt, int n, int k, int max_segments, int max_tokens);
 void launch_qgemv(const QgemvParams& p, int max_segments, cudaStream_t st);
 
 }  // namespace bq

@@ -8,28 +8,35 @@
 // (dequant_gemv_int4_expert_indexed), swiglu fused so silu stays in
 // registers.
 //
-// CTA = 32 weight rows (two m16 row tiles) of one matrix x all of K for
-// one segment of activation rows; its 4 warps split K by slabs.  Each lane
-// loads its 16 bytes of quants per row with one 128-bit load, dequantises
-// them in registers straight into mma.sync m16n8k16 A fragments (fp16,
-// scale applied), and multiplies with up to 8 activation rows (the n = 8
-// side of the MMA) with fp32 accumulation.  The 4 K-partials are summed
-// in a fixed order through shared memory, so results are bit-reproducible.
+// CTA = one 128-row tile of one matrix x a share of K for one segment of
+// activation rows; warp w takes the 32-row quarter w % 4 (two m16 row
+// tiles) over K half w / 4 of that share.  Each lane loads its 16 bytes of
+// quants per row with one 128-bit load (three slabs kept in flight),
+// dequantises them in registers straight into mma.sync m16n8k16 A
+// fragments (fp16, scale applied), and multiplies with up to 8 activation
+// rows (the n = 8 side of the MMA) with fp32 accumulation.  The two K
+// halves are summed in a fixed order through shared memory.  When the GPU
+// would otherwise get too few CTAs, K is also split across CTAs: each
+// publishes a partial, and the last one to finish sums them in split order,
+// so results stay bit-reproducible.
 //
 // K ordering inside a slab: lane t of a quad owns the contiguous quarter
 // [t*SK/4, (t+1)*SK/4) of the slab's K range; MMA step s takes the four
 // values [4s, 4s+4) of every lane's quarter.  The activation fragment is
 // read in the same order, so the contraction is unchanged.
+#include <algorithm>
+
 #include "moe_internal.cuh"
 
 namespace {
 
 template <int FMT> struct Traits;
-template <> struct Traits<BQ_FMT_Q8_0>     { static constexpr int SK = 64,  SB = 8704,  STEPS = 4,  XV = 2; };
-template <> struct Traits<BQ_FMT_Q2_K>     { static constexpr int SK = 256, SB = 10752, STEPS = 16, XV = 8; };
-template <> struct Traits<BQ_FMT_INT4_G64> { static constexpr int SK = 128, SB = 9216,  STEPS = 8,  XV = 4; };
+// DEPTH: slabs of weights kept in flight per warp.
+template <> struct Traits<BQ_FMT_Q8_0>     { static constexpr int SK = 64,  SB = 8704,  STEPS = 4,  XV = 2, DEPTH = 3; };
+template <> struct Traits<BQ_FMT_Q2_K>     { static constexpr int SK = 256, SB = 10752, STEPS = 16, XV = 8, DEPTH = 3; };
+template <> struct Traits<BQ_FMT_INT4_G64> { static constexpr int SK = 128, SB = 9216,  STEPS = 8,  XV = 4, DEPTH = 3; };
 
-constexpr int kWarps = 4;
+constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
 
 __device__ __forceinline__ uint32_t comp(const uint4& v, int i) {
@@ -56,12 +63,10 @@ struct Frag {
     uint4 q[2][2];       // [tile][row g / row g+8] 16 quant bytes
     uint32_t sc[2][2];   // scale word (format specific)
     uint32_t dm[2][2];   // Q2_K (d, dmin)
-    uint4 x[Traits<FMT>::XV];
 };
 
 template <int FMT>
-__device__ __forceinline__ void load_frag(Frag<FMT>& f, const uint8_t* slab, int rowbase, int g, int t,
-                                          const __half* xq, bool xvalid) {
+__device__ __forceinline__ void load_frag(Frag<FMT>& f, const uint8_t* slab, int rowbase, int g, int t) {
 #pragma unroll
     for (int tile = 0; tile < 2; ++tile)
 #pragma unroll
@@ -71,16 +76,12 @@ __device__ __forceinline__ void load_frag(Frag<FMT>& f, const uint8_t* slab, int
             if (FMT == BQ_FMT_Q8_0) {
                 f.sc[tile][hh] = __ldg(reinterpret_cast<const uint16_t*>(slab + 8192 + row * 4 + (t >> 1) * 2));
             } else if (FMT == BQ_FMT_Q2_K) {
-                f.sc[tile][hh] = __ldg(reinterpret_cast<const uint32_t*>(slab + 8192 + row * 16 + 4 * t));
+                f.sc[tile][hh] = __ldg(reinterpret_cast<const uint32_t*>(slab + 8192 + 512 * t + 4 * row));
                 f.dm[tile][hh] = __ldg(reinterpret_cast<const uint32_t*>(slab + 10240 + row * 4));
             } else {
-                f.sc[tile][hh] = __ldg(reinterpret_cast<const uint32_t*>(slab + 8192 + row * 8 + (t >> 1) * 4));
+                f.sc[tile][hh] = __ldg(reinterpret_cast<const uint32_t*>(slab + 8192 + 512 * (t >> 1) + 4 * row));
             }
         }
-    constexpr int XV = Traits<FMT>::XV;
-    const uint4* xp = reinterpret_cast<const uint4*>(xq + (Traits<FMT>::SK / 4) * t);
-#pragma unroll
-    for (int v = 0; v < XV; ++v) f.x[v] = xvalid ? __ldg(xp + v) : make_uint4(0, 0, 0, 0);
 }
 
 // A-fragment register (pair of fp16 weights) for row half hh, pair `lohi`
@@ -110,11 +111,19 @@ __device__ __forceinline__ uint32_t a_pair(const Frag<FMT>& f, int tile, int hh,
     }
 }
 
+// Multiplies one slab; the lane's activation values of the slab (token g,
+// its K quarter) are read here, from L1/L2, not kept in the prefetch ring.
 template <int FMT>
-__device__ __forceinline__ void mma_frag(const Frag<FMT>& f, float (&acc)[2][4]) {
+__device__ __forceinline__ void mma_frag(const Frag<FMT>& f, const __half* xq, bool xvalid, int t,
+                                         float (&acc)[2][4]) {
+    constexpr int XV = Traits<FMT>::XV;
+    uint4 x[XV];
+    const uint4* xp = reinterpret_cast<const uint4*>(xq + (Traits<FMT>::SK / 4) * t);
+#pragma unroll
+    for (int v = 0; v < XV; ++v) x[v] = xvalid ? __ldg(xp + v) : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int s = 0; s < Traits<FMT>::STEPS; ++s) {
-        const uint4 xv = f.x[s >> 1];
+        const uint4 xv = x[s >> 1];
         const uint32_t b0 = (s & 1) ? xv.z : xv.x;
         const uint32_t b1 = (s & 1) ? xv.w : xv.y;
 #pragma unroll
@@ -131,11 +140,45 @@ __device__ __forceinline__ void mma_frag(const Frag<FMT>& f, float (&acc)[2][4])
 
 __device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
+// Final values of one lane's accumulators -> output (SwiGLU fp16 or fp32 y).
+template <bool SWIGLU>
+__device__ __forceinline__ void qgemv_epilogue(const bq::QgemvParams& p, const float (&acc)[2][4], int rt, int quarter,
+                                               int g, int t, int row0, int ntok) {
+    const int rowbase = 32 * quarter, n0 = 2 * t;
+    if (!SWIGLU) {
+#pragma unroll
+        for (int tile = 0; tile < 2; ++tile)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int row = bq::logical_row(rt, rowbase + 16 * tile + 8 * hh + g, p.n, 0);
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    if (n0 + j < ntok) {
+                        const int r = row0 + n0 + j;
+                        const float v = acc[tile][2 * hh + j];
+                        p.y[(int64_t)r * p.ldy + row] = p.row_scale ? v * __ldg(p.row_scale + r) : v;
+                    }
+            }
+    } else {
+        // tile 0 = 16 gate rows, tile 1 = the matching 16 up rows
+        const int ih = p.n / 2;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int f = 64 * rt + 16 * quarter + 8 * hh + g;
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                if (n0 + j < ntok)
+                    p.h[(int64_t)(row0 + n0 + j) * ih + f] = __float2half_rn(silu_f(acc[0][2 * hh + j]) * acc[1][2 * hh + j]);
+        }
+    }
+}
+
 template <int FMT, bool SWIGLU>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 qgemv_kernel(const bq::QgemvParams p) {
     using T = Traits<FMT>;
-    __shared__ float2 red[kWarps][2][32][2];
+    __shared__ float2 red[4][2][32][2];   // K-half 1 partials: [quarter][tile][lane][row half]
+    __shared__ int s_last;
 
     const int seg = blockIdx.y;
     if (p.n_segments && seg >= __ldg(p.n_segments)) return;
@@ -143,11 +186,17 @@ qgemv_kernel(const bq::QgemvParams p) {
     const int start = p.seg_start ? __ldg(p.seg_start + seg) : 0;
     const int count = p.seg_count ? __ldg(p.seg_count + seg) : p.m;
 
-    const int rt = blockIdx.x >> 2, quarter = blockIdx.x & 3, rowbase = 32 * quarter;
+    const int rt = blockIdx.x, kp = blockIdx.z;
     const int n_tiles = p.n / bq::kTileRows, k_slabs = p.k / T::SK;
     const uint8_t* wbase = p.w + bq::slab_index(e, rt, 0, n_tiles, k_slabs) * T::SB;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int quarter = warp & 3, khalf = warp >> 2, rowbase = 32 * quarter;
+    // this CTA's share of the slabs (split K), then contiguous halves of it
+    const int ks_lo = (int)((int64_t)k_slabs * kp / p.ksplit), ks_hi = (int)((int64_t)k_slabs * (kp + 1) / p.ksplit);
+    const int ks_mid = ks_lo + (ks_hi - ks_lo + 1) / 2;
+    const int kt_begin = khalf ? ks_mid : ks_lo;
+    const int kt_end = khalf ? ks_hi : ks_mid;
 
     for (int tok0 = 0; tok0 < count; tok0 += 8) {
         const int ntok = min(8, count - tok0);
@@ -159,64 +208,85 @@ qgemv_kernel(const bq::QgemvParams p) {
             xrow = p.x + (int64_t)src * p.k;
         }
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        if (warp < k_slabs) {
-            Frag<FMT> cur, nxt;
-            load_frag<FMT>(cur, wbase + (int64_t)warp * T::SB, rowbase, g, t, xrow + warp * T::SK, xvalid);
-            for (int kt = warp; kt < k_slabs; kt += kWarps) {
-                const int kn = kt + kWarps;
-                if (kn < k_slabs)
-                    load_frag<FMT>(nxt, wbase + (int64_t)kn * T::SB, rowbase, g, t, xrow + kn * T::SK, xvalid);
-                mma_frag<FMT>(cur, acc);
-                cur = nxt;
+        // register ring of D slabs in flight (D - 1 ahead of the one being multiplied)
+        constexpr int D = T::DEPTH;
+        Frag<FMT> f[D];
+        const int n = kt_end - kt_begin;
+#pragma unroll
+        for (int d = 0; d < D - 1; ++d)
+            if (d < n) load_frag<FMT>(f[d], wbase + (int64_t)(kt_begin + d) * T::SB, rowbase, g, t);
+        for (int i = 0; i < n; i += D) {
+#pragma unroll
+            for (int d = 0; d < D; ++d) {
+                if (i + d >= n) break;
+                const int nxt = i + d + D - 1;
+                if (nxt < n)
+                    load_frag<FMT>(f[(d + D - 1) % D], wbase + (int64_t)(kt_begin + nxt) * T::SB, rowbase, g, t);
+                mma_frag<FMT>(f[d], xrow + (kt_begin + i + d) * T::SK, xvalid, t, acc);
+            }
+        }
+        __syncthreads();   // previous token group's readers of `red` are done
+        if (khalf) {
+#pragma unroll
+            for (int tile = 0; tile < 2; ++tile) {
+                red[quarter][tile][lane][0] = make_float2(acc[tile][0], acc[tile][1]);
+                red[quarter][tile][lane][1] = make_float2(acc[tile][2], acc[tile][3]);
             }
         }
         __syncthreads();
+        if (!khalf) {
+            // K half 0 adds half 1 in a fixed order: bit-reproducible
 #pragma unroll
-        for (int tile = 0; tile < 2; ++tile) {
-            red[warp][tile][lane][0] = make_float2(acc[tile][0], acc[tile][1]);
-            red[warp][tile][lane][1] = make_float2(acc[tile][2], acc[tile][3]);
+            for (int tile = 0; tile < 2; ++tile) {
+                const float2 r0 = red[quarter][tile][lane][0], r1 = red[quarter][tile][lane][1];
+                acc[tile][0] += r0.x; acc[tile][1] += r0.y; acc[tile][2] += r1.x; acc[tile][3] += r1.y;
+            }
         }
+        if (p.ksplit == 1) {
+            if (!khalf) qgemv_epilogue<SWIGLU>(p, acc, rt, quarter, g, t, start + tok0, ntok);
+            continue;
+        }
+        // Split K (one token group only): publish this CTA's partial; the last
+        // CTA of the (segment, tile) sums all partials in split order.
+        float* part = p.partial + ((int64_t)(seg * n_tiles + rt) * p.ksplit) * 1024;
+        if (!khalf) {
+#pragma unroll
+            for (int tile = 0; tile < 2; ++tile)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int row = rowbase + 16 * tile + 8 * hh + g;
+                    *reinterpret_cast<float2*>(part + (int64_t)kp * 1024 + row * 8 + 2 * t) =
+                        make_float2(acc[tile][2 * hh], acc[tile][2 * hh + 1]);
+                }
+        }
+        __threadfence();
         __syncthreads();
-        if (!SWIGLU) {
-            const int tid = threadIdx.x;  // 128 = 2 tiles x 32 lanes x 2 row halves
-            const int tile = tid >> 6, L = (tid >> 1) & 31, hh = tid & 1;
-            float v0 = 0.f, v1 = 0.f;
+        if (threadIdx.x == 0) s_last = atomicAdd(p.counters + seg * n_tiles + rt, 1) == p.ksplit - 1;
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+        if (!khalf) {
+            float sum[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            for (int q = 0; q < p.ksplit; ++q)
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float2 r = red[w][tile][L][hh];
-                v0 += r.x;
-                v1 += r.y;
-            }
-            const int row = bq::logical_row(rt, rowbase + 16 * tile + 8 * hh + (L >> 2), p.n, 0);
-            const int n0 = 2 * (L & 3);
-            if (n0 < ntok) {
-                const int r = start + tok0 + n0;
-                p.y[(int64_t)r * p.ldy + row] = p.row_scale ? v0 * __ldg(p.row_scale + r) : v0;
-            }
-            if (n0 + 1 < ntok) {
-                const int r = start + tok0 + n0 + 1;
-                p.y[(int64_t)r * p.ldy + row] = p.row_scale ? v1 * __ldg(p.row_scale + r) : v1;
-            }
-        } else if (threadIdx.x < 64) {
-            const int L = threadIdx.x >> 1, hh = threadIdx.x & 1;
-            float g0 = 0.f, g1 = 0.f, u0 = 0.f, u1 = 0.f;
+                for (int tile = 0; tile < 2; ++tile)
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float2 a = red[w][0][L][hh], b = red[w][1][L][hh];
-                g0 += a.x; g1 += a.y; u0 += b.x; u1 += b.y;
-            }
-            const int f = 64 * rt + 16 * quarter + 8 * hh + (L >> 2);
-            const int ih = p.n / 2;
-            const int n0 = 2 * (L & 3);
-            if (n0 < ntok) p.h[(int64_t)(start + tok0 + n0) * ih + f] = __float2half_rn(silu_f(g0) * u0);
-            if (n0 + 1 < ntok) p.h[(int64_t)(start + tok0 + n0 + 1) * ih + f] = __float2half_rn(silu_f(g1) * u1);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int row = rowbase + 16 * tile + 8 * hh + g;
+                        const float2 v = __ldcg(reinterpret_cast<const float2*>(part + (int64_t)q * 1024 + row * 8 + 2 * t));
+                        sum[tile][2 * hh] += v.x;
+                        sum[tile][2 * hh + 1] += v.y;
+                    }
+            qgemv_epilogue<SWIGLU>(p, sum, rt, quarter, g, t, start + tok0, ntok);
         }
+        if (threadIdx.x == 0) p.counters[seg * n_tiles + rt] = 0;   // ready for the next call
+        return;
     }
 }
 
 template <int FMT>
 void launch_fmt(const bq::QgemvParams& p, int max_segments, cudaStream_t st) {
-    dim3 grid(p.n / 32, max_segments);
+    dim3 grid(p.n / bq::kTileRows, max_segments, p.ksplit);
     if (p.swiglu) qgemv_kernel<FMT, true><<<grid, kThreads, 0, st>>>(p);
     else qgemv_kernel<FMT, false><<<grid, kThreads, 0, st>>>(p);
 }
@@ -225,8 +295,21 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, cudaStream_t st) {
 
 namespace bq {
 
-void launch_qgemv(const QgemvParams& p, int max_segments, cudaStream_t st) {
+int qgemv_ksplit(int fmt, int n, int k, int max_segments, int max_tokens) {
+    if (max_tokens > 8 || max_segments <= 0) return 1;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int ctas = (n / kTileRows) * max_segments;
+    const int want = (4 * sms + ctas - 1) / ctas;
+    const int k_slabs = k / fmt_info(fmt).slab_k;
+    return std::max(1, std::min(want, std::min(kMaxKsplit, k_slabs / 2)));
+}
+
+void launch_qgemv(const QgemvParams& params, int max_segments, cudaStream_t st) {
     if (max_segments <= 0) return;
+    QgemvParams p = params;
+    if (p.ksplit < 1 || !p.partial || !p.counters) p.ksplit = 1;
     note_launch();
     switch (p.fmt) {
         case BQ_FMT_Q8_0: launch_fmt<BQ_FMT_Q8_0>(p, max_segments, st); break;

@@ -86,8 +86,7 @@ __global__ void repack_q2_k_kernel(const uint8_t* __restrict__ src, int n, int k
             }
             *reinterpret_cast<uint32_t*>(it.slab + bq::quant_chunk_offset(it.p, j >> 2) + 4 * (j & 3)) = w;
         }
-        uint8_t* sc = it.slab + 8192 + it.p * 16;
-        for (int j = 0; j < 16; ++j) sc[j] = blk[j];
+        for (int j = 0; j < 16; ++j) it.slab[8192 + 512 * (j >> 2) + 4 * it.p + (j & 3)] = blk[j];
         uint8_t* dm = it.slab + 10240 + it.p * 4;
         for (int j = 0; j < 4; ++j) dm[j] = blk[80 + j];
     }
@@ -111,10 +110,10 @@ __global__ void repack_int4_kernel(const uint32_t* __restrict__ words, const uin
             }
             *reinterpret_cast<uint32_t*>(it.slab + bq::quant_chunk_offset(it.p, j >> 2) + 4 * (j & 3)) = w;
         }
-        uint16_t* sb = reinterpret_cast<uint16_t*>(it.slab + 8192 + it.p * 8);
         for (int g = 0; g < 2; ++g) {
-            sb[2 * g] = scales[rowbase * (k / 64) + 2 * it.kt + g];
-            sb[2 * g + 1] = biases[rowbase * (k / 64) + 2 * it.kt + g];
+            uint16_t* sb = reinterpret_cast<uint16_t*>(it.slab + 8192 + 512 * g + 4 * it.p);
+            sb[0] = scales[rowbase * (k / 64) + 2 * it.kt + g];
+            sb[1] = biases[rowbase * (k / 64) + 2 * it.kt + g];
         }
     }
 }

@@ -24,14 +24,11 @@ namespace {
 
 constexpr int kChunk = 256;
 
+// One warp: top-k of one row of z = logits (+ bias).  Lane j < k returns
+// the j-th selected expert and its renormalised weight.
 template <int NPER>
-__global__ void __launch_bounds__(256)
-route_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
-             int32_t* __restrict__ ids, float* __restrict__ weights) {
-    const int lane = threadIdx.x & 31;
-    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (t >= T) return;
-    const float* row = logits + (int64_t)t * E;
+__device__ __forceinline__ void route_row(const float* __restrict__ row, const float* __restrict__ bias, int E,
+                                          int k, int lane, int& esel, float& wsel) {
     float z[NPER];
 #pragma unroll
     for (int i = 0; i < NPER; ++i) {
@@ -40,8 +37,8 @@ route_kernel(const float* __restrict__ logits, const float* __restrict__ bias, i
         if (e < E) z[i] = bias ? __fadd_rn(__ldg(row + e), __ldg(bias + e)) : __ldg(row + e);
     }
     uint32_t taken = 0;
-    float zsel = 0.f, z0 = 0.f, denom = 0.f;
-    int esel = 0;
+    float exsel = 0.f, z0 = 0.f, denom = 0.f;
+    esel = 0;
     for (int j = 0; j < k; ++j) {
         // lane-local best among untaken entries; "none" is e = INT_MAX
         float bz = 0.f;
@@ -68,11 +65,125 @@ route_kernel(const float* __restrict__ logits, const float* __restrict__ bias, i
         if (j == 0) z0 = bz;
         const float ex = expf(bz - z0);
         denom += ex;
-        if (lane == j) { zsel = ex; esel = be; }
+        if (lane == j) { exsel = ex; esel = be; }
     }
+    wsel = exsel / denom;
+}
+
+template <int NPER>
+__global__ void __launch_bounds__(256)
+route_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
+             int32_t* __restrict__ ids, float* __restrict__ weights) {
+    const int lane = threadIdx.x & 31;
+    const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (t >= T) return;
+    int e;
+    float w;
+    route_row<NPER>(logits + (int64_t)t * E, bias, E, k, lane, e, w);
     if (lane < k) {
-        ids[(int64_t)t * k + lane] = esel;
-        weights[(int64_t)t * k + lane] = zsel / denom;
+        ids[(int64_t)t * k + lane] = e;
+        weights[(int64_t)t * k + lane] = w;
+    }
+}
+
+// Exclusive scan of one int per thread over a 1024-thread block.
+__device__ __forceinline__ int block_exclusive_scan(int v, int32_t* warp_sums, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += u;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sums[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += u;
+        }
+        warp_sums[lane] = w;
+    }
+    __syncthreads();
+    total = warp_sums[31];
+    const int r = incl - v + (warp ? warp_sums[warp - 1] : 0);
+    __syncthreads();   // warp_sums may be reused
+    return r;
+}
+
+// Whole routing front end for a small batch (T <= 32, T*k <= 256) in one
+// CTA: top-k per token, expert histogram, exclusive scan, stable
+// placement and the list of active experts.  Same results as the
+// multi-kernel path.  Optionally clears `out.zero` (split-K counters of the
+// GEMVs that follow).
+template <int NPER>
+__global__ void __launch_bounds__(1024)
+route_permute_small_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
+                           bq::MoeRouting out, int32_t* status) {
+    __shared__ int32_t s_ids[256];
+    __shared__ int32_t hist[1024];
+    __shared__ int32_t warp_sums[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int P = T * k;
+    hist[threadIdx.x] = 0;
+    for (int i = threadIdx.x; i < out.n_zero; i += blockDim.x) out.zero[i] = 0;
+    if (warp < T) {
+        int e;
+        float w;
+        route_row<NPER>(logits + (int64_t)warp * E, bias, E, k, lane, e, w);
+        if (lane < k) {
+            const int f = warp * k + lane;
+            s_ids[f] = e;
+            out.ids[f] = e;
+            out.gate[f] = w;
+        }
+    }
+    __syncthreads();
+    const int f = threadIdx.x;
+    int e = -1;
+    if (f < P) {
+        e = s_ids[f];
+        if (e < 0 || e >= E) {
+            bq::set_device_error(status, BQ_DEV_BAD_EXPERT_ID);
+            e = -1;
+        } else {
+            atomicAdd(&hist[e], 1);
+        }
+    }
+    __syncthreads();
+    const int x = threadIdx.x;
+    const int c = x < E ? hist[x] : 0;
+    int total = 0;
+    const int off = block_exclusive_scan(c, warp_sums, total);
+    int n_active = 0;
+    const int seg = block_exclusive_scan(c > 0 ? 1 : 0, warp_sums, n_active);
+    if (x < E) {
+        out.counts[x] = c;
+        out.offsets[x] = off;
+        if (x == E - 1) out.offsets[E] = off + c;
+        if (c > 0) {
+            out.seg_expert[seg] = x;
+            out.seg_start[seg] = off;
+            out.seg_count[seg] = c;
+        }
+        hist[x] = off;
+    }
+    if (x == 0) *out.n_segments = n_active;
+    __syncthreads();
+    if (f < P) {
+        if (e < 0) {
+            out.inv[f] = -1;
+        } else {
+            int rank = 0;
+            for (int i = 0; i < f; ++i) rank += s_ids[i] == e;
+            const int r = hist[e] + rank;
+            out.perm_token[r] = f / k;
+            out.perm_slot[r] = f % k;
+            out.perm_gate[r] = out.gate[f];
+            out.inv[f] = r;
+        }
     }
 }
 
@@ -213,6 +324,20 @@ void launch_route(const float* logits, const float* bias, int T, int E, int k, i
     else if (E <= 256) route_kernel<8><<<grid, 256, 0, st>>>(logits, bias, T, E, k, ids, weights);
     else if (E <= 512) route_kernel<16><<<grid, 256, 0, st>>>(logits, bias, T, E, k, ids, weights);
     else route_kernel<32><<<grid, 256, 0, st>>>(logits, bias, T, E, k, ids, weights);
+}
+
+bool route_permute_small_ok(int T, int k) { return T <= 32 && T * k <= 256; }
+
+void launch_route_permute_small(const float* logits, const float* bias, int T, int E, int k, const MoeRouting& out,
+                                cudaStream_t st) {
+    note_launch();
+    int32_t* status = device_status_ptr();
+    if (E <= 32) route_permute_small_kernel<1><<<1, 1024, 0, st>>>(logits, bias, T, E, k, out, status);
+    else if (E <= 64) route_permute_small_kernel<2><<<1, 1024, 0, st>>>(logits, bias, T, E, k, out, status);
+    else if (E <= 128) route_permute_small_kernel<4><<<1, 1024, 0, st>>>(logits, bias, T, E, k, out, status);
+    else if (E <= 256) route_permute_small_kernel<8><<<1, 1024, 0, st>>>(logits, bias, T, E, k, out, status);
+    else if (E <= 512) route_permute_small_kernel<16><<<1, 1024, 0, st>>>(logits, bias, T, E, k, out, status);
+    else route_permute_small_kernel<32><<<1, 1024, 0, st>>>(logits, bias, T, E, k, out, status);
 }
 
 size_t permute_scratch_bytes(int P, int E) {

@@ -51,6 +51,18 @@ def test_moe_bit_reproducible(lib):
     np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))
 
 
+@pytest.mark.parametrize("t", [1, 5])
+def test_moe_decode_bit_reproducible(lib, t):
+    # the decode GEMVs split K across CTAs; partials are summed in a fixed order
+    case = synth.dataclasses.replace(SMALL[2], t=t)
+    inp = synth.moe_inputs(case)
+    layer = build_layer(lib, inp)
+    a = run_moe(lib, layer, inp)
+    b = run_moe(lib, layer, inp)
+    np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))
+    assert_close_matmul(a, oracle_moe(inp), f"decode t={t}")
+
+
 def test_moe_zero_tokens_is_noop(lib):
     import torch
     case = synth.dataclasses.replace(SMALL[0], t=0)
