@@ -56,6 +56,8 @@ _SIGS = {
     "bq_moe_permute": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
                                  c_void_p, c_void_p, c_size_t, c_void_p]),
     "bq_moe_workspace_bytes": (c_size_t, [POINTER(MoEDescC)]),
+    "bq_moe_permute_noalloc": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
+                                         c_void_p, c_void_p, c_void_p]),
     "bq_set_stage_events": (c_int32, [c_int32, c_void_p, c_void_p]),
     "bq_launch_count": (c_uint64, []),
     "bq_moe_gather_qmm": (c_int32, [POINTER(MoEDescC), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -198,6 +200,17 @@ def set_stage_events(stage: int, start=None, stop=None):
 
 def launch_count() -> int:
     return int(_lib.bq_launch_count())
+
+
+def moe_permute_noalloc(ids, n_experts: int, counts, offsets, perm_token, perm_slot, inv, stream=None):
+    """bq_moe_permute without a workspace: for callers that cannot allocate
+    device memory at call time.  Scratch is a fixed array built into the
+    library (limit: ceil(T*k/256) * E <= 65536); calls that overlap on the
+    GPU race on it."""
+    t, k = ids.shape
+    _check(_lib.bq_moe_permute_noalloc(_ptr(ids), t, k, n_experts, _ptr(counts), _ptr(offsets), _ptr(perm_token),
+                                       _ptr(perm_slot), _ptr(inv), _stream(stream)),
+           "bq_moe_permute_noalloc")
 
 
 class MoELayer:

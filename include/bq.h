@@ -197,6 +197,30 @@ bq_status bq_moe_permute(const int32_t* ids, int32_t T, int32_t k, int32_t E,
                          int32_t* perm_slot, int32_t* inv, void* workspace,
                          size_t workspace_bytes, bq_stream_t stream);
 
+/*
+ * Allocation-free variant of bq_moe_permute (no counterpart on the pages;
+ * an addition of this library).  For callers that cannot provide a
+ * workspace -- e.g. code whose device memory is entirely owned by another
+ * allocator, or a latency-critical loop where cudaMalloc must not be called
+ * (it can fail there or synchronise the device).  Same arguments and
+ * outputs as bq_moe_permute minus the workspace: the chunk histograms live
+ * in a fixed 256 KiB device array built into the library, held on every GPU
+ * that loads it until the process exits.
+ *  - Limit: ceil(T*k / 256) * E <= 65536 (e.g. T*k <= 16384 for E = 1024,
+ *    T*k <= 65536 for E = 256); larger requests return BQ_ERR_SHAPE and
+ *    launch nothing.
+ *  - The first call on a device looks up the array's address on that
+ *    device; make it before any stream capture.
+ *  - All calls share the array.  Calls whose kernels overlap on the GPU
+ *    race on it; order them (one stream, or events).  Nothing needs to be
+ *    cleared between calls: every scratch value read is written first.
+ *  - Calls no cudaMalloc, cudaFree or allocating routine.
+ * Errors: as bq_moe_permute, with BQ_ERR_SHAPE for the size limit.
+ */
+bq_status bq_moe_permute_noalloc(const int32_t* ids, int32_t T, int32_t k, int32_t E,
+                                 int32_t* counts, int32_t* offsets, int32_t* perm_token,
+                                 int32_t* perm_slot, int32_t* inv, bq_stream_t stream);
+
 /* ------------------------------------------------------------------ S5..S13
  * One MoE layer: route -> permute -> grouped gate/up GEMM with SwiGLU ->
  * grouped down GEMM scaled by the gate weight -> combine, plus an
