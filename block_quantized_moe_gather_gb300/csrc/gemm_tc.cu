@@ -20,12 +20,14 @@
 //   warp 1     owns the TMEM allocation and issues tcgen05.mma (one lane;
 //              its loop is kept lean because a single issuing thread's
 //              scalar work per stage bounds the tensor-core rate);
-//   warp 2     weight producer: 1D bulk copies of raw quantised slabs, up to
-//              three slabs ahead, independent of the activation ring;
-//   warps 3-10 converters: two threads per weight row each dequantise 32
-//              K-values of a stage from the raw slab into 16 fp16 pairs and
-//              write them to a TMEM A-operand ring with tcgen05.st (the ring
-//              takes the 256 - accumulator columns, 3 to 7 stages; the MMA
+//   warp 2     weight producer: 1D bulk copies of raw quantised slabs, three
+//              (Q8_0: four) slabs ahead, independent of the activation ring;
+//   warps 3-10 converters: one thread per weight row dequantises the 64
+//              K-values of a stage from the raw slab into 32 fp16 pairs; the
+//              two warps of a TMEM lane quarter take alternate stages, so each
+//              pays its synchronisation once per two stages of MMA time.  They
+//              write a TMEM A-operand ring with tcgen05.st (the ring
+//              takes the 256 - accumulator columns, 2 to 6 stages; the MMA
 //              reads A from TMEM, so the dequantised weights never touch
 //              shared memory); after the K loop the same warps run the
 //              epilogue (tcgen05.ld -> SwiGLU / gate scale -> global).
@@ -46,22 +48,29 @@ constexpr int BK = 64;             // K per stage (one 128-byte swizzle row of f
 constexpr int kBoxRows = 32;       // activation rows per TMA box (4 KB)
 constexpr int kBBoxes = 15;        // activation ring capacity in boxes: 15 stages of 32 rows .. 3 of 160
 constexpr int kMaxStagesB = kBBoxes;
-constexpr int kMaxStagesA = 7;     // TMEM A ring: whatever the accumulator leaves of 256 columns
-constexpr int kRawSlabs = 3;       // raw quantised slabs in shared memory
-constexpr int kConvWarps = 8;      // two per TMEM lane quarter, each half a stage
+// TMEM A ring: whatever the accumulator leaves of 256 columns, rounded down to
+// an even count so that every slot is always written by the same converter warps
+constexpr int kMaxStagesA = 6;
+constexpr int kMaxRawSlabs = 4;    // raw quantised slabs in shared memory (per format below)
+constexpr int kConvWarps = 8;      // two per TMEM lane quarter, alternating stages
 constexpr int kFirstConvWarp = 3;  // warp 0: activation producer, 1: MMA, 2: weight producer
 constexpr int kThreads = 32 * (kFirstConvWarp + kConvWarps);
 constexpr uint32_t kTmemCols = 256;
 constexpr int kBoxBytes = kBoxRows * 128;
-constexpr int kRawStride = 10752;  // largest slab
-constexpr int kNumBars = 2 * kMaxStagesB + 2 * kRawSlabs + 2 * kMaxStagesA + 1;
-constexpr int kSmemBytes = 1024 + kBBoxes * kBoxBytes + kRawSlabs * kRawStride + 8 * kNumBars + 64;
+constexpr int kRawBytes = 34816;   // raw slab ring: 4 Q8_0 / 3 Q2_K / 3 int4 slabs
+constexpr int kNumBars = 2 * kMaxStagesB + 2 * kMaxRawSlabs + 2 * kMaxStagesA + 1;
+constexpr int kSmemBytes = 1024 + kBBoxes * kBoxBytes + kRawBytes + 8 * kNumBars + 64;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
 
 template <int FMT> struct G;
-template <> struct G<BQ_FMT_Q8_0>     { static constexpr int SK = 64,  SB = 8704,  SPS = 1; };
-template <> struct G<BQ_FMT_Q2_K>     { static constexpr int SK = 256, SB = 10752, SPS = 4; };
-template <> struct G<BQ_FMT_INT4_G64> { static constexpr int SK = 128, SB = 9216,  SPS = 2; };
+// SK: K per slab, SB: slab bytes, SPS: stages per slab, NR: slabs in the raw ring.
+// A one-stage slab is read only by the converter warps of that stage's parity,
+// so its ring needs an even slab count for each warp to see every phase of
+// the slots it waits on.
+template <> struct G<BQ_FMT_Q8_0>     { static constexpr int SK = 64,  SB = 8704,  SPS = 1, NR = 4; };
+template <> struct G<BQ_FMT_Q2_K>     { static constexpr int SK = 256, SB = 10752, SPS = 4, NR = 3; };
+template <> struct G<BQ_FMT_INT4_G64> { static constexpr int SK = 128, SB = 9216,  SPS = 2, NR = 3; };
+static_assert(4 * 8704 <= kRawBytes && 3 * 10752 <= kRawBytes && 3 * 9216 <= kRawBytes, "raw ring");
 
 enum { EPI_SWIGLU = 0, EPI_SCALE = 1, EPI_PLAIN = 2 };
 
@@ -218,66 +227,98 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
                  : "memory");
 }
 
-// ---------------------------------------------------------------- dequantisation of one row x 32 K
-// Output: 16 fp16 pairs, pair i = K values (32h + 2i, 32h + 2i + 1) of the
-// stage, h = the converter's half.
+// ---------------------------------------------------------------- dequantisation of one row x 64 K
+// Exact small integers from bit fields without shifting: OR a field at bit
+// offset j of each 16-bit lane into the mantissa of 2^(10-j); the field then
+// has weight 1, so subtracting 2^(10-j) leaves the field's value.
+template <int J>
+__device__ __forceinline__ __half2 field_to_half2(uint32_t w, uint32_t field_mask) {
+    static_assert(J >= 0 && J <= 8, "field must sit inside the 10 mantissa bits");   // callers: J + width <= 10
+    constexpr uint32_t e = (uint32_t)(25 - J) << 10;   // biased exponent of 2^(10-J)
+    const __half2 m = bq::u32_as_h2(e | (e << 16));
+    return __hsub2(bq::u32_as_h2((w & (field_mask << J)) | e | (e << 16)), m);
+}
+
+// One 64-value K stage of weight row p of a raw slab as 32 fp16 pairs
+// (pair i = K values 2i, 2i+1 of the stage), each value rounded once to fp16.
 template <int FMT>
-__device__ __forceinline__ void dequant_half(const uint8_t* raw, int p, int sub, int h, uint32_t (&out)[16]);
+__device__ __forceinline__ void dequant_stage(const uint8_t* raw, int p, int sub, uint32_t (&out)[32]);
 
 template <>
-__device__ __forceinline__ void dequant_half<BQ_FMT_Q8_0>(const uint8_t* raw, int p, int, int h,
-                                                          uint32_t (&out)[16]) {
-    // half h of the 64-value slab is exactly Q8_0 block h
-    const uint16_t db = *reinterpret_cast<const uint16_t*>(raw + 8192 + 4 * p + 2 * h);
-    const __half d1 = __ushort_as_half(db);
-    const __half2 d = __halves2half2(d1, d1);
+__device__ __forceinline__ void dequant_stage<BQ_FMT_Q8_0>(const uint8_t* raw, int p, int, uint32_t (&out)[32]) {
+    // the 64-value slab is Q8_0 blocks 0 and 1
+    const __half2 db = bq::u32_as_h2(*reinterpret_cast<const uint32_t*>(raw + 8192 + 4 * p));
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-        const uint4 q = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, 2 * h + c));
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    for (int h = 0; h < 2; ++h) {
+        const __half2 d = h ? __high2half2(db) : __low2half2(db);
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const uint32_t wx = w[m] ^ 0x80808080u;
-            out[8 * c + 2 * m] = bq::h2_as_u32(__hmul2(bq::s8pair_to_half2(wx, 0x4140u), d));
-            out[8 * c + 2 * m + 1] = bq::h2_as_u32(__hmul2(bq::s8pair_to_half2(wx, 0x4342u), d));
+        for (int c = 0; c < 2; ++c) {
+            const uint4 q = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, 2 * h + c));
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t wx = w[m] ^ 0x80808080u;
+                out[16 * h + 8 * c + 2 * m] = bq::h2_as_u32(__hmul2(bq::s8pair_to_half2(wx, 0x4140u), d));
+                out[16 * h + 8 * c + 2 * m + 1] = bq::h2_as_u32(__hmul2(bq::s8pair_to_half2(wx, 0x4342u), d));
+            }
         }
     }
 }
 
 template <>
-__device__ __forceinline__ void dequant_half<BQ_FMT_Q2_K>(const uint8_t* raw, int p, int sub, int h,
-                                                          uint32_t (&out)[16]) {
-    // stage `sub` of the super-block = sub-blocks 4sub..4sub+3; half h = two of them
-    const uint2 q = *reinterpret_cast<const uint2*>(raw + bq::quant_chunk_offset(p, sub) + 8 * h);
-    const uint32_t sc2 = *reinterpret_cast<const uint16_t*>(raw + 8192 + 512 * sub + 4 * p + 2 * h);
+__device__ __forceinline__ void dequant_stage<BQ_FMT_Q2_K>(const uint8_t* raw, int p, int sub, uint32_t (&out)[32]) {
+    // stage `sub` of the super-block = 16-value sub-blocks 4sub..4sub+3, one u32 of codes each
+    const uint4 q = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, sub));
+    const uint32_t sc4 = *reinterpret_cast<const uint32_t*>(raw + 8192 + 512 * sub + 4 * p);
     const __half2 dm = bq::u32_as_h2(*reinterpret_cast<const uint32_t*>(raw + 10240 + 4 * p));
-    const float d = __low2float(dm), dmin = __high2float(dm);
-    const uint32_t w[2] = {q.x, q.y};
+    const __half2 d2 = __low2half2(dm), nmin2 = __hneg2(__high2half2(dm));
+    // (d*sc, -dmin*m) of two sub-blocks per half2: the fp16 product of two exact
+    // fp16 operands is the product rounded once
+    __half2 ds[2], nm[2];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const uint32_t scb = (sc2 >> (8 * i)) & 0xFFu;
-        const __half ds = __float2half_rn(d * (float)(scb & 15u));
-        const __half ndm = __float2half_rn(-dmin * (float)(scb >> 4));
-        const __half2 ds2 = __halves2half2(ds, ds), ndm2 = __halves2half2(ndm, ndm);
+    for (int j = 0; j < 2; ++j) {
+        const uint32_t s = __byte_perm(sc4, 0u, j ? 0x4342u : 0x4140u);   // bytes 2j, 2j+1 -> lanes
+        ds[j] = __hmul2_rn(d2, field_to_half2<0>(s, 0x000F000Fu));
+        nm[j] = __hmul2_rn(nmin2, field_to_half2<4>(s, 0x000F000Fu));
+    }
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int qq = 0; qq < 8; ++qq)
-            out[8 * i + qq] = bq::h2_as_u32(__hfma2(bq::codes_to_half2((w[i] >> (2 * qq)) & 0x00030003u), ds2, ndm2));
+    for (int i = 0; i < 4; ++i) {
+        const __half2 s2 = (i & 1) ? __high2half2(ds[i >> 1]) : __low2half2(ds[i >> 1]);
+        const __half2 m2 = (i & 1) ? __high2half2(nm[i >> 1]) : __low2half2(nm[i >> 1]);
+        // value 2qq at bits 2qq, value 2qq+1 at bits 16+2qq
+        const uint32_t hi = w[i] >> 10;
+        out[8 * i + 0] = bq::h2_as_u32(__hfma2(field_to_half2<0>(w[i], 0x00030003u), s2, m2));
+        out[8 * i + 1] = bq::h2_as_u32(__hfma2(field_to_half2<2>(w[i], 0x00030003u), s2, m2));
+        out[8 * i + 2] = bq::h2_as_u32(__hfma2(field_to_half2<4>(w[i], 0x00030003u), s2, m2));
+        out[8 * i + 3] = bq::h2_as_u32(__hfma2(field_to_half2<6>(w[i], 0x00030003u), s2, m2));
+        out[8 * i + 4] = bq::h2_as_u32(__hfma2(field_to_half2<8>(w[i], 0x00030003u), s2, m2));
+        out[8 * i + 5] = bq::h2_as_u32(__hfma2(field_to_half2<0>(hi, 0x00030003u), s2, m2));
+        out[8 * i + 6] = bq::h2_as_u32(__hfma2(field_to_half2<2>(hi, 0x00030003u), s2, m2));
+        out[8 * i + 7] = bq::h2_as_u32(__hfma2(field_to_half2<4>(hi, 0x00030003u), s2, m2));
     }
 }
 
 template <>
-__device__ __forceinline__ void dequant_half<BQ_FMT_INT4_G64>(const uint8_t* raw, int p, int sub, int h,
-                                                              uint32_t (&out)[16]) {
-    // stage `sub` = K group `sub` of the 128-value slab; half h = chunk 2sub + h
-    const uint4 q = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, 2 * sub + h));
+__device__ __forceinline__ void dequant_stage<BQ_FMT_INT4_G64>(const uint8_t* raw, int p, int sub,
+                                                               uint32_t (&out)[32]) {
+    // stage `sub` = K group `sub` of the 128-value slab = chunks 2sub, 2sub+1
     const __half2 sb = bq::u32_as_h2(*reinterpret_cast<const uint32_t*>(raw + 8192 + 512 * sub + 4 * p));
     const __half2 s2 = __low2half2(sb), b2 = __high2half2(sb);
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-    for (int m = 0; m < 4; ++m)
+    for (int h = 0; h < 2; ++h) {
+        const uint4 q = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, 2 * sub + h));
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq)
-            out[4 * m + qq] = bq::h2_as_u32(__hfma2(bq::codes_to_half2((w[m] >> (4 * qq)) & 0x000F000Fu), s2, b2));
+        for (int m = 0; m < 4; ++m) {
+            // value 2qq at bits 4qq, value 2qq+1 at bits 16+4qq
+            const uint32_t hi = w[m] >> 8;
+            out[16 * h + 4 * m + 0] = bq::h2_as_u32(__hfma2(field_to_half2<0>(w[m], 0x000F000Fu), s2, b2));
+            out[16 * h + 4 * m + 1] = bq::h2_as_u32(__hfma2(field_to_half2<4>(w[m], 0x000F000Fu), s2, b2));
+            out[16 * h + 4 * m + 2] = bq::h2_as_u32(__hfma2(field_to_half2<0>(hi, 0x000F000Fu), s2, b2));
+            out[16 * h + 4 * m + 3] = bq::h2_as_u32(__hfma2(field_to_half2<4>(hi, 0x000F000Fu), s2, b2));
+        }
+    }
 }
 
 __device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
@@ -291,14 +332,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
     uint8_t* b_ring = smem;
     uint8_t* raw_ring = smem + kBBoxes * kBoxBytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(raw_ring + kRawSlabs * kRawStride);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(raw_ring + kRawBytes);
     const uint32_t bar0 = smem_u32(bars);
     auto b_full = [&](int s) { return bar0 + 8u * s; };
     auto b_empty = [&](int s) { return bar0 + 8u * (kMaxStagesB + s); };
     auto raw_full = [&](int r) { return bar0 + 8u * (2 * kMaxStagesB + r); };
-    auto raw_empty = [&](int r) { return bar0 + 8u * (2 * kMaxStagesB + kRawSlabs + r); };
-    auto a_full = [&](int s) { return bar0 + 8u * (2 * kMaxStagesB + 2 * kRawSlabs + s); };
-    auto a_empty = [&](int s) { return bar0 + 8u * (2 * kMaxStagesB + 2 * kRawSlabs + kMaxStagesA + s); };
+    auto raw_empty = [&](int r) { return bar0 + 8u * (2 * kMaxStagesB + kMaxRawSlabs + r); };
+    auto a_full = [&](int s) { return bar0 + 8u * (2 * kMaxStagesB + 2 * kMaxRawSlabs + s); };
+    auto a_empty = [&](int s) { return bar0 + 8u * (2 * kMaxStagesB + 2 * kMaxRawSlabs + kMaxStagesA + s); };
     const uint32_t acc_full = bar0 + 8u * (kNumBars - 1);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
     volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -325,7 +366,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
     // ring depths for this tile
     const int stages_b = min(kMaxStagesB, kBBoxes / n_boxes);
     const uint32_t acc_cols = (uint32_t)((n_mma + 31) & ~31);
-    const int stages_a = min(kMaxStagesA, (int)((kTmemCols - acc_cols) / 32));
+    const int stages_a = min(kMaxStagesA, (int)((kTmemCols - acc_cols) / 32)) & ~1;   // >= 2: acc_cols <= 160
     const int rt = blockIdx.x;
     const int n_tiles_w = a.n / bq::kTileRows, k_slabs = a.k / F::SK;
     const uint8_t* wslab = a.w + bq::slab_index(expert, rt, 0, n_tiles_w, k_slabs) * F::SB;
@@ -334,8 +375,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kMaxStagesB; ++i) { mbar_init(b_full(i), 1); mbar_init(b_empty(i), 1); }
-        for (int i = 0; i < kRawSlabs; ++i) { mbar_init(raw_full(i), 1); mbar_init(raw_empty(i), kConvWarps); }
-        for (int i = 0; i < kMaxStagesA; ++i) { mbar_init(a_full(i), kConvWarps); mbar_init(a_empty(i), 1); }
+        // a slab of one stage is read by the 4 warps of that stage's parity, longer slabs by all 8
+        for (int i = 0; i < F::NR; ++i) { mbar_init(raw_full(i), 1); mbar_init(raw_empty(i), F::SPS == 1 ? 4 : 8); }
+        for (int i = 0; i < kMaxStagesA; ++i) { mbar_init(a_full(i), 4); mbar_init(a_empty(i), 1); }
         mbar_init(acc_full, 1);
         *abort_flag = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -381,16 +423,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
             uint32_t ph = 0;
             bool ok = true;
             for (int kt = 0; kt < k_slabs; ++kt) {
-                if (kt >= kRawSlabs && !(ok = mbar_wait(raw_empty(r), ph ^ 1u, abort_flag, a.status))) break;
+                if (kt >= F::NR && !(ok = mbar_wait(raw_empty(r), ph ^ 1u, abort_flag, a.status))) break;
                 mbar_expect_tx(raw_full(r), F::SB);
-                bulk_load(smem_u32(raw_ring + r * kRawStride), wslab + (int64_t)kt * F::SB, F::SB, raw_full(r));
+                bulk_load(smem_u32(raw_ring + r * F::SB), wslab + (int64_t)kt * F::SB, F::SB, raw_full(r));
                 ++issued;
-                if (++r == kRawSlabs) { r = 0; ph ^= 1u; }
+                if (++r == F::NR) { r = 0; ph ^= 1u; }
             }
             if (!ok) {
                 volatile uint32_t no_abort = 0;
-                for (int u = max(0, issued - kRawSlabs); u < issued; ++u)
-                    mbar_wait(raw_full(u % kRawSlabs), (u / kRawSlabs) & 1, &no_abort, a.status);
+                for (int u = max(0, issued - F::NR); u < issued; ++u)
+                    mbar_wait(raw_full(u % F::NR), (u / F::NR) & 1, &no_abort, a.status);
             }
         }
     } else if (warp == 1) {
@@ -427,26 +469,28 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
         const int p = 32 * quarter + lane;                       // weight row = TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
         bool ok = true;
-        int sa = 0, r = 0, sub = 0;
-        uint32_t pa = 0, pr = 0;
-        for (int ks = 0; ks < KS; ++ks) {
-            if (sub == 0 && !(ok = warp_wait(raw_full(r), pr, abort_flag, a.status))) break;
+        // this warp converts stages ks = half, half + 2, ...; A-ring slot and pass parity of ks
+        int sa = half;
+        uint32_t pa = 0;
+        for (int ks = half; ks < KS; ks += 2) {
+            const int kt = ks / F::SPS, sub = ks % F::SPS, r = kt % F::NR;
+            const uint32_t pr = (uint32_t)(kt / F::NR) & 1u;
+            // first stage of the slab this warp converts: wait for the slab
+            if ((F::SPS == 1 || sub == half) && !(ok = warp_wait(raw_full(r), pr, abort_flag, a.status))) break;
             if (ks >= stages_a && !(ok = warp_wait(a_empty(sa), pa ^ 1u, abort_flag, a.status))) break;
-            uint32_t v[16];
-            dequant_half<FMT>(raw_ring + r * kRawStride, p, sub, half, v);
-            tmem_st16(tmem + lane_base + a_col0 + 32u * sa + 16u * half, v);
+            uint32_t v[32];
+            dequant_stage<FMT>(raw_ring + r * F::SB, p, sub, v);
+            tmem_st32(tmem + lane_base + a_col0 + 32u * sa, v);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                if (sub == F::SPS - 1) mbar_arrive(raw_empty(r));
+                // last stage of the slab this warp converts: release it
+                if (F::SPS == 1 || sub >= F::SPS - 2) mbar_arrive(raw_empty(r));
                 mbar_arrive(a_full(sa));
             }
-            if (++sa == stages_a) { sa = 0; pa ^= 1u; }
-            if (++sub == F::SPS) {
-                sub = 0;
-                if (++r == kRawSlabs) { r = 0; pr ^= 1u; }
-            }
+            sa += 2;
+            if (sa >= stages_a) { sa -= stages_a; pa ^= 1u; }
         }
         if (ok && warp_wait(acc_full, 0, abort_flag, a.status)) {
             tc_fence_after();
