@@ -58,7 +58,12 @@ constexpr int kThreads = 32 * (kFirstConvWarp + kConvWarps);
 constexpr uint32_t kTmemCols = 256;
 constexpr int kBoxBytes = kBoxRows * 128;
 constexpr int kRawBytes = 34816;   // raw slab ring: 4 Q8_0 / 3 Q2_K / 3 int4 slabs
-constexpr int kNumBars = 2 * kMaxStagesB + 2 * kMaxRawSlabs + 2 * kMaxStagesA + 1;
+// One "stage consumed" barrier per K stage, in a ring of 16 (a commit of the
+// MMAs of stage ks arrives on it; the converters and the activation producer
+// wait on it before reusing the A or B slot of that stage).
+constexpr int kEmptyRing = 16;
+static_assert(kMaxStagesA <= kEmptyRing && kMaxStagesB < kEmptyRing && kEmptyRing % 2 == 0, "empty ring");
+constexpr int kNumBars = kMaxStagesB + 2 * kMaxRawSlabs + kMaxStagesA + kEmptyRing + 1;
 constexpr int kSmemBytes = 1024 + kBBoxes * kBoxBytes + kRawBytes + 8 * kNumBars + 64;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
 
@@ -139,6 +144,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
             return false;
         }
     }
+}
+
+// Bounded wait for two barriers.  Both are tested at once first, so when they
+// are already complete the thread pays one test latency, not two.
+__device__ __forceinline__ bool mbar_wait2(uint32_t bar0, uint32_t parity0, uint32_t bar1, uint32_t parity1,
+                                           volatile uint32_t* abort_flag, int32_t* status) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p, q;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 q, [%3], %4;\n"
+        " and.pred p, p, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(bar0), "r"(parity0), "r"(bar1), "r"(parity1) : "memory");
+    return ok != 0 || (mbar_wait(bar0, parity0, abort_flag, status) && mbar_wait(bar1, parity1, abort_flag, status));
 }
 
 // Warp-uniform bounded wait: lane 0 polls, every lane gets its verdict.
@@ -335,11 +354,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
     uint64_t* bars = reinterpret_cast<uint64_t*>(raw_ring + kRawBytes);
     const uint32_t bar0 = smem_u32(bars);
     auto b_full = [&](int s) { return bar0 + 8u * s; };
-    auto b_empty = [&](int s) { return bar0 + 8u * (kMaxStagesB + s); };
-    auto raw_full = [&](int r) { return bar0 + 8u * (2 * kMaxStagesB + r); };
-    auto raw_empty = [&](int r) { return bar0 + 8u * (2 * kMaxStagesB + kMaxRawSlabs + r); };
-    auto a_full = [&](int s) { return bar0 + 8u * (2 * kMaxStagesB + 2 * kMaxRawSlabs + s); };
-    auto a_empty = [&](int s) { return bar0 + 8u * (2 * kMaxStagesB + 2 * kMaxRawSlabs + kMaxStagesA + s); };
+    auto raw_full = [&](int r) { return bar0 + 8u * (kMaxStagesB + r); };
+    auto raw_empty = [&](int r) { return bar0 + 8u * (kMaxStagesB + kMaxRawSlabs + r); };
+    auto a_full = [&](int s) { return bar0 + 8u * (kMaxStagesB + 2 * kMaxRawSlabs + s); };
+    // consumption of stage j: barrier j % 16, phase parity (j / 16) % 2
+    auto empty = [&](int j) { return bar0 + 8u * (kMaxStagesB + 2 * kMaxRawSlabs + kMaxStagesA + (j & (kEmptyRing - 1))); };
+    auto empty_parity = [](int j) { return (uint32_t)(j / kEmptyRing) & 1u; };
     const uint32_t acc_full = bar0 + 8u * (kNumBars - 1);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
     volatile uint32_t* abort_flag = tmem_slot + 1;
@@ -374,10 +394,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kMaxStagesB; ++i) { mbar_init(b_full(i), 1); mbar_init(b_empty(i), 1); }
+        for (int i = 0; i < kMaxStagesB; ++i) mbar_init(b_full(i), 1);
+        for (int j = 0; j < kEmptyRing; ++j) mbar_init(empty(j), 1);
         // a slab of one stage is read by the 4 warps of that stage's parity, longer slabs by all 8
         for (int i = 0; i < F::NR; ++i) { mbar_init(raw_full(i), 1); mbar_init(raw_empty(i), F::SPS == 1 ? 4 : 8); }
-        for (int i = 0; i < kMaxStagesA; ++i) { mbar_init(a_full(i), 4); mbar_init(a_empty(i), 1); }
+        for (int i = 0; i < kMaxStagesA; ++i) mbar_init(a_full(i), 4);
         mbar_init(acc_full, 1);
         *abort_flag = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -398,17 +419,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap_b)) : "memory");
             int issued = 0, s = 0;
-            uint32_t ph = 0;   // parity of the current pass over the ring
             bool ok = true;
             const uint32_t stage_bytes = n_boxes * kBoxBytes;
             for (int ks = 0; ks < KS; ++ks) {
-                if (ks >= stages_b && !(ok = mbar_wait(b_empty(s), ph ^ 1u, abort_flag, a.status))) break;
+                if (ks >= stages_b &&
+                    !(ok = mbar_wait(empty(ks - stages_b), empty_parity(ks - stages_b), abort_flag, a.status)))
+                    break;
                 mbar_expect_tx(b_full(s), stage_bytes);
                 const uint32_t dst = smem_u32(b_ring) + s * stage_bytes;
                 for (int bx = 0; bx < n_boxes; ++bx)
                     tma_load_2d(dst + bx * kBoxBytes, &tmap_b, ks * BK, row0 + bx * kBoxRows, b_full(s));
                 ++issued;
-                if (++s == stages_b) { s = 0; ph ^= 1u; }
+                if (++s == stages_b) s = 0;
             }
             if (!ok) {   // let our own copies land before the CTA leaves (bounded)
                 volatile uint32_t no_abort = 0;
@@ -449,15 +471,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
             uint32_t at = tmem + a_col0;
             bool ok = true;
             for (int ks = 0; ks < KS; ++ks) {
-                if (!(ok = mbar_wait(a_full(sa), pa, abort_flag, a.status))) break;
-                if (!(ok = mbar_wait(b_full(sb), pb, abort_flag, a.status))) break;
+                if (!(ok = mbar_wait2(a_full(sa), pa, b_full(sb), pb, abort_flag, a.status))) break;
                 tc_fence_after();
                 mma_f16_ts(tmem, at, bd, idesc, ks != 0);
                 mma_f16_ts(tmem, at + 8u, bd + 2u, idesc, 1u);      // +32 bytes along K
                 mma_f16_ts(tmem, at + 16u, bd + 4u, idesc, 1u);
                 mma_f16_ts(tmem, at + 24u, bd + 6u, idesc, 1u);
-                mma_commit(a_empty(sa));
-                mma_commit(b_empty(sb));
+                mma_commit(empty(ks));   // releases the stage's A and B slots
                 if (++sa == stages_a) { sa = 0; pa ^= 1u; at = tmem + a_col0; } else { at += 32u; }
                 if (++sb == stages_b) { sb = 0; pb ^= 1u; bd = b_desc0; } else { bd += b_step; }
             }
@@ -469,15 +489,16 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
         const int p = 32 * quarter + lane;                       // weight row = TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
         bool ok = true;
-        // this warp converts stages ks = half, half + 2, ...; A-ring slot and pass parity of ks
+        // this warp converts stages ks = half, half + 2, ...; sa = A-ring slot of ks
         int sa = half;
-        uint32_t pa = 0;
         for (int ks = half; ks < KS; ks += 2) {
             const int kt = ks / F::SPS, sub = ks % F::SPS, r = kt % F::NR;
             const uint32_t pr = (uint32_t)(kt / F::NR) & 1u;
             // first stage of the slab this warp converts: wait for the slab
             if ((F::SPS == 1 || sub == half) && !(ok = warp_wait(raw_full(r), pr, abort_flag, a.status))) break;
-            if (ks >= stages_a && !(ok = warp_wait(a_empty(sa), pa ^ 1u, abort_flag, a.status))) break;
+            if (ks >= stages_a &&
+                !(ok = warp_wait(empty(ks - stages_a), empty_parity(ks - stages_a), abort_flag, a.status)))
+                break;
             uint32_t v[32];
             dequant_stage<FMT>(raw_ring + r * F::SB, p, sub, v);
             tmem_st32(tmem + lane_base + a_col0 + 32u * sa, v);
@@ -490,7 +511,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
                 mbar_arrive(a_full(sa));
             }
             sa += 2;
-            if (sa >= stages_a) { sa -= stages_a; pa ^= 1u; }
+            if (sa >= stages_a) sa -= stages_a;
         }
         if (ok && warp_wait(acc_full, 0, abort_flag, a.status)) {
             tc_fence_after();
