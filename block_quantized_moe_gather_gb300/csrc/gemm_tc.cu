@@ -121,6 +121,17 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same test, but a thread whose phase has not completed may be suspended
+// in hardware (woken when the phase completes, or after at most 0.1 ms), so
+// waiting warps stop taking issue slots from the warps that do the work.
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(bar), "r"(parity), "r"(100000u) : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -136,7 +147,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
-            if (mbar_try(bar, parity)) return true;
+            if (mbar_try_sleep(bar, parity)) return true;
         if (*abort_flag) return false;
         if (global_ns() - t0 > kWaitLimitNs) {
             *abort_flag = 1u;
@@ -146,18 +157,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
-// Bounded wait for two barriers.  Both are tested at once first, so when they
-// are already complete the thread pays one test latency, not two.
-__device__ __forceinline__ bool mbar_wait2(uint32_t bar0, uint32_t parity0, uint32_t bar1, uint32_t parity1,
-                                           volatile uint32_t* abort_flag, int32_t* status) {
+// Non-blocking test of four barriers at once (one test latency, not four).
+__device__ __forceinline__ bool mbar_test4(const uint32_t (&bar)[4], const uint32_t (&parity)[4]) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p, q;\n"
-        " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " mbarrier.test_wait.parity.shared::cta.b64 q, [%3], %4;\n"
-        " and.pred p, p, q;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok) : "r"(bar0), "r"(parity0), "r"(bar1), "r"(parity1) : "memory");
-    return ok != 0 || (mbar_wait(bar0, parity0, abort_flag, status) && mbar_wait(bar1, parity1, abort_flag, status));
+        "{\n .reg .pred p0, p1, p2, p3;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 p0, [%1], %5;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 p1, [%2], %6;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 p2, [%3], %7;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 p3, [%4], %8;\n"
+        " and.pred p0, p0, p1;\n and.pred p2, p2, p3;\n and.pred p0, p0, p2;\n"
+        " selp.u32 %0, 1, 0, p0;\n}\n"
+        : "=r"(ok)
+        : "r"(bar[0]), "r"(bar[1]), "r"(bar[2]), "r"(bar[3]), "r"(parity[0]), "r"(parity[1]), "r"(parity[2]),
+          "r"(parity[3])
+        : "memory");
+    return ok != 0;
 }
 
 // Warp-uniform bounded wait: lane 0 polls, every lane gets its verdict.
@@ -470,16 +485,35 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
             uint64_t bd = b_desc0;
             uint32_t at = tmem + a_col0;
             bool ok = true;
-            for (int ks = 0; ks < KS; ++ks) {
-                if (!(ok = mbar_wait2(a_full(sa), pa, b_full(sb), pb, abort_flag, a.status))) break;
+            // With six A slots (tiles of up to 64 tokens), stages are taken two at
+            // a time: the A and B barriers of both are tested together, so a pair
+            // that is ready costs one barrier-test latency (a few hundred cycles
+            // here) while the converters keep filling the other four slots.
+            // With fewer slots the pairing starves the converters (measured).
+            const int batch = stages_a >= 6 ? 2 : 1;
+            for (int ks = 0; ks < KS;) {
+                const int nq = min(batch, KS - ks);
+                const int sa1 = sa + 1 == stages_a ? 0 : sa + 1, sb1 = sb + 1 == stages_b ? 0 : sb + 1;
+                uint32_t bars[4] = {a_full(sa), b_full(sb), a_full(sa), b_full(sb)};
+                uint32_t pars[4] = {pa, pb, pa, pb};
+                if (nq == 2) {
+                    bars[2] = a_full(sa1); pars[2] = sa1 == 0 ? pa ^ 1u : pa;
+                    bars[3] = b_full(sb1); pars[3] = sb1 == 0 ? pb ^ 1u : pb;
+                }
+                if (!mbar_test4(bars, pars)) {
+                    for (int q = 0; ok && q < 2 * nq; ++q) ok = mbar_wait(bars[q], pars[q], abort_flag, a.status);
+                    if (!ok) break;
+                }
                 tc_fence_after();
-                mma_f16_ts(tmem, at, bd, idesc, ks != 0);
-                mma_f16_ts(tmem, at + 8u, bd + 2u, idesc, 1u);      // +32 bytes along K
-                mma_f16_ts(tmem, at + 16u, bd + 4u, idesc, 1u);
-                mma_f16_ts(tmem, at + 24u, bd + 6u, idesc, 1u);
-                mma_commit(empty(ks));   // releases the stage's A and B slots
-                if (++sa == stages_a) { sa = 0; pa ^= 1u; at = tmem + a_col0; } else { at += 32u; }
-                if (++sb == stages_b) { sb = 0; pb ^= 1u; bd = b_desc0; } else { bd += b_step; }
+                for (int q = 0; q < nq; ++q, ++ks) {
+                    mma_f16_ts(tmem, at, bd, idesc, ks != 0);
+                    mma_f16_ts(tmem, at + 8u, bd + 2u, idesc, 1u);      // +32 bytes along K
+                    mma_f16_ts(tmem, at + 16u, bd + 4u, idesc, 1u);
+                    mma_f16_ts(tmem, at + 24u, bd + 6u, idesc, 1u);
+                    mma_commit(empty(ks));   // releases the stage's A and B slots
+                    if (++sa == stages_a) { sa = 0; pa ^= 1u; at = tmem + a_col0; } else { at += 32u; }
+                    if (++sb == stages_b) { sb = 0; pb ^= 1u; bd = b_desc0; } else { bd += b_step; }
+                }
             }
             if (ok) mma_commit(acc_full);
         }
