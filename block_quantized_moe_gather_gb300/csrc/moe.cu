@@ -19,6 +19,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "gemm_internal.cuh"
 #include "moe_internal.cuh"
@@ -178,6 +179,38 @@ bq_status validate_moe(const bq_moe_desc* d) {
     return BQ_OK;
 }
 
+// Per-device side stream and fork/join events on which the decode path runs
+// the shared expert next to the routed experts (created on first use, kept
+// for the life of the process).  Calls from several host threads take the
+// mutex around the record/wait pairs, so each join waits for its own fork.
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+SideStream g_side[64];
+std::mutex g_side_mutex;
+
+// The current device's side stream, or nullptr if it cannot be created (the
+// caller then runs everything on its own stream).  Call with g_side_mutex held.
+SideStream* side_stream() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    SideStream& ss = g_side[dev];
+    if (!ss.stream) {
+        cudaStream_t s = nullptr;
+        cudaEvent_t f = nullptr, j = nullptr;
+        if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+        if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess) {
+            if (f) cudaEventDestroy(f);
+            cudaStreamDestroy(s);
+            return nullptr;
+        }
+        ss.stream = s; ss.fork = f; ss.join = j;
+    }
+    return &ss;
+}
+
 // One dense weight over `m` rows of x (single segment).
 bq::QgemvParams dense_params(const bq_qweight* w, int m, const __half* x, float* y, __half* h, int ldy,
                              int ksplit = 1, float* partial = nullptr, int32_t* counters = nullptr) {
@@ -253,6 +286,32 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
     const int max_segments = min(E, P);
     const bool decode = T <= 8 || !bq::gemm_supported(d->w_gate_up.fmt);
 
+    // Decode: the shared expert's two GEMVs run on a side stream, concurrently
+    // with the routed experts (neither fills the GPU at these sizes); the
+    // combine waits for both.
+    int accumulate = 0;
+    std::unique_lock<std::mutex> side_lock;
+    SideStream* side = nullptr;
+    if (d->shared_gate_up && T <= 8) {
+        side_lock = std::unique_lock<std::mutex>(g_side_mutex);
+        side = side_stream();
+        cudaStream_t ss = st;
+        if (side && cudaEventRecord(side->fork, st) == cudaSuccess &&
+            cudaStreamWaitEvent(side->stream, side->fork, 0) == cudaSuccess)
+            ss = side->stream;
+        else
+            side = nullptr;
+        bq::stage_begin(BQ_STAGE_SHARED, ss);
+        bq::launch_qgemv(dense_params(d->shared_gate_up, T, xh, nullptr, w.h_shared, 0, w.ks_sgu, w.part_sgu,
+                                      w.cnt_sgu), 1, ss);
+        bq::launch_qgemv(dense_params(d->shared_down, T, w.h_shared, y, nullptr, H, w.ks_sd, w.part_sd, w.cnt_sd),
+                         1, ss);
+        bq::stage_end(BQ_STAGE_SHARED, ss);
+        if (side && cudaEventRecord(side->join, ss) != cudaSuccess)
+            return bq::fail(BQ_ERR_CUDA, "bq_moe_gather_qmm: cudaEventRecord on the side stream failed");
+        accumulate = 1;
+    }
+
     if (decode) {
         bq::QgemvParams gu{};
         gu.w = static_cast<const uint8_t*>(d->w_gate_up.data);
@@ -278,8 +337,7 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
             return s;
     }
 
-    int accumulate = 0;
-    if (d->shared_gate_up) {
+    if (d->shared_gate_up && !accumulate) {
         const int Is = d->shared_gate_up->n / 2;
         bq::stage_begin(BQ_STAGE_SHARED, st);
         if (T <= 8 || !bq::gemm_supported(d->shared_gate_up->fmt)) {
@@ -294,6 +352,11 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
         }
         bq::stage_end(BQ_STAGE_SHARED, st);
         accumulate = 1;
+    }
+    if (side) {
+        if (cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess)
+            return bq::fail(BQ_ERR_CUDA, "bq_moe_gather_qmm: cudaStreamWaitEvent on the side stream failed");
+        side_lock.unlock();
     }
     const int64_t total = (int64_t)T * (H / 4);
     const int grid = (int)std::min<int64_t>((total + 255) / 256, 152 * 8);

@@ -84,30 +84,80 @@ __device__ __forceinline__ void load_frag(Frag<FMT>& f, const uint8_t* slab, int
         }
 }
 
+// Exact small integers from bit fields without shifting: a field at bit J
+// of each 16-bit lane is ORed into the mantissa of 2^(10-J), where it has
+// weight 1; subtracting 2^(10-J) leaves its value.
+template <int J>
+__device__ __forceinline__ __half2 field_h2(uint32_t w, uint32_t mask) {
+    constexpr uint32_t e = (uint32_t)(25 - J) << 10;   // biased exponent of 2^(10-J)
+    return __hsub2(bq::u32_as_h2((w & (mask << J)) | e | (e << 16)), bq::u32_as_h2(e | (e << 16)));
+}
+
+// Pair p (values 2p, 2p+1 of a 16-value Q2_K sub-block word): bits 2p of each
+// lane; pairs 5-7 are read from the word shifted right by 10.
+__device__ __forceinline__ __half2 q2_pair(uint32_t w, int p) {
+    switch (p) {
+        case 0: return field_h2<0>(w, 0x00030003u);
+        case 1: return field_h2<2>(w, 0x00030003u);
+        case 2: return field_h2<4>(w, 0x00030003u);
+        case 3: return field_h2<6>(w, 0x00030003u);
+        case 4: return field_h2<8>(w, 0x00030003u);
+        case 5: return field_h2<0>(w >> 10, 0x00030003u);
+        case 6: return field_h2<2>(w >> 10, 0x00030003u);
+        default: return field_h2<4>(w >> 10, 0x00030003u);
+    }
+}
+
+// Pair p of an int4 word: nibble p of each lane (p >= 2 from the word >> 8).
+__device__ __forceinline__ __half2 q4_pair(uint32_t w, int p) {
+    switch (p) {
+        case 0: return field_h2<0>(w, 0x000F000Fu);
+        case 1: return field_h2<4>(w, 0x000F000Fu);
+        case 2: return field_h2<0>(w >> 8, 0x000F000Fu);
+        default: return field_h2<4>(w >> 8, 0x000F000Fu);
+    }
+}
+
+// Q2_K (d*sc, -dmin*m) of the lane's four sub-blocks of one row, as fp16
+// pairs [sub-blocks 0,1] and [2,3]: fp16 products of exact operands, rounded once.
+struct Q2Scales {
+    __half2 ds[2], nm[2];
+};
+
+__device__ __forceinline__ Q2Scales q2_scales(uint32_t sc4, uint32_t dm) {
+    Q2Scales r;
+    const __half2 dmh = bq::u32_as_h2(dm);
+    const __half2 d2 = __low2half2(dmh), nmin2 = __hneg2(__high2half2(dmh));
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const uint32_t b = __byte_perm(sc4, 0u, j ? 0x4342u : 0x4140u);   // bytes 2j, 2j+1 -> lanes
+        r.ds[j] = __hmul2_rn(d2, field_h2<0>(b, 0x000F000Fu));
+        r.nm[j] = __hmul2_rn(nmin2, field_h2<4>(b, 0x000F000Fu));
+    }
+    return r;
+}
+
 // A-fragment register (pair of fp16 weights) for row half hh, pair `lohi`
-// (0: values 4s, 4s+1; 1: values 4s+2, 4s+3) of MMA step s.
+// (0: values 4s, 4s+1; 1: values 4s+2, 4s+3) of MMA step s.  `q2` holds the
+// Q2_K sub-block scales of [tile][hh] (unused for the other formats).
 template <int FMT>
-__device__ __forceinline__ uint32_t a_pair(const Frag<FMT>& f, int tile, int hh, int s, int lohi) {
+__device__ __forceinline__ uint32_t a_pair(const Frag<FMT>& f, const Q2Scales (&q2)[2][2], int tile, int hh, int s,
+                                           int lohi) {
     if (FMT == BQ_FMT_Q8_0) {
         const uint32_t w = comp(f.q[tile][hh], s) ^ 0x80808080u;
         const __half d = __ushort_as_half((uint16_t)f.sc[tile][hh]);
         const __half2 v = bq::s8pair_to_half2(w, lohi ? 0x4342u : 0x4140u);
         return bq::h2_as_u32(__hmul2(v, __halves2half2(d, d)));
     } else if (FMT == BQ_FMT_Q2_K) {
-        const uint32_t w = comp(f.q[tile][hh], s >> 2);
-        const int p = 2 * (s & 3) + lohi;
-        const uint32_t scb = (f.sc[tile][hh] >> (8 * (s >> 2))) & 0xFFu;
-        const __half2 dd = bq::u32_as_h2(f.dm[tile][hh]);
-        const __half ds = __float2half_rn(__low2float(dd) * (float)(scb & 15u));
-        const __half dmn = __float2half_rn(-__high2float(dd) * (float)(scb >> 4));
-        const __half2 q = bq::codes_to_half2((w >> (2 * p)) & 0x00030003u);
-        return bq::h2_as_u32(__hfma2(q, __halves2half2(ds, ds), __halves2half2(dmn, dmn)));
+        const int sb = s >> 2;   // sub-block of this step
+        const uint32_t w = comp(f.q[tile][hh], sb);
+        const __half2 ds = (sb & 1) ? __high2half2(q2[tile][hh].ds[sb >> 1]) : __low2half2(q2[tile][hh].ds[sb >> 1]);
+        const __half2 nm = (sb & 1) ? __high2half2(q2[tile][hh].nm[sb >> 1]) : __low2half2(q2[tile][hh].nm[sb >> 1]);
+        return bq::h2_as_u32(__hfma2(q2_pair(w, 2 * (s & 3) + lohi), ds, nm));
     } else {
         const uint32_t w = comp(f.q[tile][hh], s >> 1);
-        const int p = 2 * (s & 1) + lohi;
         const __half2 sb = bq::u32_as_h2(f.sc[tile][hh]);
-        const __half2 q = bq::codes_to_half2((w >> (4 * p)) & 0x000F000Fu);
-        return bq::h2_as_u32(__hfma2(q, __low2half2(sb), __high2half2(sb)));
+        return bq::h2_as_u32(__hfma2(q4_pair(w, 2 * (s & 1) + lohi), __low2half2(sb), __high2half2(sb)));
     }
 }
 
@@ -121,6 +171,13 @@ __device__ __forceinline__ void mma_frag(const Frag<FMT>& f, const __half* xq, b
     const uint4* xp = reinterpret_cast<const uint4*>(xq + (Traits<FMT>::SK / 4) * t);
 #pragma unroll
     for (int v = 0; v < XV; ++v) x[v] = xvalid ? __ldg(xp + v) : make_uint4(0, 0, 0, 0);
+    Q2Scales q2[2][2];
+    if (FMT == BQ_FMT_Q2_K) {
+#pragma unroll
+        for (int tile = 0; tile < 2; ++tile)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) q2[tile][hh] = q2_scales(f.sc[tile][hh], f.dm[tile][hh]);
+    }
 #pragma unroll
     for (int s = 0; s < Traits<FMT>::STEPS; ++s) {
         const uint4 xv = x[s >> 1];
@@ -129,10 +186,10 @@ __device__ __forceinline__ void mma_frag(const Frag<FMT>& f, const __half* xq, b
 #pragma unroll
         for (int tile = 0; tile < 2; ++tile) {
             uint32_t a[4];
-            a[0] = a_pair<FMT>(f, tile, 0, s, 0);
-            a[1] = a_pair<FMT>(f, tile, 1, s, 0);
-            a[2] = a_pair<FMT>(f, tile, 0, s, 1);
-            a[3] = a_pair<FMT>(f, tile, 1, s, 1);
+            a[0] = a_pair<FMT>(f, q2, tile, 0, s, 0);
+            a[1] = a_pair<FMT>(f, q2, tile, 1, s, 0);
+            a[2] = a_pair<FMT>(f, q2, tile, 0, s, 1);
+            a[3] = a_pair<FMT>(f, q2, tile, 1, s, 1);
             mma16816(acc[tile], a, b0, b1);
         }
     }

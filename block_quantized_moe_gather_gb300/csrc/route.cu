@@ -114,76 +114,92 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int32_t* warp_sums, i
 }
 
 // Whole routing front end for a small batch (T <= 32, T*k <= 256) in one
-// CTA: top-k per token, expert histogram, exclusive scan, stable
-// placement and the list of active experts.  Same results as the
-// multi-kernel path.  Optionally clears `out.zero` (split-K counters of the
-// GEMVs that follow).
+// CTA of 256 threads and two block barriers: top-k per token (warp w takes
+// tokens w, w + 8, ...), then every expert's count and offset and every
+// pair's rank among the pairs of its expert by direct counting over the at
+// most 256 pairs held in shared memory (cheaper than block scans at these
+// sizes), then the placement and the list of active experts.  Same results
+// as the multi-kernel path (the stable counting sort).  Optionally clears
+// `out.zero` (split-K counters of the GEMVs that follow).
+constexpr int kSmallThreads = 256;
+
 template <int NPER>
-__global__ void __launch_bounds__(1024)
+__global__ void __launch_bounds__(kSmallThreads)
 route_permute_small_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
                            bq::MoeRouting out, int32_t* status) {
     __shared__ int32_t s_ids[256];
-    __shared__ int32_t hist[1024];
-    __shared__ int32_t warp_sums[32];
+    __shared__ float s_gate[256];
+    __shared__ int32_t s_first[256];   // 1 if the pair is the first of its expert
+    __shared__ int32_t s_rank[256];    // rank among the earlier pairs of its expert
+    __shared__ int32_t s_off[1024];    // per expert: pairs with a smaller expert id
+    __shared__ int32_t s_cnt[1024];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int P = T * k;
-    hist[threadIdx.x] = 0;
-    for (int i = threadIdx.x; i < out.n_zero; i += blockDim.x) out.zero[i] = 0;
-    if (warp < T) {
+    for (int i = threadIdx.x; i < out.n_zero; i += kSmallThreads) out.zero[i] = 0;
+    for (int t = warp; t < T; t += kSmallThreads / 32) {
         int e;
         float w;
-        route_row<NPER>(logits + (int64_t)warp * E, bias, E, k, lane, e, w);
+        route_row<NPER>(logits + (int64_t)t * E, bias, E, k, lane, e, w);
         if (lane < k) {
-            const int f = warp * k + lane;
+            const int f = t * k + lane;
+            if (e < 0 || e >= E) {   // cannot happen for finite logits; reported, pair dropped
+                bq::set_device_error(status, BQ_DEV_BAD_EXPERT_ID);
+                e = -1;
+            }
             s_ids[f] = e;
+            s_gate[f] = w;
             out.ids[f] = e;
             out.gate[f] = w;
         }
     }
     __syncthreads();
-    const int f = threadIdx.x;
-    int e = -1;
-    if (f < P) {
-        e = s_ids[f];
-        if (e < 0 || e >= E) {
-            bq::set_device_error(status, BQ_DEV_BAD_EXPERT_ID);
-            e = -1;
-        } else {
-            atomicAdd(&hist[e], 1);
+    // per expert: count and number of pairs with a smaller id (the exclusive scan)
+    for (int x = threadIdx.x; x < E; x += kSmallThreads) {
+        int c = 0, less = 0;
+        for (int f = 0; f < P; ++f) {
+            const int e = s_ids[f];
+            c += e == x;
+            less += (e >= 0) & (e < x);
         }
-    }
-    __syncthreads();
-    const int x = threadIdx.x;
-    const int c = x < E ? hist[x] : 0;
-    int total = 0;
-    const int off = block_exclusive_scan(c, warp_sums, total);
-    int n_active = 0;
-    const int seg = block_exclusive_scan(c > 0 ? 1 : 0, warp_sums, n_active);
-    if (x < E) {
+        s_cnt[x] = c;
+        s_off[x] = less;
         out.counts[x] = c;
-        out.offsets[x] = off;
-        if (x == E - 1) out.offsets[E] = off + c;
-        if (c > 0) {
-            out.seg_expert[seg] = x;
-            out.seg_start[seg] = off;
-            out.seg_count[seg] = c;
-        }
-        hist[x] = off;
+        out.offsets[x] = less;
+        if (x == E - 1) out.offsets[E] = less + c;
     }
-    if (x == 0) *out.n_segments = n_active;
+    // per pair: rank among the earlier pairs of the same expert
+    if (threadIdx.x < P) {
+        const int f = threadIdx.x, e = s_ids[f];
+        int rank = 0;
+        for (int i = 0; i < f; ++i) rank += s_ids[i] == e;
+        s_rank[f] = rank;
+        s_first[f] = e >= 0 && rank == 0;
+    }
     __syncthreads();
-    if (f < P) {
+    if (threadIdx.x < P) {
+        const int f = threadIdx.x, e = s_ids[f];
         if (e < 0) {
             out.inv[f] = -1;
         } else {
-            int rank = 0;
-            for (int i = 0; i < f; ++i) rank += s_ids[i] == e;
-            const int r = hist[e] + rank;
+            const int r = s_off[e] + s_rank[f];
             out.perm_token[r] = f / k;
             out.perm_slot[r] = f % k;
-            out.perm_gate[r] = out.gate[f];
+            out.perm_gate[r] = s_gate[f];
             out.inv[f] = r;
+            if (s_first[f]) {
+                // segments in ascending expert order: index = active experts below e
+                int seg = 0;
+                for (int i = 0; i < P; ++i) seg += s_first[i] & (s_ids[i] < e);
+                out.seg_expert[seg] = e;
+                out.seg_start[seg] = s_off[e];
+                out.seg_count[seg] = s_cnt[e];
+            }
         }
+    }
+    if (threadIdx.x == 0) {
+        int n = 0;
+        for (int i = 0; i < P; ++i) n += s_first[i];
+        *out.n_segments = n;
     }
 }
 
@@ -332,12 +348,12 @@ void launch_route_permute_small(const float* logits, const float* bias, int T, i
                                 cudaStream_t st) {
     note_launch();
     int32_t* status = device_status_ptr();
-    if (E <= 32) route_permute_small_kernel<1><<<1, 1024, 0, st>>>(logits, bias, T, E, k, out, status);
-    else if (E <= 64) route_permute_small_kernel<2><<<1, 1024, 0, st>>>(logits, bias, T, E, k, out, status);
-    else if (E <= 128) route_permute_small_kernel<4><<<1, 1024, 0, st>>>(logits, bias, T, E, k, out, status);
-    else if (E <= 256) route_permute_small_kernel<8><<<1, 1024, 0, st>>>(logits, bias, T, E, k, out, status);
-    else if (E <= 512) route_permute_small_kernel<16><<<1, 1024, 0, st>>>(logits, bias, T, E, k, out, status);
-    else route_permute_small_kernel<32><<<1, 1024, 0, st>>>(logits, bias, T, E, k, out, status);
+    if (E <= 32) route_permute_small_kernel<1><<<1, kSmallThreads, 0, st>>>(logits, bias, T, E, k, out, status);
+    else if (E <= 64) route_permute_small_kernel<2><<<1, kSmallThreads, 0, st>>>(logits, bias, T, E, k, out, status);
+    else if (E <= 128) route_permute_small_kernel<4><<<1, kSmallThreads, 0, st>>>(logits, bias, T, E, k, out, status);
+    else if (E <= 256) route_permute_small_kernel<8><<<1, kSmallThreads, 0, st>>>(logits, bias, T, E, k, out, status);
+    else if (E <= 512) route_permute_small_kernel<16><<<1, kSmallThreads, 0, st>>>(logits, bias, T, E, k, out, status);
+    else route_permute_small_kernel<32><<<1, kSmallThreads, 0, st>>>(logits, bias, T, E, k, out, status);
 }
 
 size_t permute_scratch_bytes(int P, int E) {
