@@ -357,10 +357,14 @@ int qgemv_ksplit(int fmt, int n, int k, int max_segments, int max_tokens) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // About one CTA per SM: a split adds a partial round trip and a last-CTA
+    // reduction, and short K shares never fill the register prefetch ring,
+    // so K is split only as far as needed to reach the SM count, keeping at
+    // least 8 slabs (4 per K-half warp) per CTA.
     const int ctas = (n / kTileRows) * max_segments;
-    const int want = (4 * sms + ctas - 1) / ctas;
+    const int want = (sms + ctas - 1) / ctas;
     const int k_slabs = k / fmt_info(fmt).slab_k;
-    return std::max(1, std::min(want, std::min(kMaxKsplit, k_slabs / 2)));
+    return std::max(1, std::min(want, std::min(kMaxKsplit, k_slabs / 8)));
 }
 
 void launch_qgemv(const QgemvParams& params, int max_segments, cudaStream_t st) {
