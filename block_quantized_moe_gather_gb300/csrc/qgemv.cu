@@ -137,32 +137,12 @@ __device__ __forceinline__ Q2Scales q2_scales(uint32_t sc4, uint32_t dm) {
     return r;
 }
 
-// A-fragment register (pair of fp16 weights) for row half hh, pair `lohi`
-// (0: values 4s, 4s+1; 1: values 4s+2, 4s+3) of MMA step s.  `q2` holds the
-// Q2_K sub-block scales of [tile][hh] (unused for the other formats).
-template <int FMT>
-__device__ __forceinline__ uint32_t a_pair(const Frag<FMT>& f, const Q2Scales (&q2)[2][2], int tile, int hh, int s,
-                                           int lohi) {
-    if (FMT == BQ_FMT_Q8_0) {
-        const uint32_t w = comp(f.q[tile][hh], s) ^ 0x80808080u;
-        const __half d = __ushort_as_half((uint16_t)f.sc[tile][hh]);
-        const __half2 v = bq::s8pair_to_half2(w, lohi ? 0x4342u : 0x4140u);
-        return bq::h2_as_u32(__hmul2(v, __halves2half2(d, d)));
-    } else if (FMT == BQ_FMT_Q2_K) {
-        const int sb = s >> 2;   // sub-block of this step
-        const uint32_t w = comp(f.q[tile][hh], sb);
-        const __half2 ds = (sb & 1) ? __high2half2(q2[tile][hh].ds[sb >> 1]) : __low2half2(q2[tile][hh].ds[sb >> 1]);
-        const __half2 nm = (sb & 1) ? __high2half2(q2[tile][hh].nm[sb >> 1]) : __low2half2(q2[tile][hh].nm[sb >> 1]);
-        return bq::h2_as_u32(__hfma2(q2_pair(w, 2 * (s & 3) + lohi), ds, nm));
-    } else {
-        const uint32_t w = comp(f.q[tile][hh], s >> 1);
-        const __half2 sb = bq::u32_as_h2(f.sc[tile][hh]);
-        return bq::h2_as_u32(__hfma2(q4_pair(w, 2 * (s & 1) + lohi), __low2half2(sb), __high2half2(sb)));
-    }
-}
-
 // Multiplies one slab; the lane's activation values of the slab (token g,
 // its K quarter) are read here, from L1/L2, not kept in the prefetch ring.
+// MMA step s covers the lane's K values 4s..4s+3: A register pairs (4s, 4s+1)
+// and (4s+2, 4s+3) of rows g (hh = 0) and g + 8 (hh = 1) of each 16-row tile.
+// The per-row scale terms are broadcast to both fp16 lanes once per Q2_K
+// sub-block (four steps) or once per slab, not once per pair.
 template <int FMT>
 __device__ __forceinline__ void mma_frag(const Frag<FMT>& f, const __half* xq, bool xvalid, int t,
                                          float (&acc)[2][4]) {
@@ -171,26 +151,79 @@ __device__ __forceinline__ void mma_frag(const Frag<FMT>& f, const __half* xq, b
     const uint4* xp = reinterpret_cast<const uint4*>(xq + (Traits<FMT>::SK / 4) * t);
 #pragma unroll
     for (int v = 0; v < XV; ++v) x[v] = xvalid ? __ldg(xp + v) : make_uint4(0, 0, 0, 0);
-    Q2Scales q2[2][2];
     if (FMT == BQ_FMT_Q2_K) {
+        Q2Scales q2[2][2];
 #pragma unroll
         for (int tile = 0; tile < 2; ++tile)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) q2[tile][hh] = q2_scales(f.sc[tile][hh], f.dm[tile][hh]);
-    }
 #pragma unroll
-    for (int s = 0; s < Traits<FMT>::STEPS; ++s) {
-        const uint4 xv = x[s >> 1];
-        const uint32_t b0 = (s & 1) ? xv.z : xv.x;
-        const uint32_t b1 = (s & 1) ? xv.w : xv.y;
+        for (int sb = 0; sb < 4; ++sb) {
+            __half2 ds[2][2], nm[2][2];
+            uint32_t w[2][2];
 #pragma unroll
-        for (int tile = 0; tile < 2; ++tile) {
-            uint32_t a[4];
-            a[0] = a_pair<FMT>(f, q2, tile, 0, s, 0);
-            a[1] = a_pair<FMT>(f, q2, tile, 1, s, 0);
-            a[2] = a_pair<FMT>(f, q2, tile, 0, s, 1);
-            a[3] = a_pair<FMT>(f, q2, tile, 1, s, 1);
-            mma16816(acc[tile], a, b0, b1);
+            for (int tile = 0; tile < 2; ++tile)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const __half2 dsp = q2[tile][hh].ds[sb >> 1], nmp = q2[tile][hh].nm[sb >> 1];
+                    ds[tile][hh] = (sb & 1) ? __high2half2(dsp) : __low2half2(dsp);
+                    nm[tile][hh] = (sb & 1) ? __high2half2(nmp) : __low2half2(nmp);
+                    w[tile][hh] = comp(f.q[tile][hh], sb);
+                }
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) {
+                const int s = 4 * sb + s4;
+                const uint4 xv = x[s >> 1];
+                const uint32_t b0 = (s & 1) ? xv.z : xv.x;
+                const uint32_t b1 = (s & 1) ? xv.w : xv.y;
+#pragma unroll
+                for (int tile = 0; tile < 2; ++tile) {
+                    uint32_t a[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {   // r = hh + 2 * lohi
+                        const int hh = r & 1, p = 2 * s4 + (r >> 1);
+                        a[r] = bq::h2_as_u32(__hfma2(q2_pair(w[tile][hh], p), ds[tile][hh], nm[tile][hh]));
+                    }
+                    mma16816(acc[tile], a, b0, b1);
+                }
+            }
+        }
+    } else {
+        __half2 sc2[2][2], bi2[2][2], d2[2][2];
+#pragma unroll
+        for (int tile = 0; tile < 2; ++tile)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                if (FMT == BQ_FMT_INT4_G64) {
+                    const __half2 sbh = bq::u32_as_h2(f.sc[tile][hh]);
+                    sc2[tile][hh] = __low2half2(sbh);
+                    bi2[tile][hh] = __high2half2(sbh);
+                } else {
+                    const __half d = __ushort_as_half((uint16_t)f.sc[tile][hh]);
+                    d2[tile][hh] = __halves2half2(d, d);
+                }
+            }
+#pragma unroll
+        for (int s = 0; s < Traits<FMT>::STEPS; ++s) {
+            const uint4 xv = x[s >> 1];
+            const uint32_t b0 = (s & 1) ? xv.z : xv.x;
+            const uint32_t b1 = (s & 1) ? xv.w : xv.y;
+#pragma unroll
+            for (int tile = 0; tile < 2; ++tile) {
+                uint32_t a[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {   // r = hh + 2 * lohi
+                    const int hh = r & 1, lohi = r >> 1;
+                    if (FMT == BQ_FMT_Q8_0) {
+                        const uint32_t wx = comp(f.q[tile][hh], s) ^ 0x80808080u;
+                        a[r] = bq::h2_as_u32(__hmul2(bq::s8pair_to_half2(wx, lohi ? 0x4342u : 0x4140u), d2[tile][hh]));
+                    } else {
+                        const uint32_t w = comp(f.q[tile][hh], s >> 1);
+                        a[r] = bq::h2_as_u32(__hfma2(q4_pair(w, 2 * (s & 1) + lohi), sc2[tile][hh], bi2[tile][hh]));
+                    }
+                }
+                mma16816(acc[tile], a, b0, b1);
+            }
         }
     }
 }
