@@ -355,6 +355,76 @@ __device__ __forceinline__ void dequant_stage<BQ_FMT_INT4_G64>(const uint8_t* ra
     }
 }
 
+// Half h (K values 32h .. 32h + 31) of a 64-K stage as 16 fp16 pairs, the
+// same values dequant_stage gives for that half.
+template <int FMT>
+__device__ __forceinline__ void dequant_half(const uint8_t* raw, int p, int sub, int h, uint32_t (&out)[16]);
+
+template <>
+__device__ __forceinline__ void dequant_half<BQ_FMT_Q8_0>(const uint8_t* raw, int p, int, int h,
+                                                          uint32_t (&out)[16]) {
+    // half h of the 64-value slab is Q8_0 block h
+    const __half db = __ushort_as_half(*reinterpret_cast<const uint16_t*>(raw + 8192 + 4 * p + 2 * h));
+    const __half2 d = __halves2half2(db, db);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const uint4 q = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, 2 * h + c));
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const uint32_t wx = w[m] ^ 0x80808080u;
+            out[8 * c + 2 * m] = bq::h2_as_u32(__hmul2(bq::s8pair_to_half2(wx, 0x4140u), d));
+            out[8 * c + 2 * m + 1] = bq::h2_as_u32(__hmul2(bq::s8pair_to_half2(wx, 0x4342u), d));
+        }
+    }
+}
+
+template <>
+__device__ __forceinline__ void dequant_half<BQ_FMT_Q2_K>(const uint8_t* raw, int p, int sub, int h,
+                                                          uint32_t (&out)[16]) {
+    // stage `sub` = sub-blocks 4sub..4sub+3; half h = sub-blocks 4sub + 2h, 4sub + 2h + 1
+    const uint2 q = *reinterpret_cast<const uint2*>(raw + bq::quant_chunk_offset(p, sub) + 8 * h);
+    const uint32_t s2 = *reinterpret_cast<const uint16_t*>(raw + 8192 + 512 * sub + 4 * p + 2 * h);
+    const __half2 dm = bq::u32_as_h2(*reinterpret_cast<const uint32_t*>(raw + 10240 + 4 * p));
+    const __half2 d2 = __low2half2(dm), nmin2 = __hneg2(__high2half2(dm));
+    const uint32_t b = __byte_perm(s2, 0u, 0x4140u);   // bytes 0, 1 -> lanes
+    const __half2 dsp = __hmul2_rn(d2, field_to_half2<0>(b, 0x000F000Fu));
+    const __half2 nmp = __hmul2_rn(nmin2, field_to_half2<4>(b, 0x000F000Fu));
+    const uint32_t w[2] = {q.x, q.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const __half2 s2h = i ? __high2half2(dsp) : __low2half2(dsp);
+        const __half2 m2 = i ? __high2half2(nmp) : __low2half2(nmp);
+        const uint32_t hi = w[i] >> 10;
+        out[8 * i + 0] = bq::h2_as_u32(__hfma2(field_to_half2<0>(w[i], 0x00030003u), s2h, m2));
+        out[8 * i + 1] = bq::h2_as_u32(__hfma2(field_to_half2<2>(w[i], 0x00030003u), s2h, m2));
+        out[8 * i + 2] = bq::h2_as_u32(__hfma2(field_to_half2<4>(w[i], 0x00030003u), s2h, m2));
+        out[8 * i + 3] = bq::h2_as_u32(__hfma2(field_to_half2<6>(w[i], 0x00030003u), s2h, m2));
+        out[8 * i + 4] = bq::h2_as_u32(__hfma2(field_to_half2<8>(w[i], 0x00030003u), s2h, m2));
+        out[8 * i + 5] = bq::h2_as_u32(__hfma2(field_to_half2<0>(hi, 0x00030003u), s2h, m2));
+        out[8 * i + 6] = bq::h2_as_u32(__hfma2(field_to_half2<2>(hi, 0x00030003u), s2h, m2));
+        out[8 * i + 7] = bq::h2_as_u32(__hfma2(field_to_half2<4>(hi, 0x00030003u), s2h, m2));
+    }
+}
+
+template <>
+__device__ __forceinline__ void dequant_half<BQ_FMT_INT4_G64>(const uint8_t* raw, int p, int sub, int h,
+                                                              uint32_t (&out)[16]) {
+    // stage `sub` = K group `sub`; half h = chunk 2sub + h
+    const __half2 sb = bq::u32_as_h2(*reinterpret_cast<const uint32_t*>(raw + 8192 + 512 * sub + 4 * p));
+    const __half2 s2 = __low2half2(sb), b2 = __high2half2(sb);
+    const uint4 q = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, 2 * sub + h));
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const uint32_t hi = w[m] >> 8;
+        out[4 * m + 0] = bq::h2_as_u32(__hfma2(field_to_half2<0>(w[m], 0x000F000Fu), s2, b2));
+        out[4 * m + 1] = bq::h2_as_u32(__hfma2(field_to_half2<4>(w[m], 0x000F000Fu), s2, b2));
+        out[4 * m + 2] = bq::h2_as_u32(__hfma2(field_to_half2<0>(hi, 0x000F000Fu), s2, b2));
+        out[4 * m + 3] = bq::h2_as_u32(__hfma2(field_to_half2<4>(hi, 0x000F000Fu), s2, b2));
+    }
+}
+
 __device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
 // ---------------------------------------------------------------- the kernel
@@ -401,7 +471,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
     // ring depths for this tile
     const int stages_b = min(kMaxStagesB, kBBoxes / n_boxes);
     const uint32_t acc_cols = (uint32_t)((n_mma + 31) & ~31);
-    const int stages_a = min(kMaxStagesA, (int)((kTmemCols - acc_cols) / 32)) & ~1;   // >= 2: acc_cols <= 160
+    // A ring: the columns the accumulator leaves.  With three slots (tiles of
+    // 129-160 tokens) every converter warp works on every stage, each on half
+    // of its K range, so the ring keeps all three slots; otherwise the two
+    // warps of a lane quarter take alternate stages and the ring is rounded
+    // down to an even count (so a slot always belongs to the same warps).
+    const int free_slots = (int)((kTmemCols - acc_cols) / 32);                 // 3 .. 7
+    const bool split_k = free_slots == 3;
+    const int stages_a = split_k ? 3 : min(kMaxStagesA, free_slots) & ~1;   // >= 4 otherwise
     const int rt = blockIdx.x;
     const int n_tiles_w = a.n / bq::kTileRows, k_slabs = a.k / F::SK;
     const uint8_t* wslab = a.w + bq::slab_index(expert, rt, 0, n_tiles_w, k_slabs) * F::SB;
@@ -412,8 +489,13 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
         for (int i = 0; i < kMaxStagesB; ++i) mbar_init(b_full(i), 1);
         for (int j = 0; j < kEmptyRing; ++j) mbar_init(empty(j), 1);
         // a slab of one stage is read by the 4 warps of that stage's parity, longer slabs by all 8
-        for (int i = 0; i < F::NR; ++i) { mbar_init(raw_full(i), 1); mbar_init(raw_empty(i), F::SPS == 1 ? 4 : 8); }
-        for (int i = 0; i < kMaxStagesA; ++i) mbar_init(a_full(i), 4);
+        // split K: all 8 converter warps read every slab and write every stage;
+        // alternating: a slab of one stage is read by the 4 warps of that stage's parity
+        for (int i = 0; i < F::NR; ++i) {
+            mbar_init(raw_full(i), 1);
+            mbar_init(raw_empty(i), split_k || F::SPS > 1 ? 8 : 4);
+        }
+        for (int i = 0; i < kMaxStagesA; ++i) mbar_init(a_full(i), split_k ? 8 : 4);
         mbar_init(acc_full, 1);
         *abort_flag = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -523,9 +605,32 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
         const int p = 32 * quarter + lane;                       // weight row = TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
         bool ok = true;
-        // this warp converts stages ks = half, half + 2, ...; sa = A-ring slot of ks
+        if (split_k) {
+            // every stage: this warp converts K values 32*half .. +31 of it
+            int sa = 0;
+            for (int ks = 0; ks < KS; ++ks) {
+                const int kt = ks / F::SPS, sub = ks % F::SPS, r = kt % F::NR;
+                if (sub == 0 && !(ok = warp_wait(raw_full(r), (uint32_t)(kt / F::NR) & 1u, abort_flag, a.status)))
+                    break;
+                if (ks >= stages_a &&
+                    !(ok = warp_wait(empty(ks - stages_a), empty_parity(ks - stages_a), abort_flag, a.status)))
+                    break;
+                uint32_t v[16];
+                dequant_half<FMT>(raw_ring + r * F::SB, p, sub, half, v);
+                tmem_st16(tmem + lane_base + a_col0 + 32u * sa + 16u * half, v);
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (sub == F::SPS - 1) mbar_arrive(raw_empty(r));
+                    mbar_arrive(a_full(sa));
+                }
+                if (++sa == stages_a) sa = 0;
+            }
+        }
+        // otherwise this warp converts stages ks = half, half + 2, ...; sa = A-ring slot of ks
         int sa = half;
-        for (int ks = half; ks < KS; ks += 2) {
+        for (int ks = half; !split_k && ks < KS; ks += 2) {
             const int kt = ks / F::SPS, sub = ks % F::SPS, r = kt % F::NR;
             const uint32_t pr = (uint32_t)(kt / F::NR) & 1u;
             // first stage of the slab this warp converts: wait for the slab
