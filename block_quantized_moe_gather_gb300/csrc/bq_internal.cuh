@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/bq.h"
 
 // --------------------------------------------------------------------------
@@ -27,6 +29,31 @@ void stage_begin(int stage, cudaStream_t st);
 void stage_end(int stage, cudaStream_t st);
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Programmatic dependent launch: `launch_after` starts a kernel that may be
+// scheduled while the previous kernel on the stream is still running; the
+// kernel calls grid_dependency_wait() before it reads what that kernel wrote
+// (a no-op when it was launched without the attribute).  The previous kernel
+// calls allow_dependents() once all of its CTAs may be resident, so waiting
+// dependents never keep its CTAs off the GPU.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                         Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // --------------------------------------------------------------------------
 // Device weight layout (tile-major slabs)

@@ -62,6 +62,7 @@ segments_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ 
 // y[t][c] (+)= sum_{j < k} y_slot[inv[t*k + j]][c], slots in order.
 __global__ void combine_kernel(const float* __restrict__ y_slot, const int32_t* __restrict__ inv, int T,
                                int k, int H, int accumulate, float* __restrict__ y) {
+    bq::grid_dependency_wait();   // may be launched behind the down projection
     const int h4 = H / 4;
     const int64_t total = (int64_t)T * h4;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
@@ -320,7 +321,7 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
         gu.n_segments = w.n_segments; gu.src_row = w.perm_token; gu.x = xh; gu.h = w.h;
         gu.ksplit = w.ks_gu; gu.partial = w.part_gu; gu.counters = w.cnt_gu;
         bq::stage_begin(BQ_STAGE_GATE_UP, st);
-        bq::launch_qgemv(gu, max_segments, st);
+        bq::launch_qgemv(gu, max_segments, st, /*after_previous=*/true);
         bq::stage_end(BQ_STAGE_GATE_UP, st);
 
         bq::QgemvParams dn = gu;
@@ -329,7 +330,7 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
         dn.src_row = nullptr; dn.x = w.h; dn.h = nullptr; dn.y = w.y_slot; dn.ldy = H; dn.row_scale = w.perm_gate;
         dn.ksplit = w.ks_d; dn.partial = w.part_d; dn.counters = w.cnt_d;
         bq::stage_begin(BQ_STAGE_DOWN, st);
-        bq::launch_qgemv(dn, max_segments, st);
+        bq::launch_qgemv(dn, max_segments, st, /*after_previous=*/true);
         bq::stage_end(BQ_STAGE_DOWN, st);
     } else {
         if ((s = bq::launch_gemm_moe(d, xh, w.perm_token, w.perm_gate, w.seg_expert, w.seg_start, w.seg_count,
@@ -361,7 +362,11 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
     const int64_t total = (int64_t)T * (H / 4);
     const int grid = (int)std::min<int64_t>((total + 255) / 256, 152 * 8);
     bq::stage_begin(BQ_STAGE_COMBINE, st);
-    combine_kernel<<<grid, 256, 0, st>>>(w.y_slot, w.inv, T, k, H, accumulate, y);
+    if (decode && !side)   // directly behind the down projection on this stream
+        bq::launch_after(combine_kernel, dim3(grid), dim3(256), 0, st, (const float*)w.y_slot, (const int32_t*)w.inv,
+                         T, k, H, accumulate, y);
+    else
+        combine_kernel<<<grid, 256, 0, st>>>(w.y_slot, w.inv, T, k, H, accumulate, y);
     bq::note_launch();
     bq::stage_end(BQ_STAGE_COMBINE, st);
     (void)P;

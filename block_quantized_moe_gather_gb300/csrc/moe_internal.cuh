@@ -69,6 +69,6 @@ struct QgemvParams {
 constexpr int kMaxKsplit = 16;
 // Split factor that gives the GPU enough CTAs for this shape.
 int qgemv_ksplit(int fmt, int n, int k, int max_segments, int max_tokens);
-void launch_qgemv(const QgemvParams& p, int max_segments, cudaStream_t st);
+void launch_qgemv(const QgemvParams& p, int max_segments, cudaStream_t st, bool after_previous = false);
 
 }  // namespace bq

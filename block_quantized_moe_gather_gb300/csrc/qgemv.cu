@@ -270,6 +270,9 @@ qgemv_kernel(const bq::QgemvParams p) {
     __shared__ float2 red[4][2][32][2];   // K-half 1 partials: [quarter][tile][lane][row half]
     __shared__ int s_last;
 
+    // launched right behind the kernel that produced the routing / activations
+    bq::grid_dependency_wait();
+    bq::allow_dependents();
     const int seg = blockIdx.y;
     if (p.n_segments && seg >= __ldg(p.n_segments)) return;
     const int e = p.seg_expert ? __ldg(p.seg_expert + seg) : 0;
@@ -375,10 +378,11 @@ qgemv_kernel(const bq::QgemvParams p) {
 }
 
 template <int FMT>
-void launch_fmt(const bq::QgemvParams& p, int max_segments, cudaStream_t st) {
+void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous, cudaStream_t st) {
     dim3 grid(p.n / bq::kTileRows, max_segments, p.ksplit);
-    if (p.swiglu) qgemv_kernel<FMT, true><<<grid, kThreads, 0, st>>>(p);
-    else qgemv_kernel<FMT, false><<<grid, kThreads, 0, st>>>(p);
+    auto kernel = p.swiglu ? qgemv_kernel<FMT, true> : qgemv_kernel<FMT, false>;
+    if (after_previous) bq::launch_after(kernel, grid, dim3(kThreads), 0, st, p);
+    else kernel<<<grid, kThreads, 0, st>>>(p);
 }
 
 }  // namespace
@@ -400,15 +404,15 @@ int qgemv_ksplit(int fmt, int n, int k, int max_segments, int max_tokens) {
     return std::max(1, std::min(want, std::min(kMaxKsplit, k_slabs / 8)));
 }
 
-void launch_qgemv(const QgemvParams& params, int max_segments, cudaStream_t st) {
+void launch_qgemv(const QgemvParams& params, int max_segments, cudaStream_t st, bool after_previous) {
     if (max_segments <= 0) return;
     QgemvParams p = params;
     if (p.ksplit < 1 || !p.partial || !p.counters) p.ksplit = 1;
     note_launch();
     switch (p.fmt) {
-        case BQ_FMT_Q8_0: launch_fmt<BQ_FMT_Q8_0>(p, max_segments, st); break;
-        case BQ_FMT_Q2_K: launch_fmt<BQ_FMT_Q2_K>(p, max_segments, st); break;
-        default: launch_fmt<BQ_FMT_INT4_G64>(p, max_segments, st); break;
+        case BQ_FMT_Q8_0: launch_fmt<BQ_FMT_Q8_0>(p, max_segments, after_previous, st); break;
+        case BQ_FMT_Q2_K: launch_fmt<BQ_FMT_Q2_K>(p, max_segments, after_previous, st); break;
+        default: launch_fmt<BQ_FMT_INT4_G64>(p, max_segments, after_previous, st); break;
     }
 }
 

@@ -135,6 +135,7 @@ route_permute_small_kernel(const float* __restrict__ logits, const float* __rest
     __shared__ int32_t s_cnt[1024];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int P = T * k;
+    bq::allow_dependents();   // the GEMV that follows may be scheduled now; it waits for this grid
     for (int i = threadIdx.x; i < out.n_zero; i += kSmallThreads) out.zero[i] = 0;
     for (int t = warp; t < T; t += kSmallThreads / 32) {
         int e;
