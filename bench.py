@@ -203,6 +203,16 @@ class L2Flush:
         torch.sum(self.rbuf, dim=0, out=self.sink)
 
 
+# DRAM bytes (read + write) of one routed gate/up GEMM launch, per workload, from one
+# capture of the current kernel:
+#   ncu --set full --clock-control none --kernel-name-base demangled \
+#       -k regex:"gemm_kernel<.int.2, .int.0" -c 1 -o gemm_q2k_full \
+#       python bench.py --steps 2 --warmup 1 --no-secondary --no-cpu-baseline
+# (689,886,976 read + 42,269,440 written; the algorithmic bytes are 740 MB).  Set to
+# None whenever the GEMM kernel changes until it is captured again.
+GATE_UP_DRAM_BYTES = {"q2k": 689886976 + 42269440, "int4": None}
+
+
 def time_steps(fn, k, flush, stage_events=None):
     """Runs fn() k times, flushing L2 before each, timing each call with CUDA
     events on the current stream.  Returns (per-step ms list, per-stage ms
@@ -291,7 +301,7 @@ def run_main(args, world, rank, local):
     achieved_tf = gu_flops / (gu_ms / 1e3) / 1e12
     roofline = {"kernel": "gate_up grouped GEMM + SwiGLU (stage timing)", "bound": "tensor",
                 "achieved": round(achieved_tf, 2), "peak": peak_tf, "unit": "TFLOP/s",
-                "frac": round(achieved_tf / peak_tf, 4), "traffic": None,
+                "frac": round(achieved_tf / peak_tf, 4), "traffic": GATE_UP_DRAM_BYTES.get(args.workload),
                 "peak_source": f"{pk_src} bf16 sustained (fp16 operands, same tensor rate)",
                 "stage_ms": {"gate_up": round(gu_ms, 4), "down": round(statistics.mean(stage_ms[2]), 4),
                              "shared": round(statistics.mean(stage_ms[3]), 4) if 3 in stage_ms else None}}

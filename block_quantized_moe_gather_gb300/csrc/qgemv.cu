@@ -263,11 +263,18 @@ __device__ __forceinline__ void qgemv_epilogue(const bq::QgemvParams& p, const f
     }
 }
 
-template <int FMT, bool SWIGLU>
+// KW = 2: a CTA covers a whole 128-row tile, warp w takes row quarter w % 4
+// and K half w / 4.  KW = 8 (for grids that would otherwise be too small to
+// fill the GPU, without a K split across CTAs): a CTA covers one 32-row
+// quarter of a tile and its 8 warps take 8 contiguous K pieces; the partials
+// are summed in warp order, so results stay bit-reproducible either way.
+template <int FMT, bool SWIGLU, int KW>
 __global__ void __launch_bounds__(kThreads, 2)
 qgemv_kernel(const bq::QgemvParams p) {
     using T = Traits<FMT>;
-    __shared__ float2 red[4][2][32][2];   // K-half 1 partials: [quarter][tile][lane][row half]
+    static_assert(KW == 2 || KW == 8, "K ways per CTA");
+    // partials of the warps with K piece > 0: [quarter (KW 2) or piece - 1 (KW 8)][tile][lane][row half]
+    __shared__ float2 red[KW == 8 ? 7 : 4][2][32][2];
     __shared__ int s_last;
 
     // launched right behind the kernel that produced the routing / activations
@@ -279,17 +286,17 @@ qgemv_kernel(const bq::QgemvParams p) {
     const int start = p.seg_start ? __ldg(p.seg_start + seg) : 0;
     const int count = p.seg_count ? __ldg(p.seg_count + seg) : p.m;
 
-    const int rt = blockIdx.x, kp = blockIdx.z;
+    const int rt = KW == 8 ? (int)(blockIdx.x >> 2) : (int)blockIdx.x, kp = blockIdx.z;
     const int n_tiles = p.n / bq::kTileRows, k_slabs = p.k / T::SK;
     const uint8_t* wbase = p.w + bq::slab_index(e, rt, 0, n_tiles, k_slabs) * T::SB;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int quarter = warp & 3, khalf = warp >> 2, rowbase = 32 * quarter;
-    // this CTA's share of the slabs (split K), then contiguous halves of it
+    const int quarter = KW == 8 ? (int)(blockIdx.x & 3) : (warp & 3), rowbase = 32 * quarter;
+    const int kw = KW == 8 ? warp : (warp >> 2);   // this warp's K piece
+    // this CTA's share of the slabs (split K), then KW contiguous pieces of it
     const int ks_lo = (int)((int64_t)k_slabs * kp / p.ksplit), ks_hi = (int)((int64_t)k_slabs * (kp + 1) / p.ksplit);
-    const int ks_mid = ks_lo + (ks_hi - ks_lo + 1) / 2;
-    const int kt_begin = khalf ? ks_mid : ks_lo;
-    const int kt_end = khalf ? ks_hi : ks_mid;
+    const int kt_begin = ks_lo + ((ks_hi - ks_lo) * kw + KW - 1) / KW;
+    const int kt_end = ks_lo + ((ks_hi - ks_lo) * (kw + 1) + KW - 1) / KW;
 
     for (int tok0 = 0; tok0 < count; tok0 += 8) {
         const int ntok = min(8, count - tok0);
@@ -319,30 +326,35 @@ qgemv_kernel(const bq::QgemvParams p) {
             }
         }
         __syncthreads();   // previous token group's readers of `red` are done
-        if (khalf) {
+        if (kw) {
+            const int slot = KW == 8 ? kw - 1 : quarter;
 #pragma unroll
             for (int tile = 0; tile < 2; ++tile) {
-                red[quarter][tile][lane][0] = make_float2(acc[tile][0], acc[tile][1]);
-                red[quarter][tile][lane][1] = make_float2(acc[tile][2], acc[tile][3]);
+                red[slot][tile][lane][0] = make_float2(acc[tile][0], acc[tile][1]);
+                red[slot][tile][lane][1] = make_float2(acc[tile][2], acc[tile][3]);
             }
         }
         __syncthreads();
-        if (!khalf) {
-            // K half 0 adds half 1 in a fixed order: bit-reproducible
+        if (!kw) {
+            // piece 0 adds the other pieces in a fixed order: bit-reproducible
 #pragma unroll
-            for (int tile = 0; tile < 2; ++tile) {
-                const float2 r0 = red[quarter][tile][lane][0], r1 = red[quarter][tile][lane][1];
-                acc[tile][0] += r0.x; acc[tile][1] += r0.y; acc[tile][2] += r1.x; acc[tile][3] += r1.y;
+            for (int j = 0; j < KW - 1; ++j) {
+                const int slot = KW == 8 ? j : quarter;
+#pragma unroll
+                for (int tile = 0; tile < 2; ++tile) {
+                    const float2 r0 = red[slot][tile][lane][0], r1 = red[slot][tile][lane][1];
+                    acc[tile][0] += r0.x; acc[tile][1] += r0.y; acc[tile][2] += r1.x; acc[tile][3] += r1.y;
+                }
             }
         }
         if (p.ksplit == 1) {
-            if (!khalf) qgemv_epilogue<SWIGLU>(p, acc, rt, quarter, g, t, start + tok0, ntok);
+            if (!kw) qgemv_epilogue<SWIGLU>(p, acc, rt, quarter, g, t, start + tok0, ntok);
             continue;
         }
         // Split K (one token group only): publish this CTA's partial; the last
         // CTA of the (segment, tile) sums all partials in split order.
         float* part = p.partial + ((int64_t)(seg * n_tiles + rt) * p.ksplit) * 1024;
-        if (!khalf) {
+        if (!kw) {
 #pragma unroll
             for (int tile = 0; tile < 2; ++tile)
 #pragma unroll
@@ -358,7 +370,7 @@ qgemv_kernel(const bq::QgemvParams p) {
         __syncthreads();
         if (!s_last) return;
         __threadfence();
-        if (!khalf) {
+        if (!kw) {
             float sum[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             for (int q = 0; q < p.ksplit; ++q)
 #pragma unroll
@@ -377,10 +389,29 @@ qgemv_kernel(const bq::QgemvParams p) {
     }
 }
 
+int sm_count() {
+    static int cached[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 148;
+    }
+    return cached[dev];
+}
+
 template <int FMT>
 void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous, cudaStream_t st) {
-    dim3 grid(p.n / bq::kTileRows, max_segments, p.ksplit);
-    auto kernel = p.swiglu ? qgemv_kernel<FMT, true> : qgemv_kernel<FMT, false>;
+    const int tiles = p.n / bq::kTileRows;
+    // one CTA per 32-row quarter when a dense weight's whole-tile CTAs would
+    // leave SMs idle and K is not split across CTAs (no workspace for partials);
+    // the expert GEMVs of a MoE step are left whole-tile (measured no better)
+    const bool quarters = p.ksplit == 1 && !p.seg_expert && tiles * max_segments < sm_count();
+    dim3 grid(tiles * (quarters ? 4 : 1), max_segments, p.ksplit);
+    auto kernel = quarters ? (p.swiglu ? qgemv_kernel<FMT, true, 8> : qgemv_kernel<FMT, false, 8>)
+                           : (p.swiglu ? qgemv_kernel<FMT, true, 2> : qgemv_kernel<FMT, false, 2>);
     if (after_previous) bq::launch_after(kernel, grid, dim3(kThreads), 0, st, p);
     else kernel<<<grid, kThreads, 0, st>>>(p);
 }
