@@ -122,3 +122,44 @@ def test_moe_decode_full_shapes(lib, base, batch):
     inp = synth.moe_inputs(case, weights, act_seed=synth.decode_step_seed(batch))
     inp.bias = None   # decode steps use plain N(0,1) logits
     assert_close_matmul(run_moe(lib, layer, inp), oracle_moe(inp), case.name)
+
+
+def test_moe_decode_concurrent_streams(lib):
+    # Two decode layer calls (each with its shared expert on the library's side
+    # stream) issued from two host threads onto two streams, many times, without
+    # synchronising in between: every output equals the sequential result.
+    import threading
+
+    import torch
+
+    from helpers import dev, half_dev
+    case = synth.dataclasses.replace(SMALL[2], t=3)
+    inps = [synth.moe_inputs(case, act_seed=11), synth.moe_inputs(case, act_seed=12)]
+    layer = build_layer(lib, inps[0])
+    ref = [run_moe(lib, layer, inp) for inp in inps]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [[], []]
+
+    def worker(i):
+        torch.cuda.set_device(0)
+        inp = inps[i]
+        with torch.cuda.stream(streams[i]):   # uploads and calls in this thread's stream order
+            x, lg = half_dev(inp.x), dev(inp.logits)
+            bias = dev(inp.bias) if inp.bias is not None else None
+            ws = torch.empty(layer.workspace_bytes(), dtype=torch.uint8, device="cuda")
+            for _ in range(20):
+                y = torch.empty((case.t, case.hidden), dtype=torch.float32, device="cuda")
+                lib.moe_gather_qmm(layer, x, lg, bias, y, ws, stream=streams[i])
+                outs[i].append(y)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    for i in range(2):
+        assert len(outs[i]) == 20
+        for y in outs[i]:
+            np.testing.assert_array_equal(y.cpu().numpy().view(np.uint32), ref[i].view(np.uint32))
+    assert_close_matmul(ref[0], oracle_moe(inps[0]), "concurrent streams")
