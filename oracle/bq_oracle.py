@@ -32,6 +32,11 @@ Readings taken where the pages are silent (each also listed in the design doc):
   selection and weighting.
 * Fused gate/up weight: rows [0, I) are the gate, rows [I, 2I) the up
   projection.
+* Scored routing: ``softmax_then_bias`` selects on softmax(logits) + bias
+  and weights the selected unbiased probabilities renormalised to 1;
+  ``sqrtsoftplus`` selects on sqrt(softplus(logit)) + bias and weights the
+  selected unbiased scores times the routed scaling factor, without
+  renormalising (the pages name no renormalisation for it).
 """
 from __future__ import annotations
 
@@ -39,6 +44,7 @@ import numpy as np
 
 __all__ = [
     "dequant_q8_0", "dequant_q2_k", "dequant_int4", "qmm", "route",
+    "SCORINGS", "softplus", "route_scored",
     "permute", "silu", "swiglu_ffn", "moe_ffn", "moe_ffn_tokens",
 ]
 
@@ -166,6 +172,67 @@ def route(logits: np.ndarray, k: int, bias: np.ndarray | None = None):
     ex = np.exp(zs - zs[:, :1])
     weights = ex / ex.sum(axis=1, keepdims=True)
     return ids, weights
+
+
+SCORINGS = ("softmax", "softmax_then_bias", "sqrtsoftplus")
+
+
+def softplus(x):
+    """Overflow-free softplus ``max(x, 0) + log(1 + exp(-|x|))`` in fp64.
+
+    *iron #9*, DeepSeek V4 routing scoring kernel: the naive
+    ``log(1 + exp(x))`` overflows for large x; this form is exact in
+    infinite precision and never evaluates exp of a positive number.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    return np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
+
+
+def route_scored(logits: np.ndarray, k: int, bias: np.ndarray | None = None, scoring: str = "softmax",
+                 scale: float = 1.0):
+    """Router top-k for the three scoring rules, in fp64.
+
+    * ``softmax``: ``route`` (bias added to the logits, select on them,
+      weights = softmax of the selected, renormalised).
+    * ``softmax_then_bias``: *SlimServe #2*, LFM2-MoE routing — the
+      softmax ``p`` over all experts, then the per-expert bias added only
+      for selection (select the k largest ``p + bias``); the weights are the
+      unbiased ``p`` of the selected experts, renormalised to sum to 1.
+    * ``sqrtsoftplus``: *iron #9*, DeepSeek V4 scoring
+      ``s = sqrt(softplus(logit))``; selection on ``s + bias`` (aux-loss-free
+      bias), weights = the unbiased ``s`` of the selected experts times the
+      routed scaling factor ``scale`` (not renormalised).
+
+    Selection: descending key, ties to the lower expert index.  Returns ids
+    int32 [T, k], weights fp64 [T, k] and the selection keys fp64 [T, E] (so a
+    caller can tell exact ties from near-ties).
+    """
+    if scoring == "softmax":
+        ids, w = route(logits, k, bias)
+        z = np.asarray(logits, dtype=np.float32)
+        if bias is not None:
+            z = z + np.asarray(bias, dtype=np.float32)[None, :]
+        return ids, w, z.astype(np.float64)
+    x = np.asarray(logits, dtype=np.float64)
+    t, e = x.shape
+    assert 1 <= k <= e
+    b = np.zeros(e) if bias is None else np.asarray(bias, dtype=np.float64)
+    if scoring == "softmax_then_bias":
+        ex = np.exp(x - x.max(axis=1, keepdims=True))
+        score = ex / ex.sum(axis=1, keepdims=True)
+    elif scoring == "sqrtsoftplus":
+        score = np.sqrt(softplus(x))
+    else:
+        raise ValueError(scoring)
+    key = score + b[None, :]
+    order = np.argsort(-key, axis=1, kind="stable")
+    ids = order[:, :k].astype(np.int32)
+    sel = np.take_along_axis(score, order[:, :k], axis=1)
+    if scoring == "softmax_then_bias":
+        w = sel / sel.sum(axis=1, keepdims=True)
+    else:
+        w = sel * float(scale)
+    return ids, w, key
 
 
 def permute(ids: np.ndarray, n_experts: int):

@@ -435,3 +435,80 @@ def test_moe_tokens_subset_matches_full():
     full = O.moe_ffn(x, ids, wts, lambda e: gu[e], lambda e: dd[e])
     sub = O.moe_ffn_tokens(x, ids, wts, [3, 1], lambda e: gu[e], lambda e: dd[e])
     np.testing.assert_allclose(sub, full[[3, 1]], rtol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# Scored routing rules (DeepSeek V4 sqrt-softplus, LFM2-MoE softmax-then-bias)
+# ---------------------------------------------------------------------------
+
+def test_softplus_closed_forms_and_stability():
+    import math
+    assert O.softplus(0.0) == pytest.approx(math.log(2.0), abs=1e-15)
+    # the overflow-free form: softplus(x) = x for large x, exp(x) for very negative x
+    assert O.softplus(1000.0) == 1000.0
+    assert O.softplus(-50.0) == pytest.approx(math.exp(-50.0), rel=1e-12)
+    xs = np.linspace(-30, 30, 241)
+    np.testing.assert_allclose(O.softplus(xs) - O.softplus(-xs), xs, atol=1e-12)   # softplus(x) - softplus(-x) = x
+    mid = np.linspace(-5, 5, 41)
+    np.testing.assert_allclose(O.softplus(mid), [math.log1p(math.exp(v)) for v in mid], rtol=1e-14)
+
+
+def test_sqrtsoftplus_selects_on_biased_weights_unbiased_times_scale():
+    import math
+    # softplus(ln(e - 1)) = 1, softplus(0) = ln 2: unbiased scores (sqrt ln2, 1, ~0.08)
+    logits = np.array([[0.0, math.log(math.e - 1.0), -5.0]])
+    bias = np.array([0.5, 0.0, 0.0])
+    ids, w, key = O.route_scored(logits, 1, bias, "sqrtsoftplus", scale=2.5)
+    assert ids.tolist() == [[0]]                                  # the bias wins the selection
+    assert w[0, 0] == pytest.approx(math.sqrt(math.log(2.0)) * 2.5, rel=1e-14)   # weight is unbiased x scale
+    ids2, w2, _ = O.route_scored(logits, 2, None, "sqrtsoftplus", scale=1.0)
+    assert ids2.tolist() == [[1, 0]]
+    np.testing.assert_allclose(w2[0], [1.0, math.sqrt(math.log(2.0))], rtol=1e-14)   # not renormalised
+
+
+def test_softmax_then_bias_closed_form():
+    import math
+    logits = np.array([[0.0, 0.0, math.log(3.0)]])    # softmax p = (1/5, 1/5, 3/5)
+    bias = np.array([0.5, 0.0, 0.0])                  # keys (0.7, 0.2, 0.6)
+    ids, w, key = O.route_scored(logits, 2, bias, "softmax_then_bias")
+    assert ids.tolist() == [[0, 2]]
+    np.testing.assert_allclose(w[0], [0.25, 0.75], rtol=1e-14)   # unbiased p, renormalised
+    np.testing.assert_allclose(key[0], [0.7, 0.2, 0.6], rtol=1e-14)
+    # the plain rule adds the bias to the logits instead: a different choice and weights
+    ids_p, w_p = O.route(logits, 2, bias)
+    assert ids_p.tolist() == [[2, 0]]
+    assert not np.allclose(np.sort(w_p[0]), np.sort(w[0]))
+
+
+def test_scored_routing_brute_force():
+    import math
+    g = np.random.default_rng(5)
+    for scoring in ("softmax_then_bias", "sqrtsoftplus"):
+        for _ in range(20):
+            e, k = int(g.integers(2, 12)), 0
+            k = int(g.integers(1, e + 1))
+            x = g.standard_normal((3, e)) * 3
+            b = g.standard_normal(e) * 0.2
+            ids, w, _ = O.route_scored(x, k, b, scoring, scale=1.7)
+            for t in range(3):
+                if scoring == "softmax_then_bias":
+                    m = max(x[t])
+                    ex = [math.exp(v - m) for v in x[t]]
+                    sc = [v / sum(ex) for v in ex]
+                else:
+                    sc = [math.sqrt(max(v, 0.0) + math.log1p(math.exp(-abs(v)))) for v in x[t]]
+                order = sorted(range(e), key=lambda i: (-(sc[i] + b[i]), i))[:k]
+                assert ids[t].tolist() == order
+                sel = [sc[i] for i in order]
+                want = [v / sum(sel) for v in sel] if scoring == "softmax_then_bias" else [v * 1.7 for v in sel]
+                np.testing.assert_allclose(w[t], want, rtol=1e-12)
+
+
+def test_scored_softmax_is_the_plain_rule():
+    g = np.random.default_rng(6)
+    x = g.standard_normal((5, 16)).astype(np.float32)
+    b = (g.standard_normal(16) * 0.3).astype(np.float32)
+    ids, w, _ = O.route_scored(x, 4, b, "softmax")
+    ids0, w0 = O.route(x, 4, b)
+    np.testing.assert_array_equal(ids, ids0)
+    np.testing.assert_array_equal(w, w0)
