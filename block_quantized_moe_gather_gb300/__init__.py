@@ -10,7 +10,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from ctypes import POINTER, c_char_p, c_int32, c_int64, c_size_t, c_uint64, c_void_p
+from ctypes import POINTER, c_char_p, c_float, c_int32, c_int64, c_size_t, c_uint64, c_void_p
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libbq.so")
@@ -36,8 +36,9 @@ class QWeightC(ctypes.Structure):
 
 class MoEDescC(ctypes.Structure):
     _fields_ = [("T", c_int32), ("hidden", c_int32), ("inter", c_int32), ("n_experts", c_int32),
-                ("topk", c_int32), ("reserved", c_int32), ("w_gate_up", QWeightC), ("w_down", QWeightC),
-                ("shared_gate_up", POINTER(QWeightC)), ("shared_down", POINTER(QWeightC))]
+                ("topk", c_int32), ("scoring", c_int32), ("w_gate_up", QWeightC), ("w_down", QWeightC),
+                ("shared_gate_up", POINTER(QWeightC)), ("shared_down", POINTER(QWeightC)),
+                ("route_scale", c_float), ("reserved", c_int32)]
 
 
 _SIGS = {
@@ -52,6 +53,8 @@ _SIGS = {
     "bq_repack_int4": (c_int32, [c_void_p, c_void_p, c_void_p, POINTER(QWeightC), c_void_p]),
     "bq_qmm": (c_int32, [c_void_p, c_int32, POINTER(QWeightC), c_void_p, c_void_p]),
     "bq_moe_route": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p]),
+    "bq_moe_route_scored": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_float, c_void_p,
+                                      c_void_p, c_void_p]),
     "bq_moe_permute_workspace_bytes": (c_size_t, [c_int32, c_int32, c_int32]),
     "bq_moe_permute": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
                                  c_void_p, c_void_p, c_size_t, c_void_p]),
@@ -177,6 +180,19 @@ def moe_route(logits, bias, k: int, ids, weights, stream=None):
            "bq_moe_route")
 
 
+# bq_scoring
+SCORE_SOFTMAX, SCORE_SOFTMAX_THEN_BIAS, SCORE_SQRTSOFTPLUS = 0, 1, 2
+SCORING_BY_NAME = {"softmax": SCORE_SOFTMAX, "softmax_then_bias": SCORE_SOFTMAX_THEN_BIAS,
+                   "sqrtsoftplus": SCORE_SQRTSOFTPLUS}
+
+
+def moe_route_scored(logits, bias, k: int, scoring: int, scale: float, ids, weights, stream=None):
+    t, e = logits.shape
+    _check(_lib.bq_moe_route_scored(_ptr(logits), _ptr(bias), t, e, k, scoring, scale, _ptr(ids), _ptr(weights),
+                                    _stream(stream)),
+           "bq_moe_route_scored")
+
+
 def moe_permute_workspace_bytes(t: int, k: int, e: int) -> int:
     return int(_lib.bq_moe_permute_workspace_bytes(t, k, e))
 
@@ -217,13 +233,14 @@ class MoELayer:
     """Descriptor of one MoE layer over repacked weights (host struct)."""
 
     def __init__(self, t: int, hidden: int, inter: int, n_experts: int, topk: int, w_gate_up: QWeight,
-                 w_down: QWeight, shared_gate_up: QWeight | None = None, shared_down: QWeight | None = None):
+                 w_down: QWeight, shared_gate_up: QWeight | None = None, shared_down: QWeight | None = None,
+                 scoring: int = 0, route_scale: float = 1.0):
         self.weights = (w_gate_up, w_down, shared_gate_up, shared_down)  # keep buffers alive
         self._s_gu = shared_gate_up.c if shared_gate_up else None
         self._s_d = shared_down.c if shared_down else None
-        self.c = MoEDescC(t, hidden, inter, n_experts, topk, 0, w_gate_up.c, w_down.c,
+        self.c = MoEDescC(t, hidden, inter, n_experts, topk, scoring, w_gate_up.c, w_down.c,
                           ctypes.pointer(self._s_gu) if self._s_gu else None,
-                          ctypes.pointer(self._s_d) if self._s_d else None)
+                          ctypes.pointer(self._s_d) if self._s_d else None, route_scale, 0)
 
     def set_tokens(self, t: int):
         self.c.T = t

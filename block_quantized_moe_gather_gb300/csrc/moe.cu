@@ -166,6 +166,8 @@ bq_status validate_moe(const bq_moe_desc* d) {
     if (!d) return bq::fail(BQ_ERR_NULL, "bq_moe: desc is NULL");
     bq_status s = bq::validate_route("bq_moe_gather_qmm", d->T, d->n_experts, d->topk);
     if (s != BQ_OK) return s;
+    if (d->scoring < BQ_SCORE_SOFTMAX || d->scoring > BQ_SCORE_SQRTSOFTPLUS)
+        return bq::fail(BQ_ERR_SHAPE, "bq_moe_gather_qmm: unknown scoring rule %d", d->scoring);
     if (d->hidden < 1 || d->inter < 1)
         return bq::fail(BQ_ERR_SHAPE, "bq_moe_gather_qmm: hidden %d, inter %d", d->hidden, d->inter);
     if ((s = check_weight("w_gate_up", &d->w_gate_up, d->n_experts, 2 * d->inter, d->hidden, 1)) != BQ_OK) return s;
@@ -274,9 +276,9 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
         const bq::MoeRouting r{w.ids, w.gate, w.counts, w.offsets, w.perm_token, w.perm_slot, w.perm_gate,
                                w.inv, w.seg_expert, w.seg_start, w.seg_count, w.n_segments,
                                w.n_counters ? w.cnt_gu : nullptr, w.n_counters};
-        bq::launch_route_permute_small(router_logits, logit_bias, T, E, k, r, st);
+        bq::launch_route_permute_small(router_logits, logit_bias, T, E, k, r, st, d->scoring, d->route_scale);
     } else {
-        bq::launch_route(router_logits, logit_bias, T, E, k, w.ids, w.gate, st);
+        bq::launch_route(router_logits, logit_bias, T, E, k, w.ids, w.gate, st, d->scoring, d->route_scale);
         bq::launch_permute(w.ids, w.gate, T, k, E, w.counts, w.offsets, w.perm_token, w.perm_slot, w.perm_gate,
                            w.inv, w.scratch, st);
         segments_kernel<<<1, 1024, 0, st>>>(w.counts, w.offsets, E, w.seg_expert, w.seg_start, w.seg_count,

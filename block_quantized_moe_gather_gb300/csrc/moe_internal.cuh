@@ -8,8 +8,9 @@ namespace bq {
 
 // ---- routing / permute (route.cu)
 bq_status validate_route(const char* name, int T, int E, int k);
+// rule: bq_scoring; scale: the routed scaling factor of BQ_SCORE_SQRTSOFTPLUS
 void launch_route(const float* logits, const float* bias, int T, int E, int k, int32_t* ids,
-                  float* weights, cudaStream_t st);
+                  float* weights, cudaStream_t st, int rule = 0, float scale = 1.f);
 size_t permute_scratch_bytes(int P, int E);
 void launch_permute(const int32_t* ids, const float* gate, int T, int k, int E, int32_t* counts,
                     int32_t* offsets, int32_t* perm_token, int32_t* perm_slot, float* perm_gate,
@@ -35,7 +36,7 @@ struct MoeRouting {
 // One-CTA routing front end for small batches (T <= 32, T*k <= 256).
 bool route_permute_small_ok(int T, int k);
 void launch_route_permute_small(const float* logits, const float* bias, int T, int E, int k, const MoeRouting& out,
-                                cudaStream_t st);
+                                cudaStream_t st, int rule = 0, float scale = 1.f);
 
 // ---- grouped qgemv (qgemv.cu)
 //

@@ -24,62 +24,122 @@ namespace {
 
 constexpr int kChunk = 256;
 
-// One warp: top-k of one row of z = logits (+ bias).  Lane j < k returns
-// the j-th selected expert and its renormalised weight.
-template <int NPER>
+// Selection rules (bq_scoring): 0 = softmax of logit + bias, 1 = softmax then
+// bias (LFM2-MoE), 2 = sqrt(softplus) with bias for selection only (DeepSeek V4).
+enum { RULE_SOFTMAX = 0, RULE_SOFTMAX_THEN_BIAS = 1, RULE_SQRTSOFTPLUS = 2 };
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+// One warp: top-k of one row.  Each lane holds NPER experts (e = lane + 32i);
+// key = the selection key of the rule, score = the unbiased score the weight
+// is made from (rules 1, 2).  Lane j < k returns the j-th selected expert and
+// its weight.
+template <int NPER, int RULE>
 __device__ __forceinline__ void route_row(const float* __restrict__ row, const float* __restrict__ bias, int E,
-                                          int k, int lane, int& esel, float& wsel) {
-    float z[NPER];
+                                          int k, float scale, int lane, int& esel, float& wsel) {
+    float key[NPER], score[NPER];
 #pragma unroll
     for (int i = 0; i < NPER; ++i) {
         const int e = lane + 32 * i;
-        z[i] = 0.f;
-        if (e < E) z[i] = bias ? __fadd_rn(__ldg(row + e), __ldg(bias + e)) : __ldg(row + e);
+        key[i] = 0.f;
+        score[i] = 0.f;
+        if (e < E) {
+            const float x = __ldg(row + e);
+            if (RULE == RULE_SOFTMAX) {
+                key[i] = bias ? __fadd_rn(x, __ldg(bias + e)) : x;
+            } else if (RULE == RULE_SQRTSOFTPLUS) {
+                // softplus(x) = max(x, 0) + log1p(exp(-|x|)): never exp of a positive number
+                score[i] = sqrtf(fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))));
+                key[i] = bias ? __fadd_rn(score[i], __ldg(bias + e)) : score[i];
+            } else {
+                score[i] = x;   // the logit for now; turned into the softmax below
+            }
+        }
+    }
+    if (RULE == RULE_SOFTMAX_THEN_BIAS) {
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < NPER; ++i)
+            if (lane + 32 * i < E) m = fmaxf(m, score[i]);
+        m = warp_max(m);
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < NPER; ++i) {
+            const int e = lane + 32 * i;
+            score[i] = e < E ? expf(score[i] - m) : 0.f;
+            sum += score[i];
+        }
+        sum = warp_sum(sum);
+#pragma unroll
+        for (int i = 0; i < NPER; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) {
+                score[i] = __fdiv_rn(score[i], sum);
+                key[i] = bias ? __fadd_rn(score[i], __ldg(bias + e)) : score[i];
+            }
+        }
     }
     uint32_t taken = 0;
     float exsel = 0.f, z0 = 0.f, denom = 0.f;
     esel = 0;
     for (int j = 0; j < k; ++j) {
         // lane-local best among untaken entries; "none" is e = INT_MAX
-        float bz = 0.f;
+        float bz = 0.f, bs = 0.f;
         int be = 0x7fffffff;
 #pragma unroll
         for (int i = 0; i < NPER; ++i) {
             const int e = lane + 32 * i;
             if (e < E && !(taken >> i & 1u)) {
                 // e ascends within a lane, so ties keep the lower id; a NaN loses to any number
-                const bool better = be == 0x7fffffff || z[i] > bz || (!(bz == bz) && z[i] == z[i]);
-                if (better) { bz = z[i]; be = e; }
+                const bool better = be == 0x7fffffff || key[i] > bz || (!(bz == bz) && key[i] == key[i]);
+                if (better) { bz = key[i]; bs = score[i]; be = e; }
             }
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
             const float oz = __shfl_xor_sync(0xffffffffu, bz, off);
+            const float os = __shfl_xor_sync(0xffffffffu, bs, off);
             const int oe = __shfl_xor_sync(0xffffffffu, be, off);
             const bool take = oe != 0x7fffffff &&
                               (be == 0x7fffffff || oz > bz || (oz == bz && oe < be) ||
                                (!(bz == bz) && oz == oz));
-            if (take) { bz = oz; be = oe; }
+            if (take) { bz = oz; bs = os; be = oe; }
         }
         if ((be & 31) == lane && be != 0x7fffffff) taken |= 1u << (be >> 5);
-        if (j == 0) z0 = bz;
-        const float ex = expf(bz - z0);
-        denom += ex;
-        if (lane == j) { exsel = ex; esel = be; }
+        float part;
+        if (RULE == RULE_SOFTMAX) {
+            if (j == 0) z0 = bz;
+            part = expf(bz - z0);
+        } else {
+            part = bs;
+        }
+        denom += part;
+        if (lane == j) { exsel = part; esel = be; }
     }
-    wsel = exsel / denom;
+    if (RULE == RULE_SQRTSOFTPLUS) wsel = exsel * scale;
+    else wsel = exsel / denom;
 }
 
-template <int NPER>
+template <int NPER, int RULE>
 __global__ void __launch_bounds__(256)
-route_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
+route_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k, float scale,
              int32_t* __restrict__ ids, float* __restrict__ weights) {
     const int lane = threadIdx.x & 31;
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= T) return;
     int e;
     float w;
-    route_row<NPER>(logits + (int64_t)t * E, bias, E, k, lane, e, w);
+    route_row<NPER, RULE>(logits + (int64_t)t * E, bias, E, k, scale, lane, e, w);
     if (lane < k) {
         ids[(int64_t)t * k + lane] = e;
         weights[(int64_t)t * k + lane] = w;
@@ -123,10 +183,10 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int32_t* warp_sums, i
 // `out.zero` (split-K counters of the GEMVs that follow).
 constexpr int kSmallThreads = 256;
 
-template <int NPER>
+template <int NPER, int RULE>
 __global__ void __launch_bounds__(kSmallThreads)
 route_permute_small_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
-                           bq::MoeRouting out, int32_t* status) {
+                           float scale, bq::MoeRouting out, int32_t* status) {
     __shared__ int32_t s_ids[256];
     __shared__ float s_gate[256];
     __shared__ int32_t s_first[256];   // 1 if the pair is the first of its expert
@@ -140,7 +200,7 @@ route_permute_small_kernel(const float* __restrict__ logits, const float* __rest
     for (int t = warp; t < T; t += kSmallThreads / 32) {
         int e;
         float w;
-        route_row<NPER>(logits + (int64_t)t * E, bias, E, k, lane, e, w);
+        route_row<NPER, RULE>(logits + (int64_t)t * E, bias, E, k, scale, lane, e, w);
         if (lane < k) {
             const int f = t * k + lane;
             if (e < 0 || e >= E) {   // cannot happen for finite logits; reported, pair dropped
@@ -330,31 +390,54 @@ bq_status validate_route(const char* name, int T, int E, int k) {
     return BQ_OK;
 }
 
-void launch_route(const float* logits, const float* bias, int T, int E, int k, int32_t* ids,
-                  float* weights, cudaStream_t st) {
+template <int RULE>
+void launch_route_rule(const float* logits, const float* bias, int T, int E, int k, float scale, int32_t* ids,
+                       float* weights, cudaStream_t st) {
+    const int grid = (T + 7) / 8;
+    if (E <= 32) route_kernel<1, RULE><<<grid, 256, 0, st>>>(logits, bias, T, E, k, scale, ids, weights);
+    else if (E <= 64) route_kernel<2, RULE><<<grid, 256, 0, st>>>(logits, bias, T, E, k, scale, ids, weights);
+    else if (E <= 128) route_kernel<4, RULE><<<grid, 256, 0, st>>>(logits, bias, T, E, k, scale, ids, weights);
+    else if (E <= 256) route_kernel<8, RULE><<<grid, 256, 0, st>>>(logits, bias, T, E, k, scale, ids, weights);
+    else if (E <= 512) route_kernel<16, RULE><<<grid, 256, 0, st>>>(logits, bias, T, E, k, scale, ids, weights);
+    else route_kernel<32, RULE><<<grid, 256, 0, st>>>(logits, bias, T, E, k, scale, ids, weights);
+}
+
+void launch_route(const float* logits, const float* bias, int T, int E, int k, int32_t* ids, float* weights,
+                  cudaStream_t st, int rule, float scale) {
     if (T == 0) return;
     note_launch();
-    const int grid = (T + 7) / 8;
-    if (E <= 32) route_kernel<1><<<grid, 256, 0, st>>>(logits, bias, T, E, k, ids, weights);
-    else if (E <= 64) route_kernel<2><<<grid, 256, 0, st>>>(logits, bias, T, E, k, ids, weights);
-    else if (E <= 128) route_kernel<4><<<grid, 256, 0, st>>>(logits, bias, T, E, k, ids, weights);
-    else if (E <= 256) route_kernel<8><<<grid, 256, 0, st>>>(logits, bias, T, E, k, ids, weights);
-    else if (E <= 512) route_kernel<16><<<grid, 256, 0, st>>>(logits, bias, T, E, k, ids, weights);
-    else route_kernel<32><<<grid, 256, 0, st>>>(logits, bias, T, E, k, ids, weights);
+    if (rule == RULE_SOFTMAX_THEN_BIAS)
+        launch_route_rule<RULE_SOFTMAX_THEN_BIAS>(logits, bias, T, E, k, scale, ids, weights, st);
+    else if (rule == RULE_SQRTSOFTPLUS)
+        launch_route_rule<RULE_SQRTSOFTPLUS>(logits, bias, T, E, k, scale, ids, weights, st);
+    else
+        launch_route_rule<RULE_SOFTMAX>(logits, bias, T, E, k, scale, ids, weights, st);
 }
 
 bool route_permute_small_ok(int T, int k) { return T <= 32 && T * k <= 256; }
 
+template <int RULE>
+void launch_small_rule(const float* logits, const float* bias, int T, int E, int k, float scale,
+                       const MoeRouting& out, int32_t* status, cudaStream_t st) {
+    const dim3 g(1), b(kSmallThreads);
+    if (E <= 32) route_permute_small_kernel<1, RULE><<<g, b, 0, st>>>(logits, bias, T, E, k, scale, out, status);
+    else if (E <= 64) route_permute_small_kernel<2, RULE><<<g, b, 0, st>>>(logits, bias, T, E, k, scale, out, status);
+    else if (E <= 128) route_permute_small_kernel<4, RULE><<<g, b, 0, st>>>(logits, bias, T, E, k, scale, out, status);
+    else if (E <= 256) route_permute_small_kernel<8, RULE><<<g, b, 0, st>>>(logits, bias, T, E, k, scale, out, status);
+    else if (E <= 512) route_permute_small_kernel<16, RULE><<<g, b, 0, st>>>(logits, bias, T, E, k, scale, out, status);
+    else route_permute_small_kernel<32, RULE><<<g, b, 0, st>>>(logits, bias, T, E, k, scale, out, status);
+}
+
 void launch_route_permute_small(const float* logits, const float* bias, int T, int E, int k, const MoeRouting& out,
-                                cudaStream_t st) {
+                                cudaStream_t st, int rule, float scale) {
     note_launch();
     int32_t* status = device_status_ptr();
-    if (E <= 32) route_permute_small_kernel<1><<<1, kSmallThreads, 0, st>>>(logits, bias, T, E, k, out, status);
-    else if (E <= 64) route_permute_small_kernel<2><<<1, kSmallThreads, 0, st>>>(logits, bias, T, E, k, out, status);
-    else if (E <= 128) route_permute_small_kernel<4><<<1, kSmallThreads, 0, st>>>(logits, bias, T, E, k, out, status);
-    else if (E <= 256) route_permute_small_kernel<8><<<1, kSmallThreads, 0, st>>>(logits, bias, T, E, k, out, status);
-    else if (E <= 512) route_permute_small_kernel<16><<<1, kSmallThreads, 0, st>>>(logits, bias, T, E, k, out, status);
-    else route_permute_small_kernel<32><<<1, kSmallThreads, 0, st>>>(logits, bias, T, E, k, out, status);
+    if (rule == RULE_SOFTMAX_THEN_BIAS)
+        launch_small_rule<RULE_SOFTMAX_THEN_BIAS>(logits, bias, T, E, k, scale, out, status, st);
+    else if (rule == RULE_SQRTSOFTPLUS)
+        launch_small_rule<RULE_SQRTSOFTPLUS>(logits, bias, T, E, k, scale, out, status, st);
+    else
+        launch_small_rule<RULE_SOFTMAX>(logits, bias, T, E, k, scale, out, status, st);
 }
 
 size_t permute_scratch_bytes(int P, int E) {
@@ -390,6 +473,22 @@ extern "C" bq_status bq_moe_route(const float* logits, const float* bias, int32_
     if ((s = bq::check_arch()) != BQ_OK) return s;
     bq::launch_route(logits, bias, T, E, k, ids, weights, (cudaStream_t)stream);
     return bq::check_launch("bq_moe_route");
+}
+
+extern "C" bq_status bq_moe_route_scored(const float* logits, const float* bias, int32_t T, int32_t E, int32_t k,
+                                         int32_t scoring, float scale, int32_t* ids, float* weights,
+                                         bq_stream_t stream) {
+    bq_status s = bq::validate_route("bq_moe_route_scored", T, E, k);
+    if (s == BQ_OK && (scoring < BQ_SCORE_SOFTMAX || scoring > BQ_SCORE_SQRTSOFTPLUS))
+        s = bq::fail(BQ_ERR_SHAPE, "bq_moe_route_scored: unknown scoring rule %d", scoring);
+    if (s != BQ_OK || T == 0) return s;
+    if (!logits || !ids || !weights) return bq::fail(BQ_ERR_NULL, "bq_moe_route_scored: NULL pointer");
+    if (!bq::aligned(logits, 4) || !bq::aligned(ids, 4) || !bq::aligned(weights, 4) ||
+        (bias && !bq::aligned(bias, 4)))
+        return bq::fail(BQ_ERR_ALIGN, "bq_moe_route_scored: pointers must be 4-byte aligned");
+    if ((s = bq::check_arch()) != BQ_OK) return s;
+    bq::launch_route(logits, bias, T, E, k, ids, weights, (cudaStream_t)stream, scoring, scale);
+    return bq::check_launch("bq_moe_route_scored");
 }
 
 extern "C" size_t bq_moe_permute_workspace_bytes(int32_t T, int32_t k, int32_t E) {

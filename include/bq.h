@@ -176,6 +176,34 @@ bq_status bq_qmm(const uint16_t* x, int32_t m, const bq_qweight* w, float* y,
 bq_status bq_moe_route(const float* logits, const float* bias, int32_t T, int32_t E,
                        int32_t k, int32_t* ids, float* weights, bq_stream_t stream);
 
+/* Router scoring rules (S5 variants). */
+typedef enum {
+    /* bq_moe_route above: bias added to the logits, softmax over the selected */
+    BQ_SCORE_SOFTMAX = 0,
+    /* [slimserve] LFM2-MoE "softmax-then-bias": p = softmax(logits) over all
+     * E; select the k largest p[e] + bias[e]; weights = the selected p,
+     * renormalised to sum to 1 */
+    BQ_SCORE_SOFTMAX_THEN_BIAS = 1,
+    /* [iron] DeepSeek V4 scoring: s = sqrt(softplus(logit)) with softplus(x) =
+     * max(x, 0) + log1p(exp(-|x|)); select the k largest s[e] + bias[e]
+     * (aux-loss-free bias); weights = the selected unbiased s times `scale`
+     * (the routed scaling factor), not renormalised */
+    BQ_SCORE_SQRTSOFTPLUS = 2
+} bq_scoring;
+
+/*
+ * Router top-k under a scoring rule.  Same layouts, ordering (descending
+ * selection key, ties to the lower e) and errors as bq_moe_route, plus
+ * BQ_ERR_SHAPE for an unknown `scoring`.  `scale` is used by
+ * BQ_SCORE_SQRTSOFTPLUS only.  For BQ_SCORE_SOFTMAX the result equals
+ * bq_moe_route.  Keys of the two other rules are computed in fp32 with
+ * expf / log1pf / sqrtf, so where two keys differ by a rounding error the
+ * choice between them may differ from an exact evaluation.
+ */
+bq_status bq_moe_route_scored(const float* logits, const float* bias, int32_t T, int32_t E,
+                              int32_t k, int32_t scoring, float scale, int32_t* ids,
+                              float* weights, bq_stream_t stream);
+
 /* ------------------------------------------------------------------ S6, S7
  * Expert histogram, exclusive scan and deterministic token permutation
  * (the per-expert work queue of [slimserve] qc_moe_mm_map0 and the
@@ -239,8 +267,10 @@ bq_status bq_moe_permute_noalloc(const int32_t* ids, int32_t T, int32_t k, int32
  *   shared_gate_up / shared_down: NULL, or dense weights (n_mats = 1) of
  *   the shared expert, with its own intermediate size.
  * x: device fp16 [T][hidden]; router_logits: device fp32 [T][E];
- * logit_bias: device fp32 [E] or NULL (added before selection and
- * weighting); y: device fp32 [T][hidden].
+ * logit_bias: device fp32 [E] or NULL; how it and the logits become the
+ * routing is set by desc->scoring (bq_scoring; BQ_SCORE_SOFTMAX adds the bias
+ * before selection and weighting) and desc->route_scale (the routed scaling
+ * factor of BQ_SCORE_SQRTSOFTPLUS); y: device fp32 [T][hidden].
  * workspace: device, >= bq_moe_workspace_bytes(desc) bytes, 256-aligned.
  * Errors: as above, plus BQ_ERR_FORMAT if the weights' shapes disagree
  * with the descriptor.
@@ -251,11 +281,13 @@ typedef struct {
     int32_t inter;
     int32_t n_experts;   /* E, 1..1024 */
     int32_t topk;        /* 1..min(8, E) */
-    int32_t reserved;
+    int32_t scoring;     /* bq_scoring (0 = BQ_SCORE_SOFTMAX) */
     bq_qweight w_gate_up;
     bq_qweight w_down;
     const bq_qweight* shared_gate_up;  /* host pointer or NULL */
     const bq_qweight* shared_down;     /* host pointer or NULL */
+    float route_scale;   /* routed scaling factor (BQ_SCORE_SQRTSOFTPLUS) */
+    int32_t reserved;
 } bq_moe_desc;
 
 size_t bq_moe_workspace_bytes(const bq_moe_desc* desc);

@@ -73,7 +73,7 @@ def expert_slice(fmt: str, w, e: int):
     return w[e]
 
 
-def build_layer(bq, inp: synth.MoEInputs):
+def build_layer(bq, inp: synth.MoEInputs, scoring: str = "softmax", route_scale: float = 1.0):
     """Device weights + descriptor for a MoE case."""
     c = inp.case
     gu = make_qweight(bq, c.fmt, inp.w_gu, c.experts, 2 * c.inter, c.hidden, swiglu=True)
@@ -82,7 +82,8 @@ def build_layer(bq, inp: synth.MoEInputs):
     if inp.shared_gu is not None:
         s_gu = make_qweight(bq, "q8_0", inp.shared_gu, 1, 2 * c.inter, c.hidden, swiglu=True)
         s_d = make_qweight(bq, "q8_0", inp.shared_d, 1, c.hidden, c.inter)
-    return bq.MoELayer(c.t, c.hidden, c.inter, c.experts, c.topk, gu, dn, s_gu, s_d)
+    return bq.MoELayer(c.t, c.hidden, c.inter, c.experts, c.topk, gu, dn, s_gu, s_d,
+                       scoring=bq.SCORING_BY_NAME[scoring], route_scale=route_scale)
 
 
 def run_moe(bq, layer, inp: synth.MoEInputs):
@@ -98,10 +99,12 @@ def run_moe(bq, layer, inp: synth.MoEInputs):
     return y.cpu().numpy()
 
 
-def oracle_moe(inp: synth.MoEInputs, tokens=None):
-    """fp64 oracle of the MoE layer (optionally on a subset of tokens)."""
+def oracle_moe(inp: synth.MoEInputs, tokens=None, ids=None, wts=None):
+    """fp64 oracle of the MoE layer (optionally on a subset of tokens, and
+    optionally with given routing ids / weights instead of the plain rule)."""
     c = inp.case
-    ids, wts = O.route(inp.logits, c.topk, inp.bias)
+    if ids is None:
+        ids, wts = O.route(inp.logits, c.topk, inp.bias)
     cache = {}
 
     def gu(e):
@@ -123,3 +126,42 @@ def oracle_moe(inp: synth.MoEInputs, tokens=None):
     if tokens is None:
         return O.moe_ffn(inp.x, ids, wts, gu, dn, shared)
     return O.moe_ffn_tokens(inp.x, ids, wts, tokens, gu, dn, shared)
+
+
+def route_scored_dev(bq, logits, k, bias, scoring: str, scale: float = 1.0):
+    """The GPU router under a scoring rule (ids, weights as numpy)."""
+    import torch
+    t, e = logits.shape
+    ids = torch.empty((t, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((t, k), dtype=torch.float32, device="cuda")
+    bq.moe_route_scored(dev(np.ascontiguousarray(logits, dtype=np.float32)),
+                        dev(np.ascontiguousarray(bias, dtype=np.float32)) if bias is not None else None,
+                        k, bq.SCORING_BY_NAME[scoring], scale, ids, w)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), w.cpu().numpy()
+
+
+def check_scored_choice(ids, key, k, rtol=2e-5):
+    """ids [T, k] must be a top-k of the exact keys [T, E], in descending key
+    order, up to keys closer than the fp32 evaluation error (where either
+    choice is correct)."""
+    for t in range(key.shape[0]):
+        sel = ids[t]
+        assert len(set(sel.tolist())) == k, (t, sel)
+        kt = key[t]
+        kth = np.sort(kt)[::-1][k - 1]
+        tol = rtol * max(1.0, abs(kth))
+        assert np.all(kt[sel] >= kth - tol), (t, sel, kt[sel], kth)
+        assert np.all(np.diff(kt[sel]) <= tol), (t, sel, kt[sel])
+
+
+def scored_weights(logits, ids, scoring: str, scale: float = 1.0):
+    """fp64 weights of the rule for the given (device-chosen) experts."""
+    x = np.asarray(logits, dtype=np.float64)
+    if scoring == "softmax_then_bias":
+        ex = np.exp(x - x.max(axis=1, keepdims=True))
+        p = ex / ex.sum(axis=1, keepdims=True)
+        sel = np.take_along_axis(p, ids.astype(np.int64), axis=1)
+        return sel / sel.sum(axis=1, keepdims=True)
+    s = np.sqrt(O.softplus(x))
+    return np.take_along_axis(s, ids.astype(np.int64), axis=1) * scale

@@ -68,7 +68,8 @@ def test_permute_workspace_query(bq):
 def test_struct_layout_matches_header(bq):
     assert ctypes.sizeof(bq.QWeightC) == 32
     assert bq.MoEDescC.w_gate_up.offset == 24
-    assert ctypes.sizeof(bq.MoEDescC) == 24 + 32 + 32 + 16
+    assert ctypes.sizeof(bq.MoEDescC) == 24 + 32 + 32 + 16 + 8
+    assert bq.MoEDescC.route_scale.offset == 104
 
 
 def test_host_validation_rejects_before_launch(bq):
@@ -76,6 +77,7 @@ def test_host_validation_rejects_before_launch(bq):
     lib = bq._lib
     assert lib.bq_moe_route(None, None, 4, 2000, 2, None, None, None) == 2        # E > 1024
     assert lib.bq_moe_route(None, None, 4, 16, 9, None, None, None) == 2          # k > 8
+    assert lib.bq_moe_route_scored(None, None, 4, 16, 2, 3, 1.0, None, None, None) == 2   # unknown rule
     assert lib.bq_gguf_dequant_q8_0(None, -1, None, None) == 2
     assert lib.bq_gguf_dequant_q8_0(None, 5, None, None) == 1
     assert lib.bq_gguf_dequant_q2_k(ctypes.c_void_p(8), 5, ctypes.c_void_p(16), None) == 3   # misaligned

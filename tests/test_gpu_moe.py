@@ -163,3 +163,23 @@ def test_moe_decode_concurrent_streams(lib):
         for y in outs[i]:
             np.testing.assert_array_equal(y.cpu().numpy().view(np.uint32), ref[i].view(np.uint32))
     assert_close_matmul(ref[0], oracle_moe(inps[0]), "concurrent streams")
+
+
+@pytest.mark.parametrize("scoring", ["softmax_then_bias", "sqrtsoftplus"])
+@pytest.mark.parametrize("t", [3, 45])   # decode path and tensor-core path
+def test_moe_scored_routing(lib, scoring, t):
+    # The layer routes with the rule; its choice is checked against the exact
+    # keys (up to fp32 near-ties) and the expert math against the oracle on
+    # the same choice, with the rule's fp64 weights.
+    import oracle as O
+    from helpers import check_scored_choice, route_scored_dev, scored_weights
+    case = synth.dataclasses.replace(SMALL[2], t=t, name=f"scored_{scoring}_{t}")
+    inp = synth.moe_inputs(case)
+    scale = 2.5 if scoring == "sqrtsoftplus" else 1.0
+    layer = build_layer(lib, inp, scoring=scoring, route_scale=scale)
+    got = run_moe(lib, layer, inp)
+    ids, _ = route_scored_dev(lib, inp.logits, case.topk, inp.bias, scoring, scale)
+    _, _, key = O.route_scored(inp.logits, case.topk, inp.bias, scoring, scale)
+    check_scored_choice(ids, key, case.topk)
+    ref = oracle_moe(inp, ids=ids, wts=scored_weights(inp.logits, ids, scoring, scale))
+    assert_close_matmul(got, ref, case.name)

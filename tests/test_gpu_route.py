@@ -94,3 +94,36 @@ def test_permute_flags_bad_expert_ids(lib):
     assert lib.device_status() == lib.DEV_OK       # reading clears it
     assert got["counts"].sum() == 5
     assert got["inv"][2] == -1
+
+
+@pytest.mark.parametrize("scoring", ["softmax_then_bias", "sqrtsoftplus"])
+@pytest.mark.parametrize("e,k,t", [(8, 2, 33), (128, 8, 300), (256, 6, 517), (288, 8, 64), (1024, 4, 40)])
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_route_scored_matches_oracle(lib, scoring, e, k, t, with_bias):
+    from helpers import check_scored_choice, route_scored_dev, scored_weights
+    g = np.random.default_rng(e * 131 + k * 7 + t + with_bias)
+    logits = (g.standard_normal((t, e)) * 2).astype(np.float32)
+    bias = (g.standard_normal(e) * 0.05).astype(np.float32) if with_bias else None
+    ids, w = route_scored_dev(lib, logits, k, bias, scoring, scale=2.5)
+    _, _, key = O.route_scored(logits, k, bias, scoring, scale=2.5)
+    check_scored_choice(ids, key, k)
+    np.testing.assert_allclose(w, scored_weights(logits, ids, scoring, 2.5), rtol=2e-5, atol=1e-7)
+
+
+def test_route_scored_softmax_is_bq_moe_route(lib):
+    from helpers import route_scored_dev
+    g = np.random.default_rng(17)
+    logits = g.standard_normal((77, 64)).astype(np.float32)
+    bias = (g.standard_normal(64) * 0.3).astype(np.float32)
+    ids_a, w_a = route_scored_dev(lib, logits, 6, bias, "softmax")
+    ids_b, w_b = _route(lib, logits, 6, bias)
+    np.testing.assert_array_equal(ids_a, ids_b)
+    np.testing.assert_array_equal(w_a.view(np.uint32), w_b.view(np.uint32))
+
+
+def test_route_sqrtsoftplus_large_logits_do_not_overflow(lib):
+    from helpers import route_scored_dev
+    logits = np.array([[100.0, 88.5, -100.0, 0.0, 30.0, -3.0, 95.0, 89.0]], dtype=np.float32)
+    ids, w = route_scored_dev(lib, logits, 3, None, "sqrtsoftplus", scale=1.0)
+    assert ids.tolist() == [[0, 6, 7]]                       # 89.0 beats 88.5, no inf / NaN
+    np.testing.assert_allclose(w[0], np.sqrt([100.0, 95.0, 89.0]), rtol=1e-6)
