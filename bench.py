@@ -447,6 +447,22 @@ def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "dense")):
             dense[f"dequant_{case.fmt}_4096x4096"] = {"us": round(t * 1e6, 2), "GB_s": round(byt / t / 1e9, 1),
                                                        "frac_hbm": round(byt / t / 1e9 / pk["hbm_gbs"], 4)}
     out["dense"] = dense
+    # router rules on the prefill router shape (T = 2048, E = 256, top-6, with a bias)
+    route = {}
+    g = synth.rng(4242)
+    lg = upload(synth.fp32_normal(g, (2048, 256)))
+    rb = upload((synth.fp32_normal(g, (256,)) * 0.05).astype(np.float32))
+    ids = torch.empty((2048, 6), dtype=torch.int32, device="cuda")
+    wts = torch.empty((2048, 6), dtype=torch.float32, device="cuda")
+    for name, rule in bq.SCORING_BY_NAME.items():
+        fn = lambda: bq.moe_route_scored(lg, rb, 6, rule, 2.5, ids, wts)
+        for _ in range(3):
+            fn()
+        ms, _ = time_steps(fn, 20, flush)
+        t = statistics.median(ms) / 1e3
+        byt = 2048 * 256 * 4 + 256 * 4 + 2048 * 6 * 8
+        route[name] = {"us": round(t * 1e6, 2), "GB_s": round(byt / t / 1e9, 1)}
+    out["route_t2048_e256_k6"] = route
     return out
 
 
