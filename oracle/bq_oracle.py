@@ -27,6 +27,8 @@ Readings taken where the pages are silent (each also listed in the design doc):
   d @80, dmin @82.
 * Q8_0 block: fp16 d first, then 32 quant bytes.
 * int4: value ``8w + i`` is bits ``4i..4i+3`` of word w (low nibble first).
+* MXFP4: byte ``i`` of a block's 16 code bytes holds value ``2i`` in its low
+  nibble and ``2i + 1`` in its high nibble ("low nibble first").
 * Top-k: the k largest ``z = logit (+ bias)`` computed in fp32, ties to
   the lower expert index, output in descending z; the bias enters both
   selection and weighting.
@@ -43,7 +45,7 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
-    "dequant_q8_0", "dequant_q2_k", "dequant_int4", "qmm", "route",
+    "dequant_q8_0", "dequant_q2_k", "dequant_int4", "dequant_mxfp4", "MXFP4_VALUES", "qmm", "route",
     "SCORINGS", "softplus", "route_scored",
     "permute", "silu", "swiglu_ffn", "moe_ffn", "moe_ffn_tokens",
 ]
@@ -124,6 +126,35 @@ def dequant_int4(words: np.ndarray, scales: np.ndarray, biases: np.ndarray,
     s = np.repeat(scales.astype(np.float64), group, axis=-1)
     b = np.repeat(biases.astype(np.float64), group, axis=-1)
     return q * s + b
+
+
+MXFP4_BLOCK_VALUES = 32
+MXFP4_BLOCK_BYTES = 17
+# the 4-bit element codes: bit 3 = sign, bits 0-2 index the magnitudes
+MXFP4_VALUES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+                         -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0])
+
+
+def dequant_mxfp4(blocks: np.ndarray) -> np.ndarray:
+    """MXFP4 (OCP MX v1.0): 17 bytes per 32 values, ``w = table[code] * 2^(e-127)``.
+
+    Follows *iron #9* (DeepSeek V4-Flash MXFP4 experts): a block is one E8M0
+    exponent byte ``e`` (the block scale ``2^(e - 127)``; ``e = 0xFF`` is the
+    NaN scale) followed by 16 bytes holding the 32 4-bit codes, low nibble
+    first (value ``2i`` in the low nibble of byte ``i``, value ``2i + 1`` in
+    the high nibble); each code indexes the value table
+    {0, +-0.5, +-1, +-1.5, +-2, +-3, +-4, +-6}, and no code is NaN.
+
+    blocks: uint8 [..., nb, 17].  Returns fp64 [..., nb * 32].
+    """
+    b = np.asarray(blocks, dtype=np.uint8)
+    assert b.shape[-1] == MXFP4_BLOCK_BYTES
+    e = b[..., 0].astype(np.float64)
+    scale = np.where(e == 255.0, np.nan, np.exp2(e - 127.0))          # [..., nb]
+    qs = b[..., 1:].astype(np.int64)                                   # [..., nb, 16]
+    codes = np.stack([qs & 0xF, qs >> 4], axis=-1).reshape(b.shape[:-1] + (32,))
+    vals = MXFP4_VALUES[codes] * scale[..., None]
+    return vals.reshape(b.shape[:-2] + (b.shape[-2] * 32,))
 
 
 # --------------------------------------------------------------------------

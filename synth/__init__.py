@@ -18,6 +18,9 @@ sizes and field roles, the byte order is the GGUF convention):
   PR #2, the ``moe_mm_id`` note on the AoS quant base ``84*blk+16``).
   Because every field is drawn uniformly, each quant/scale byte is a
   uniform byte.
+* MXFP4, 17 bytes per 32 values: the E8M0 exponent byte, then 16 bytes of
+  4-bit codes ("iron" PR #9, the DeepSeek V4-Flash MXFP4 block).  Exponents
+  are drawn in [118, 124] (block scales 2^-9 .. 2^-3), codes uniform.
 * int4 affine (MLX style), eight 4-bit codes per little-endian u32,
   one fp16 scale and one fp16 bias per group of 64 values along K
   ("butter" PR #10, the stacked ``[nExperts, outDim, inDim/8]`` weight of
@@ -81,6 +84,22 @@ def q2_k_blocks(g: np.random.Generator, rows: int, k: int,
     dmin = _fp16_uniform(g, d_range[0], d_range[1], (rows, nb))
     out[:, :, 80:82] = d.view(np.uint8).reshape(rows, nb, 2)
     out[:, :, 82:84] = dmin.view(np.uint8).reshape(rows, nb, 2)
+    return out
+
+
+MXFP4_BLOCK_VALUES = 32
+MXFP4_BLOCK_BYTES = 17
+
+
+def mxfp4_blocks(g: np.random.Generator, rows: int, k: int, e_range=(118, 124)) -> np.ndarray:
+    """MXFP4 weight [rows, k] as uint8 blocks [rows, k/32, 17]: the E8M0
+    exponent byte uniform in e_range (block scale 2^(e-127)), then 16 bytes
+    of uniform 4-bit codes."""
+    assert k % MXFP4_BLOCK_VALUES == 0
+    nb = k // MXFP4_BLOCK_VALUES
+    out = np.empty((rows, nb, MXFP4_BLOCK_BYTES), dtype=np.uint8)
+    out[:, :, 0] = g.integers(e_range[0], e_range[1] + 1, size=(rows, nb), dtype=np.uint8)
+    out[:, :, 1:] = g.integers(0, 256, size=(rows, nb, 16), dtype=np.uint8)
     return out
 
 

@@ -512,3 +512,63 @@ def test_scored_softmax_is_the_plain_rule():
     ids0, w0 = O.route(x, 4, b)
     np.testing.assert_array_equal(ids, ids0)
     np.testing.assert_array_equal(w, w0)
+
+
+# ---------------------------------------------------------------------------
+# MXFP4 (OCP MX v1.0 blocks of the DeepSeek V4-Flash experts)
+# ---------------------------------------------------------------------------
+
+def _mx_block(e, codes):
+    """One 17-byte block from an exponent byte and 32 codes (value 2i low nibble)."""
+    b = np.zeros(17, dtype=np.uint8)
+    b[0] = e
+    c = np.asarray(codes, dtype=np.uint8)
+    b[1:] = c[0::2] | (c[1::2] << 4)
+    return b
+
+
+def test_mxfp4_every_code_is_the_table():
+    # e = 127 -> scale 1: each code gives the page's value table entry
+    table = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+    codes = np.arange(32) % 16
+    v = O.dequant_mxfp4(_mx_block(127, codes)[None, :])
+    np.testing.assert_array_equal(v, [table[c] for c in codes])
+    assert np.signbit(v[8]) and not np.signbit(v[0])            # code 8 is -0
+    assert not np.any(np.isnan(v))                               # no code is NaN
+
+
+def test_mxfp4_scale_is_e8m0():
+    codes = np.full(32, 2)                                       # value 1.0
+    for e, want in ((127, 1.0), (128, 2.0), (120, 2.0 ** -7), (1, 2.0 ** -126), (0, 2.0 ** -127),
+                    (254, 2.0 ** 127)):
+        np.testing.assert_array_equal(O.dequant_mxfp4(_mx_block(e, codes)[None, :]), np.full(32, want))
+    assert np.all(np.isnan(O.dequant_mxfp4(_mx_block(255, codes)[None, :])))   # 0xFF is the NaN scale
+
+
+def test_mxfp4_low_nibble_first_and_block_order():
+    codes = np.zeros(32, dtype=np.int64)
+    codes[6] = 7                                                 # value 6 -> byte 3, low nibble
+    codes[7] = 15                                                # value 7 -> byte 3, high nibble
+    b = _mx_block(126, codes)
+    assert b[1 + 3] == 0xF7
+    v = O.dequant_mxfp4(b[None, :])
+    assert v[6] == 3.0 and v[7] == -3.0 and np.count_nonzero(v) == 2
+    two = np.stack([_mx_block(127, np.full(32, 2)), _mx_block(128, np.full(32, 4))])[None]   # [1, 2, 17]
+    v2 = O.dequant_mxfp4(two)
+    assert v2.shape == (1, 64) and np.all(v2[0, :32] == 1.0) and np.all(v2[0, 32:] == 4.0)
+
+
+def test_mxfp4_round_trip_quantiser():
+    # quantise random values to the nearest representable value of a block and
+    # decode: the error is at most half the largest gap of the scaled table
+    g = np.random.default_rng(3)
+    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    for _ in range(20):
+        e = int(g.integers(110, 135))
+        s = 2.0 ** (e - 127)
+        x = g.uniform(-6, 6, 32) * s
+        idx = np.abs(np.abs(x)[:, None] / s - mags[None, :]).argmin(axis=1)
+        codes = idx + 8 * (x < 0)
+        v = O.dequant_mxfp4(_mx_block(e, codes)[None, :])
+        assert np.all(np.abs(v - x) <= 1.0 * s + 1e-30)          # largest gap 2 (4 -> 6), half = 1
+        np.testing.assert_array_equal(np.abs(v), mags[idx] * s)
