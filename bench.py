@@ -47,7 +47,7 @@ def parse_args():
                     help="q2k: Q2_K experts + Q8_0 shared (default); int4: int4 experts, E=128, top-8")
     ap.add_argument("--decode-steps", type=int, default=200)
     ap.add_argument("--no-secondary", action="store_true", help="only the main step (faster)")
-    ap.add_argument("--only", choices=["decode", "int4", "dense"], default=None,
+    ap.add_argument("--only", choices=["decode", "int4", "mxfp4", "dense"], default=None,
                     help="run one secondary section alone and print it (no main step; for profiling)")
     ap.add_argument("--dense-case", default=None, help="with --only dense: run just this dense case")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -165,6 +165,8 @@ def qweight(bq, fmt, w, n_mats, n, k, swiglu=False):
     elif fmt == "q2_k":
         src = upload(np.asarray(w).reshape(-1))
         bq.repack_q2_k(src, q)
+    elif fmt == "mxfp4":
+        bq.repack_mxfp4(upload(np.asarray(w).reshape(-1)), q)
     else:
         bq.repack_int4(upload(w.words.reshape(-1).view(np.int32)), upload(w.scales.reshape(-1).view(np.int16)),
                        upload(w.biases.reshape(-1).view(np.int16)), q)
@@ -350,12 +352,12 @@ def run_main(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "dense")):
+def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "mxfp4", "dense")):
     import torch
     out = {}
-    # decode sweep: C4 shapes (primary reading) and C3 shapes
-    for base in (synth.MOE_Q2K, synth.MOE_INT4):
-        if "decode" not in sections and not (base.fmt == "int4" and "int4" in sections):
+    # decode sweep on each MoE workload; prefill of the int4 and MXFP4 ones
+    for base in (synth.MOE_Q2K, synth.MOE_INT4, synth.MOE_MXFP4):
+        if "decode" not in sections and base.fmt not in sections:
             continue
         weights = synth.moe_weights(base)
         layer = build_layer(bq, base, weights)
@@ -394,7 +396,7 @@ def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "dense")):
                             "tok_s": round(b * len(ms) / (sum(ms) / 1e3), 1)}
         if res:
             out[f"decode_{base.fmt}"] = res
-        if base.fmt == "int4" and "int4" in sections:
+        if base.fmt in ("int4", "mxfp4") and base.fmt in sections:
             layer.set_tokens(base.t)
             xh, lh = synth.moe_activations(base)
             x = upload(xh.view(np.uint16)).view(torch.float16)
@@ -407,7 +409,7 @@ def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "dense")):
                                  flush, stage_events=[1])
             fl = synth.moe_flops(base)
             gu = 2.0 * base.t * base.topk * 2 * base.inter * base.hidden
-            out["prefill_int4"] = {"workload": base.name, "tok_s": round(base.t / (statistics.mean(ms) / 1e3), 1),
+            out[f"prefill_{base.fmt}"] = {"workload": base.name, "tok_s": round(base.t / (statistics.mean(ms) / 1e3), 1),
                                    "ms": round(statistics.mean(ms), 4),
                                    "tflops": round(fl / (statistics.mean(ms) / 1e3) / 1e12, 2),
                                    "gate_up_tflops": round(gu / (statistics.mean(stg[1]) / 1e3) / 1e12, 2)}
@@ -446,6 +448,16 @@ def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "dense")):
             byt = flat.numel() + o.numel() * 4
             dense[f"dequant_{case.fmt}_4096x4096"] = {"us": round(t * 1e6, 2), "GB_s": round(byt / t / 1e9, 1),
                                                        "frac_hbm": round(byt / t / 1e9 / pk["hbm_gbs"], 4)}
+    # standalone MXFP4 dequantisation of a 4096 x 4096 weight
+    wm = upload(synth.mxfp4_blocks(synth.rng(4343), 4096, 4096).reshape(-1))
+    om = torch.empty(4096 * 4096, dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        bq.dequant_mxfp4(wm, om)
+    ms, _ = time_steps(lambda: bq.dequant_mxfp4(wm, om), 20, flush)
+    t = statistics.median(ms) / 1e3
+    byt = wm.numel() + om.numel() * 4
+    dense["dequant_mxfp4_4096x4096"] = {"us": round(t * 1e6, 2), "GB_s": round(byt / t / 1e9, 1),
+                                        "frac_hbm": round(byt / t / 1e9 / pk["hbm_gbs"], 4)}
     out["dense"] = dense
     # router rules on the prefill router shape (T = 2048, E = 256, top-6, with a bias)
     route = {}

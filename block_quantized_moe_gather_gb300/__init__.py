@@ -22,9 +22,9 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 # ---------------------------------------------------------------- constants
 OK = 0
-FMT_Q8_0, FMT_Q2_K, FMT_INT4_G64 = 1, 2, 3
-FMT_BY_NAME = {"q8_0": FMT_Q8_0, "q2_k": FMT_Q2_K, "int4": FMT_INT4_G64}
-DEV_OK, DEV_BAD_EXPERT_ID, DEV_WAIT_TIMEOUT = 0, 1, 2
+FMT_Q8_0, FMT_Q2_K, FMT_INT4_G64, FMT_MXFP4 = 1, 2, 3, 4
+FMT_BY_NAME = {"q8_0": FMT_Q8_0, "q2_k": FMT_Q2_K, "int4": FMT_INT4_G64, "mxfp4": FMT_MXFP4}
+DEV_OK, DEV_BAD_EXPERT_ID, DEV_WAIT_TIMEOUT, DEV_SCALE_RANGE = 0, 1, 2, 3
 STATUS_NAMES = {0: "BQ_OK", 1: "BQ_ERR_NULL", 2: "BQ_ERR_SHAPE", 3: "BQ_ERR_ALIGN", 4: "BQ_ERR_FORMAT",
                 5: "BQ_ERR_WORKSPACE", 6: "BQ_ERR_CUDA", 7: "BQ_ERR_DEVICE", 8: "BQ_ERR_ARCH"}
 
@@ -47,10 +47,12 @@ _SIGS = {
     "bq_device_status": (c_int32, [c_void_p, POINTER(c_int32)]),
     "bq_gguf_dequant_q8_0": (c_int32, [c_void_p, c_int64, c_void_p, c_void_p]),
     "bq_gguf_dequant_q2_k": (c_int32, [c_void_p, c_int64, c_void_p, c_void_p]),
+    "bq_dequant_mxfp4": (c_int32, [c_void_p, c_int64, c_void_p, c_void_p]),
     "bq_qweight_bytes": (c_size_t, [c_int32, c_int32, c_int32, c_int32]),
     "bq_repack_q8_0": (c_int32, [c_void_p, POINTER(QWeightC), c_void_p]),
     "bq_repack_q2_k": (c_int32, [c_void_p, POINTER(QWeightC), c_void_p]),
     "bq_repack_int4": (c_int32, [c_void_p, c_void_p, c_void_p, POINTER(QWeightC), c_void_p]),
+    "bq_repack_mxfp4": (c_int32, [c_void_p, POINTER(QWeightC), c_void_p]),
     "bq_qmm": (c_int32, [c_void_p, c_int32, POINTER(QWeightC), c_void_p, c_void_p]),
     "bq_moe_route": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p]),
     "bq_moe_route_scored": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_float, c_void_p,
@@ -126,6 +128,13 @@ def gguf_dequant_q2_k(blocks, out, stream=None):
     return out
 
 
+def dequant_mxfp4(blocks, out, stream=None):
+    """blocks: uint8 device tensor of n*17 bytes; out: fp32 device tensor of n*32."""
+    n = blocks.numel() // 17
+    _check(_lib.bq_dequant_mxfp4(_ptr(blocks), n, _ptr(out), _stream(stream)), "bq_dequant_mxfp4")
+    return out
+
+
 # ---------------------------------------------------------------- weights
 def qweight_bytes(fmt: int, n_mats: int, n: int, k: int) -> int:
     return int(_lib.bq_qweight_bytes(fmt, n_mats, n, k))
@@ -163,6 +172,11 @@ def repack_q2_k(blocks, w: QWeight, stream=None) -> QWeight:
 def repack_int4(words, scales, biases, w: QWeight, stream=None) -> QWeight:
     _check(_lib.bq_repack_int4(_ptr(words), _ptr(scales), _ptr(biases), ctypes.byref(w.c), _stream(stream)),
            "bq_repack_int4")
+    return w
+
+
+def repack_mxfp4(blocks, w: QWeight, stream=None) -> QWeight:
+    _check(_lib.bq_repack_mxfp4(_ptr(blocks), ctypes.byref(w.c), _stream(stream)), "bq_repack_mxfp4")
     return w
 
 

@@ -67,6 +67,9 @@ __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontro
 //                      (d,dmin) half2 [128]                          = 10752 B
 // int4  slab = 128 K : words u32 [128][16], (scale,bias) half2 [2][128]
 //                      (group g of row p at g*512 + 4p)              = 9216 B
+// MXFP4 slab = 128 K : words u32 [128][16] (codes, int4 word order),
+//                      E8M0 exponent bytes [128][4] (block b of row p
+//                      at 4p + b)                                     = 8704 B
 // Scale fields are stored group-major so that threads reading one group
 // of consecutive rows read consecutive words (no bank conflicts).
 //
@@ -75,6 +78,8 @@ __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontro
 // the pair (2p, 2p+1) in the two 16-bit lanes.
 // int4 word: value 2p in bits 4p..4p+3, value 2p+1 in bits 16+4p..19+4p
 // (p = 0..3), so (w >> 4p) & 0x000F000F holds the pair (2p, 2p+1).
+// MXFP4 codes use the same word order (one 16-byte chunk = one 32-value
+// block).
 //
 // The 64 quant bytes of physical row p are four 16-byte chunks; logical
 // chunk c (quant bytes 16c..16c+15 in K order) is stored at position
@@ -98,6 +103,7 @@ __host__ __device__ constexpr Fmt fmt_info(int fmt) {
     return fmt == BQ_FMT_Q8_0   ? Fmt{64, 8704, 8192}
          : fmt == BQ_FMT_Q2_K   ? Fmt{256, 10752, 8192}
          : fmt == BQ_FMT_INT4_G64 ? Fmt{128, 9216, 8192}
+         : fmt == BQ_FMT_MXFP4  ? Fmt{128, 8704, 8192}
                                   : Fmt{0, 0, 0};
 }
 
@@ -141,6 +147,40 @@ __device__ __forceinline__ __half2 s8pair_to_half2(uint32_t w_xor80, uint32_t se
     uint32_t h = __byte_perm(w_xor80, 0x64646464u, sel);
     __half2 v = *reinterpret_cast<__half2*>(&h);
     return __hsub2(v, __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+}
+
+// ---- MXFP4 (OCP MX v1.0 FP4: e2m1 codes, E8M0 block exponent)
+//
+// An e2m1 code s|E1 E0|M has magnitude 2^(E-1) * (1 + M/2) for E > 0 and
+// M/2 for E = 0.  Written into an fp16 as exponent field E (bits 10-11),
+// mantissa bit M (bit 9) and sign s (bit 15), the fp16 reads as exactly
+// that value times 2^-14: for E > 0 it is 2^(E-15) * (1 + M/2); for E = 0
+// it is the fp16 subnormal M * 2^-15.  So code -> fp16 costs only bit moves.
+//
+// Pair Q of an MXFP4 code word (nibble Q of each 16-bit lane, int4 word
+// order) as two such fp16 values.
+template <int Q>
+__device__ __forceinline__ uint32_t mx_pair_bits(uint32_t w) {
+    static_assert(Q >= 0 && Q <= 3, "four pairs per word");
+    const uint32_t mag = Q < 3 ? (w << (9 - 4 * Q)) : (w >> 3);   // nibble bits 0-2 -> 9-11
+    const uint32_t sgn = w << (12 - 4 * Q);                        // nibble bit 3 -> 15
+    return (mag & 0x0E000E00u) | (sgn & 0x80008000u);
+}
+
+// fp16 bits of 2^(e - 113), the factor that turns a code above into its
+// value times the block scale 2^(e - 127).  Exact for e in 89..128 (e 89..98
+// are fp16 subnormals).  For e <= 88 every scaled value rounds to 0 in fp16,
+// so 0 is returned; e = 255 (the E8M0 NaN) gives NaN; e in 129..254 gives
+// +inf (not representable here; the repack flags such blocks).
+__device__ __forceinline__ uint32_t mx_scale_bits(uint32_t e) {
+    uint32_t b = e >= 99u ? (e - 98u) << 10 : (e >= 89u ? 1u << (e - 89u) : 0u);
+    b = e > 128u ? 0x7C00u : b;
+    return e == 255u ? 0x7E00u : b;
+}
+
+__device__ __forceinline__ __half2 mx_scale_h2(uint32_t e) {
+    const uint32_t b = mx_scale_bits(e);
+    return u32_as_h2(b | (b << 16));
 }
 
 }  // namespace bq

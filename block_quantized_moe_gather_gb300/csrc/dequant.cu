@@ -1,4 +1,4 @@
-// Standalone GGUF block dequantisation to fp32 (Q8_0 and Q2_K).
+// Standalone block dequantisation to fp32: GGUF Q8_0 and Q2_K, and MXFP4.
 //
 // "feat(gguf,dsv4): GGUF block-dequant + DSv4 kernel surface (WIP)"
 // (thewafflehaus/iron PR #9), kernels 1 and 2: Q8_0 out[i] = qs[i] *
@@ -8,7 +8,11 @@
 // Each CTA stages a chunk of whole blocks into shared memory with 16-byte
 // loads (the chunk sizes keep every chunk start 16-byte aligned), then
 // writes the decoded values with 16-byte float4 stores.  The path is bound
-// by the fp32 writes (4 bytes out per 1.06 or 0.33 bytes in).
+// by the fp32 writes (4 bytes out per 1.06, 0.33 or 0.53 bytes in).
+//
+// Same page, MXFP4 section (DeepSeek V4-Flash MoE experts, OCP MX v1.0):
+// 17-byte blocks of one E8M0 exponent and 16 bytes of e2m1 codes, low
+// nibble first; value = table[code] * 2^(e - 127), NaN only through e = 255.
 #include <algorithm>
 
 #include "bq_internal.cuh"
@@ -18,6 +22,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kQ8BlocksPerChunk = 64;   // 64 * 34 = 2176 bytes = 136 x 16
 constexpr int kQ2BlocksPerChunk = 32;   // 32 * 84 = 2688 bytes = 168 x 16
+constexpr int kMxBlocksPerChunk = 64;   // 64 * 17 = 1088 bytes = 68 x 16
 
 // Copies `bytes` bytes from a 16-byte aligned global address to shared memory.
 __device__ __forceinline__ void stage_bytes(uint8_t* smem, const uint8_t* src, int bytes) {
@@ -92,6 +97,43 @@ dequant_q2_k_kernel(const uint8_t* __restrict__ blocks, int64_t n_blocks, float*
     }
 }
 
+// e2m1 code -> its value as an exact fp32: exponent field E and mantissa
+// bit M placed at the bottom of the fp32 exponent and the top of the
+// mantissa read as value * 2^-126 (E = 0: the subnormal M * 2^-127), and the
+// power-of-two factor is exact.
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+    const uint32_t bits = ((c & 7u) << 22) | ((c & 8u) << 28);
+    return __fmul_rn(__uint_as_float(bits), 0x1p126f);
+}
+
+// E8M0 exponent -> 2^(e - 127) as fp32 (e = 0: the subnormal 2^-127; 255: NaN).
+__device__ __forceinline__ float e8m0_scale(uint32_t e) {
+    return __uint_as_float(e == 255u ? 0x7FC00000u : e == 0u ? 0x00400000u : e << 23);
+}
+
+__global__ void __launch_bounds__(kThreads)
+dequant_mxfp4_kernel(const uint8_t* __restrict__ blocks, int64_t n_blocks, float* __restrict__ out) {
+    __shared__ __align__(16) uint8_t sm[kMxBlocksPerChunk * 17];
+    const int64_t n_chunks = (n_blocks + kMxBlocksPerChunk - 1) / kMxBlocksPerChunk;
+    for (int64_t c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+        const int64_t b0 = c * kMxBlocksPerChunk;
+        const int nb = (int)std::min<int64_t>(kMxBlocksPerChunk, n_blocks - b0);
+        __syncthreads();
+        stage_bytes(sm, blocks + b0 * 17, nb * 17);
+        __syncthreads();
+        const int n_vec = nb * 8;  // groups of 4 outputs
+        float4* o4 = reinterpret_cast<float4*>(out + b0 * 32);
+        for (int g = threadIdx.x; g < n_vec; g += kThreads) {
+            const int b = g >> 3, i0 = (g & 7) * 4;
+            const uint8_t* blk = sm + b * 17;
+            const float sc = e8m0_scale(blk[0]);
+            const uint32_t q01 = blk[1 + (i0 >> 1)], q23 = blk[2 + (i0 >> 1)];
+            o4[g] = make_float4(__fmul_rn(e2m1_value(q01 & 15u), sc), __fmul_rn(e2m1_value(q01 >> 4), sc),
+                                __fmul_rn(e2m1_value(q23 & 15u), sc), __fmul_rn(e2m1_value(q23 >> 4), sc));
+        }
+    }
+}
+
 int grid_for(int64_t chunks) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
@@ -131,4 +173,15 @@ extern "C" bq_status bq_gguf_dequant_q2_k(const void* blocks, int64_t n_blocks, 
         static_cast<const uint8_t*>(blocks), n_blocks, out);
     bq::note_launch();
     return bq::check_launch("bq_gguf_dequant_q2_k");
+}
+
+extern "C" bq_status bq_dequant_mxfp4(const void* blocks, int64_t n_blocks, float* out, bq_stream_t stream) {
+    bq_status s = validate("bq_dequant_mxfp4", blocks, n_blocks, out);
+    if (s != BQ_OK || n_blocks == 0) return s;
+    if ((s = bq::check_arch()) != BQ_OK) return s;
+    const int64_t chunks = (n_blocks + kMxBlocksPerChunk - 1) / kMxBlocksPerChunk;
+    dequant_mxfp4_kernel<<<grid_for(chunks), kThreads, 0, (cudaStream_t)stream>>>(
+        static_cast<const uint8_t*>(blocks), n_blocks, out);
+    bq::note_launch();
+    return bq::check_launch("bq_dequant_mxfp4");
 }

@@ -75,6 +75,7 @@ template <int FMT> struct G;
 template <> struct G<BQ_FMT_Q8_0>     { static constexpr int SK = 64,  SB = 8704,  SPS = 1, NR = 4; };
 template <> struct G<BQ_FMT_Q2_K>     { static constexpr int SK = 256, SB = 10752, SPS = 4, NR = 3; };
 template <> struct G<BQ_FMT_INT4_G64> { static constexpr int SK = 128, SB = 9216,  SPS = 2, NR = 3; };
+template <> struct G<BQ_FMT_MXFP4>    { static constexpr int SK = 128, SB = 8704,  SPS = 2, NR = 4; };
 static_assert(4 * 8704 <= kRawBytes && 3 * 10752 <= kRawBytes && 3 * 9216 <= kRawBytes, "raw ring");
 
 enum { EPI_SWIGLU = 0, EPI_SCALE = 1, EPI_PLAIN = 2 };
@@ -355,6 +356,29 @@ __device__ __forceinline__ void dequant_stage<BQ_FMT_INT4_G64>(const uint8_t* ra
     }
 }
 
+// MXFP4 block c of the slab (chunk c: four code words) scaled by the block's
+// exponent: 16 fp16 pairs.  The code fp16 (value * 2^-14) and the factor
+// 2^(e - 113) are exact, so the product is the scaled value rounded once.
+__device__ __forceinline__ void mx_block(const uint8_t* raw, int p, int c, uint32_t* out) {
+    const __half2 s2 = bq::mx_scale_h2(raw[8192 + 4 * p + c]);
+    const uint4 q = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, c));
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        out[4 * m + 0] = bq::h2_as_u32(__hmul2_rn(bq::u32_as_h2(bq::mx_pair_bits<0>(w[m])), s2));
+        out[4 * m + 1] = bq::h2_as_u32(__hmul2_rn(bq::u32_as_h2(bq::mx_pair_bits<1>(w[m])), s2));
+        out[4 * m + 2] = bq::h2_as_u32(__hmul2_rn(bq::u32_as_h2(bq::mx_pair_bits<2>(w[m])), s2));
+        out[4 * m + 3] = bq::h2_as_u32(__hmul2_rn(bq::u32_as_h2(bq::mx_pair_bits<3>(w[m])), s2));
+    }
+}
+
+template <>
+__device__ __forceinline__ void dequant_stage<BQ_FMT_MXFP4>(const uint8_t* raw, int p, int sub, uint32_t (&out)[32]) {
+    // stage `sub` = blocks 2sub, 2sub+1 of the 128-value slab
+    mx_block(raw, p, 2 * sub, out);
+    mx_block(raw, p, 2 * sub + 1, out + 16);
+}
+
 // Half h (K values 32h .. 32h + 31) of a 64-K stage as 16 fp16 pairs, the
 // same values dequant_stage gives for that half.
 template <int FMT>
@@ -423,6 +447,12 @@ __device__ __forceinline__ void dequant_half<BQ_FMT_INT4_G64>(const uint8_t* raw
         out[4 * m + 2] = bq::h2_as_u32(__hfma2(field_to_half2<0>(hi, 0x000F000Fu), s2, b2));
         out[4 * m + 3] = bq::h2_as_u32(__hfma2(field_to_half2<4>(hi, 0x000F000Fu), s2, b2));
     }
+}
+
+template <>
+__device__ __forceinline__ void dequant_half<BQ_FMT_MXFP4>(const uint8_t* raw, int p, int sub, int h,
+                                                           uint32_t (&out)[16]) {
+    mx_block(raw, p, 2 * sub + h, out);
 }
 
 __device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
@@ -787,6 +817,7 @@ void launch_epi(int fmt, const CUtensorMap& map, const GemmArgs& a, dim3 grid, c
     switch (fmt) {
         case BQ_FMT_Q8_0: launch_one<BQ_FMT_Q8_0, EPI>(map, a, grid, st); break;
         case BQ_FMT_Q2_K: launch_one<BQ_FMT_Q2_K, EPI>(map, a, grid, st); break;
+        case BQ_FMT_MXFP4: launch_one<BQ_FMT_MXFP4, EPI>(map, a, grid, st); break;
         default: launch_one<BQ_FMT_INT4_G64, EPI>(map, a, grid, st); break;
     }
 }
@@ -848,7 +879,8 @@ GemmWs carve(const bq_moe_desc* d, uint8_t* base) {
 namespace bq {
 
 bool gemm_supported(int fmt) {
-    return (fmt == BQ_FMT_Q8_0 || fmt == BQ_FMT_Q2_K || fmt == BQ_FMT_INT4_G64) && encode_fn() != nullptr;
+    return (fmt == BQ_FMT_Q8_0 || fmt == BQ_FMT_Q2_K || fmt == BQ_FMT_INT4_G64 || fmt == BQ_FMT_MXFP4) &&
+           encode_fn() != nullptr;
 }
 
 size_t gemm_moe_workspace_bytes(const bq_moe_desc* d) { return carve(d, nullptr).bytes; }

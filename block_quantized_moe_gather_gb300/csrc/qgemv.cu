@@ -35,6 +35,7 @@ template <int FMT> struct Traits;
 template <> struct Traits<BQ_FMT_Q8_0>     { static constexpr int SK = 64,  SB = 8704,  STEPS = 4,  XV = 2, DEPTH = 3; };
 template <> struct Traits<BQ_FMT_Q2_K>     { static constexpr int SK = 256, SB = 10752, STEPS = 16, XV = 8, DEPTH = 3; };
 template <> struct Traits<BQ_FMT_INT4_G64> { static constexpr int SK = 128, SB = 9216,  STEPS = 8,  XV = 4, DEPTH = 3; };
+template <> struct Traits<BQ_FMT_MXFP4>    { static constexpr int SK = 128, SB = 8704,  STEPS = 8,  XV = 4, DEPTH = 3; };
 
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
@@ -78,6 +79,8 @@ __device__ __forceinline__ void load_frag(Frag<FMT>& f, const uint8_t* slab, int
             } else if (FMT == BQ_FMT_Q2_K) {
                 f.sc[tile][hh] = __ldg(reinterpret_cast<const uint32_t*>(slab + 8192 + 512 * t + 4 * row));
                 f.dm[tile][hh] = __ldg(reinterpret_cast<const uint32_t*>(slab + 10240 + row * 4));
+            } else if (FMT == BQ_FMT_MXFP4) {
+                f.sc[tile][hh] = __ldg(slab + 8192 + 4 * row + t);   // the lane's quarter = block t
             } else {
                 f.sc[tile][hh] = __ldg(reinterpret_cast<const uint32_t*>(slab + 8192 + 512 * (t >> 1) + 4 * row));
             }
@@ -115,6 +118,16 @@ __device__ __forceinline__ __half2 q4_pair(uint32_t w, int p) {
         case 1: return field_h2<4>(w, 0x000F000Fu);
         case 2: return field_h2<0>(w >> 8, 0x000F000Fu);
         default: return field_h2<4>(w >> 8, 0x000F000Fu);
+    }
+}
+
+// Pair p of an MXFP4 code word as fp16 values times 2^-14 (see mx_pair_bits).
+__device__ __forceinline__ __half2 mx_pair(uint32_t w, int p) {
+    switch (p) {
+        case 0: return bq::u32_as_h2(bq::mx_pair_bits<0>(w));
+        case 1: return bq::u32_as_h2(bq::mx_pair_bits<1>(w));
+        case 2: return bq::u32_as_h2(bq::mx_pair_bits<2>(w));
+        default: return bq::u32_as_h2(bq::mx_pair_bits<3>(w));
     }
 }
 
@@ -198,6 +211,8 @@ __device__ __forceinline__ void mma_frag(const Frag<FMT>& f, const __half* xq, b
                     const __half2 sbh = bq::u32_as_h2(f.sc[tile][hh]);
                     sc2[tile][hh] = __low2half2(sbh);
                     bi2[tile][hh] = __high2half2(sbh);
+                } else if (FMT == BQ_FMT_MXFP4) {
+                    sc2[tile][hh] = bq::mx_scale_h2(f.sc[tile][hh]);
                 } else {
                     const __half d = __ushort_as_half((uint16_t)f.sc[tile][hh]);
                     d2[tile][hh] = __halves2half2(d, d);
@@ -217,6 +232,10 @@ __device__ __forceinline__ void mma_frag(const Frag<FMT>& f, const __half* xq, b
                     if (FMT == BQ_FMT_Q8_0) {
                         const uint32_t wx = comp(f.q[tile][hh], s) ^ 0x80808080u;
                         a[r] = bq::h2_as_u32(__hmul2(bq::s8pair_to_half2(wx, lohi ? 0x4342u : 0x4140u), d2[tile][hh]));
+                    } else if (FMT == BQ_FMT_MXFP4) {
+                        // exact fp16 operands: the product is the scaled value rounded once
+                        const uint32_t w = comp(f.q[tile][hh], s >> 1);
+                        a[r] = bq::h2_as_u32(__hmul2_rn(mx_pair(w, 2 * (s & 1) + lohi), sc2[tile][hh]));
                     } else {
                         const uint32_t w = comp(f.q[tile][hh], s >> 1);
                         a[r] = bq::h2_as_u32(__hfma2(q4_pair(w, 2 * (s & 1) + lohi), sc2[tile][hh], bi2[tile][hh]));
@@ -443,6 +462,7 @@ void launch_qgemv(const QgemvParams& params, int max_segments, cudaStream_t st, 
     switch (p.fmt) {
         case BQ_FMT_Q8_0: launch_fmt<BQ_FMT_Q8_0>(p, max_segments, after_previous, st); break;
         case BQ_FMT_Q2_K: launch_fmt<BQ_FMT_Q2_K>(p, max_segments, after_previous, st); break;
+        case BQ_FMT_MXFP4: launch_fmt<BQ_FMT_MXFP4>(p, max_segments, after_previous, st); break;
         default: launch_fmt<BQ_FMT_INT4_G64>(p, max_segments, after_previous, st); break;
     }
 }

@@ -118,6 +118,36 @@ __global__ void repack_int4_kernel(const uint32_t* __restrict__ words, const uin
     }
 }
 
+// MXFP4: the four 32-value blocks of the slab's K range; block b's 16 code
+// bytes (value 2i in the low nibble of byte i) go to chunk b in int4 word
+// order, its exponent byte to 8192 + 4p + b.  Exponents the matmul kernels
+// cannot represent (129..254) are kept but flagged.
+__global__ void repack_mxfp4_kernel(const uint8_t* __restrict__ src, int n, int k, int swiglu, int n_tiles,
+                                    int k_slabs, int64_t total, uint8_t* __restrict__ dst, int32_t* status) {
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        Item it = item_of(idx, n, swiglu, n_tiles, k_slabs, 8704, dst);
+        const int nb = k / 32;
+        const uint8_t* row = src + (((int64_t)it.e * n + it.row) * nb + 4 * it.kt) * 17;
+        for (int b = 0; b < 4; ++b) {
+            const uint8_t* blk = row + 17 * b;
+            const uint32_t e = blk[0];
+            if (e > 128u && e < 255u) bq::set_device_error(status, BQ_DEV_SCALE_RANGE);
+            it.slab[8192 + 4 * it.p + b] = (uint8_t)e;
+            for (int j = 0; j < 4; ++j) {
+                uint32_t w = 0;
+                for (int i = 0; i < 8; ++i) {
+                    const int v = 8 * j + i;   // value of the block
+                    const uint32_t q = (blk[1 + (v >> 1)] >> (4 * (v & 1))) & 15u;
+                    const int bit = (i & 1) ? 16 + 4 * (i >> 1) : 4 * (i >> 1);
+                    w |= q << bit;
+                }
+                *reinterpret_cast<uint32_t*>(it.slab + bq::quant_chunk_offset(it.p, b) + 4 * j) = w;
+            }
+        }
+    }
+}
+
 bq_status check_dst(const char* name, const bq_qweight* w, int want_fmt) {
     if (!w || !w->data) return bq::fail(BQ_ERR_NULL, "%s: dst or dst->data is NULL", name);
     if (w->fmt != want_fmt) return bq::fail(BQ_ERR_FORMAT, "%s: dst->fmt = %d", name, w->fmt);
@@ -181,4 +211,17 @@ extern "C" bq_status bq_repack_int4(const uint32_t* words, const uint16_t* scale
         static_cast<uint8_t*>(dst->data));
     bq::note_launch();
     return bq::check_launch("bq_repack_int4");
+}
+
+extern "C" bq_status bq_repack_mxfp4(const void* blocks, const bq_qweight* dst, bq_stream_t stream) {
+    bq_status s = check_dst("bq_repack_mxfp4", dst, BQ_FMT_MXFP4);
+    if (s != BQ_OK) return s;
+    if (!blocks) return bq::fail(BQ_ERR_NULL, "bq_repack_mxfp4: blocks is NULL");
+    if ((s = bq::check_arch()) != BQ_OK) return s;
+    Geometry g = geometry(dst);
+    repack_mxfp4_kernel<<<grid_for(g.rows_total), 256, 0, (cudaStream_t)stream>>>(
+        static_cast<const uint8_t*>(blocks), dst->n, dst->k, dst->swiglu, g.n_tiles, g.k_slabs, g.rows_total,
+        static_cast<uint8_t*>(dst->data), bq::device_status_ptr());
+    bq::note_launch();
+    return bq::check_launch("bq_repack_mxfp4");
 }

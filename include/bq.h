@@ -60,13 +60,16 @@ typedef enum {
 enum {
     BQ_DEV_OK = 0,
     BQ_DEV_BAD_EXPERT_ID = 1,   /* a routed expert id was outside [0, E)        */
-    BQ_DEV_WAIT_TIMEOUT = 2     /* a bounded mbarrier / flag wait ran out       */
+    BQ_DEV_WAIT_TIMEOUT = 2,    /* a bounded mbarrier / flag wait ran out       */
+    BQ_DEV_SCALE_RANGE = 3      /* an MXFP4 block exponent the device path cannot
+                                   represent (129..254) met bq_repack_mxfp4       */
 };
 
 typedef enum {
     BQ_FMT_Q8_0 = 1,      /* GGUF Q8_0: 32-value blocks, fp16 d + 32 int8 ([iron] kernel 1) */
     BQ_FMT_Q2_K = 2,      /* GGUF Q2_K: 256-value super-blocks of 84 bytes ([iron] kernel 2) */
-    BQ_FMT_INT4_G64 = 3   /* MLX int4 affine, 8 codes per u32, fp16 scale+bias per 64 ([butter]) */
+    BQ_FMT_INT4_G64 = 3,  /* MLX int4 affine, 8 codes per u32, fp16 scale+bias per 64 ([butter]) */
+    BQ_FMT_MXFP4 = 4      /* OCP MX FP4: 32 e2m1 codes + one E8M0 exponent per block ([iron]) */
 } bq_format;
 
 /*
@@ -80,14 +83,15 @@ typedef enum {
  *
  * Layout (informative): for each matrix, 128-row tile and K-slab, one
  * contiguous slab of bytes holding 64 quant bytes per row followed by the
- * slab's scale fields.  K-slab width: Q8_0 64, Q2_K 256, int4 128 values.
- * Bytes per weight equal the on-disk format's (34/32, 84/256, 9/16).
+ * slab's scale fields.  K-slab width: Q8_0 64, Q2_K 256, int4 and MXFP4
+ * 128 values.  Bytes per weight equal the on-disk format's (34/32, 84/256,
+ * 9/16, 17/32).
  */
 typedef struct {
     int32_t fmt;      /* bq_format */
     int32_t n_mats;
     int32_t n;        /* multiple of 128 */
-    int32_t k;        /* multiple of 256 (Q2_K), 128 (int4) or 64 (Q8_0) */
+    int32_t k;        /* multiple of 256 (Q2_K), 128 (int4, MXFP4) or 64 (Q8_0) */
     int32_t swiglu;   /* 0 or 1 */
     int32_t reserved;
     void* data;       /* device */
@@ -126,6 +130,24 @@ bq_status bq_gguf_dequant_q8_0(const void* blocks, int64_t n_blocks, float* out,
 bq_status bq_gguf_dequant_q2_k(const void* blocks, int64_t n_blocks, float* out,
                                bq_stream_t stream);
 
+/*
+ * Standalone MXFP4 block dequantisation to fp32 ([iron]: DeepSeek V4-Flash
+ * MXFP4 experts, OCP MX v1.0 block of 17 bytes per 32 values).  Block b is
+ * one E8M0 exponent byte e followed by 16 code bytes; code byte i holds
+ * value 2i in its low nibble and value 2i + 1 in its high nibble.
+ *   out[32b + v] = lut[code_v] * 2^(e - 127),
+ *   lut = {0, 0.5, 1, 1.5, 2, 3, 4, 6, -0, -0.5, -1, -1.5, -2, -3, -4, -6}
+ * and e = 255 gives NaN for every value of the block (the only NaN of the
+ * format).  Every output is the exact value in fp32 (e = 0 gives fp32
+ * subnormals), except magnitudes of 2^128 and above (e >= 253), which
+ * overflow to +-inf as fp32 rounding gives.
+ * blocks: device, n_blocks blocks of 17 bytes back to back.
+ * out:    device fp32 [n_blocks * 32].
+ * Errors: BQ_ERR_NULL, BQ_ERR_SHAPE (n_blocks < 0), BQ_ERR_ALIGN, BQ_ERR_CUDA.
+ * n_blocks == 0 is a no-op.
+ */
+bq_status bq_dequant_mxfp4(const void* blocks, int64_t n_blocks, float* out, bq_stream_t stream);
+
 /* ------------------------------------------------------------------ S0
  * Load-time repack of on-disk blocks into the device layout ([iron]:
  * CPU-side decomposition of each block into separate GPU tensors;
@@ -136,8 +158,16 @@ bq_status bq_gguf_dequant_q2_k(const void* blocks, int64_t n_blocks, float* out,
  *   Q2_K: blocks [n_mats][n][k/256] x 84 bytes
  *   int4: words [n_mats][n][k/8] u32 (value 8w+i in bits 4i..4i+3),
  *         scales and biases [n_mats][n][k/64] fp16 (passed as uint16 bits)
+ *   MXFP4: blocks [n_mats][n][k/32] x 17 bytes (as bq_dequant_mxfp4; any
+ *         alignment)
  * dst->fmt/n_mats/n/k/swiglu/data must be filled in by the caller.
  * Errors: BQ_ERR_NULL, BQ_ERR_FORMAT, BQ_ERR_SHAPE, BQ_ERR_ALIGN, BQ_ERR_CUDA.
+ *
+ * MXFP4 on the device: the matmul kernels turn each value into the fp16
+ * rounding of lut[code] * 2^(e - 127), which they can form exactly for
+ * e <= 128 (for e <= 88 that rounding is 0) and for e = 255 (NaN).  Blocks
+ * with e in 129..254 (block scales of 4 and above) are stored unchanged but set
+ * BQ_DEV_SCALE_RANGE on the device; matmuls over them give +-inf or NaN.
  */
 size_t bq_qweight_bytes(int32_t fmt, int32_t n_mats, int32_t n, int32_t k);
 bq_status bq_repack_q8_0(const void* blocks, const bq_qweight* dst, bq_stream_t stream);
@@ -145,6 +175,7 @@ bq_status bq_repack_q2_k(const void* blocks, const bq_qweight* dst, bq_stream_t 
 bq_status bq_repack_int4(const uint32_t* words, const uint16_t* scales,
                          const uint16_t* biases, const bq_qweight* dst,
                          bq_stream_t stream);
+bq_status bq_repack_mxfp4(const void* blocks, const bq_qweight* dst, bq_stream_t stream);
 
 /* ------------------------------------------------------------------ S3, S4
  * Dense qmm: Y[m][r] = sum_k X[m][k] * W[r][k] with W the dequantised

@@ -149,7 +149,7 @@ class DenseCase:
 @dataclasses.dataclass(frozen=True)
 class MoECase:
     name: str
-    fmt: str          # routed expert format: "int4" | "q2_k"
+    fmt: str          # routed expert format: "int4" | "q2_k" | "mxfp4"
     t: int            # tokens
     hidden: int
     inter: int
@@ -172,6 +172,14 @@ MOE_INT4 = MoECase("moe_int4_t2048_h2048_e128_top8_i768", "int4", 2048, 2048, 76
                    128, 8, False, None, 1002)
 MOE_Q2K = MoECase("moe_q2k_t2048_h4096_e256_top6_i2048_zipf_sharedq8", "q2_k", 2048,
                   4096, 2048, 256, 6, True, "q8_0", 1003)
+
+
+# The int4 MoE shapes with MXFP4 experts (DeepSeek V4-Flash ships its MoE
+# experts as MXFP4).  Block exponents 116..122: block scales 2^-11..2^-5, so
+# weights of magnitude up to about 0.2, typical around 0.01.
+MXFP4_EXPERT_E_RANGE = (116, 122)
+MOE_MXFP4 = MoECase("moe_mxfp4_t2048_h2048_e128_top8_i768", "mxfp4", 2048, 2048, 768,
+                    128, 8, False, None, 1005)
 
 
 def decode_case(base: MoECase, batch: int) -> MoECase:
@@ -207,6 +215,9 @@ def moe_weights(case: MoECase):
     elif case.fmt == "q2_k":
         w_gu = q2_k_blocks(g, e * 2 * i, h).reshape(e, 2 * i, h // 256, 84)
         w_d = q2_k_blocks(g, e * h, i).reshape(e, h, i // 256, 84)
+    elif case.fmt == "mxfp4":
+        w_gu = mxfp4_blocks(g, e * 2 * i, h, MXFP4_EXPERT_E_RANGE).reshape(e, 2 * i, h // 32, 17)
+        w_d = mxfp4_blocks(g, e * h, i, MXFP4_EXPERT_E_RANGE).reshape(e, h, i // 32, 17)
     else:
         raise ValueError(case.fmt)
     shared_gu = shared_d = None
@@ -245,7 +256,7 @@ def dense_inputs(case: DenseCase):
 
 
 def bytes_per_weight(fmt: str) -> float:
-    return {"q8_0": 34 / 32, "q2_k": 84 / 256, "int4": 0.5 + 4 / 64}[fmt]
+    return {"q8_0": 34 / 32, "q2_k": 84 / 256, "int4": 0.5 + 4 / 64, "mxfp4": 17 / 32}[fmt]
 
 
 def expert_weight_bytes(case: MoECase) -> float:

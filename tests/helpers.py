@@ -50,6 +50,8 @@ def make_qweight(bq, fmt: str, w, n_mats: int, n: int, k: int, swiglu: bool = Fa
         bq.repack_q8_0(dev(np.asarray(w).reshape(-1)), qw)
     elif fmt == "q2_k":
         bq.repack_q2_k(dev(np.asarray(w).reshape(-1)), qw)
+    elif fmt == "mxfp4":
+        bq.repack_mxfp4(dev(np.asarray(w).reshape(-1)), qw)
     else:
         bq.repack_int4(dev(w.words.reshape(-1).view(np.int32)),
                        dev(w.scales.reshape(-1).view(np.int16)),
@@ -64,6 +66,8 @@ def dequant(fmt: str, w):
         return O.dequant_q8_0(np.asarray(w))
     if fmt == "q2_k":
         return O.dequant_q2_k(np.asarray(w))
+    if fmt == "mxfp4":
+        return O.dequant_mxfp4(np.asarray(w))
     return O.dequant_int4(w.words, w.scales, w.biases)
 
 

@@ -34,7 +34,8 @@ def bq():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for must in ("bq_gguf_dequant_q8_0", "bq_gguf_dequant_q2_k", "bq_qmm", "bq_moe_gather_qmm",
-                 "bq_moe_route", "bq_moe_permute", "bq_repack_q8_0", "bq_repack_q2_k", "bq_repack_int4"):
+                 "bq_moe_route", "bq_moe_permute", "bq_repack_q8_0", "bq_repack_q2_k", "bq_repack_int4",
+                 "bq_dequant_mxfp4", "bq_repack_mxfp4"):
         assert must in names
 
 
@@ -50,10 +51,12 @@ def test_status_strings(bq):
 
 
 def test_qweight_bytes_match_format_density(bq):
-    # bytes per weight equal the on-disk formats: 34/32, 84/256, 9/16
+    # bytes per weight equal the on-disk formats: 34/32, 84/256, 9/16, 17/32
     assert bq.qweight_bytes(bq.FMT_Q8_0, 1, 256, 2048) == 256 * 2048 * 34 // 32
     assert bq.qweight_bytes(bq.FMT_Q2_K, 1, 4096, 4096) == 4096 * 4096 * 84 // 256
     assert bq.qweight_bytes(bq.FMT_INT4_G64, 128, 1536, 2048) == 128 * 1536 * 2048 * 9 // 16
+    assert bq.qweight_bytes(bq.FMT_MXFP4, 128, 1536, 2048) == 128 * 1536 * 2048 * 17 // 32
+    assert bq.qweight_bytes(bq.FMT_MXFP4, 1, 128, 64) == 0       # k not a multiple of 128
     assert bq.qweight_bytes(bq.FMT_Q2_K, 1, 100, 4096) == 0      # n not a multiple of 128
     assert bq.qweight_bytes(bq.FMT_Q2_K, 1, 128, 200) == 0       # k not a multiple of 256
     assert bq.qweight_bytes(9, 1, 128, 256) == 0                 # unknown format

@@ -75,3 +75,60 @@ def test_dequant_empty_is_noop(lib):
     lib.gguf_dequant_q8_0(torch.zeros(0, dtype=torch.uint8, device="cuda"), out)
     torch.cuda.synchronize()
     assert out.abs().sum().item() == 0
+
+
+# ---------------------------------------------------------------- MXFP4
+def _run_mx(lib, blocks):
+    import torch
+    flat = dev(np.ascontiguousarray(blocks, dtype=np.uint8).reshape(-1))
+    nb = flat.numel() // 17
+    out = torch.full((nb * 32,), 12345.0, dtype=torch.float32, device="cuda")
+    lib.dequant_mxfp4(flat, out)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def _exact_mx(got, ref):
+    """Bit-exact outside NaN; NaN exactly where the oracle has NaN (the GPU's
+    NaN payload is its own).  fp32 overflow of the oracle value gives inf."""
+    with np.errstate(over="ignore"):
+        ref32 = ref.astype(np.float32)
+    nan = np.isnan(ref)
+    np.testing.assert_array_equal(np.isnan(got), nan)
+    fin = np.isfinite(ref32)
+    assert np.array_equal(ref32[fin].astype(np.float64), ref[fin]), "oracle value not fp32-exact"
+    np.testing.assert_array_equal(got[~nan].view(np.uint32), ref32[~nan].view(np.uint32))
+
+
+@pytest.mark.parametrize("n_blocks", [1, 63, 64, 65, 1000, 4097])
+def test_mxfp4_bit_exact_ragged(lib, n_blocks):
+    blocks = synth.mxfp4_blocks(synth.rng(300 + n_blocks), n_blocks, 32).reshape(-1, 17)
+    _exact_mx(_run_mx(lib, blocks), O.dequant_mxfp4(blocks))
+
+
+def test_mxfp4_every_exponent_and_code(lib):
+    # all 256 exponents (0: fp32 subnormals, 253+: overflow, 255: NaN) x all 16 codes
+    b = np.zeros((256, 17), dtype=np.uint8)
+    b[:, 0] = np.arange(256)
+    b[:, 1:9] = np.array([0x10, 0x32, 0x54, 0x76, 0x98, 0xBA, 0xDC, 0xFE], dtype=np.uint8)
+    b[:, 9:] = np.array([0x01, 0x23, 0x45, 0x67, 0x89, 0xAB, 0xCD, 0xEF], dtype=np.uint8)
+    got = _run_mx(lib, b)
+    _exact_mx(got, O.dequant_mxfp4(b))
+    one = got.reshape(256, 32)[127]
+    np.testing.assert_array_equal(one[:16], O.MXFP4_VALUES.astype(np.float32))
+
+
+def test_mxfp4_full_size_expert_weights(lib):
+    # one routed expert's gate/up and down weights of the MXFP4 MoE workload
+    w_gu, w_d, _, _, _ = synth.moe_weights(synth.dataclasses.replace(synth.MOE_MXFP4, experts=2))
+    for w in (w_gu, w_d):
+        blocks = w.reshape(-1, 17)
+        _exact_mx(_run_mx(lib, blocks), O.dequant_mxfp4(blocks))
+
+
+def test_mxfp4_empty_is_noop(lib):
+    import torch
+    out = torch.zeros(4, device="cuda")
+    lib.dequant_mxfp4(torch.zeros(0, dtype=torch.uint8, device="cuda"), out)
+    torch.cuda.synchronize()
+    assert out.abs().sum().item() == 0

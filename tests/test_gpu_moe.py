@@ -20,6 +20,8 @@ SMALL = [
     _case("q2k_e1", "q2_k", 21, 256, 256, 1, 1),
     _case("int4_many_tokens", "int4", 300, 256, 256, 4, 2),
     _case("q2k_ragged", "q2_k", 131, 256, 256, 12, 6, zipf=True),
+    _case("mxfp4_small", "mxfp4", 37, 256, 128, 16, 4),
+    _case("mxfp4_many_tokens_shared", "mxfp4", 300, 256, 256, 4, 2, zipf=True, shared="q8_0"),
 ]
 
 
@@ -33,7 +35,8 @@ def test_moe_small(lib, case):
 
 @pytest.mark.parametrize("t", [1, 2, 5, 8])
 @pytest.mark.parametrize("base", [_case("dec_int4", "int4", 0, 256, 128, 32, 8),
-                                  _case("dec_q2k", "q2_k", 0, 512, 256, 64, 6, shared="q8_0")],
+                                  _case("dec_q2k", "q2_k", 0, 512, 256, 64, 6, shared="q8_0"),
+                                  _case("dec_mxfp4", "mxfp4", 0, 256, 256, 32, 8)],
                          ids=lambda c: c.name)
 def test_moe_decode_small(lib, base, t):
     case = synth.dataclasses.replace(base, t=t)
@@ -102,7 +105,7 @@ def _full(lib, base):
     return _FULL[base.name]
 
 
-@pytest.mark.parametrize("base", [synth.MOE_INT4, synth.MOE_Q2K], ids=lambda c: c.name)
+@pytest.mark.parametrize("base", [synth.MOE_INT4, synth.MOE_Q2K, synth.MOE_MXFP4], ids=lambda c: c.name)
 def test_moe_prefill_full_size_sampled(lib, base):
     weights, layer = _full(lib, base)
     inp = synth.moe_inputs(base, weights)
@@ -114,7 +117,7 @@ def test_moe_prefill_full_size_sampled(lib, base):
 
 
 @pytest.mark.parametrize("batch", [1, 2, 4, 8])
-@pytest.mark.parametrize("base", [synth.MOE_Q2K, synth.MOE_INT4], ids=lambda c: c.name)
+@pytest.mark.parametrize("base", [synth.MOE_Q2K, synth.MOE_INT4, synth.MOE_MXFP4], ids=lambda c: c.name)
 def test_moe_decode_full_shapes(lib, base, batch):
     weights, layer = _full(lib, base)
     case = synth.decode_case(base, batch)

@@ -19,7 +19,8 @@ def _qmm(lib, qw, x):
 
 
 @pytest.mark.parametrize("fmt,n,k", [("q8_0", 128, 64), ("q8_0", 384, 576), ("q2_k", 256, 512),
-                                     ("q2_k", 128, 256), ("int4", 256, 384), ("int4", 128, 128)])
+                                     ("q2_k", 128, 256), ("int4", 256, 384), ("int4", 128, 128),
+                                     ("mxfp4", 256, 384), ("mxfp4", 128, 128)])
 @pytest.mark.parametrize("m", [1, 3, 8, 13, 40, 130])
 def test_qmm_small_shapes(lib, fmt, n, k, m):
     g = synth.rng(n + k + m)
@@ -27,6 +28,8 @@ def test_qmm_small_shapes(lib, fmt, n, k, m):
         w = synth.q8_0_blocks(g, n, k)
     elif fmt == "q2_k":
         w = synth.q2_k_blocks(g, n, k)
+    elif fmt == "mxfp4":
+        w = synth.mxfp4_blocks(g, n, k)
     else:
         w = synth.int4_weight(g, (n,), k)
     qw = make_qweight(lib, fmt, w, 1, n, k)
@@ -63,3 +66,56 @@ def test_qmm_rejects_bad_shapes(lib):
     qs = lib.QWeight(lib.FMT_Q8_0, 1, 256, 64, swiglu=True)
     with pytest.raises(lib.BQError):
         lib.qmm(x, qs, y)          # fused gate/up weight is not a dense weight
+
+
+# ---------------------------------------------------------------- MXFP4 operand exactness
+def _mx_onehot(lib, blocks, n, k, rows):
+    """qmm of one-hot activation rows: y[j][r] = W[r][j] exactly (every other
+    product is 0 * finite), so y shows the device's fp16 weight operands."""
+    qw = make_qweight(lib, "mxfp4", blocks, 1, n, k)
+    x = np.zeros((len(rows), k), dtype=np.float16)
+    x[np.arange(len(rows)), rows] = 1.0
+    return _qmm(lib, qw, x)
+
+
+@pytest.mark.parametrize("m", [8, 128])   # qgemv path and tensor-core path
+def test_mxfp4_operands_are_fp16_roundings(lib, m):
+    # every code and every exponent 0..128: the operand must be the fp16
+    # rounding of the oracle value (exact for e >= 104, rounded subnormals
+    # below, 0 for e <= 88)
+    n, k = 128, 256
+    g = synth.rng(77 + m)
+    blocks = synth.mxfp4_blocks(g, n, k, e_range=(0, 128))
+    blocks[:, :, 0].flat[:129] = np.arange(129)
+    wd = O.dequant_mxfp4(blocks).reshape(n, k)
+    want16 = wd.astype(np.float16).astype(np.float64)
+    for r0 in range(0, k, m):
+        rows = np.arange(r0, r0 + m)
+        got = _mx_onehot(lib, blocks, n, k, rows)
+        np.testing.assert_array_equal(got, want16[:, rows].T)
+
+
+def test_mxfp4_nan_block_poisons_its_rows_only(lib):
+    n, k = 128, 128
+    blocks = synth.mxfp4_blocks(synth.rng(5), n, k)
+    blocks[3, 1, 0] = 255      # row 3, block 1: the E8M0 NaN scale
+    qw = make_qweight(lib, "mxfp4", blocks, 1, n, k)
+    x = synth.fp16_normal(synth.rng(6), (2, k))
+    for m in (1, 2):            # qgemv
+        y = _qmm(lib, qw, x[:m])
+        assert np.all(np.isnan(y[:, 3])) and np.all(np.isfinite(np.delete(y, 3, axis=1)))
+    xb = synth.fp16_normal(synth.rng(7), (40, k))   # tensor-core GEMM
+    y = _qmm(lib, qw, xb)
+    assert np.all(np.isnan(y[:, 3])) and np.all(np.isfinite(np.delete(y, 3, axis=1)))
+
+
+def test_mxfp4_out_of_range_exponent_is_flagged(lib):
+    n, k = 128, 128
+    blocks = synth.mxfp4_blocks(synth.rng(8), n, k)
+    lib.device_status()                         # clear what earlier calls left
+    make_qweight(lib, "mxfp4", blocks, 1, n, k)
+    assert lib.device_status() == lib.DEV_OK
+    blocks[5, 2, 0] = 129
+    make_qweight(lib, "mxfp4", blocks, 1, n, k)
+    assert lib.device_status() == lib.DEV_SCALE_RANGE
+    assert lib.device_status() == lib.DEV_OK   # read clears it
