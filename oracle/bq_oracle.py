@@ -18,7 +18,7 @@ Every function is pinned by tests in ``tests/test_oracle_pins.py``
 invariants and brute force on tiny inputs).  No function here is
 "parity unpinned".
 
-Readings taken where the pages are silent (each also listed in the design doc):
+Readings taken where the pages are silent:
 
 * Q2_K quant placement: value ``v = 128h + 32g + l`` (h in 0..1, g in 0..3,
   l in 0..31) sits in quant byte ``32h + l`` at bits ``2g..2g+1``; the
@@ -29,6 +29,10 @@ Readings taken where the pages are silent (each also listed in the design doc):
 * int4: value ``8w + i`` is bits ``4i..4i+3`` of word w (low nibble first).
 * MXFP4: byte ``i`` of a block's 16 code bytes holds value ``2i`` in its low
   nibble and ``2i + 1`` in its high nibble ("low nibble first").
+* FP8 block weight: ``weight`` is row-major [n, k] e4m3 bytes and
+  ``scales`` row-major [ceil(n/128), ceil(k/128)] fp32 (the page's
+  ``scales[i/128, j/128]``); a partial last block takes the scale of its
+  block.
 * Top-k: the k largest ``z = logit (+ bias)`` computed in fp32, ties to
   the lower expert index, output in descending z; the bias enters both
   selection and weighting.
@@ -45,7 +49,8 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
-    "dequant_q8_0", "dequant_q2_k", "dequant_int4", "dequant_mxfp4", "MXFP4_VALUES", "qmm", "route",
+    "dequant_q8_0", "dequant_q2_k", "dequant_int4", "dequant_mxfp4", "MXFP4_VALUES",
+    "e4m3_value", "dequant_fp8_block", "FP8_BLOCK", "qmm", "route",
     "SCORINGS", "softplus", "route_scored",
     "permute", "silu", "swiglu_ffn", "moe_ffn", "moe_ffn_tokens",
 ]
@@ -155,6 +160,46 @@ def dequant_mxfp4(blocks: np.ndarray) -> np.ndarray:
     codes = np.stack([qs & 0xF, qs >> 4], axis=-1).reshape(b.shape[:-1] + (32,))
     vals = MXFP4_VALUES[codes] * scale[..., None]
     return vals.reshape(b.shape[:-2] + (b.shape[-2] * 32,))
+
+
+FP8_BLOCK = 128
+
+
+def e4m3_value(codes: np.ndarray) -> np.ndarray:
+    """FP8 e4m3 byte -> its value (fp64), from the encoding's definition.
+
+    Follows *iron #9* (DeepSeek V3/V4 FP8 block weights): 1 sign bit, 4
+    exponent bits with bias 7, 3 mantissa bits, largest magnitude 448; the
+    two codes with all exponent and mantissa bits set (0x7F, 0xFF) are NaN
+    and there are no infinities.  Exponent field 0 holds the subnormals
+    ``(m / 8) * 2^(1 - 7)``; otherwise the value is ``2^(E - 7) * (1 + m / 8)``.
+    """
+    c = np.asarray(codes).astype(np.int64)
+    sign = (c >> 7) & 1
+    ex = (c >> 3) & 0xF
+    man = (c & 7).astype(np.float64)
+    mag = np.where(ex == 0, man / 8.0 * 2.0 ** (1 - 7), np.exp2(ex - 7.0) * (1.0 + man / 8.0))
+    mag = np.where((ex == 15) & (man == 7), np.nan, mag)
+    return np.where(sign == 1, -mag, mag)
+
+
+def dequant_fp8_block(weight: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """FP8 e4m3 weight with one fp32 scale per 128 x 128 block:
+    ``out[i, j] = e4m3(weight[i, j]) * scales[i // 128, j // 128]``.
+
+    Follows *iron #9* (``dsv4_fp8_block_dequant``: weight [M, N] u8 e4m3
+    bytes, scales [M/128, N/128] f32, the formula above).
+
+    weight: uint8 [..., n, k]; scales: [..., ceil(n/128), ceil(k/128)].
+    Returns fp64 [..., n, k].
+    """
+    w = np.asarray(weight, dtype=np.uint8)
+    sc = np.asarray(scales, dtype=np.float32).astype(np.float64)
+    n, k = w.shape[-2:]
+    nb, kb = -(-n // FP8_BLOCK), -(-k // FP8_BLOCK)
+    assert sc.shape[-2:] == (nb, kb), (sc.shape, (nb, kb))
+    full = np.repeat(np.repeat(sc, FP8_BLOCK, axis=-2), FP8_BLOCK, axis=-1)[..., :n, :k]
+    return e4m3_value(w) * full
 
 
 # --------------------------------------------------------------------------

@@ -103,6 +103,30 @@ def mxfp4_blocks(g: np.random.Generator, rows: int, k: int, e_range=(118, 124)) 
     return out
 
 
+FP8_BLOCK = 128
+
+
+@dataclasses.dataclass
+class Fp8Weight:
+    """FP8 e4m3 weight with 128 x 128 block scales: ``bytes`` [..., n, k]
+    uint8, ``scales`` [..., ceil(n/128), ceil(k/128)] fp32."""
+    bytes: np.ndarray
+    scales: np.ndarray
+
+
+def fp8_block_weight(g: np.random.Generator, lead_shape, n: int, k: int,
+                     s_range=(5e-5, 2e-4)) -> Fp8Weight:
+    """Uniform e4m3 codes over the 254 non-NaN bytes (every code occurs;
+    0x7F and 0xFF, the NaN codes, are skipped) and fp32 block scales uniform
+    in s_range."""
+    lead_shape = tuple(lead_shape)
+    u = g.integers(0, 254, size=lead_shape + (n, k), dtype=np.int64)
+    codes = (u + (u >= 0x7F)).astype(np.uint8)     # 0..126, 128..254: skips 0x7F and 0xFF
+    nb, kb = -(-n // FP8_BLOCK), -(-k // FP8_BLOCK)
+    scales = g.uniform(s_range[0], s_range[1], size=lead_shape + (nb, kb)).astype(np.float32)
+    return Fp8Weight(codes, scales)
+
+
 @dataclasses.dataclass
 class Int4Weight:
     """MLX-style int4 affine weight: ``words`` [..., n, k/8] u32 (value

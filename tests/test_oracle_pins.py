@@ -572,3 +572,85 @@ def test_mxfp4_round_trip_quantiser():
         v = O.dequant_mxfp4(_mx_block(e, codes)[None, :])
         assert np.all(np.abs(v - x) <= 1.0 * s + 1e-30)          # largest gap 2 (4 -> 6), half = 1
         np.testing.assert_array_equal(np.abs(v), mags[idx] * s)
+
+
+# ---------------------------------------------------------------------------
+# FP8 e4m3 with 128 x 128 block scales (DeepSeek V3 / V4 block weights)
+# ---------------------------------------------------------------------------
+
+def test_fp8_e4m3_page_facts():
+    f = _read_golden("fp8_e4m3_facts.txt")
+    v = O.e4m3_value(np.arange(256))
+    nan_codes = [int(c, 16) for c in f["nan_codes"]]
+    assert sorted(np.flatnonzero(np.isnan(v)).tolist()) == nan_codes
+    assert np.nanmax(np.abs(v)) == float(f["max_abs"][0])
+    bias = int(f["bias"][0])
+    assert int(f["sign_bits"][0]) + int(f["exponent_bits"][0]) + int(f["mantissa_bits"][0]) == 8
+    # exponent field = bias, mantissa 0 -> 1.0; exponent field 1 -> the smallest normal 2^(1 - bias)
+    assert v[bias << 3] == 1.0 and v[1 << 3] == 2.0 ** (1 - bias)
+    assert O.FP8_BLOCK == int(f["block"][0])
+
+
+def test_fp8_e4m3_matches_torch_float8():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("no float8_e4m3fn in this torch")
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    v = O.e4m3_value(np.arange(256))
+    np.testing.assert_array_equal(np.isnan(v), np.isnan(ref))
+    ok = ~np.isnan(v)
+    np.testing.assert_array_equal(v[ok], ref[ok])
+    np.testing.assert_array_equal(np.signbit(v[ok]), np.signbit(ref[ok]))
+
+
+def test_fp8_e4m3_subnormals_sign_and_order():
+    v = O.e4m3_value(np.arange(256))
+    assert v[0] == 0.0 and v[0x80] == 0.0 and np.signbit(v[0x80])
+    np.testing.assert_array_equal(v[1:8], np.arange(1, 8) * 2.0 ** -9)   # subnormals m/8 * 2^-6
+    assert np.all(np.diff(v[:0x7F]) > 0)                                  # positive codes increase
+    np.testing.assert_array_equal(v[0x80:0xFF], -v[0:0x7F])               # sign bit only flips the sign
+    assert v[0x7E] == 448.0 and v[0x77] == 240.0 and v[0x3C] == 1.5
+
+
+def test_fp8_block_scale_indexing_ragged():
+    # every weight 1.0 (code 0x38): the output is the scale grid, expanded by 128 in
+    # both directions and cut to the ragged shape; a transposed index would not fit
+    n, k = 300, 200
+    w = np.full((n, k), 0x38, dtype=np.uint8)
+    sc = np.array([[2.0, 3.0], [5.0, 7.0], [11.0, 13.0]], dtype=np.float32)
+    out = O.dequant_fp8_block(w, sc)
+    i, j = np.meshgrid(np.arange(n), np.arange(k), indexing="ij")
+    np.testing.assert_array_equal(out, sc[i // 128, j // 128])
+    w2 = w.copy()
+    w2[129, 130] = 0xB8                                                   # -1.0 in block (1, 1)
+    assert O.dequant_fp8_block(w2, sc)[129, 130] == -7.0
+    # a stack of matrices keeps its own grids
+    st = O.dequant_fp8_block(np.stack([w, w]), np.stack([sc, 2 * sc]))
+    np.testing.assert_array_equal(st[1], 2 * st[0])
+
+
+def test_fp8_page_quantiser_round_trip():
+    # the page's reference quantiser: scale = max_abs / 448 per block, nearest code;
+    # decoding gives back each value to within half the gap around it
+    f = _read_golden("fp8_e4m3_facts.txt")
+    div = float(f["quant_divisor"][0])
+    g = np.random.default_rng(11)
+    table = O.e4m3_value(np.arange(256))
+    finite = np.flatnonzero(~np.isnan(table))
+    x = g.normal(0, 0.02, (256, 384))
+    sc = np.zeros((2, 3), dtype=np.float32)
+    codes = np.zeros(x.shape, dtype=np.uint8)
+    for bi in range(2):
+        for bj in range(3):
+            blk = x[128 * bi:128 * bi + 128, 128 * bj:128 * bj + 128]
+            s = np.float32(np.abs(blk).max() / div)
+            sc[bi, bj] = s
+            q = blk / float(s)
+            c = finite[np.abs(q[..., None] - table[finite][None, None, :]).argmin(axis=-1)]
+            codes[128 * bi:128 * bi + 128, 128 * bj:128 * bj + 128] = c
+    back = O.dequant_fp8_block(codes, sc)
+    # largest relative gap between neighbouring normal codes is 1/8; absolute gap 2^-9 below
+    s_full = np.repeat(np.repeat(sc.astype(np.float64), 128, 0), 128, 1)
+    tol = np.maximum(np.abs(x) / 16.0, 2.0 ** -10 * s_full) + 1e-30
+    assert np.all(np.abs(back - x) <= tol)
+    assert np.abs(back).max() <= 448.0 * sc.max() * (1 + 1e-7)
