@@ -47,7 +47,7 @@ def parse_args():
                     help="q2k: Q2_K experts + Q8_0 shared (default); int4: int4 experts, E=128, top-8")
     ap.add_argument("--decode-steps", type=int, default=200)
     ap.add_argument("--no-secondary", action="store_true", help="only the main step (faster)")
-    ap.add_argument("--only", choices=["decode", "int4", "mxfp4", "dense"], default=None,
+    ap.add_argument("--only", choices=["decode", "int4", "mxfp4", "fp8_b128", "dense"], default=None,
                     help="run one secondary section alone and print it (no main step; for profiling)")
     ap.add_argument("--dense-case", default=None, help="with --only dense: run just this dense case")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -167,6 +167,8 @@ def qweight(bq, fmt, w, n_mats, n, k, swiglu=False):
         bq.repack_q2_k(src, q)
     elif fmt == "mxfp4":
         bq.repack_mxfp4(upload(np.asarray(w).reshape(-1)), q)
+    elif fmt == "fp8_b128":
+        bq.repack_fp8_b128(upload(w.bytes.reshape(-1)), upload(w.scales.reshape(-1)), q)
     else:
         bq.repack_int4(upload(w.words.reshape(-1).view(np.int32)), upload(w.scales.reshape(-1).view(np.int16)),
                        upload(w.biases.reshape(-1).view(np.int16)), q)
@@ -352,11 +354,11 @@ def run_main(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "mxfp4", "dense")):
+def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "mxfp4", "fp8_b128", "dense")):
     import torch
     out = {}
-    # decode sweep on each MoE workload; prefill of the int4 and MXFP4 ones
-    for base in (synth.MOE_Q2K, synth.MOE_INT4, synth.MOE_MXFP4):
+    # decode sweep on each MoE workload; prefill of the int4, MXFP4 and FP8 ones
+    for base in (synth.MOE_Q2K, synth.MOE_INT4, synth.MOE_MXFP4, synth.MOE_FP8):
         if "decode" not in sections and base.fmt not in sections:
             continue
         weights = synth.moe_weights(base)
@@ -396,7 +398,7 @@ def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "mxfp4", "den
                             "tok_s": round(b * len(ms) / (sum(ms) / 1e3), 1)}
         if res:
             out[f"decode_{base.fmt}"] = res
-        if base.fmt in ("int4", "mxfp4") and base.fmt in sections:
+        if base.fmt in ("int4", "mxfp4", "fp8_b128") and base.fmt in sections:
             layer.set_tokens(base.t)
             xh, lh = synth.moe_activations(base)
             x = upload(xh.view(np.uint16)).view(torch.float16)
@@ -458,6 +460,17 @@ def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "mxfp4", "den
     byt = wm.numel() + om.numel() * 4
     dense["dequant_mxfp4_4096x4096"] = {"us": round(t * 1e6, 2), "GB_s": round(byt / t / 1e9, 1),
                                         "frac_hbm": round(byt / t / 1e9 / pk["hbm_gbs"], 4)}
+    # standalone FP8 block dequantisation of a 4096 x 4096 weight
+    w8 = synth.fp8_block_weight(synth.rng(4444), (), 4096, 4096)
+    wb8, sb8 = upload(w8.bytes), upload(w8.scales)
+    o8 = torch.empty((4096, 4096), dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        bq.dequant_fp8_b128(wb8, sb8, o8)
+    ms, _ = time_steps(lambda: bq.dequant_fp8_b128(wb8, sb8, o8), 20, flush)
+    t = statistics.median(ms) / 1e3
+    byt = wb8.numel() + sb8.numel() * 4 + o8.numel() * 4
+    dense["dequant_fp8_b128_4096x4096"] = {"us": round(t * 1e6, 2), "GB_s": round(byt / t / 1e9, 1),
+                                           "frac_hbm": round(byt / t / 1e9 / pk["hbm_gbs"], 4)}
     out["dense"] = dense
     # router rules on the prefill router shape (T = 2048, E = 256, top-6, with a bias)
     route = {}

@@ -22,8 +22,9 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 # ---------------------------------------------------------------- constants
 OK = 0
-FMT_Q8_0, FMT_Q2_K, FMT_INT4_G64, FMT_MXFP4 = 1, 2, 3, 4
-FMT_BY_NAME = {"q8_0": FMT_Q8_0, "q2_k": FMT_Q2_K, "int4": FMT_INT4_G64, "mxfp4": FMT_MXFP4}
+FMT_Q8_0, FMT_Q2_K, FMT_INT4_G64, FMT_MXFP4, FMT_FP8_B128 = 1, 2, 3, 4, 5
+FMT_BY_NAME = {"q8_0": FMT_Q8_0, "q2_k": FMT_Q2_K, "int4": FMT_INT4_G64, "mxfp4": FMT_MXFP4,
+               "fp8_b128": FMT_FP8_B128}
 DEV_OK, DEV_BAD_EXPERT_ID, DEV_WAIT_TIMEOUT, DEV_SCALE_RANGE = 0, 1, 2, 3
 STATUS_NAMES = {0: "BQ_OK", 1: "BQ_ERR_NULL", 2: "BQ_ERR_SHAPE", 3: "BQ_ERR_ALIGN", 4: "BQ_ERR_FORMAT",
                 5: "BQ_ERR_WORKSPACE", 6: "BQ_ERR_CUDA", 7: "BQ_ERR_DEVICE", 8: "BQ_ERR_ARCH"}
@@ -48,11 +49,13 @@ _SIGS = {
     "bq_gguf_dequant_q8_0": (c_int32, [c_void_p, c_int64, c_void_p, c_void_p]),
     "bq_gguf_dequant_q2_k": (c_int32, [c_void_p, c_int64, c_void_p, c_void_p]),
     "bq_dequant_mxfp4": (c_int32, [c_void_p, c_int64, c_void_p, c_void_p]),
+    "bq_dequant_fp8_b128": (c_int32, [c_void_p, c_void_p, c_int64, c_int64, c_void_p, c_void_p]),
     "bq_qweight_bytes": (c_size_t, [c_int32, c_int32, c_int32, c_int32]),
     "bq_repack_q8_0": (c_int32, [c_void_p, POINTER(QWeightC), c_void_p]),
     "bq_repack_q2_k": (c_int32, [c_void_p, POINTER(QWeightC), c_void_p]),
     "bq_repack_int4": (c_int32, [c_void_p, c_void_p, c_void_p, POINTER(QWeightC), c_void_p]),
     "bq_repack_mxfp4": (c_int32, [c_void_p, POINTER(QWeightC), c_void_p]),
+    "bq_repack_fp8_b128": (c_int32, [c_void_p, c_void_p, POINTER(QWeightC), c_void_p]),
     "bq_qmm": (c_int32, [c_void_p, c_int32, POINTER(QWeightC), c_void_p, c_void_p]),
     "bq_moe_route": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p]),
     "bq_moe_route_scored": (c_int32, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_float, c_void_p,
@@ -135,6 +138,15 @@ def dequant_mxfp4(blocks, out, stream=None):
     return out
 
 
+def dequant_fp8_b128(weight, scales, out, stream=None):
+    """weight: uint8 device tensor [n, k] (e4m3 bytes); scales: fp32 [ceil(n/128), ceil(k/128)];
+    out: fp32 [n, k]."""
+    n, k = weight.shape
+    _check(_lib.bq_dequant_fp8_b128(_ptr(weight), _ptr(scales), n, k, _ptr(out), _stream(stream)),
+           "bq_dequant_fp8_b128")
+    return out
+
+
 # ---------------------------------------------------------------- weights
 def qweight_bytes(fmt: int, n_mats: int, n: int, k: int) -> int:
     return int(_lib.bq_qweight_bytes(fmt, n_mats, n, k))
@@ -177,6 +189,12 @@ def repack_int4(words, scales, biases, w: QWeight, stream=None) -> QWeight:
 
 def repack_mxfp4(blocks, w: QWeight, stream=None) -> QWeight:
     _check(_lib.bq_repack_mxfp4(_ptr(blocks), ctypes.byref(w.c), _stream(stream)), "bq_repack_mxfp4")
+    return w
+
+
+def repack_fp8_b128(weight, scales, w: QWeight, stream=None) -> QWeight:
+    _check(_lib.bq_repack_fp8_b128(_ptr(weight), _ptr(scales), ctypes.byref(w.c), _stream(stream)),
+           "bq_repack_fp8_b128")
     return w
 
 

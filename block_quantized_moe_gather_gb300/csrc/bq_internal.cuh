@@ -70,6 +70,11 @@ __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontro
 // MXFP4 slab = 128 K : words u32 [128][16] (codes, int4 word order),
 //                      E8M0 exponent bytes [128][4] (block b of row p
 //                      at 4p + b)                                     = 8704 B
+// FP8   slab = 64 K  : e4m3 bytes [128][64] (K order), then fp16(256 * s)
+//                      of the block scale of rows 0-15 of each 32-row
+//                      quarter at 8192 and of rows 16-31 at 8194 (the
+//                      gate and up blocks of a fused gate/up weight;
+//                      equal otherwise), zero padding to 16 bytes      = 8208 B
 // Scale fields are stored group-major so that threads reading one group
 // of consecutive rows read consecutive words (no bank conflicts).
 //
@@ -104,6 +109,7 @@ __host__ __device__ constexpr Fmt fmt_info(int fmt) {
          : fmt == BQ_FMT_Q2_K   ? Fmt{256, 10752, 8192}
          : fmt == BQ_FMT_INT4_G64 ? Fmt{128, 9216, 8192}
          : fmt == BQ_FMT_MXFP4  ? Fmt{128, 8704, 8192}
+         : fmt == BQ_FMT_FP8_B128 ? Fmt{64, 8208, 8192}
                                   : Fmt{0, 0, 0};
 }
 
@@ -182,5 +188,20 @@ __device__ __forceinline__ __half2 mx_scale_h2(uint32_t e) {
     const uint32_t b = mx_scale_bits(e);
     return u32_as_h2(b | (b << 16));
 }
+
+// ---- FP8 e4m3 (OCP OFP8, as DeepSeek V3 / V4 block weights)
+//
+// Two e4m3 values (low byte -> low lane) as an fp16 pair.  Every e4m3 value
+// is an fp16 value (3 mantissa bits, exponents 2^-9 .. 2^8), so this is
+// exact; the NaN codes give NaN.
+__device__ __forceinline__ __half2 e4m3x2_to_half2(uint32_t two_bytes) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((unsigned short)two_bytes));
+    return u32_as_h2(r);
+}
+
+// The exact factor the FP8 matmuls remove from their fp32 accumulators (the
+// slab scales are stored as fp16(256 * s)).
+constexpr float kFp8ScaleOffset = 256.0f;
 
 }  // namespace bq

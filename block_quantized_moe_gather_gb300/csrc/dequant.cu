@@ -13,6 +13,10 @@
 // Same page, MXFP4 section (DeepSeek V4-Flash MoE experts, OCP MX v1.0):
 // 17-byte blocks of one E8M0 exponent and 16 bytes of e2m1 codes, low
 // nibble first; value = table[code] * 2^(e - 127), NaN only through e = 255.
+// Same page, FP8 block section (DeepSeek V3 / V4): e4m3 bytes [n][k] with
+// fp32 scales [n/128][k/128]; out = e4m3(w) * scale of the (i/128, j/128)
+// block.  Here the e4m3 -> fp16 conversion instruction replaces the
+// page's 256-entry table (exact: e4m3 is a subset of fp16).
 #include <algorithm>
 
 #include "bq_internal.cuh"
@@ -134,6 +138,41 @@ dequant_mxfp4_kernel(const uint8_t* __restrict__ blocks, int64_t n_blocks, float
     }
 }
 
+// FP8: 16 consecutive bytes of one row per thread (k % 16 == 0 and 16-byte
+// aligned rows), else one byte per thread.  16 bytes never straddle a
+// 128-column scale block.
+__global__ void __launch_bounds__(kThreads)
+dequant_fp8_vec_kernel(const uint8_t* __restrict__ w, const float* __restrict__ scales, int64_t n, int64_t k,
+                       float* __restrict__ out) {
+    const int64_t groups = n * (k / 16), kb = (k + 127) / 128;
+    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = g / (k / 16), j0 = (g % (k / 16)) * 16;
+        const float s = __ldg(scales + (i / 128) * kb + j0 / 128);
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(w + i * k + j0));
+        const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+        float4* o = reinterpret_cast<float4*>(out + i * k + j0);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const __half2 a = bq::e4m3x2_to_half2(words[m]), b = bq::e4m3x2_to_half2(words[m] >> 16);
+            o[m] = make_float4(__fmul_rn(__low2float(a), s), __fmul_rn(__high2float(a), s),
+                               __fmul_rn(__low2float(b), s), __fmul_rn(__high2float(b), s));
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+dequant_fp8_kernel(const uint8_t* __restrict__ w, const float* __restrict__ scales, int64_t n, int64_t k,
+                   float* __restrict__ out) {
+    const int64_t total = n * k, kb = (k + 127) / 128;
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = e / k, j = e % k;
+        const float s = __ldg(scales + (i / 128) * kb + j / 128);
+        out[e] = __fmul_rn(__low2float(bq::e4m3x2_to_half2(__ldg(w + e))), s);
+    }
+}
+
 int grid_for(int64_t chunks) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
@@ -184,4 +223,26 @@ extern "C" bq_status bq_dequant_mxfp4(const void* blocks, int64_t n_blocks, floa
         static_cast<const uint8_t*>(blocks), n_blocks, out);
     bq::note_launch();
     return bq::check_launch("bq_dequant_mxfp4");
+}
+
+extern "C" bq_status bq_dequant_fp8_b128(const void* weight, const float* scales, int64_t n, int64_t k, float* out,
+                                         bq_stream_t stream) {
+    if (n < 0 || k < 0) return bq::fail(BQ_ERR_SHAPE, "bq_dequant_fp8_b128: n = %lld, k = %lld", (long long)n,
+                                        (long long)k);
+    if (n == 0 || k == 0) return BQ_OK;
+    if (!weight || !scales || !out) return bq::fail(BQ_ERR_NULL, "bq_dequant_fp8_b128: NULL pointer");
+    if (!bq::aligned(scales, 4) || !bq::aligned(out, 4))
+        return bq::fail(BQ_ERR_ALIGN, "bq_dequant_fp8_b128: scales and out must be 4-byte aligned");
+    bq_status s = bq::check_arch();
+    if (s != BQ_OK) return s;
+    const uint8_t* w = static_cast<const uint8_t*>(weight);
+    if (k % 16 == 0 && bq::aligned(w, 16) && bq::aligned(out, 16)) {
+        dequant_fp8_vec_kernel<<<grid_for((n * (k / 16) + kThreads - 1) / kThreads), kThreads, 0,
+                                 (cudaStream_t)stream>>>(w, scales, n, k, out);
+    } else {
+        dequant_fp8_kernel<<<grid_for((n * k + kThreads - 1) / kThreads), kThreads, 0, (cudaStream_t)stream>>>(
+            w, scales, n, k, out);
+    }
+    bq::note_launch();
+    return bq::check_launch("bq_dequant_fp8_b128");
 }

@@ -76,7 +76,9 @@ template <> struct G<BQ_FMT_Q8_0>     { static constexpr int SK = 64,  SB = 8704
 template <> struct G<BQ_FMT_Q2_K>     { static constexpr int SK = 256, SB = 10752, SPS = 4, NR = 3; };
 template <> struct G<BQ_FMT_INT4_G64> { static constexpr int SK = 128, SB = 9216,  SPS = 2, NR = 3; };
 template <> struct G<BQ_FMT_MXFP4>    { static constexpr int SK = 128, SB = 8704,  SPS = 2, NR = 4; };
-static_assert(4 * 8704 <= kRawBytes && 3 * 10752 <= kRawBytes && 3 * 9216 <= kRawBytes, "raw ring");
+template <> struct G<BQ_FMT_FP8_B128> { static constexpr int SK = 64,  SB = 8208,  SPS = 1, NR = 4; };
+static_assert(4 * 8704 <= kRawBytes && 3 * 10752 <= kRawBytes && 3 * 9216 <= kRawBytes && 4 * 8208 <= kRawBytes,
+              "raw ring");
 
 enum { EPI_SWIGLU = 0, EPI_SCALE = 1, EPI_PLAIN = 2 };
 
@@ -379,6 +381,30 @@ __device__ __forceinline__ void dequant_stage<BQ_FMT_MXFP4>(const uint8_t* raw, 
     mx_block(raw, p, 2 * sub + 1, out + 16);
 }
 
+// FP8: chunk c (16 e4m3 bytes of row p) as 8 fp16 pairs, each the exact
+// fp16 of the code times the slab's stored fp16(256 s), rounded once.
+__device__ __forceinline__ void fp8_chunk(const uint8_t* raw, int p, int c, __half2 s2, uint32_t* out) {
+    const uint4 q = *reinterpret_cast<const uint4*>(raw + bq::quant_chunk_offset(p, c));
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        out[2 * m] = bq::h2_as_u32(__hmul2_rn(bq::e4m3x2_to_half2(w[m]), s2));
+        out[2 * m + 1] = bq::h2_as_u32(__hmul2_rn(bq::e4m3x2_to_half2(w[m] >> 16), s2));
+    }
+}
+
+__device__ __forceinline__ __half2 fp8_scale(const uint8_t* raw, int p) {
+    const uint32_t b = *reinterpret_cast<const uint16_t*>(raw + 8192 + 2 * ((p >> 4) & 1));
+    return bq::u32_as_h2(b | (b << 16));
+}
+
+template <>
+__device__ __forceinline__ void dequant_stage<BQ_FMT_FP8_B128>(const uint8_t* raw, int p, int, uint32_t (&out)[32]) {
+    const __half2 s2 = fp8_scale(raw, p);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) fp8_chunk(raw, p, c, s2, out + 8 * c);
+}
+
 // Half h (K values 32h .. 32h + 31) of a 64-K stage as 16 fp16 pairs, the
 // same values dequant_stage gives for that half.
 template <int FMT>
@@ -453,6 +479,14 @@ template <>
 __device__ __forceinline__ void dequant_half<BQ_FMT_MXFP4>(const uint8_t* raw, int p, int sub, int h,
                                                            uint32_t (&out)[16]) {
     mx_block(raw, p, 2 * sub + h, out);
+}
+
+template <>
+__device__ __forceinline__ void dequant_half<BQ_FMT_FP8_B128>(const uint8_t* raw, int p, int, int h,
+                                                              uint32_t (&out)[16]) {
+    const __half2 s2 = fp8_scale(raw, p);
+    fp8_chunk(raw, p, 2 * h, s2, out);
+    fp8_chunk(raw, p, 2 * h + 1, s2, out + 8);
 }
 
 __device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
@@ -691,6 +725,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
                 uint32_t v[32];
                 tmem_ld32(tmem + lane_base + (uint32_t)c0, v);
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (FMT == BQ_FMT_FP8_B128) {   // the FP8 slab scales carry a factor 256 (exact to remove)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * (1.0f / bq::kFp8ScaleOffset));
+                }
                 if (EPI == EPI_SWIGLU) {
                     // lanes 0-15 hold gate rows, 16-31 the matching up rows
 #pragma unroll
@@ -818,6 +856,7 @@ void launch_epi(int fmt, const CUtensorMap& map, const GemmArgs& a, dim3 grid, c
         case BQ_FMT_Q8_0: launch_one<BQ_FMT_Q8_0, EPI>(map, a, grid, st); break;
         case BQ_FMT_Q2_K: launch_one<BQ_FMT_Q2_K, EPI>(map, a, grid, st); break;
         case BQ_FMT_MXFP4: launch_one<BQ_FMT_MXFP4, EPI>(map, a, grid, st); break;
+        case BQ_FMT_FP8_B128: launch_one<BQ_FMT_FP8_B128, EPI>(map, a, grid, st); break;
         default: launch_one<BQ_FMT_INT4_G64, EPI>(map, a, grid, st); break;
     }
 }
@@ -879,7 +918,8 @@ GemmWs carve(const bq_moe_desc* d, uint8_t* base) {
 namespace bq {
 
 bool gemm_supported(int fmt) {
-    return (fmt == BQ_FMT_Q8_0 || fmt == BQ_FMT_Q2_K || fmt == BQ_FMT_INT4_G64 || fmt == BQ_FMT_MXFP4) &&
+    return (fmt == BQ_FMT_Q8_0 || fmt == BQ_FMT_Q2_K || fmt == BQ_FMT_INT4_G64 || fmt == BQ_FMT_MXFP4 ||
+            fmt == BQ_FMT_FP8_B128) &&
            encode_fn() != nullptr;
 }
 

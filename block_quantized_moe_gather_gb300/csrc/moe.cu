@@ -158,6 +158,9 @@ bq_status check_weight(const char* name, const bq_qweight* w, int n_mats, int n,
     if ((n_mats > 0 && w->n_mats != n_mats) || (n > 0 && w->n != n) || w->k != k || w->swiglu != swiglu)
         return bq::fail(BQ_ERR_FORMAT, "%s: weight is %d x %d x %d (swiglu %d), expected %d x %d x %d (swiglu %d)",
                         name, w->n_mats, w->n, w->k, w->swiglu, n_mats, n, k, swiglu);
+    if (w->fmt == BQ_FMT_FP8_B128 && swiglu && (w->n / 2) % 128 != 0)
+        return bq::fail(BQ_ERR_FORMAT, "%s: an FP8 gate/up weight needs n/2 = %d to be a multiple of 128", name,
+                        w->n / 2);
     if (!bq::aligned(w->data, 256)) return bq::fail(BQ_ERR_ALIGN, "%s: weight data must be 256-byte aligned", name);
     return BQ_OK;
 }

@@ -36,6 +36,7 @@ template <> struct Traits<BQ_FMT_Q8_0>     { static constexpr int SK = 64,  SB =
 template <> struct Traits<BQ_FMT_Q2_K>     { static constexpr int SK = 256, SB = 10752, STEPS = 16, XV = 8, DEPTH = 3; };
 template <> struct Traits<BQ_FMT_INT4_G64> { static constexpr int SK = 128, SB = 9216,  STEPS = 8,  XV = 4, DEPTH = 3; };
 template <> struct Traits<BQ_FMT_MXFP4>    { static constexpr int SK = 128, SB = 8704,  STEPS = 8,  XV = 4, DEPTH = 3; };
+template <> struct Traits<BQ_FMT_FP8_B128> { static constexpr int SK = 64,  SB = 8208,  STEPS = 4,  XV = 2, DEPTH = 3; };
 
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
@@ -81,6 +82,9 @@ __device__ __forceinline__ void load_frag(Frag<FMT>& f, const uint8_t* slab, int
                 f.dm[tile][hh] = __ldg(reinterpret_cast<const uint32_t*>(slab + 10240 + row * 4));
             } else if (FMT == BQ_FMT_MXFP4) {
                 f.sc[tile][hh] = __ldg(slab + 8192 + 4 * row + t);   // the lane's quarter = block t
+            } else if (FMT == BQ_FMT_FP8_B128) {
+                // rows 16 * tile .. + 15 of the quarter share one block scale
+                f.sc[tile][hh] = __ldg(reinterpret_cast<const uint16_t*>(slab + 8192) + tile);
             } else {
                 f.sc[tile][hh] = __ldg(reinterpret_cast<const uint32_t*>(slab + 8192 + 512 * (t >> 1) + 4 * row));
             }
@@ -213,6 +217,8 @@ __device__ __forceinline__ void mma_frag(const Frag<FMT>& f, const __half* xq, b
                     bi2[tile][hh] = __high2half2(sbh);
                 } else if (FMT == BQ_FMT_MXFP4) {
                     sc2[tile][hh] = bq::mx_scale_h2(f.sc[tile][hh]);
+                } else if (FMT == BQ_FMT_FP8_B128) {
+                    sc2[tile][hh] = bq::u32_as_h2(f.sc[tile][hh] | (f.sc[tile][hh] << 16));
                 } else {
                     const __half d = __ushort_as_half((uint16_t)f.sc[tile][hh]);
                     d2[tile][hh] = __halves2half2(d, d);
@@ -232,6 +238,10 @@ __device__ __forceinline__ void mma_frag(const Frag<FMT>& f, const __half* xq, b
                     if (FMT == BQ_FMT_Q8_0) {
                         const uint32_t wx = comp(f.q[tile][hh], s) ^ 0x80808080u;
                         a[r] = bq::h2_as_u32(__hmul2(bq::s8pair_to_half2(wx, lohi ? 0x4342u : 0x4140u), d2[tile][hh]));
+                    } else if (FMT == BQ_FMT_FP8_B128) {
+                        // exact e4m3 -> fp16, times the stored fp16(256 s), rounded once
+                        const uint32_t w = comp(f.q[tile][hh], s);
+                        a[r] = bq::h2_as_u32(__hmul2_rn(bq::e4m3x2_to_half2(lohi ? w >> 16 : w), sc2[tile][hh]));
                     } else if (FMT == BQ_FMT_MXFP4) {
                         // exact fp16 operands: the product is the scaled value rounded once
                         const uint32_t w = comp(f.q[tile][hh], s >> 1);
@@ -343,6 +353,12 @@ qgemv_kernel(const bq::QgemvParams p) {
                     load_frag<FMT>(f[(d + D - 1) % D], wbase + (int64_t)(kt_begin + nxt) * T::SB, rowbase, g, t);
                 mma_frag<FMT>(f[d], xrow + (kt_begin + i + d) * T::SK, xvalid, t, acc);
             }
+        }
+        if (FMT == BQ_FMT_FP8_B128) {   // the FP8 slab scales carry a factor 256 (exact to remove)
+#pragma unroll
+            for (int tile = 0; tile < 2; ++tile)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[tile][j] *= 1.0f / bq::kFp8ScaleOffset;
         }
         __syncthreads();   // previous token group's readers of `red` are done
         if (kw) {
@@ -463,6 +479,7 @@ void launch_qgemv(const QgemvParams& params, int max_segments, cudaStream_t st, 
         case BQ_FMT_Q8_0: launch_fmt<BQ_FMT_Q8_0>(p, max_segments, after_previous, st); break;
         case BQ_FMT_Q2_K: launch_fmt<BQ_FMT_Q2_K>(p, max_segments, after_previous, st); break;
         case BQ_FMT_MXFP4: launch_fmt<BQ_FMT_MXFP4>(p, max_segments, after_previous, st); break;
+        case BQ_FMT_FP8_B128: launch_fmt<BQ_FMT_FP8_B128>(p, max_segments, after_previous, st); break;
         default: launch_fmt<BQ_FMT_INT4_G64>(p, max_segments, after_previous, st); break;
     }
 }

@@ -148,10 +148,38 @@ __global__ void repack_mxfp4_kernel(const uint8_t* __restrict__ src, int n, int 
     }
 }
 
+// FP8: 64 bytes of row `row` per slab (K order, rotated 16-byte chunks);
+// thread p = 0 of a slab also writes the slab's two block scales as
+// fp16(256 s) (rows 0-15 and 16-31 of each quarter) and the padding.
+__global__ void repack_fp8_kernel(const uint8_t* __restrict__ src, const float* __restrict__ scales, int n, int k,
+                                  int swiglu, int n_tiles, int k_slabs, int64_t total, uint8_t* __restrict__ dst,
+                                  int32_t* status) {
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        Item it = item_of(idx, n, swiglu, n_tiles, k_slabs, 8208, dst);
+        const uint8_t* row = src + ((int64_t)it.e * n + it.row) * k + 64 * it.kt;
+        for (int c = 0; c < 4; ++c)
+            for (int i = 0; i < 16; ++i) it.slab[bq::quant_chunk_offset(it.p, c) + i] = row[16 * c + i];
+        if (it.p == 0) {
+            const int kb = k / 128, blk_k = it.kt / 2;
+            uint16_t* sc = reinterpret_cast<uint16_t*>(it.slab + 8192);
+            for (int h = 0; h < 2; ++h) {
+                const int lrow = bq::logical_row(it.rt, 16 * h, n, swiglu);
+                const float s = scales[((int64_t)it.e * (n / 128) + lrow / 128) * kb + blk_k];
+                const float s256 = s * bq::kFp8ScaleOffset;
+                if (!(fabsf(s256) * 448.0f <= 65504.0f)) bq::set_device_error(status, BQ_DEV_SCALE_RANGE);
+                sc[h] = __half_as_ushort(__float2half_rn(s256));
+            }
+            for (int i = 4; i < 16; ++i) it.slab[8192 + i] = 0;
+        }
+    }
+}
+
 bq_status check_dst(const char* name, const bq_qweight* w, int want_fmt) {
     if (!w || !w->data) return bq::fail(BQ_ERR_NULL, "%s: dst or dst->data is NULL", name);
     if (w->fmt != want_fmt) return bq::fail(BQ_ERR_FORMAT, "%s: dst->fmt = %d", name, w->fmt);
-    if (bq_qweight_bytes(w->fmt, w->n_mats, w->n, w->k) == 0 || (w->swiglu != 0 && w->swiglu != 1))
+    if (bq_qweight_bytes(w->fmt, w->n_mats, w->n, w->k) == 0 || (w->swiglu != 0 && w->swiglu != 1) ||
+        (w->fmt == BQ_FMT_FP8_B128 && w->swiglu && (w->n / 2) % 128 != 0))
         return bq::fail(BQ_ERR_SHAPE, "%s: invalid shape n_mats=%d n=%d k=%d swiglu=%d", name,
                         w->n_mats, w->n, w->k, w->swiglu);
     if (!bq::aligned(w->data, 256)) return bq::fail(BQ_ERR_ALIGN, "%s: dst->data must be 256-byte aligned", name);
@@ -168,6 +196,7 @@ extern "C" size_t bq_qweight_bytes(int32_t fmt, int32_t n_mats, int32_t n, int32
     Fmt f = fmt_info(fmt);
     if (f.slab_k == 0 || n_mats < 1 || n < bq::kTileRows || k < f.slab_k) return 0;
     if (n % bq::kTileRows || k % f.slab_k) return 0;
+    if (fmt == BQ_FMT_FP8_B128 && k % 128) return 0;   // whole 128-column scale blocks
     return (size_t)n_mats * (n / bq::kTileRows) * (k / f.slab_k) * (size_t)f.slab_bytes;
 }
 
@@ -224,4 +253,19 @@ extern "C" bq_status bq_repack_mxfp4(const void* blocks, const bq_qweight* dst, 
         static_cast<uint8_t*>(dst->data), bq::device_status_ptr());
     bq::note_launch();
     return bq::check_launch("bq_repack_mxfp4");
+}
+
+extern "C" bq_status bq_repack_fp8_b128(const void* weight, const float* scales, const bq_qweight* dst,
+                                        bq_stream_t stream) {
+    bq_status s = check_dst("bq_repack_fp8_b128", dst, BQ_FMT_FP8_B128);
+    if (s != BQ_OK) return s;
+    if (!weight || !scales) return bq::fail(BQ_ERR_NULL, "bq_repack_fp8_b128: NULL source");
+    if (!bq::aligned(scales, 4)) return bq::fail(BQ_ERR_ALIGN, "bq_repack_fp8_b128: scales must be 4-byte aligned");
+    if ((s = bq::check_arch()) != BQ_OK) return s;
+    Geometry g = geometry(dst);
+    repack_fp8_kernel<<<grid_for(g.rows_total), 256, 0, (cudaStream_t)stream>>>(
+        static_cast<const uint8_t*>(weight), scales, dst->n, dst->k, dst->swiglu, g.n_tiles, g.k_slabs,
+        g.rows_total, static_cast<uint8_t*>(dst->data), bq::device_status_ptr());
+    bq::note_launch();
+    return bq::check_launch("bq_repack_fp8_b128");
 }

@@ -61,15 +61,16 @@ enum {
     BQ_DEV_OK = 0,
     BQ_DEV_BAD_EXPERT_ID = 1,   /* a routed expert id was outside [0, E)        */
     BQ_DEV_WAIT_TIMEOUT = 2,    /* a bounded mbarrier / flag wait ran out       */
-    BQ_DEV_SCALE_RANGE = 3      /* an MXFP4 block exponent the device path cannot
-                                   represent (129..254) met bq_repack_mxfp4       */
+    BQ_DEV_SCALE_RANGE = 3      /* a block scale the device path cannot represent
+                                   met bq_repack_mxfp4 / bq_repack_fp8_b128       */
 };
 
 typedef enum {
     BQ_FMT_Q8_0 = 1,      /* GGUF Q8_0: 32-value blocks, fp16 d + 32 int8 ([iron] kernel 1) */
     BQ_FMT_Q2_K = 2,      /* GGUF Q2_K: 256-value super-blocks of 84 bytes ([iron] kernel 2) */
     BQ_FMT_INT4_G64 = 3,  /* MLX int4 affine, 8 codes per u32, fp16 scale+bias per 64 ([butter]) */
-    BQ_FMT_MXFP4 = 4      /* OCP MX FP4: 32 e2m1 codes + one E8M0 exponent per block ([iron]) */
+    BQ_FMT_MXFP4 = 4,     /* OCP MX FP4: 32 e2m1 codes + one E8M0 exponent per block ([iron]) */
+    BQ_FMT_FP8_B128 = 5   /* FP8 e4m3 bytes, one fp32 scale per 128 x 128 block ([iron]) */
 } bq_format;
 
 /*
@@ -83,15 +84,15 @@ typedef enum {
  *
  * Layout (informative): for each matrix, 128-row tile and K-slab, one
  * contiguous slab of bytes holding 64 quant bytes per row followed by the
- * slab's scale fields.  K-slab width: Q8_0 64, Q2_K 256, int4 and MXFP4
- * 128 values.  Bytes per weight equal the on-disk format's (34/32, 84/256,
- * 9/16, 17/32).
+ * slab's scale fields.  K-slab width: Q8_0 and FP8 64, Q2_K 256, int4 and
+ * MXFP4 128 values.  Bytes per weight equal the on-disk format's (34/32,
+ * 84/256, 9/16, 17/32), and for FP8 1 + 16/8192.
  */
 typedef struct {
     int32_t fmt;      /* bq_format */
     int32_t n_mats;
     int32_t n;        /* multiple of 128 */
-    int32_t k;        /* multiple of 256 (Q2_K), 128 (int4, MXFP4) or 64 (Q8_0) */
+    int32_t k;        /* multiple of 256 (Q2_K), 128 (int4, MXFP4, FP8) or 64 (Q8_0) */
     int32_t swiglu;   /* 0 or 1 */
     int32_t reserved;
     void* data;       /* device */
@@ -148,6 +149,23 @@ bq_status bq_gguf_dequant_q2_k(const void* blocks, int64_t n_blocks, float* out,
  */
 bq_status bq_dequant_mxfp4(const void* blocks, int64_t n_blocks, float* out, bq_stream_t stream);
 
+/*
+ * Standalone FP8 block dequantisation to fp32 ([iron]: DeepSeek V3 / V4
+ * FP8 e4m3 weights with per-(128 x 128)-block fp32 scales):
+ *   out[i][j] = e4m3(weight[i][j]) * scales[i / 128][j / 128]
+ * e4m3: sign, 4 exponent bits (bias 7), 3 mantissa bits, largest 448,
+ * 0x7F / 0xFF NaN, no infinities.  The product is one fp32 multiply
+ * (round to nearest even, subnormals kept), so it is the fp32 rounding of
+ * the exact product.
+ * weight: device uint8 [n][k] row-major; scales: device fp32
+ * [ceil(n/128)][ceil(k/128)] row-major (4-byte aligned); out: device fp32
+ * [n][k].  n, k >= 0 (any values; a partial last block uses its scale).
+ * Errors: BQ_ERR_NULL, BQ_ERR_SHAPE (n or k < 0), BQ_ERR_ALIGN, BQ_ERR_CUDA.
+ * n * k == 0 is a no-op.
+ */
+bq_status bq_dequant_fp8_b128(const void* weight, const float* scales, int64_t n, int64_t k,
+                              float* out, bq_stream_t stream);
+
 /* ------------------------------------------------------------------ S0
  * Load-time repack of on-disk blocks into the device layout ([iron]:
  * CPU-side decomposition of each block into separate GPU tensors;
@@ -160,6 +178,8 @@ bq_status bq_dequant_mxfp4(const void* blocks, int64_t n_blocks, float* out, bq_
  *         scales and biases [n_mats][n][k/64] fp16 (passed as uint16 bits)
  *   MXFP4: blocks [n_mats][n][k/32] x 17 bytes (as bq_dequant_mxfp4; any
  *         alignment)
+ *   FP8:  weight bytes [n_mats][n][k] e4m3 (any alignment), scales fp32
+ *         [n_mats][n/128][k/128] (4-byte aligned)
  * dst->fmt/n_mats/n/k/swiglu/data must be filled in by the caller.
  * Errors: BQ_ERR_NULL, BQ_ERR_FORMAT, BQ_ERR_SHAPE, BQ_ERR_ALIGN, BQ_ERR_CUDA.
  *
@@ -168,6 +188,16 @@ bq_status bq_dequant_mxfp4(const void* blocks, int64_t n_blocks, float* out, bq_
  * e <= 128 (for e <= 88 that rounding is 0) and for e = 255 (NaN).  Blocks
  * with e in 129..254 (block scales of 4 and above) are stored unchanged but set
  * BQ_DEV_SCALE_RANGE on the device; matmuls over them give +-inf or NaN.
+ *
+ * FP8 on the device: each block scale s is stored as the fp16 rounding of
+ * 256 * s; a weight enters the matmul as the fp16 rounding of
+ * e4m3 * fp16(256 s), and the factor 2^-8 is applied exactly to the fp32
+ * accumulators.  Relative error per weight <= 2^-11 + 2^-11 (against 2^-12
+ * for a single rounding of the exact product).  Scales with 448 * 256 * |s|
+ * above 65504 (|s| > 0.571, block values above 256) or NaN set
+ * BQ_DEV_SCALE_RANGE; matmuls over them give +-inf or NaN.  A fused gate/up
+ * FP8 weight needs n/2 to be a multiple of 128 (each half has its own
+ * scale rows).
  */
 size_t bq_qweight_bytes(int32_t fmt, int32_t n_mats, int32_t n, int32_t k);
 bq_status bq_repack_q8_0(const void* blocks, const bq_qweight* dst, bq_stream_t stream);
@@ -176,6 +206,8 @@ bq_status bq_repack_int4(const uint32_t* words, const uint16_t* scales,
                          const uint16_t* biases, const bq_qweight* dst,
                          bq_stream_t stream);
 bq_status bq_repack_mxfp4(const void* blocks, const bq_qweight* dst, bq_stream_t stream);
+bq_status bq_repack_fp8_b128(const void* weight, const float* scales, const bq_qweight* dst,
+                             bq_stream_t stream);
 
 /* ------------------------------------------------------------------ S3, S4
  * Dense qmm: Y[m][r] = sum_k X[m][k] * W[r][k] with W the dequantised

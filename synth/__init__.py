@@ -120,8 +120,8 @@ def fp8_block_weight(g: np.random.Generator, lead_shape, n: int, k: int,
     0x7F and 0xFF, the NaN codes, are skipped) and fp32 block scales uniform
     in s_range."""
     lead_shape = tuple(lead_shape)
-    u = g.integers(0, 254, size=lead_shape + (n, k), dtype=np.int64)
-    codes = (u + (u >= 0x7F)).astype(np.uint8)     # 0..126, 128..254: skips 0x7F and 0xFF
+    codes = g.integers(0, 254, size=lead_shape + (n, k), dtype=np.uint8)
+    codes += codes >= 0x7F                          # 0..126, 128..254: skips 0x7F and 0xFF
     nb, kb = -(-n // FP8_BLOCK), -(-k // FP8_BLOCK)
     scales = g.uniform(s_range[0], s_range[1], size=lead_shape + (nb, kb)).astype(np.float32)
     return Fp8Weight(codes, scales)
@@ -173,7 +173,7 @@ class DenseCase:
 @dataclasses.dataclass(frozen=True)
 class MoECase:
     name: str
-    fmt: str          # routed expert format: "int4" | "q2_k" | "mxfp4"
+    fmt: str          # routed expert format: "int4" | "q2_k" | "mxfp4" | "fp8_b128"
     t: int            # tokens
     hidden: int
     inter: int
@@ -204,6 +204,12 @@ MOE_Q2K = MoECase("moe_q2k_t2048_h4096_e256_top6_i2048_zipf_sharedq8", "q2_k", 2
 MXFP4_EXPERT_E_RANGE = (116, 122)
 MOE_MXFP4 = MoECase("moe_mxfp4_t2048_h2048_e128_top8_i768", "mxfp4", 2048, 2048, 768,
                     128, 8, False, None, 1005)
+
+
+# The int4 MoE shapes with FP8 e4m3 experts and 128 x 128 block scales
+# (DeepSeek V3 / V4 block weights; I = 768 is six scale blocks).
+MOE_FP8 = MoECase("moe_fp8_t2048_h2048_e128_top8_i768", "fp8_b128", 2048, 2048, 768,
+                  128, 8, False, None, 1006)
 
 
 def decode_case(base: MoECase, batch: int) -> MoECase:
@@ -239,6 +245,9 @@ def moe_weights(case: MoECase):
     elif case.fmt == "q2_k":
         w_gu = q2_k_blocks(g, e * 2 * i, h).reshape(e, 2 * i, h // 256, 84)
         w_d = q2_k_blocks(g, e * h, i).reshape(e, h, i // 256, 84)
+    elif case.fmt == "fp8_b128":
+        w_gu = fp8_block_weight(g, (e,), 2 * i, h)
+        w_d = fp8_block_weight(g, (e,), h, i)
     elif case.fmt == "mxfp4":
         w_gu = mxfp4_blocks(g, e * 2 * i, h, MXFP4_EXPERT_E_RANGE).reshape(e, 2 * i, h // 32, 17)
         w_d = mxfp4_blocks(g, e * h, i, MXFP4_EXPERT_E_RANGE).reshape(e, h, i // 32, 17)
@@ -280,7 +289,8 @@ def dense_inputs(case: DenseCase):
 
 
 def bytes_per_weight(fmt: str) -> float:
-    return {"q8_0": 34 / 32, "q2_k": 84 / 256, "int4": 0.5 + 4 / 64, "mxfp4": 17 / 32}[fmt]
+    return {"q8_0": 34 / 32, "q2_k": 84 / 256, "int4": 0.5 + 4 / 64, "mxfp4": 17 / 32,
+            "fp8_b128": 1 + 4 / (128 * 128)}[fmt]
 
 
 def expert_weight_bytes(case: MoECase) -> float:

@@ -52,6 +52,8 @@ def make_qweight(bq, fmt: str, w, n_mats: int, n: int, k: int, swiglu: bool = Fa
         bq.repack_q2_k(dev(np.asarray(w).reshape(-1)), qw)
     elif fmt == "mxfp4":
         bq.repack_mxfp4(dev(np.asarray(w).reshape(-1)), qw)
+    elif fmt == "fp8_b128":
+        bq.repack_fp8_b128(dev(w.bytes.reshape(-1)), dev(w.scales.reshape(-1)), qw)
     else:
         bq.repack_int4(dev(w.words.reshape(-1).view(np.int32)),
                        dev(w.scales.reshape(-1).view(np.int16)),
@@ -68,12 +70,16 @@ def dequant(fmt: str, w):
         return O.dequant_q2_k(np.asarray(w))
     if fmt == "mxfp4":
         return O.dequant_mxfp4(np.asarray(w))
+    if fmt == "fp8_b128":
+        return O.dequant_fp8_block(w.bytes, w.scales)
     return O.dequant_int4(w.words, w.scales, w.biases)
 
 
 def expert_slice(fmt: str, w, e: int):
     if fmt == "int4":
         return synth.Int4Weight(w.words[e], w.scales[e], w.biases[e])
+    if fmt == "fp8_b128":
+        return synth.Fp8Weight(w.bytes[e], w.scales[e])
     return w[e]
 
 

@@ -132,3 +132,52 @@ def test_mxfp4_empty_is_noop(lib):
     lib.dequant_mxfp4(torch.zeros(0, dtype=torch.uint8, device="cuda"), out)
     torch.cuda.synchronize()
     assert out.abs().sum().item() == 0
+
+
+# ---------------------------------------------------------------- FP8 e4m3, 128 x 128 block scales
+def _run_fp8(lib, w8, sc):
+    import torch
+    n, k = w8.shape
+    out = torch.full((n, k), 12345.0, dtype=torch.float32, device="cuda")
+    lib.dequant_fp8_b128(dev(w8), dev(sc), out)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def _exact_fp8(got, ref):
+    """The fp32 product of the code and the scale is the fp32 rounding of the
+    exact product: bit-exact against the fp64 oracle value cast to fp32 (NaN
+    positions compared, payloads not)."""
+    nan = np.isnan(ref)
+    np.testing.assert_array_equal(np.isnan(got), nan)
+    np.testing.assert_array_equal(got[~nan].view(np.uint32), ref[~nan].astype(np.float32).view(np.uint32))
+
+
+@pytest.mark.parametrize("n,k", [(1, 1), (5, 300), (128, 128), (300, 200), (257, 1024), (3, 16), (130, 48)])
+def test_fp8_bit_exact_ragged(lib, n, k):
+    w = synth.fp8_block_weight(synth.rng(400 + n + k), (), n, k, s_range=(1e-6, 3.0))
+    _exact_fp8(_run_fp8(lib, w.bytes, w.scales), O.dequant_fp8_block(w.bytes, w.scales))
+
+
+def test_fp8_every_code_and_nan(lib):
+    w8 = np.arange(256, dtype=np.uint8).reshape(2, 128).repeat(64, axis=0)   # [128, 128]
+    for s in (1.0, 2.0 ** -20, 1.7e-4, 3.0e38 / 448.0):
+        sc = np.array([[s]], dtype=np.float32)
+        got = _run_fp8(lib, w8, sc)
+        _exact_fp8(got, O.dequant_fp8_block(w8, sc))
+    got = _run_fp8(lib, w8, np.array([[1.0]], dtype=np.float32))
+    np.testing.assert_array_equal(got[0, :127], O.e4m3_value(np.arange(127)).astype(np.float32))
+
+
+def test_fp8_full_size_expert_weights(lib):
+    w_gu, w_d, _, _, _ = synth.moe_weights(synth.dataclasses.replace(synth.MOE_FP8, experts=2))
+    for w in (w_gu, w_d):
+        _exact_fp8(_run_fp8(lib, w.bytes[1], w.scales[1]), O.dequant_fp8_block(w.bytes[1], w.scales[1]))
+
+
+def test_fp8_empty_is_noop(lib):
+    import torch
+    out = torch.zeros(4, device="cuda")
+    st = lib._lib.bq_dequant_fp8_b128(None, None, 0, 7, lib._ptr(out), lib._stream(None))
+    torch.cuda.synchronize()
+    assert st == lib.OK and out.abs().sum().item() == 0

@@ -22,6 +22,8 @@ SMALL = [
     _case("q2k_ragged", "q2_k", 131, 256, 256, 12, 6, zipf=True),
     _case("mxfp4_small", "mxfp4", 37, 256, 128, 16, 4),
     _case("mxfp4_many_tokens_shared", "mxfp4", 300, 256, 256, 4, 2, zipf=True, shared="q8_0"),
+    _case("fp8_small", "fp8_b128", 37, 256, 128, 16, 4),
+    _case("fp8_ragged_shared", "fp8_b128", 131, 384, 256, 12, 6, zipf=True, shared="q8_0"),
 ]
 
 
@@ -36,7 +38,8 @@ def test_moe_small(lib, case):
 @pytest.mark.parametrize("t", [1, 2, 5, 8])
 @pytest.mark.parametrize("base", [_case("dec_int4", "int4", 0, 256, 128, 32, 8),
                                   _case("dec_q2k", "q2_k", 0, 512, 256, 64, 6, shared="q8_0"),
-                                  _case("dec_mxfp4", "mxfp4", 0, 256, 256, 32, 8)],
+                                  _case("dec_mxfp4", "mxfp4", 0, 256, 256, 32, 8),
+                                  _case("dec_fp8", "fp8_b128", 0, 256, 256, 32, 8)],
                          ids=lambda c: c.name)
 def test_moe_decode_small(lib, base, t):
     case = synth.dataclasses.replace(base, t=t)
@@ -105,7 +108,8 @@ def _full(lib, base):
     return _FULL[base.name]
 
 
-@pytest.mark.parametrize("base", [synth.MOE_INT4, synth.MOE_Q2K, synth.MOE_MXFP4], ids=lambda c: c.name)
+@pytest.mark.parametrize("base", [synth.MOE_INT4, synth.MOE_Q2K, synth.MOE_MXFP4, synth.MOE_FP8],
+                         ids=lambda c: c.name)
 def test_moe_prefill_full_size_sampled(lib, base):
     weights, layer = _full(lib, base)
     inp = synth.moe_inputs(base, weights)
@@ -117,7 +121,8 @@ def test_moe_prefill_full_size_sampled(lib, base):
 
 
 @pytest.mark.parametrize("batch", [1, 2, 4, 8])
-@pytest.mark.parametrize("base", [synth.MOE_Q2K, synth.MOE_INT4, synth.MOE_MXFP4], ids=lambda c: c.name)
+@pytest.mark.parametrize("base", [synth.MOE_Q2K, synth.MOE_INT4, synth.MOE_MXFP4, synth.MOE_FP8],
+                         ids=lambda c: c.name)
 def test_moe_decode_full_shapes(lib, base, batch):
     weights, layer = _full(lib, base)
     case = synth.decode_case(base, batch)

@@ -20,7 +20,8 @@ def _qmm(lib, qw, x):
 
 @pytest.mark.parametrize("fmt,n,k", [("q8_0", 128, 64), ("q8_0", 384, 576), ("q2_k", 256, 512),
                                      ("q2_k", 128, 256), ("int4", 256, 384), ("int4", 128, 128),
-                                     ("mxfp4", 256, 384), ("mxfp4", 128, 128)])
+                                     ("mxfp4", 256, 384), ("mxfp4", 128, 128),
+                                     ("fp8_b128", 256, 384), ("fp8_b128", 128, 128)])
 @pytest.mark.parametrize("m", [1, 3, 8, 13, 40, 130])
 def test_qmm_small_shapes(lib, fmt, n, k, m):
     g = synth.rng(n + k + m)
@@ -30,6 +31,8 @@ def test_qmm_small_shapes(lib, fmt, n, k, m):
         w = synth.q2_k_blocks(g, n, k)
     elif fmt == "mxfp4":
         w = synth.mxfp4_blocks(g, n, k)
+    elif fmt == "fp8_b128":
+        w = synth.fp8_block_weight(g, (), n, k)
     else:
         w = synth.int4_weight(g, (n,), k)
     qw = make_qweight(lib, fmt, w, 1, n, k)
@@ -119,3 +122,53 @@ def test_mxfp4_out_of_range_exponent_is_flagged(lib):
     make_qweight(lib, "mxfp4", blocks, 1, n, k)
     assert lib.device_status() == lib.DEV_SCALE_RANGE
     assert lib.device_status() == lib.DEV_OK   # read clears it
+
+
+# ---------------------------------------------------------------- FP8 operand exactness
+@pytest.mark.parametrize("m", [8, 128])   # qgemv path and tensor-core path
+def test_fp8_operands_are_the_stated_roundings(lib, m):
+    # every code and scales over a wide range; the device weight is
+    # fp16(e4m3 * fp16(256 s)) / 256 (one-hot rows read it back exactly)
+    n, k = 256, 256
+    g = synth.rng(91 + m)
+    w = synth.fp8_block_weight(g, (), n, k, s_range=(1e-6, 0.5))
+    w.bytes[0, :254] = np.r_[np.arange(127), np.arange(128, 255)]
+    qw = make_qweight(lib, "fp8_b128", w, 1, n, k)
+    s16 = (w.scales.astype(np.float64) * 256.0).astype(np.float16).astype(np.float64)
+    s_full = np.repeat(np.repeat(s16, 128, 0), 128, 1)
+    want = (O.e4m3_value(w.bytes) * s_full).astype(np.float16).astype(np.float64) / 256.0
+    for r0 in range(0, k, m):
+        rows = np.arange(r0, r0 + m)
+        x = np.zeros((m, k), dtype=np.float16)
+        x[np.arange(m), rows] = 1.0
+        np.testing.assert_array_equal(_qmm(lib, qw, x), want[:, rows].T)
+
+
+def test_fp8_swiglu_halves_use_their_own_scales(lib):
+    # a fused gate/up weight [2I, K]: gate rows and up rows read different scale
+    # rows; through the MoE layer with one expert and k = 1 this is the dense FFN
+    import helpers
+    case = synth.MoECase("fp8_e1", "fp8_b128", 19, 256, 128, 1, 1, False, None, 3)
+    inp = synth.moe_inputs(case)
+    inp.w_gu.scales[0, 0, :] *= 4.0            # gate block rows only
+    layer = helpers.build_layer(lib, inp)
+    assert_close_matmul(helpers.run_moe(lib, layer, inp), helpers.oracle_moe(inp), case.name)
+
+
+def test_fp8_out_of_range_scale_is_flagged(lib):
+    n, k = 128, 128
+    w = synth.fp8_block_weight(synth.rng(9), (), n, k)
+    lib.device_status()
+    make_qweight(lib, "fp8_b128", w, 1, n, k)
+    assert lib.device_status() == lib.DEV_OK
+    w.scales[0, 0] = 1.0                       # 448 * 256 > 65504
+    make_qweight(lib, "fp8_b128", w, 1, n, k)
+    assert lib.device_status() == lib.DEV_SCALE_RANGE
+
+
+def test_fp8_rejects_gate_up_halves_off_the_scale_grid(lib):
+    qw = lib.QWeight(lib.FMT_FP8_B128, 1, 384, 128, swiglu=True)      # n/2 = 192
+    w = synth.fp8_block_weight(synth.rng(10), (), 384, 128)
+    import torch
+    with pytest.raises(lib.BQError, match="SHAPE"):
+        lib.repack_fp8_b128(torch.from_numpy(w.bytes).cuda(), torch.from_numpy(w.scales).cuda(), qw)
