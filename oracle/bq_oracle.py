@@ -33,6 +33,10 @@ Readings taken where the pages are silent:
   ``scales`` row-major [ceil(n/128), ceil(k/128)] fp32 (the page's
   ``scales[i/128, j/128]``); a partial last block takes the scale of its
   block.
+* RMSNorm (the pages name the fused ``rmsNormQgemvInt4Fast`` and the
+  ``mt_rms_norm`` kernels but print no formula): the usual
+  ``x = gamma * h / sqrt(mean(h^2) + eps)``, mean over the row, eps inside
+  the root, elementwise gain gamma.
 * Top-k: the k largest ``z = logit (+ bias)`` computed in fp32, ties to
   the lower expert index, output in descending z; the bias enters both
   selection and weighting.
@@ -50,7 +54,7 @@ import numpy as np
 
 __all__ = [
     "dequant_q8_0", "dequant_q2_k", "dequant_int4", "dequant_mxfp4", "MXFP4_VALUES",
-    "e4m3_value", "dequant_fp8_block", "FP8_BLOCK", "qmm", "route",
+    "e4m3_value", "dequant_fp8_block", "FP8_BLOCK", "rmsnorm", "qmm", "route",
     "SCORINGS", "softplus", "route_scored",
     "permute", "silu", "swiglu_ffn", "moe_ffn", "moe_ffn_tokens",
 ]
@@ -200,6 +204,25 @@ def dequant_fp8_block(weight: np.ndarray, scales: np.ndarray) -> np.ndarray:
     assert sc.shape[-2:] == (nb, kb), (sc.shape, (nb, kb))
     full = np.repeat(np.repeat(sc, FP8_BLOCK, axis=-2), FP8_BLOCK, axis=-1)[..., :n, :k]
     return e4m3_value(w) * full
+
+
+# --------------------------------------------------------------------------
+# RMSNorm (the normalisation fused ahead of the router / head GEMV)
+# --------------------------------------------------------------------------
+
+def rmsnorm(h: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
+    """``x = gamma * h / sqrt(mean(h^2) + eps)`` per row, in fp64.
+
+    Follows *butter #10* (``rmsNormQgemvInt4Fast``: the final norm fused with
+    the int4 GEMV that consumes it; ``mt_rms_norm`` over rows of up to 4096)
+    with the standard RMSNorm definition.
+
+    h: [..., H] (any float dtype, widened exactly); gamma: [H]; eps >= 0.
+    Returns fp64 [..., H].
+    """
+    h64 = np.asarray(h, dtype=np.float64)
+    ms = np.mean(h64 * h64, axis=-1, keepdims=True)
+    return np.asarray(gamma, dtype=np.float64) * h64 / np.sqrt(ms + float(eps))
 
 
 # --------------------------------------------------------------------------

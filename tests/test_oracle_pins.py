@@ -654,3 +654,34 @@ def test_fp8_page_quantiser_round_trip():
     tol = np.maximum(np.abs(x) / 16.0, 2.0 ** -10 * s_full) + 1e-30
     assert np.all(np.abs(back - x) <= tol)
     assert np.abs(back).max() <= 448.0 * sc.max() * (1 + 1e-7)
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm
+# ---------------------------------------------------------------------------
+
+def test_rmsnorm_closed_forms():
+    g = np.array([1.0, -2.0, 0.5, 3.0])
+    # a constant row c: mean(h^2) = c^2, so x = gamma * c / sqrt(c^2 + eps)
+    np.testing.assert_allclose(O.rmsnorm(np.full(4, 3.0), g, 0.0), g, rtol=1e-15)
+    np.testing.assert_allclose(O.rmsnorm(np.full(4, -3.0), g, 7.0), -g * 3.0 / 4.0, rtol=1e-15)
+    # h = (3, 4, 0, 0): mean(h^2) = 25 / 4, rms = 2.5
+    np.testing.assert_allclose(O.rmsnorm(np.array([3.0, 4.0, 0.0, 0.0]), g, 0.0), [1.2, -3.2, 0.0, 0.0],
+                               rtol=1e-15)
+    # a zero row stays zero (no 0/0) when eps > 0
+    assert np.all(O.rmsnorm(np.zeros(4), g, 1e-6) == 0.0)
+
+
+def test_rmsnorm_invariants_and_brute_force():
+    rng = np.random.default_rng(5)
+    h = rng.normal(0, 3, (5, 64))
+    g = rng.uniform(0.5, 2, 64)
+    x = O.rmsnorm(h, g, 0.0)
+    np.testing.assert_allclose(np.mean((x / g) ** 2, axis=-1), 1.0, rtol=1e-13)   # unit mean square
+    np.testing.assert_allclose(O.rmsnorm(-7.5 * h, g, 0.0), -x, rtol=1e-13)         # scale invariance
+    eps = 0.3
+    xe = O.rmsnorm(h, g, eps)
+    for r in range(5):
+        rms = math.sqrt(math.fsum(v * v for v in h[r]) / 64 + eps)
+        for c in range(64):
+            assert abs(xe[r, c] - g[c] * h[r, c] / rms) <= 1e-13 * abs(g[c] * h[r, c] / rms) + 1e-300
