@@ -354,6 +354,38 @@ def run_main(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def decode_from_hidden(args, bq, flush, base, layer):
+    """Decode steps that start from hidden states: RMSNorm + the router matmul
+    (Q8_0 router [E][H], one norm-fused GEMV) and then the layer, against the
+    same layer started from precomputed logits.  Reports both step times and
+    the norm + router stage alone."""
+    import torch
+    g = synth.rng(4545)
+    router = qweight(bq, "q8_0", synth.q8_0_blocks(g, base.experts, base.hidden, d_range=(1e-4, 2e-3)), 1,
+                     base.experts, base.hidden)
+    gamma = upload(g.uniform(0.5, 1.5, base.hidden).astype(np.float16).view(np.uint16)).view(torch.float16)
+    res = {}
+    for b in (1, 8):
+        case = synth.decode_case(base, b)
+        layer.set_tokens(b)
+        hs = [upload(synth.moe_activations(case, synth.decode_step_seed(s))[0].view(np.uint16)).view(torch.float16)
+              for s in range(args.decode_steps)]
+        y = torch.empty((b, base.hidden), dtype=torch.float32, device="cuda")
+        ws = torch.empty(layer.hidden_workspace_bytes(), dtype=torch.uint8, device="cuda")
+        it = iter(range(10 ** 9))
+
+        def hstep():
+            bq.moe_gather_qmm_hidden(layer, router, hs[next(it) % len(hs)], gamma, 1e-6, None, y, ws)
+
+        for _ in range(3):
+            hstep()
+        it = iter(range(10 ** 9))
+        ms, stg = time_steps(hstep, args.decode_steps, flush, stage_events=[bq.STAGE_NORM_ROUTER])
+        res[f"B{b}"] = {"us_per_step": round(1e3 * statistics.mean(ms), 2),
+                        "norm_router_us": round(1e3 * statistics.mean(stg[bq.STAGE_NORM_ROUTER]), 2)}
+    return res
+
+
 def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "mxfp4", "fp8_b128", "dense")):
     import torch
     out = {}
@@ -398,6 +430,8 @@ def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "mxfp4", "fp8
                             "tok_s": round(b * len(ms) / (sum(ms) / 1e3), 1)}
         if res:
             out[f"decode_{base.fmt}"] = res
+        if base.fmt == "q2_k" and "decode" in sections:
+            out["decode_from_hidden_q2_k"] = decode_from_hidden(args, bq, flush, base, layer)
         if base.fmt in ("int4", "mxfp4", "fp8_b128") and base.fmt in sections:
             layer.set_tokens(base.t)
             xh, lh = synth.moe_activations(base)

@@ -67,6 +67,12 @@ _SIGS = {
     "bq_moe_permute_noalloc": (c_int32, [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p,
                                          c_void_p, c_void_p, c_void_p]),
     "bq_set_stage_events": (c_int32, [c_int32, c_void_p, c_void_p]),
+    "bq_rmsnorm": (c_int32, [c_void_p, c_int32, c_int32, c_void_p, c_float, c_void_p, c_void_p]),
+    "bq_rmsnorm_qmm": (c_int32, [c_void_p, c_int32, c_void_p, c_float, POINTER(QWeightC), c_void_p, c_void_p,
+                                 c_void_p]),
+    "bq_moe_hidden_workspace_bytes": (c_size_t, [POINTER(MoEDescC)]),
+    "bq_moe_gather_qmm_hidden": (c_int32, [POINTER(MoEDescC), POINTER(QWeightC), c_void_p, c_void_p, c_float,
+                                           c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "bq_launch_count": (c_uint64, []),
     "bq_moe_gather_qmm": (c_int32, [POINTER(MoEDescC), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                     c_size_t, c_void_p]),
@@ -236,7 +242,7 @@ def moe_permute(ids, n_experts: int, counts, offsets, perm_token, perm_slot, inv
            "bq_moe_permute")
 
 
-STAGE_ROUTE_PERMUTE, STAGE_GATE_UP, STAGE_DOWN, STAGE_SHARED, STAGE_COMBINE = range(5)
+STAGE_ROUTE_PERMUTE, STAGE_GATE_UP, STAGE_DOWN, STAGE_SHARED, STAGE_COMBINE, STAGE_NORM_ROUTER = range(6)
 
 
 def set_stage_events(stage: int, start=None, stop=None):
@@ -280,6 +286,10 @@ class MoELayer:
     def workspace_bytes(self) -> int:
         return int(_lib.bq_moe_workspace_bytes(ctypes.byref(self.c)))
 
+    def hidden_workspace_bytes(self) -> int:
+        """Workspace of moe_gather_qmm_hidden (layer + normalised x + logits)."""
+        return int(_lib.bq_moe_hidden_workspace_bytes(ctypes.byref(self.c)))
+
 
 def moe_workspace_bytes(layer: MoELayer) -> int:
     return layer.workspace_bytes()
@@ -289,4 +299,32 @@ def moe_gather_qmm(layer: MoELayer, x, router_logits, logit_bias, y, workspace, 
     _check(_lib.bq_moe_gather_qmm(ctypes.byref(layer.c), _ptr(x), _ptr(router_logits), _ptr(logit_bias),
                                   _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream)),
            "bq_moe_gather_qmm")
+    return y
+
+
+# ---------------------------------------------------------------- RMSNorm, fused
+def rmsnorm(h, gamma, eps: float, x, stream=None):
+    """x = gamma * h / sqrt(mean(h^2) + eps) per row; h, x fp16 [T, H], gamma fp16 [H]."""
+    t, hdim = h.shape
+    _check(_lib.bq_rmsnorm(_ptr(h), t, hdim, _ptr(gamma), eps, _ptr(x), _stream(stream)), "bq_rmsnorm")
+    return x
+
+
+def rmsnorm_qmm(h, gamma, eps: float, w: QWeight, y, x_out=None, stream=None):
+    """y = W rmsnorm(h) (fp32 [m, n]); x_out (fp16 [m, k]) receives the normalised
+    rows (required for m > 8)."""
+    m = h.shape[0]
+    _check(_lib.bq_rmsnorm_qmm(_ptr(h), m, _ptr(gamma), eps, ctypes.byref(w.c), _ptr(x_out), _ptr(y),
+                               _stream(stream)),
+           "bq_rmsnorm_qmm")
+    return y
+
+
+def moe_gather_qmm_hidden(layer: MoELayer, router: QWeight, hidden, gamma, eps: float, logit_bias, y, workspace,
+                          stream=None):
+    """The MoE layer from hidden states: RMSNorm + router matmul, then moe_gather_qmm."""
+    _check(_lib.bq_moe_gather_qmm_hidden(ctypes.byref(layer.c), ctypes.byref(router.c), _ptr(hidden), _ptr(gamma),
+                                         eps, _ptr(logit_bias), _ptr(y), _ptr(workspace), workspace.numel(),
+                                         _stream(stream)),
+           "bq_moe_gather_qmm_hidden")
     return y

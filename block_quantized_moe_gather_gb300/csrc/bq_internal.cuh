@@ -189,6 +189,43 @@ __device__ __forceinline__ __half2 mx_scale_h2(uint32_t e) {
     return u32_as_h2(b | (b << 16));
 }
 
+// ---- RMSNorm: x = gamma * h / sqrt(mean(h^2) + eps)
+//
+// 1 / sqrt(mean(h^2) + eps) of one fp16 row of length k (k % 8 == 0, row
+// 16-byte aligned), computed by one warp: lane-strided 16-byte loads, fp32
+// sum of squares per lane, butterfly sum.  The standalone norm kernel and the
+// norm-fused GEMV both use this, so their results agree bit for bit.
+__device__ __forceinline__ float row_inv_rms(const __half* row, int k, float eps, int lane) {
+    float ss = 0.f;
+    const uint4* r4 = reinterpret_cast<const uint4*>(row);
+    for (int i = lane; i < k / 8; i += 32) {
+        const uint4 v = __ldg(r4 + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __half22float2(u32_as_h2(w[j]));
+            ss = __fmaf_rn(f.x, f.x, ss);
+            ss = __fmaf_rn(f.y, f.y, ss);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    return rsqrtf(ss / (float)k + eps);
+}
+
+// Eight normalised values: fp16((h * gamma) * inv), products in fp32.
+__device__ __forceinline__ uint4 norm8(uint4 h, uint4 g, float inv) {
+    const uint32_t hw[4] = {h.x, h.y, h.z, h.w}, gw[4] = {g.x, g.y, g.z, g.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 hf = __half22float2(u32_as_h2(hw[j])), gf = __half22float2(u32_as_h2(gw[j]));
+        o[j] = h2_as_u32(__floats2half2_rn(__fmul_rn(__fmul_rn(hf.x, gf.x), inv),
+                                           __fmul_rn(__fmul_rn(hf.y, gf.y), inv)));
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // ---- FP8 e4m3 (OCP OFP8, as DeepSeek V3 / V4 block weights)
 //
 // Two e4m3 values (low byte -> low lane) as an fp16 pair.  Every e4m3 value

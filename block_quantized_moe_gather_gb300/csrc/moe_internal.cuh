@@ -66,10 +66,24 @@ struct QgemvParams {
     int ksplit;
     float* partial;
     int32_t* counters;
+    // RMSNorm in front of the GEMV (single segment only): when `gamma` is set,
+    // each activation row r of x is replaced by gamma * x_r / sqrt(mean(x_r^2)
+    // + eps) (fp16), and the normalised rows go to x_out (if set) as well.
+    const __half* gamma;
+    float eps;
+    __half* x_out;
 };
 constexpr int kMaxKsplit = 16;
 // Split factor that gives the GPU enough CTAs for this shape.
 int qgemv_ksplit(int fmt, int n, int k, int max_segments, int max_tokens);
 void launch_qgemv(const QgemvParams& p, int max_segments, cudaStream_t st, bool after_previous = false);
+
+// ---- RMSNorm (norm.cu)
+// x[r] = gamma * h[r] / sqrt(mean(h[r]^2) + eps) for rows r < T of length H.
+void launch_rmsnorm(const __half* h, int T, int H, const __half* gamma, float eps, __half* x, cudaStream_t st);
+// y = W rmsnorm(h) for m rows: the norm-fused GEMV for m <= 8 (x_out
+// optional), else the norm kernel into x_out (required) and the GEMM.
+bq_status launch_rmsnorm_qmm(const __half* h, int m, const __half* gamma, float eps, const bq_qweight* w,
+                             __half* x_out, float* y, cudaStream_t st);
 
 }  // namespace bq

@@ -160,14 +160,28 @@ __device__ __forceinline__ Q2Scales q2_scales(uint32_t sc4, uint32_t dm) {
 // and (4s+2, 4s+3) of rows g (hh = 0) and g + 8 (hh = 1) of each 16-row tile.
 // The per-row scale terms are broadcast to both fp16 lanes once per Q2_K
 // sub-block (four steps) or once per slab, not once per pair.
-template <int FMT>
+// NORM: the activations are normalised on the fly, x = (h * gamma) * inv
+// (gq: gamma at the slab's first column; inv: the token's 1/rms), and, when
+// xo is set, stored there (the slab's first column of the token's x row).
+template <int FMT, bool NORM>
 __device__ __forceinline__ void mma_frag(const Frag<FMT>& f, const __half* xq, bool xvalid, int t,
-                                         float (&acc)[2][4]) {
+                                         float (&acc)[2][4], const __half* gq = nullptr, float inv = 0.f,
+                                         __half* xo = nullptr) {
     constexpr int XV = Traits<FMT>::XV;
     uint4 x[XV];
     const uint4* xp = reinterpret_cast<const uint4*>(xq + (Traits<FMT>::SK / 4) * t);
 #pragma unroll
     for (int v = 0; v < XV; ++v) x[v] = xvalid ? __ldg(xp + v) : make_uint4(0, 0, 0, 0);
+    if (NORM && xvalid) {
+        const uint4* gp = reinterpret_cast<const uint4*>(gq + (Traits<FMT>::SK / 4) * t);
+#pragma unroll
+        for (int v = 0; v < XV; ++v) x[v] = bq::norm8(x[v], __ldg(gp + v), inv);
+        if (xo) {
+            uint4* op = reinterpret_cast<uint4*>(xo + (Traits<FMT>::SK / 4) * t);
+#pragma unroll
+            for (int v = 0; v < XV; ++v) op[v] = x[v];
+        }
+    }
     if (FMT == BQ_FMT_Q2_K) {
         Q2Scales q2[2][2];
 #pragma unroll
@@ -297,14 +311,22 @@ __device__ __forceinline__ void qgemv_epilogue(const bq::QgemvParams& p, const f
 // fill the GPU, without a K split across CTAs): a CTA covers one 32-row
 // quarter of a tile and its 8 warps take 8 contiguous K pieces; the partials
 // are summed in warp order, so results stay bit-reproducible either way.
-template <int FMT, bool SWIGLU, int KW>
-__global__ void __launch_bounds__(kThreads, 2)
+//
+// NORM (single segment, no SwiGLU): RMSNorm in front of the GEMV.  Every CTA
+// first computes 1/rms of its token rows over the whole K (warp w: token w),
+// then normalises its activation fragments as it loads them; the CTAs of
+// row tile 0, row quarter 0 also store the normalised rows of their K share
+// to x_out, so each value is written once.
+template <int FMT, bool SWIGLU, int KW, bool NORM>
+__global__ void __launch_bounds__(kThreads, NORM ? 1 : 2)   // the norm-fused GEMV needs more registers
 qgemv_kernel(const bq::QgemvParams p) {
     using T = Traits<FMT>;
     static_assert(KW == 2 || KW == 8, "K ways per CTA");
+    static_assert(!(NORM && SWIGLU), "the norm-fused GEMV has a plain epilogue");
     // partials of the warps with K piece > 0: [quarter (KW 2) or piece - 1 (KW 8)][tile][lane][row half]
     __shared__ float2 red[KW == 8 ? 7 : 4][2][32][2];
     __shared__ int s_last;
+    __shared__ float s_inv[NORM ? 8 : 1];
 
     // launched right behind the kernel that produced the routing / activations
     bq::grid_dependency_wait();
@@ -336,6 +358,17 @@ qgemv_kernel(const bq::QgemvParams p) {
             const int src = p.src_row ? __ldg(p.src_row + lr) : lr;
             xrow = p.x + (int64_t)src * p.k;
         }
+        float inv = 0.f;
+        __half* xo = nullptr;
+        if (NORM) {
+            __syncthreads();   // the previous token group is done with s_inv
+            if (warp < ntok) s_inv[warp] = bq::row_inv_rms(p.x + (int64_t)(start + tok0 + warp) * p.k, p.k, p.eps, lane);
+            __syncthreads();
+            if (xvalid) {
+                inv = s_inv[g];
+                if (p.x_out && rt == 0 && quarter == 0) xo = p.x_out + (int64_t)(start + tok0 + g) * p.k;
+            }
+        }
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         // register ring of D slabs in flight (D - 1 ahead of the one being multiplied)
         constexpr int D = T::DEPTH;
@@ -351,7 +384,11 @@ qgemv_kernel(const bq::QgemvParams p) {
                 const int nxt = i + d + D - 1;
                 if (nxt < n)
                     load_frag<FMT>(f[(d + D - 1) % D], wbase + (int64_t)(kt_begin + nxt) * T::SB, rowbase, g, t);
-                mma_frag<FMT>(f[d], xrow + (kt_begin + i + d) * T::SK, xvalid, t, acc);
+                const int kc = (kt_begin + i + d) * T::SK;
+                if (NORM)
+                    mma_frag<FMT, true>(f[d], xrow + kc, xvalid, t, acc, p.gamma + kc, inv, xo ? xo + kc : nullptr);
+                else
+                    mma_frag<FMT, false>(f[d], xrow + kc, xvalid, t, acc);
             }
         }
         if (FMT == BQ_FMT_FP8_B128) {   // the FP8 slab scales carry a factor 256 (exact to remove)
@@ -445,8 +482,9 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
     // the expert GEMVs of a MoE step are left whole-tile (measured no better)
     const bool quarters = p.ksplit == 1 && !p.seg_expert && tiles * max_segments < sm_count();
     dim3 grid(tiles * (quarters ? 4 : 1), max_segments, p.ksplit);
-    auto kernel = quarters ? (p.swiglu ? qgemv_kernel<FMT, true, 8> : qgemv_kernel<FMT, false, 8>)
-                           : (p.swiglu ? qgemv_kernel<FMT, true, 2> : qgemv_kernel<FMT, false, 2>);
+    auto kernel = p.gamma ? (quarters ? qgemv_kernel<FMT, false, 8, true> : qgemv_kernel<FMT, false, 2, true>)
+                : quarters ? (p.swiglu ? qgemv_kernel<FMT, true, 8, false> : qgemv_kernel<FMT, false, 8, false>)
+                           : (p.swiglu ? qgemv_kernel<FMT, true, 2, false> : qgemv_kernel<FMT, false, 2, false>);
     if (after_previous) bq::launch_after(kernel, grid, dim3(kThreads), 0, st, p);
     else kernel<<<grid, kThreads, 0, st>>>(p);
 }

@@ -359,6 +359,43 @@ bq_status bq_moe_gather_qmm(const bq_moe_desc* desc, const uint16_t* x,
                             float* y, void* workspace, size_t workspace_bytes,
                             bq_stream_t stream);
 
+/* ------------------------------------------------------------------ RMSNorm, fused
+ * RMSNorm and RMSNorm fused with the quantised matmul behind it ([butter]:
+ * rmsNormQgemvInt4Fast, the final norm fused with the int4 GEMV; the
+ * mt_rms_norm row kernels).  For each row r of length H:
+ *   x[r] = gamma * h[r] / sqrt(mean(h[r]^2) + eps)
+ * computed in fp32 (1/sqrt by rsqrtf; each value (h * gamma) * inv, then
+ * rounded to fp16).  Both entry points compute inv and x identically, so x
+ * from bq_rmsnorm_qmm equals bq_rmsnorm's bit for bit.
+ * h, x: device fp16 [T][H] row-major; gamma: device fp16 [H]; H a multiple
+ * of 8; eps finite and >= 0.
+ * bq_rmsnorm_qmm: y[r] = W x[r] (fp32 [m][w->n]) for a plain weight w
+ * (n_mats 1, swiglu 0, k = H).  m <= 8 runs one norm-fused GEMV kernel
+ * (x_out may be NULL; if set it receives x); larger m runs the norm kernel
+ * into x_out (then required) and the tensor-core GEMM.
+ * Errors: BQ_ERR_NULL, BQ_ERR_SHAPE, BQ_ERR_FORMAT, BQ_ERR_ALIGN, BQ_ERR_CUDA.
+ * T == 0 / m == 0 is a no-op.
+ */
+bq_status bq_rmsnorm(const uint16_t* h, int32_t T, int32_t H, const uint16_t* gamma, float eps,
+                     uint16_t* x, bq_stream_t stream);
+bq_status bq_rmsnorm_qmm(const uint16_t* h, int32_t m, const uint16_t* gamma, float eps,
+                         const bq_qweight* w, uint16_t* x_out, float* y, bq_stream_t stream);
+
+/*
+ * One MoE layer from the hidden states: x = RMSNorm(hidden) (as above),
+ * router_logits = W_router x (fp32; `router` a plain weight with n =
+ * n_experts, k = hidden, n_experts a multiple of 128), then exactly
+ * bq_moe_gather_qmm(desc, x, router_logits, logit_bias, y, ...).  x and the
+ * logits live in the workspace.  workspace: device, >=
+ * bq_moe_hidden_workspace_bytes(desc) bytes, 256-byte aligned.
+ * Errors: as bq_moe_gather_qmm and bq_rmsnorm_qmm.
+ */
+size_t bq_moe_hidden_workspace_bytes(const bq_moe_desc* desc);
+bq_status bq_moe_gather_qmm_hidden(const bq_moe_desc* desc, const bq_qweight* router,
+                                   const uint16_t* hidden, const uint16_t* gamma, float eps,
+                                   const float* logit_bias, float* y, void* workspace,
+                                   size_t workspace_bytes, bq_stream_t stream);
+
 /* ------------------------------------------------------------------ observability
  * Stage timing: while set, every bq_moe_gather_qmm call on this host thread
  * records `start` (a cudaEvent_t) on its stream immediately before the
@@ -374,7 +411,8 @@ typedef enum {
     BQ_STAGE_DOWN = 2,           /* routed down GEMM scaled by the gate weight */
     BQ_STAGE_SHARED = 3,         /* shared expert (gate/up + down) */
     BQ_STAGE_COMBINE = 4,        /* gate-weighted combine */
-    BQ_STAGE_COUNT = 5
+    BQ_STAGE_NORM_ROUTER = 5,    /* RMSNorm + router matmul (bq_moe_gather_qmm_hidden) */
+    BQ_STAGE_COUNT = 6
 } bq_stage;
 bq_status bq_set_stage_events(int32_t stage, void* start_event, void* stop_event);
 
