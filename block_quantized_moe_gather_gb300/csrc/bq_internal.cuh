@@ -191,26 +191,56 @@ __device__ __forceinline__ __half2 mx_scale_h2(uint32_t e) {
 
 // ---- RMSNorm: x = gamma * h / sqrt(mean(h^2) + eps)
 //
-// 1 / sqrt(mean(h^2) + eps) of one fp16 row of length k (k % 8 == 0, row
-// 16-byte aligned), computed by one warp: lane-strided 16-byte loads, fp32
-// sum of squares per lane, butterfly sum.  The standalone norm kernel and the
-// norm-fused GEMV both use this, so their results agree bit for bit.
-__device__ __forceinline__ float row_inv_rms(const __half* row, int k, float eps, int lane) {
-    float ss = 0.f;
-    const uint4* r4 = reinterpret_cast<const uint4*>(row);
-    for (int i = lane; i < k / 8; i += 32) {
-        const uint4 v = __ldg(r4 + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+// 1 / sqrt(mean(h^2) + eps) of up to 8 fp16 rows of length k (k % 8 == 0,
+// rows 16-byte aligned, row r at h + r * ld), computed by a whole CTA of
+// 256 threads: thread j sums the squares of the 8-value groups i = j, j + 256,
+// ... in fp32 (fused multiply-adds in value order), the lanes of a warp are
+// summed by a butterfly, and the 8 warp partials in warp order.  Each row's
+// result depends only on that row, so the standalone norm kernel and the
+// norm-fused GEMV, which both call this, agree bit for bit.  The loads of all
+// rows are issued together.  s_part: shared [8][8]; s_inv: shared [8] (rows
+// >= nrows are left unset).  Contains __syncthreads: call from all threads.
+constexpr int kNormThreads = 256;
+__device__ __forceinline__ void rows_inv_rms(const __half* h, int64_t ld, int nrows, int k, float eps,
+                                             float (*s_part)[8], float* s_inv) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float ss[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float2 f = __half22float2(u32_as_h2(w[j]));
-            ss = __fmaf_rn(f.x, f.x, ss);
-            ss = __fmaf_rn(f.y, f.y, ss);
-        }
+    for (int r = 0; r < 8; ++r) ss[r] = 0.f;
+    for (int i = tid; i < k / 8; i += kNormThreads) {
+        uint4 v[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+            if (r < nrows) v[r] = __ldg(reinterpret_cast<const uint4*>(h + r * ld) + i);
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+            if (r < nrows) {
+                const uint32_t w[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 f = __half22float2(u32_as_h2(w[j]));
+                    ss[r] = __fmaf_rn(f.x, f.x, ss[r]);
+                    ss[r] = __fmaf_rn(f.y, f.y, ss[r]);
+                }
+            }
     }
 #pragma unroll
-    for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    return rsqrtf(ss / (float)k + eps);
+    for (int r = 0; r < 8; ++r) {
+#pragma unroll
+        for (int off = 16; off; off >>= 1) ss[r] += __shfl_xor_sync(0xffffffffu, ss[r], off);
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) s_part[warp][r] = ss[r];
+    }
+    __syncthreads();
+    if (tid < nrows) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < kNormThreads / 32; ++w) t += s_part[w][tid];
+        s_inv[tid] = rsqrtf(t / (float)k + eps);
+    }
+    __syncthreads();
 }
 
 // Eight normalised values: fp16((h * gamma) * inv), products in fp32.

@@ -17,20 +17,24 @@
 
 namespace {
 
-constexpr int kWarps = 8;
-
-// One warp per row: 1/rms (bq::row_inv_rms), then the normalised row.
-__global__ void __launch_bounds__(32 * kWarps)
+// A CTA takes 8 rows at a time: 1/rms of each (bq::rows_inv_rms), then the
+// normalised rows.
+__global__ void __launch_bounds__(bq::kNormThreads)
 rmsnorm_kernel(const __half* __restrict__ h, int T, int H, const __half* __restrict__ gamma, float eps,
                __half* __restrict__ x) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int r = blockIdx.x * kWarps + warp; r < T; r += gridDim.x * kWarps) {
-        const __half* row = h + (int64_t)r * H;
-        const float inv = bq::row_inv_rms(row, H, eps, lane);
-        const uint4* r4 = reinterpret_cast<const uint4*>(row);
+    __shared__ float s_part[bq::kNormThreads / 32][8];
+    __shared__ float s_inv[8];
+    for (int r0 = blockIdx.x * 8; r0 < T; r0 += gridDim.x * 8) {
+        const int nr = min(8, T - r0);
+        bq::rows_inv_rms(h + (int64_t)r0 * H, H, nr, H, eps, s_part, s_inv);
         const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
-        uint4* o4 = reinterpret_cast<uint4*>(x + (int64_t)r * H);
-        for (int i = lane; i < H / 8; i += 32) o4[i] = bq::norm8(__ldg(r4 + i), __ldg(g4 + i), inv);
+        for (int r = 0; r < nr; ++r) {
+            const uint4* r4 = reinterpret_cast<const uint4*>(h + (int64_t)(r0 + r) * H);
+            uint4* o4 = reinterpret_cast<uint4*>(x + (int64_t)(r0 + r) * H);
+            const float inv = s_inv[r];
+            for (int i = threadIdx.x; i < H / 8; i += bq::kNormThreads) o4[i] = bq::norm8(__ldg(r4 + i), __ldg(g4 + i), inv);
+        }
+        __syncthreads();   // s_inv is reused by the next row group
     }
 }
 
@@ -60,8 +64,8 @@ size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
 namespace bq {
 
 void launch_rmsnorm(const __half* h, int T, int H, const __half* gamma, float eps, __half* x, cudaStream_t st) {
-    const int grid = std::max(1, std::min((T + kWarps - 1) / kWarps, 152 * 8));
-    rmsnorm_kernel<<<grid, 32 * kWarps, 0, st>>>(h, T, H, gamma, eps, x);
+    const int grid = std::max(1, std::min((T + 7) / 8, 152 * 8));
+    rmsnorm_kernel<<<grid, bq::kNormThreads, 0, st>>>(h, T, H, gamma, eps, x);
     note_launch();
 }
 

@@ -313,7 +313,7 @@ __device__ __forceinline__ void qgemv_epilogue(const bq::QgemvParams& p, const f
 // are summed in warp order, so results stay bit-reproducible either way.
 //
 // NORM (single segment, no SwiGLU): RMSNorm in front of the GEMV.  Every CTA
-// first computes 1/rms of its token rows over the whole K (warp w: token w),
+// first computes 1/rms of its token rows over the whole K (bq::rows_inv_rms),
 // then normalises its activation fragments as it loads them; the CTAs of
 // row tile 0, row quarter 0 also store the normalised rows of their K share
 // to x_out, so each value is written once.
@@ -327,6 +327,8 @@ qgemv_kernel(const bq::QgemvParams p) {
     __shared__ float2 red[KW == 8 ? 7 : 4][2][32][2];
     __shared__ int s_last;
     __shared__ float s_inv[NORM ? 8 : 1];
+    __shared__ float s_part[NORM ? 8 : 1][8];
+    static_assert(!NORM || kThreads == bq::kNormThreads, "the norm prologue is written for 256 threads");
 
     // launched right behind the kernel that produced the routing / activations
     bq::grid_dependency_wait();
@@ -358,25 +360,25 @@ qgemv_kernel(const bq::QgemvParams p) {
             const int src = p.src_row ? __ldg(p.src_row + lr) : lr;
             xrow = p.x + (int64_t)src * p.k;
         }
-        float inv = 0.f;
-        __half* xo = nullptr;
-        if (NORM) {
-            __syncthreads();   // the previous token group is done with s_inv
-            if (warp < ntok) s_inv[warp] = bq::row_inv_rms(p.x + (int64_t)(start + tok0 + warp) * p.k, p.k, p.eps, lane);
-            __syncthreads();
-            if (xvalid) {
-                inv = s_inv[g];
-                if (p.x_out && rt == 0 && quarter == 0) xo = p.x_out + (int64_t)(start + tok0 + g) * p.k;
-            }
-        }
-        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        // register ring of D slabs in flight (D - 1 ahead of the one being multiplied)
+        // register ring of D slabs in flight (D - 1 ahead of the one being multiplied);
+        // the first loads go out before the norm prologue below
         constexpr int D = T::DEPTH;
         Frag<FMT> f[D];
         const int n = kt_end - kt_begin;
 #pragma unroll
         for (int d = 0; d < D - 1; ++d)
             if (d < n) load_frag<FMT>(f[d], wbase + (int64_t)(kt_begin + d) * T::SB, rowbase, g, t);
+        float inv = 0.f;
+        __half* xo = nullptr;
+        if (NORM) {
+            __syncthreads();   // the previous token group is done with s_inv
+            bq::rows_inv_rms(p.x + (int64_t)(start + tok0) * p.k, p.k, ntok, p.k, p.eps, s_part, s_inv);
+            if (xvalid) {
+                inv = s_inv[g];
+                if (p.x_out && rt == 0 && quarter == 0) xo = p.x_out + (int64_t)(start + tok0 + g) * p.k;
+            }
+        }
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         for (int i = 0; i < n; i += D) {
 #pragma unroll
             for (int d = 0; d < D; ++d) {
