@@ -389,6 +389,13 @@ def decode_from_hidden(args, bq, flush, base, layer):
 def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "mxfp4", "fp8_b128", "dense")):
     import torch
     out = {}
+    # the floor of this timing method: one trivial kernel (a one-element add) between
+    # the same events after the same L2 flush; every small-kernel time below includes it
+    one = torch.zeros(1, device="cuda")
+    for _ in range(3):
+        one.add_(1)
+    ms, _ = time_steps(lambda: one.add_(1), 30, flush)
+    out["event_floor_us"] = round(1e3 * statistics.mean(ms), 2)
     # decode sweep on each MoE workload; prefill of the int4, MXFP4 and FP8 ones
     for base in (synth.MOE_Q2K, synth.MOE_INT4, synth.MOE_MXFP4, synth.MOE_FP8):
         if "decode" not in sections and base.fmt not in sections:
