@@ -178,6 +178,18 @@ __device__ __forceinline__ bool mbar_test4(const uint32_t (&bar)[4], const uint3
     return ok != 0;
 }
 
+// Bounded wait by every lane of a warp: one test instruction and a vote when
+// the phase has completed (the common case), no broadcast or warp barrier.
+// Lanes may leave the slow path at different times; that is safe because the
+// barriers waited on here cannot complete another phase of the same parity
+// before this warp itself moves on.
+__device__ __forceinline__ bool warp_wait_all(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                              int32_t* status) {
+    if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
+    const bool ok = mbar_wait(bar, parity, abort_flag, status);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // Warp-uniform bounded wait: lane 0 polls, every lane gets its verdict.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
                                           int32_t* status) {
@@ -557,9 +569,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
         // alternating: a slab of one stage is read by the 4 warps of that stage's parity
         for (int i = 0; i < F::NR; ++i) {
             mbar_init(raw_full(i), 1);
-            mbar_init(raw_empty(i), split_k || F::SPS > 1 ? 8 : 4);
+            mbar_init(raw_empty(i), 32 * (split_k || F::SPS > 1 ? 8 : 4));   // every converter lane arrives
         }
-        for (int i = 0; i < kMaxStagesA; ++i) mbar_init(a_full(i), split_k ? 8 : 4);
+        for (int i = 0; i < kMaxStagesA; ++i) mbar_init(a_full(i), 32 * (split_k ? 8 : 4));
         mbar_init(acc_full, 1);
         *abort_flag = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -670,51 +682,55 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
         const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
         bool ok = true;
         if (split_k) {
-            // every stage: this warp converts K values 32*half .. +31 of it
-            int sa = 0;
+            // every stage: this warp converts K values 32*half .. +31 of it;
+            // r / pr: raw-ring slot and phase of the stage's slab
+            int sa = 0, sub = 0, r = 0;
+            uint32_t pr = 0;
             for (int ks = 0; ks < KS; ++ks) {
-                const int kt = ks / F::SPS, sub = ks % F::SPS, r = kt % F::NR;
-                if (sub == 0 && !(ok = warp_wait(raw_full(r), (uint32_t)(kt / F::NR) & 1u, abort_flag, a.status)))
-                    break;
+                if (sub == 0 && !(ok = warp_wait_all(raw_full(r), pr, abort_flag, a.status))) break;
                 if (ks >= stages_a &&
-                    !(ok = warp_wait(empty(ks - stages_a), empty_parity(ks - stages_a), abort_flag, a.status)))
+                    !(ok = warp_wait_all(empty(ks - stages_a), empty_parity(ks - stages_a), abort_flag, a.status)))
                     break;
                 uint32_t v[16];
                 dequant_half<FMT>(raw_ring + r * F::SB, p, sub, half, v);
                 tmem_st16(tmem + lane_base + a_col0 + 32u * sa + 16u * half, v);
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    if (sub == F::SPS - 1) mbar_arrive(raw_empty(r));
-                    mbar_arrive(a_full(sa));
-                }
+                // every lane arrives (after its own fence): no warp barrier needed
+                if (sub == F::SPS - 1) mbar_arrive(raw_empty(r));
+                mbar_arrive(a_full(sa));
                 if (++sa == stages_a) sa = 0;
+                if (++sub == F::SPS) {
+                    sub = 0;
+                    if (++r == F::NR) { r = 0; pr ^= 1u; }
+                }
             }
         }
         // otherwise this warp converts stages ks = half, half + 2, ...; sa = A-ring slot of ks
         int sa = half;
+        // r / pr: raw-ring slot and phase of slab ks / SPS, advanced with ks
+        int r = (half / F::SPS) % F::NR;
+        uint32_t pr = 0;
         for (int ks = half; !split_k && ks < KS; ks += 2) {
-            const int kt = ks / F::SPS, sub = ks % F::SPS, r = kt % F::NR;
-            const uint32_t pr = (uint32_t)(kt / F::NR) & 1u;
+            const int sub = ks % F::SPS;
             // first stage of the slab this warp converts: wait for the slab
-            if ((F::SPS == 1 || sub == half) && !(ok = warp_wait(raw_full(r), pr, abort_flag, a.status))) break;
+            if ((F::SPS == 1 || sub == half) && !(ok = warp_wait_all(raw_full(r), pr, abort_flag, a.status))) break;
             if (ks >= stages_a &&
-                !(ok = warp_wait(empty(ks - stages_a), empty_parity(ks - stages_a), abort_flag, a.status)))
+                !(ok = warp_wait_all(empty(ks - stages_a), empty_parity(ks - stages_a), abort_flag, a.status)))
                 break;
             uint32_t v[32];
             dequant_stage<FMT>(raw_ring + r * F::SB, p, sub, v);
             tmem_st32(tmem + lane_base + a_col0 + 32u * sa, v);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                // last stage of the slab this warp converts: release it
-                if (F::SPS == 1 || sub >= F::SPS - 2) mbar_arrive(raw_empty(r));
-                mbar_arrive(a_full(sa));
-            }
+            // every lane arrives (after its own fence); last stage of the slab
+            // this warp converts: release the slab
+            if (F::SPS == 1 || sub >= F::SPS - 2) mbar_arrive(raw_empty(r));
+            mbar_arrive(a_full(sa));
             sa += 2;
             if (sa >= stages_a) sa -= stages_a;
+            r += (ks + 2) / F::SPS - ks / F::SPS;   // slabs advanced: 0, 1 or 2 (< NR)
+            if (r >= F::NR) { r -= F::NR; pr ^= 1u; }
         }
         if (ok && warp_wait(acc_full, 0, abort_flag, a.status)) {
             tc_fence_after();
