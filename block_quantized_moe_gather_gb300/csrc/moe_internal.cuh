@@ -83,7 +83,12 @@ void launch_qgemv(const QgemvParams& p, int max_segments, cudaStream_t st, bool 
 void launch_rmsnorm(const __half* h, int T, int H, const __half* gamma, float eps, __half* x, cudaStream_t st);
 // y = W rmsnorm(h) for m rows: the norm-fused GEMV for m <= 8 (x_out
 // optional), else the norm kernel into x_out (required) and the GEMM.
+// partial / counters (optional, m <= 8): scratch for a K split of the GEMV
+// (norm_qmm_ksplit(w) ways; partials [n/128][kMaxKsplit][128][8] fp32 and n/128
+// counters, which this call clears first).
 bq_status launch_rmsnorm_qmm(const __half* h, int m, const __half* gamma, float eps, const bq_qweight* w,
-                             __half* x_out, float* y, cudaStream_t st);
+                             __half* x_out, float* y, cudaStream_t st, float* partial = nullptr,
+                             int32_t* counters = nullptr);
+int norm_qmm_ksplit(const bq_qweight* w);
 
 }  // namespace bq

@@ -59,9 +59,21 @@ bq_status check_plain_weight(const char* name, const bq_qweight* w, int k) {
 
 size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
 
+// Workspace of the split router GEMV: partials [row tiles][kMaxKsplit][128][8]
+// fp32, then one counter per row tile.
+size_t router_split_bytes(int n) {
+    return up256((size_t)(n / bq::kTileRows) * bq::kMaxKsplit * 1024 * 4) + up256((size_t)(n / bq::kTileRows) * 4);
+}
+
 }  // namespace
 
 namespace bq {
+
+// K split of the norm-fused router GEMV: about four slabs per CTA.
+int norm_qmm_ksplit(const bq_qweight* w) {
+    const int k_slabs = w->k / fmt_info(w->fmt).slab_k;
+    return std::max(1, std::min(kMaxKsplit, k_slabs / 4));
+}
 
 void launch_rmsnorm(const __half* h, int T, int H, const __half* gamma, float eps, __half* x, cudaStream_t st) {
     const int grid = std::max(1, std::min((T + 7) / 8, 152 * 8));
@@ -70,7 +82,7 @@ void launch_rmsnorm(const __half* h, int T, int H, const __half* gamma, float ep
 }
 
 bq_status launch_rmsnorm_qmm(const __half* h, int m, const __half* gamma, float eps, const bq_qweight* w,
-                             __half* x_out, float* y, cudaStream_t st) {
+                             __half* x_out, float* y, cudaStream_t st, float* partial, int32_t* counters) {
     if (m <= 8 || !gemm_supported(w->fmt)) {
         if (m > 8) {   // no tensor-core path for this format: norm, then the plain GEMV
             launch_rmsnorm(h, m, w->k, gamma, eps, x_out, st);
@@ -84,6 +96,14 @@ bq_status launch_rmsnorm_qmm(const __half* h, int m, const __half* gamma, float 
         p.w = static_cast<const uint8_t*>(w->data);
         p.fmt = w->fmt; p.n = w->n; p.k = w->k; p.m = m; p.x = h; p.y = y; p.ldy = w->n; p.ksplit = 1;
         p.gamma = gamma; p.eps = eps; p.x_out = x_out;
+        if (partial && counters) {
+            // a router has few row tiles: split K over more CTAs (partials summed in split order)
+            p.ksplit = norm_qmm_ksplit(w);
+            p.partial = partial;
+            p.counters = counters;
+            if (p.ksplit > 1 && cudaMemsetAsync(counters, 0, (w->n / kTileRows) * sizeof(int32_t), st) != cudaSuccess)
+                return fail(BQ_ERR_CUDA, "bq_moe_gather_qmm_hidden: cudaMemsetAsync of the split counters failed");
+        }
         launch_qgemv(p, 1, st);
         return BQ_OK;
     }
@@ -125,7 +145,8 @@ extern "C" bq_status bq_rmsnorm_qmm(const uint16_t* h, int32_t m, const uint16_t
 extern "C" size_t bq_moe_hidden_workspace_bytes(const bq_moe_desc* desc) {
     const size_t moe = bq_moe_workspace_bytes(desc);
     if (moe == 0) return 0;
-    return up256(moe) + up256((size_t)desc->T * desc->hidden * 2) + up256((size_t)desc->T * desc->n_experts * 4);
+    return up256(moe) + up256((size_t)desc->T * desc->hidden * 2) + up256((size_t)desc->T * desc->n_experts * 4) +
+           router_split_bytes(desc->n_experts);
 }
 
 extern "C" bq_status bq_moe_gather_qmm_hidden(const bq_moe_desc* d, const bq_qweight* router, const uint16_t* hidden,
@@ -150,10 +171,14 @@ extern "C" bq_status bq_moe_gather_qmm_hidden(const bq_moe_desc* d, const bq_qwe
     uint8_t* base = static_cast<uint8_t*>(workspace);
     __half* x = reinterpret_cast<__half*>(base + moe);
     float* logits = reinterpret_cast<float*>(base + moe + up256((size_t)d->T * d->hidden * 2));
+    uint8_t* split = base + moe + up256((size_t)d->T * d->hidden * 2) + up256((size_t)d->T * d->n_experts * 4);
+    float* partial = reinterpret_cast<float*>(split);
+    int32_t* counters = reinterpret_cast<int32_t*>(
+        split + up256((size_t)(d->n_experts / bq::kTileRows) * bq::kMaxKsplit * 1024 * 4));
     cudaStream_t st = (cudaStream_t)stream;
     bq::stage_begin(BQ_STAGE_NORM_ROUTER, st);
     if ((s = bq::launch_rmsnorm_qmm(reinterpret_cast<const __half*>(hidden), d->T, reinterpret_cast<const __half*>(gamma),
-                                    eps, router, x, logits, st)) != BQ_OK)
+                                    eps, router, x, logits, st, partial, counters)) != BQ_OK)
         return s;
     bq::stage_end(BQ_STAGE_NORM_ROUTER, st);
     return bq_moe_gather_qmm(d, reinterpret_cast<const uint16_t*>(x), logits, logit_bias, y, workspace, moe, stream);

@@ -120,27 +120,44 @@ def test_moe_from_hidden_states(lib, case, router_fmt):
     hid = (inp.x.astype(np.float32) * 4.0).astype(np.float16)
     gamma = _gamma(g, case.hidden)
     bias = dev(inp.bias) if inp.bias is not None else None
-    # the whole layer from hidden states
     y = torch.full((case.t, case.hidden), float("nan"), dtype=torch.float32, device="cuda")
     ws = torch.empty(layer.hidden_workspace_bytes(), dtype=torch.uint8, device="cuda")
     lib.moe_gather_qmm_hidden(layer, router, half_dev(hid), half_dev(gamma), EPS, bias, y, ws)
-    # the same two stages called one by one
-    x = torch.empty((case.t, case.hidden), dtype=torch.float16, device="cuda")
-    logits = torch.empty((case.t, case.experts), dtype=torch.float32, device="cuda")
-    lib.rmsnorm_qmm(half_dev(hid), half_dev(gamma), EPS, router, logits, x)
-    y2 = torch.empty_like(y)
-    ws2 = torch.empty(layer.workspace_bytes(), dtype=torch.uint8, device="cuda")
-    lib.moe_gather_qmm(layer, x, logits, bias, y2, ws2)
+    y2 = torch.full_like(y, float("nan"))
+    lib.moe_gather_qmm_hidden(layer, router, half_dev(hid), half_dev(gamma), EPS, bias, y2, ws)
     torch.cuda.synchronize()
-    yd, lg = y.cpu().numpy(), logits.cpu().numpy()
-    np.testing.assert_array_equal(yd, y2.cpu().numpy())
+    yd = y.cpu().numpy()
+    np.testing.assert_array_equal(yd, y2.cpu().numpy())          # bit-reproducible, workspace reused
+    # The router logits come from fp16 x (and, for <= 8 tokens, as partial sums
+    # over a K split), so where two keys are within rounding the device may pick
+    # either expert.  The logits it routed on sit in its workspace (after the
+    # layer's own part, then x): check them against the oracle, then check the
+    # layer against the oracle run on exact x with the routing taken from them.
+    up = lambda v: (v + 255) // 256 * 256
+    off = up(layer.workspace_bytes()) + up(case.t * case.hidden * 2)
+    lg_dev = ws[off:off + case.t * case.experts * 4].cpu().numpy().view(np.float32).reshape(case.t, case.experts)
     x_ref = O.rmsnorm(hid, gamma, EPS)
-    assert_close_matmul(lg, O.qmm(x_ref, dequant(router_fmt, wr).reshape(case.experts, case.hidden)), "router logits")
-    # routing is taken from the device logits (ties at rounding level may pick
-    # either expert); the expert FFN then runs on the exact normalised x
-    ids, wts = O.route(lg, case.topk, inp.bias)
+    lg_ref = O.qmm(x_ref, dequant(router_fmt, wr).reshape(case.experts, case.hidden))
+    assert_close_matmul(lg_dev, lg_ref, "router logits")
+    ids, wts = O.route(lg_dev, case.topk, inp.bias)
     inp.x = x_ref
     assert_close_matmul(yd, oracle_moe(inp, ids=ids, wts=wts), case.name)
+
+
+def test_rmsnorm_qmm_router_sized(lib):
+    """The public norm + matmul on a router-sized weight (E = 256, H = 2048) matches the oracle."""
+    import torch
+    g = synth.rng(12)
+    e, hdim = 256, 2048
+    wr = synth.q8_0_blocks(g, e, hdim)
+    router = make_qweight(lib, "q8_0", wr, 1, e, hdim)
+    hid = synth.fp16_normal(g, (3, hdim))
+    gamma = _gamma(g, hdim)
+    y = torch.empty((3, e), dtype=torch.float32, device="cuda")
+    lib.rmsnorm_qmm(half_dev(hid), half_dev(gamma), EPS, router, y)
+    torch.cuda.synchronize()
+    ref = O.qmm(O.rmsnorm(hid, gamma, EPS), O.dequant_q8_0(wr).reshape(e, hdim))
+    assert_close_matmul(y.cpu().numpy(), ref, "router logits")
 
 
 def test_moe_hidden_rejects_bad_router(lib):
