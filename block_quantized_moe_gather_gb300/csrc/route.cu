@@ -299,22 +299,38 @@ scan_kernel(int32_t* __restrict__ chunk_hist, int n_chunks, int E, int32_t* __re
     __shared__ int32_t cnt[1024];
     __shared__ int32_t warp_sums[32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int e = warp; e < E; e += 32) {
-        int32_t* row = chunk_hist + (int64_t)e * n_chunks;
-        int32_t total = 0;
+    // warp w scans experts w + 32i over the chunks; eight experts at a time, so
+    // that their loads are in flight together
+    for (int e0 = warp; e0 < E; e0 += 32 * 8) {
+        int32_t total[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) total[i] = 0;
         for (int c0 = 0; c0 < n_chunks; c0 += 32) {
             const int c = c0 + lane;
-            const int32_t v = c < n_chunks ? row[c] : 0;
-            int32_t incl = v;
+            int32_t v[8];
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int32_t u = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += u;
+            for (int i = 0; i < 8; ++i) {
+                const int e = e0 + 32 * i;
+                v[i] = (e < E && c < n_chunks) ? chunk_hist[(int64_t)e * n_chunks + c] : 0;
             }
-            if (c < n_chunks) row[c] = total + incl - v;
-            total += __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = e0 + 32 * i;
+                int32_t incl = v[i];
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const int32_t u = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off) incl += u;
+                }
+                if (e < E && c < n_chunks) chunk_hist[(int64_t)e * n_chunks + c] = total[i] + incl - v[i];
+                total[i] += __shfl_sync(0xffffffffu, incl, 31);
+            }
         }
-        if (lane == 0) cnt[e] = total;
+        if (lane == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (e0 + 32 * i < E) cnt[e0 + 32 * i] = total[i];
+        }
     }
     __syncthreads();
     const int e = threadIdx.x;
