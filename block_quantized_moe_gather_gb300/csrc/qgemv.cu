@@ -31,11 +31,9 @@
 namespace {
 
 template <int FMT> struct Traits;
-// DEPTH: slabs of weights kept in flight per warp.  Q2_K keeps two, so that its
-// GEMV fits three CTAs per SM (measured faster for decode; the other formats
-// spill at that register budget and stay at two CTAs).
+// DEPTH: slabs of weights kept in flight per warp.
 template <> struct Traits<BQ_FMT_Q8_0>     { static constexpr int SK = 64,  SB = 8704,  STEPS = 4,  XV = 2, DEPTH = 3; };
-template <> struct Traits<BQ_FMT_Q2_K>     { static constexpr int SK = 256, SB = 10752, STEPS = 16, XV = 8, DEPTH = 2; };
+template <> struct Traits<BQ_FMT_Q2_K>     { static constexpr int SK = 256, SB = 10752, STEPS = 16, XV = 8, DEPTH = 3; };
 template <> struct Traits<BQ_FMT_INT4_G64> { static constexpr int SK = 128, SB = 9216,  STEPS = 8,  XV = 4, DEPTH = 3; };
 template <> struct Traits<BQ_FMT_MXFP4>    { static constexpr int SK = 128, SB = 8704,  STEPS = 8,  XV = 4, DEPTH = 3; };
 template <> struct Traits<BQ_FMT_FP8_B128> { static constexpr int SK = 64,  SB = 8208,  STEPS = 4,  XV = 2, DEPTH = 3; };
@@ -320,7 +318,7 @@ __device__ __forceinline__ void qgemv_epilogue(const bq::QgemvParams& p, const f
 // row tile 0, row quarter 0 also store the normalised rows of their K share
 // to x_out, so each value is written once.
 template <int FMT, bool SWIGLU, int KW, bool NORM>
-__global__ void __launch_bounds__(kThreads, NORM ? 1 : FMT == BQ_FMT_Q2_K ? 3 : 2)   // norm-fused: more registers
+__global__ void __launch_bounds__(kThreads, NORM ? 1 : 2)   // the norm-fused GEMV needs more registers
 qgemv_kernel(const bq::QgemvParams p) {
     using T = Traits<FMT>;
     static_assert(KW == 2 || KW == 8, "K ways per CTA");
