@@ -249,6 +249,13 @@ extern "C" bq_status bq_qmm(const uint16_t* x, int32_t m, const bq_qweight* w, f
 
 extern "C" size_t bq_moe_workspace_bytes(const bq_moe_desc* desc) {
     if (!desc || desc->T < 0 || desc->topk < 1 || desc->n_experts < 1 || desc->n_experts > 1024) return 0;
+    const bq_qweight *gu = &desc->w_gate_up, *dn = &desc->w_down;
+    if (bq_qweight_bytes(gu->fmt, gu->n_mats, gu->n, gu->k) == 0 || bq_qweight_bytes(dn->fmt, dn->n_mats, dn->n, dn->k) == 0)
+        return 0;
+    if (desc->shared_gate_up && desc->shared_down &&
+        (bq_qweight_bytes(desc->shared_gate_up->fmt, 1, desc->shared_gate_up->n, desc->shared_gate_up->k) == 0 ||
+         bq_qweight_bytes(desc->shared_down->fmt, 1, desc->shared_down->n, desc->shared_down->k) == 0))
+        return 0;
     return carve(desc, nullptr).bytes + bq::gemm_moe_workspace_bytes(desc);
 }
 

@@ -506,7 +506,9 @@ int qgemv_ksplit(int fmt, int n, int k, int max_segments, int max_tokens) {
     // least 8 slabs (4 per K-half warp) per CTA.
     const int ctas = (n / kTileRows) * max_segments;
     const int want = (sms + ctas - 1) / ctas;
-    const int k_slabs = k / fmt_info(fmt).slab_k;
+    const int slab_k = fmt_info(fmt).slab_k;
+    if (slab_k <= 0) return 1;   // unknown format: callers reject it before any launch
+    const int k_slabs = k / slab_k;
     return std::max(1, std::min(want, std::min(kMaxKsplit, k_slabs / 8)));
 }
 

@@ -334,7 +334,9 @@ bq_status bq_moe_permute_noalloc(const int32_t* ids, int32_t T, int32_t k, int32
  * routing is set by desc->scoring (bq_scoring; BQ_SCORE_SOFTMAX adds the bias
  * before selection and weighting) and desc->route_scale (the routed scaling
  * factor of BQ_SCORE_SQRTSOFTPLUS); y: device fp32 [T][hidden].
- * workspace: device, >= bq_moe_workspace_bytes(desc) bytes, 256-aligned.
+ * workspace: device, >= bq_moe_workspace_bytes(desc) bytes, 256-aligned
+ * (the query returns 0 for a descriptor it cannot size: bad T, E or k, or a
+ * weight of unknown format or invalid shape).
  * Errors: as above, plus BQ_ERR_FORMAT if the weights' shapes disagree
  * with the descriptor.
  */

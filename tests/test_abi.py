@@ -102,3 +102,41 @@ def test_import_fails_loudly_without_the_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", "import block_quantized_moe_gather_gb300"], cwd=tmp_path,
                        capture_output=True, text=True)
     assert r.returncode != 0 and "ImportError" in r.stderr
+
+
+def test_host_validation_of_the_block_format_and_norm_entry_points(bq):
+    # MXFP4 / FP8 dequant, FP8 repack shapes and the RMSNorm calls, all rejected on the host
+    lib = bq._lib
+    assert lib.bq_dequant_mxfp4(None, -1, None, None) == 2
+    assert lib.bq_dequant_mxfp4(None, 3, None, None) == 1
+    assert lib.bq_dequant_mxfp4(None, 0, None, None) == 0                       # empty is a no-op
+    assert lib.bq_dequant_fp8_b128(None, None, -1, 4, None, None) == 2
+    assert lib.bq_dequant_fp8_b128(None, None, 4, 0, None, None) == 0
+    assert lib.bq_dequant_fp8_b128(None, None, 4, 4, None, None) == 1
+    assert lib.bq_dequant_fp8_b128(ctypes.c_void_p(16), ctypes.c_void_p(2), 4, 4, ctypes.c_void_p(16), None) == 3
+    # FP8 weights need k a multiple of 128, and fused gate/up halves on the 128-row scale grid
+    assert bq.qweight_bytes(bq.FMT_FP8_B128, 1, 128, 64) == 0
+    assert bq.qweight_bytes(bq.FMT_FP8_B128, 2, 256, 256) == 2 * 2 * 4 * 8208
+    w = bq.QWeightC(bq.FMT_FP8_B128, 1, 384, 128, 1, 0, 4096)
+    assert lib.bq_repack_fp8_b128(ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.byref(w), None) == 2
+    w = bq.QWeightC(bq.FMT_MXFP4, 1, 128, 128, 0, 0, 4096)
+    assert lib.bq_repack_mxfp4(None, ctypes.byref(w), None) == 1
+    assert lib.bq_rmsnorm(None, 2, 12, None, 1e-6, None, None) == 2              # H not a multiple of 8
+    assert lib.bq_rmsnorm(None, 2, 16, None, -1.0, None, None) == 2              # eps < 0
+    assert lib.bq_rmsnorm(None, 0, 16, None, 1e-6, None, None) == 0              # T == 0 is a no-op
+    assert lib.bq_rmsnorm(None, 2, 16, None, 1e-6, None, None) == 1
+    q = bq.QWeightC(bq.FMT_Q8_0, 1, 128, 64, 1, 0, 4096)                         # fused gate/up: rejected
+    assert lib.bq_rmsnorm_qmm(None, 1, None, 1e-6, ctypes.byref(q), None, None, None) == 4
+
+
+def test_hidden_layer_workspace_query(bq):
+    gu = bq.QWeightC(bq.FMT_INT4_G64, 128, 256, 256, 1, 0, 4096)
+    dn = bq.QWeightC(bq.FMT_INT4_G64, 128, 256, 128, 0, 0, 4096)
+    d = bq.MoEDescC(4, 256, 128, 128, 4, 0, gu, dn, None, None, 1.0, 0)
+    base = bq._lib.bq_moe_workspace_bytes(ctypes.byref(d))
+    hidden = bq._lib.bq_moe_hidden_workspace_bytes(ctypes.byref(d))
+    assert base > 0 and hidden >= base + 4 * 256 * 2 + 4 * 128 * 4
+    # a descriptor whose weights have no valid format has no workspace size
+    bad = bq.MoEDescC(4, 256, 128, 128, 4, 0, bq.QWeightC(), bq.QWeightC(), None, None, 1.0, 0)
+    assert bq._lib.bq_moe_workspace_bytes(ctypes.byref(bad)) == 0
+    assert bq._lib.bq_moe_hidden_workspace_bytes(ctypes.byref(bad)) == 0
