@@ -48,8 +48,9 @@ def test_moe_decode_small(lib, base, t):
     assert_close_matmul(run_moe(lib, layer, inp), oracle_moe(inp), f"{case.name} t={t}")
 
 
-def test_moe_bit_reproducible(lib):
-    case = SMALL[2]
+@pytest.mark.parametrize("idx", [2, 6, 8], ids=lambda i: SMALL[i].name)   # Q2_K, MXFP4, FP8 experts
+def test_moe_bit_reproducible(lib, idx):
+    case = SMALL[idx]
     inp = synth.moe_inputs(case)
     layer = build_layer(lib, inp)
     a = run_moe(lib, layer, inp)
@@ -58,9 +59,10 @@ def test_moe_bit_reproducible(lib):
 
 
 @pytest.mark.parametrize("t", [1, 5])
-def test_moe_decode_bit_reproducible(lib, t):
+@pytest.mark.parametrize("idx", [2, 6, 8], ids=lambda i: SMALL[i].name)
+def test_moe_decode_bit_reproducible(lib, t, idx):
     # the decode GEMVs split K across CTAs; partials are summed in a fixed order
-    case = synth.dataclasses.replace(SMALL[2], t=t)
+    case = synth.dataclasses.replace(SMALL[idx], t=t)
     inp = synth.moe_inputs(case)
     layer = build_layer(lib, inp)
     a = run_moe(lib, layer, inp)
@@ -191,3 +193,25 @@ def test_moe_scored_routing(lib, scoring, t):
     check_scored_choice(ids, key, case.topk)
     ref = oracle_moe(inp, ids=ids, wts=scored_weights(inp.logits, ids, scoring, scale))
     assert_close_matmul(got, ref, case.name)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "fp8_b128"])
+@pytest.mark.parametrize("t", [2, 33])   # decode path and tensor-core path
+def test_moe_block_formats_single_expert_k1(lib, fmt, t):
+    # E = 1, k = 1: every token goes to the one expert with weight 1 (a dense SwiGLU FFN)
+    case = _case(f"{fmt}_e1", fmt, t, 256, 128, 1, 1)
+    inp = synth.moe_inputs(case)
+    layer = build_layer(lib, inp)
+    assert_close_matmul(run_moe(lib, layer, inp), oracle_moe(inp), case.name)
+
+
+@pytest.mark.parametrize("scoring", ["softmax_then_bias", "sqrtsoftplus"])
+def test_moe_block_formats_with_scored_routing(lib, scoring):
+    import helpers
+    case = _case("fp8_scored", "fp8_b128", 19, 256, 128, 16, 4, zipf=True)
+    inp = synth.moe_inputs(case)
+    layer = build_layer(lib, inp, scoring=scoring, route_scale=1.5)
+    got = run_moe(lib, layer, inp)
+    ids = helpers.route_scored_dev(lib, inp.logits, case.topk, inp.bias, scoring, 1.5)[0]
+    wts = helpers.scored_weights(inp.logits, ids, scoring, 1.5)
+    assert_close_matmul(got, oracle_moe(inp, ids=ids, wts=wts), f"fp8 {scoring}")
