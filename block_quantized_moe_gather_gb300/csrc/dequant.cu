@@ -138,25 +138,37 @@ dequant_mxfp4_kernel(const uint8_t* __restrict__ blocks, int64_t n_blocks, float
     }
 }
 
-// FP8: 16 consecutive bytes of one row per thread (k % 16 == 0 and 16-byte
-// aligned rows), else one byte per thread.  16 bytes never straddle a
-// 128-column scale block.
+// FP8: four consecutive bytes of one row per group (k % 4 == 0), so a warp
+// reads 128 contiguous bytes and writes 512 contiguous bytes per round (four
+// values never straddle a 128-column scale block); else one byte per thread.
+// A thread takes four groups a grid stride apart per round and issues their
+// loads before it converts, so four loads are in flight.
 __global__ void __launch_bounds__(kThreads)
 dequant_fp8_vec_kernel(const uint8_t* __restrict__ w, const float* __restrict__ scales, int64_t n, int64_t k,
                        float* __restrict__ out) {
-    const int64_t groups = n * (k / 16), kb = (k + 127) / 128;
-    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
-         g += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t i = g / (k / 16), j0 = (g % (k / 16)) * 16;
-        const float s = __ldg(scales + (i / 128) * kb + j0 / 128);
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(w + i * k + j0));
-        const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-        float4* o = reinterpret_cast<float4*>(out + i * k + j0);
+    const int64_t k4 = k / 4, groups = n * k4, kb = (k + 127) / 128;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t g0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g0 < groups; g0 += 4 * stride) {
+        uint32_t q[4];
+        float s[4];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const __half2 a = bq::e4m3x2_to_half2(words[m]), b = bq::e4m3x2_to_half2(words[m] >> 16);
-            o[m] = make_float4(__fmul_rn(__low2float(a), s), __fmul_rn(__high2float(a), s),
-                               __fmul_rn(__low2float(b), s), __fmul_rn(__high2float(b), s));
+        for (int u = 0; u < 4; ++u) {
+            const int64_t g = g0 + u * stride;
+            if (g < groups) {
+                const int64_t i = g / k4, j0 = (g - i * k4) * 4;
+                s[u] = __ldg(scales + (i / 128) * kb + j0 / 128);
+                q[u] = __ldg(reinterpret_cast<const uint32_t*>(w + i * k + j0));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t g = g0 + u * stride;
+            if (g < groups) {
+                const __half2 a = bq::e4m3x2_to_half2(q[u]), b = bq::e4m3x2_to_half2(q[u] >> 16);
+                reinterpret_cast<float4*>(out)[g] =
+                    make_float4(__fmul_rn(__low2float(a), s[u]), __fmul_rn(__high2float(a), s[u]),
+                                __fmul_rn(__low2float(b), s[u]), __fmul_rn(__high2float(b), s[u]));
+            }
         }
     }
 }
@@ -236,8 +248,8 @@ extern "C" bq_status bq_dequant_fp8_b128(const void* weight, const float* scales
     bq_status s = bq::check_arch();
     if (s != BQ_OK) return s;
     const uint8_t* w = static_cast<const uint8_t*>(weight);
-    if (k % 16 == 0 && bq::aligned(w, 16) && bq::aligned(out, 16)) {
-        dequant_fp8_vec_kernel<<<grid_for((n * (k / 16) + kThreads - 1) / kThreads), kThreads, 0,
+    if (k % 4 == 0 && bq::aligned(w, 4) && bq::aligned(out, 16)) {
+        dequant_fp8_vec_kernel<<<grid_for((n * (k / 4) + kThreads - 1) / kThreads), kThreads, 0,
                                  (cudaStream_t)stream>>>(w, scales, n, k, out);
     } else {
         dequant_fp8_kernel<<<grid_for((n * k + kThreads - 1) / kThreads), kThreads, 0, (cudaStream_t)stream>>>(

@@ -153,7 +153,8 @@ def _exact_fp8(got, ref):
     np.testing.assert_array_equal(got[~nan].view(np.uint32), ref[~nan].astype(np.float32).view(np.uint32))
 
 
-@pytest.mark.parametrize("n,k", [(1, 1), (5, 300), (128, 128), (300, 200), (257, 1024), (3, 16), (130, 48)])
+@pytest.mark.parametrize("n,k", [(1, 1), (5, 300), (128, 128), (300, 200), (257, 1024), (3, 16), (130, 48),
+                                 (7, 130), (2, 6)])   # the last two: k % 4 != 0, one byte per thread
 def test_fp8_bit_exact_ragged(lib, n, k):
     w = synth.fp8_block_weight(synth.rng(400 + n + k), (), n, k, s_range=(1e-6, 3.0))
     _exact_fp8(_run_fp8(lib, w.bytes, w.scales), O.dequant_fp8_block(w.bytes, w.scales))
