@@ -146,33 +146,6 @@ route_kernel(const float* __restrict__ logits, const float* __restrict__ bias, i
     }
 }
 
-// Exclusive scan of one int per thread over a 1024-thread block.
-__device__ __forceinline__ int block_exclusive_scan(int v, int32_t* warp_sums, int& total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = v;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += u;
-    }
-    if (lane == 31) warp_sums[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        int w = warp_sums[lane];
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, w, off);
-            if (lane >= off) w += u;
-        }
-        warp_sums[lane] = w;
-    }
-    __syncthreads();
-    total = warp_sums[31];
-    const int r = incl - v + (warp ? warp_sums[warp - 1] : 0);
-    __syncthreads();   // warp_sums may be reused
-    return r;
-}
-
 // Whole routing front end for a small batch (T <= 32, T*k <= 256) in one
 // CTA of 256 threads and two block barriers: top-k per token (warp w takes
 // tokens w, w + 8, ...), then every expert's count and offset and every
