@@ -81,9 +81,15 @@ def max_over_ranks(world, v: float) -> float:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if _has_cuda() else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(world: int, units_per_rank: int, steps: int, max_total_ms: float) -> float:
+    """Whole-job throughput of N replicas: the units all ranks processed over
+    the slowest rank's time."""
+    return world * units_per_rank * steps / (max_total_ms / 1e3)
 
 
 def peaks():
@@ -295,7 +301,7 @@ def run_main(args, world, rank, local):
     barrier(world)
     total_ms = max_over_ranks(world, sum(step_ms))
     ms_per_step = total_ms / args.steps
-    value = world * case.t * args.steps / (total_ms / 1e3)
+    value = job_throughput(world, case.t, args.steps, total_ms)
 
     # dominant kernel: the routed gate/up grouped GEMM (+ SwiGLU epilogue)
     pairs = case.t * case.topk
@@ -325,7 +331,7 @@ def run_main(args, world, rank, local):
         e2e_step()
     e2e_ms, _ = time_steps(e2e_step, args.steps, flush)
     e2e_total = max_over_ranks(world, sum(e2e_ms))
-    e2e = {"value": round(world * case.t * args.steps / (e2e_total / 1e3), 1), "unit": "tok/s",
+    e2e = {"value": round(job_throughput(world, case.t, args.steps, e2e_total), 1), "unit": "tok/s",
            "h2d_bytes_per_step": int(xp.numel() * 2 + lp.numel() * 4),
            "d2h_bytes_per_step": int(yp.numel() * 4)}
 
