@@ -140,3 +140,25 @@ def test_hidden_layer_workspace_query(bq):
     bad = bq.MoEDescC(4, 256, 128, 128, 4, 0, bq.QWeightC(), bq.QWeightC(), None, None, 1.0, 0)
     assert bq._lib.bq_moe_workspace_bytes(ctypes.byref(bad)) == 0
     assert bq._lib.bq_moe_hidden_workspace_bytes(ctypes.byref(bad)) == 0
+
+
+def test_host_validation_of_the_layer_and_matmul_entry_points(bq):
+    lib = bq._lib
+    assert lib.bq_qmm(None, 1, None, None, None) == 1                                   # w NULL
+    q = bq.QWeightC(bq.FMT_Q8_0, 1, 128, 64, 0, 0, 4096)
+    assert lib.bq_qmm(None, -1, ctypes.byref(q), None, None) == 2                       # m < 0
+    bad = bq.QWeightC(7, 1, 128, 64, 0, 0, 4096)
+    assert lib.bq_qmm(None, 1, ctypes.byref(bad), None, None) == 4                      # unknown format
+    assert lib.bq_moe_gather_qmm(None, None, None, None, None, None, 0, None) == 1       # desc NULL
+    gu = bq.QWeightC(bq.FMT_INT4_G64, 8, 256, 256, 1, 0, 4096)
+    dn = bq.QWeightC(bq.FMT_INT4_G64, 8, 256, 128, 0, 0, 4096)
+    d = bq.MoEDescC(4, 256, 128, 8, 4, 9, gu, dn, None, None, 1.0, 0)                   # scoring 9
+    assert lib.bq_moe_gather_qmm(ctypes.byref(d), None, None, None, None, None, 0, None) == 2
+    d = bq.MoEDescC(4, 256, 128, 8, 9, 0, gu, dn, None, None, 1.0, 0)                   # top-k 9 > 8
+    assert lib.bq_moe_gather_qmm(ctypes.byref(d), None, None, None, None, None, 0, None) == 2
+    d = bq.MoEDescC(4, 256, 128, 8, 4, 0, gu, dn, None, None, 1.0, 0)
+    assert lib.bq_moe_gather_qmm(ctypes.byref(d), None, None, None, None, None, 0, None) == 1   # NULL x
+    x = ctypes.c_void_p(4096)
+    assert lib.bq_moe_gather_qmm(ctypes.byref(d), x, x, None, x, None, 0, None) == 5    # no workspace
+    assert lib.bq_set_stage_events(6, None, None) == 2                                  # unknown stage
+    assert lib.bq_set_stage_events(5, None, None) == 0                                  # norm + router stage
