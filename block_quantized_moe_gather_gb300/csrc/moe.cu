@@ -217,6 +217,13 @@ SideStream* side_stream() {
     return &ss;
 }
 
+// Up to this many rows a dense qmm runs the GEMV (token groups as separate
+// CTAs) rather than the tensor-core GEMM, whose grid is only
+// (N / 128) x ceil(m / 160) CTAs walking all of K (measured on N = 256 and 4096:
+// the GEMV wins up to 32 rows for every format and up to 64 for the formats
+// below one byte per weight; every token group reads the weights again, from L2).
+int qmm_gemv_rows(int fmt) { return fmt == BQ_FMT_Q8_0 || fmt == BQ_FMT_FP8_B128 ? 32 : 64; }
+
 // One dense weight over `m` rows of x (single segment).
 bq::QgemvParams dense_params(const bq_qweight* w, int m, const __half* x, float* y, __half* h, int ldy,
                              int ksplit = 1, float* partial = nullptr, int32_t* counters = nullptr) {
@@ -239,8 +246,11 @@ extern "C" bq_status bq_qmm(const uint16_t* x, int32_t m, const bq_qweight* w, f
     if (!bq::aligned(x, 16) || !bq::aligned(y, 16)) return bq::fail(BQ_ERR_ALIGN, "bq_qmm: x and y must be 16-byte aligned");
     if ((s = bq::check_arch()) != BQ_OK) return s;
     cudaStream_t st = (cudaStream_t)stream;
-    if (m <= 8 || !bq::gemm_supported(w->fmt)) {
-        bq::launch_qgemv(dense_params(w, m, reinterpret_cast<const __half*>(x), y, nullptr, w->n), 1, st);
+    if (m <= qmm_gemv_rows(w->fmt) || !bq::gemm_supported(w->fmt)) {
+        // small m: the GEMV, one CTA row of the grid per 8-row token group
+        bq::QgemvParams p = dense_params(w, m, reinterpret_cast<const __half*>(x), y, nullptr, w->n);
+        p.grid_groups = 1;
+        bq::launch_qgemv(p, 1, st);
     } else if ((s = bq::launch_gemm_dense(w, m, reinterpret_cast<const __half*>(x), y, st)) != BQ_OK) {
         return s;
     }

@@ -72,6 +72,10 @@ struct QgemvParams {
     const __half* gamma;
     float eps;
     __half* x_out;
+    // Single segment without segment arrays: 1 = each 8-row token group of
+    // the m rows is its own CTA row of the grid (grid.y = ceil(m / 8)) instead
+    // of a loop inside every CTA.
+    int grid_groups;
 };
 constexpr int kMaxKsplit = 16;
 // Split factor that gives the GPU enough CTAs for this shape.

@@ -333,11 +333,13 @@ qgemv_kernel(const bq::QgemvParams p) {
     // launched right behind the kernel that produced the routing / activations
     bq::grid_dependency_wait();
     bq::allow_dependents();
-    const int seg = blockIdx.y;
+    const bool gg = p.grid_groups && !p.seg_expert;   // grid.y = token groups of one segment
+    const int seg = gg ? 0 : (int)blockIdx.y;
     if (p.n_segments && seg >= __ldg(p.n_segments)) return;
     const int e = p.seg_expert ? __ldg(p.seg_expert + seg) : 0;
     const int start = p.seg_start ? __ldg(p.seg_start + seg) : 0;
     const int count = p.seg_count ? __ldg(p.seg_count + seg) : p.m;
+    const int tok_lo = gg ? 8 * (int)blockIdx.y : 0, tok_hi = gg ? min(count, tok_lo + 8) : count;
 
     const int rt = KW == 8 ? (int)(blockIdx.x >> 2) : (int)blockIdx.x, kp = blockIdx.z;
     const int n_tiles = p.n / bq::kTileRows, k_slabs = p.k / T::SK;
@@ -351,7 +353,7 @@ qgemv_kernel(const bq::QgemvParams p) {
     const int kt_begin = ks_lo + ((ks_hi - ks_lo) * kw + KW - 1) / KW;
     const int kt_end = ks_lo + ((ks_hi - ks_lo) * (kw + 1) + KW - 1) / KW;
 
-    for (int tok0 = 0; tok0 < count; tok0 += 8) {
+    for (int tok0 = tok_lo; tok0 < tok_hi; tok0 += 8) {
         const int ntok = min(8, count - tok0);
         const bool xvalid = g < ntok;
         const __half* xrow = p.x;
@@ -482,8 +484,9 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
     // one CTA per 32-row quarter when a dense weight's whole-tile CTAs would
     // leave SMs idle and K is not split across CTAs (no workspace for partials);
     // the expert GEMVs of a MoE step are left whole-tile (measured no better)
-    const bool quarters = p.ksplit == 1 && !p.seg_expert && tiles * max_segments < sm_count();
-    dim3 grid(tiles * (quarters ? 4 : 1), max_segments, p.ksplit);
+    const int ny = p.grid_groups && !p.seg_expert ? (p.m + 7) / 8 : max_segments;
+    const bool quarters = p.ksplit == 1 && !p.seg_expert && tiles * ny < sm_count();
+    dim3 grid(tiles * (quarters ? 4 : 1), ny, p.ksplit);
     auto kernel = p.gamma ? (quarters ? qgemv_kernel<FMT, false, 8, true> : qgemv_kernel<FMT, false, 2, true>)
                 : quarters ? (p.swiglu ? qgemv_kernel<FMT, true, 8, false> : qgemv_kernel<FMT, false, 8, false>)
                            : (p.swiglu ? qgemv_kernel<FMT, true, 2, false> : qgemv_kernel<FMT, false, 2, false>);

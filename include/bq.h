@@ -215,7 +215,8 @@ bq_status bq_repack_fp8_b128(const void* weight, const float* scales, const bq_q
  * ([vllm]: mt_qmm_mma, dense activations x 4-bit weights; [butter]:
  * dequantGemmDynamicM; [slimserve]: qc_mmvq batch 2-8 qgemv and the q8_0
  * qgemm).  Weights are dequantised in registers to fp16; products are
- * accumulated in fp32.  m <= 8 runs the split-K qgemv; larger m the
+ * accumulated in fp32.  Up to 32 rows (Q8_0, FP8) or 64 rows (the other
+ * formats) run the GEMV (mma.sync fragments, 8 rows per CTA); more rows the
  * tensor-core (tcgen05) GEMM.
  * x: device fp16 [m][k] row-major (uint16 bits), k = w->k.
  * y: device fp32 [m][w->n] row-major.

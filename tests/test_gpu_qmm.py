@@ -1,5 +1,5 @@
-"""GPU parity: dense qmm (split-K qgemv for m <= 8, tensor-core GEMM above)
-against the fp64 oracle on the same dequantised weights."""
+"""GPU parity: dense qmm (the GEMV up to 32 / 64 rows, 8 rows per CTA; the
+tensor-core GEMM above) against the fp64 oracle on the same dequantised weights."""
 import numpy as np
 import pytest
 
@@ -22,7 +22,7 @@ def _qmm(lib, qw, x):
                                      ("q2_k", 128, 256), ("int4", 256, 384), ("int4", 128, 128),
                                      ("mxfp4", 256, 384), ("mxfp4", 128, 128),
                                      ("fp8_b128", 256, 384), ("fp8_b128", 128, 128)])
-@pytest.mark.parametrize("m", [1, 3, 8, 13, 40, 130])
+@pytest.mark.parametrize("m", [1, 3, 8, 13, 40, 70, 130])
 def test_qmm_small_shapes(lib, fmt, n, k, m):
     g = synth.rng(n + k + m)
     if fmt == "q8_0":
@@ -107,7 +107,7 @@ def test_mxfp4_nan_block_poisons_its_rows_only(lib):
     for m in (1, 2):            # qgemv
         y = _qmm(lib, qw, x[:m])
         assert np.all(np.isnan(y[:, 3])) and np.all(np.isfinite(np.delete(y, 3, axis=1)))
-    xb = synth.fp16_normal(synth.rng(7), (40, k))   # tensor-core GEMM
+    xb = synth.fp16_normal(synth.rng(7), (80, k))   # tensor-core GEMM (more than 64 rows)
     y = _qmm(lib, qw, xb)
     assert np.all(np.isnan(y[:, 3])) and np.all(np.isfinite(np.delete(y, 3, axis=1)))
 
