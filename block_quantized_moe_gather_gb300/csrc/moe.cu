@@ -224,6 +224,12 @@ SideStream* side_stream() {
 // below one byte per weight; every token group reads the weights again, from L2).
 int qmm_gemv_rows(int fmt) { return fmt == BQ_FMT_Q8_0 || fmt == BQ_FMT_FP8_B128 ? 32 : 64; }
 
+// Up to this many tokens a MoE layer runs its experts as GEMVs over their
+// segments (each expert's few tokens, 8 rows per pass) and routes with the
+// one-CTA front end; the grouped tensor-core GEMM would give every expert a
+// tile of a handful of tokens that still dequantises all of its weights.
+constexpr int kMoeGemvTokens = 32;
+
 // One dense weight over `m` rows of x (single segment).
 bq::QgemvParams dense_params(const bq_qweight* w, int m, const __half* x, float* y, __half* h, int ldy,
                              int ksplit = 1, float* partial = nullptr, int32_t* counters = nullptr) {
@@ -307,7 +313,9 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
     }
     bq::stage_end(BQ_STAGE_ROUTE_PERMUTE, st);
     const int max_segments = min(E, P);
-    const bool decode = T <= 8 || !bq::gemm_supported(d->w_gate_up.fmt);
+    // up to kMoeGemvTokens tokens the experts run as GEMVs over their (short) segments;
+    // above, the tensor-core grouped GEMM
+    const bool decode = T <= kMoeGemvTokens || !bq::gemm_supported(d->w_gate_up.fmt);
 
     // Decode: the shared expert's two GEMVs run on a side stream, concurrently
     // with the routed experts (neither fills the GPU at these sizes); the
@@ -315,7 +323,7 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
     int accumulate = 0;
     std::unique_lock<std::mutex> side_lock;
     SideStream* side = nullptr;
-    if (d->shared_gate_up && T <= 8) {
+    if (d->shared_gate_up && T <= kMoeGemvTokens) {
         side_lock = std::unique_lock<std::mutex>(g_side_mutex);
         side = side_stream();
         cudaStream_t ss = st;
@@ -325,10 +333,12 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
         else
             side = nullptr;
         bq::stage_begin(BQ_STAGE_SHARED, ss);
-        bq::launch_qgemv(dense_params(d->shared_gate_up, T, xh, nullptr, w.h_shared, 0, w.ks_sgu, w.part_sgu,
-                                      w.cnt_sgu), 1, ss);
-        bq::launch_qgemv(dense_params(d->shared_down, T, w.h_shared, y, nullptr, H, w.ks_sd, w.part_sd, w.cnt_sd),
-                         1, ss);
+        bq::QgemvParams sgu = dense_params(d->shared_gate_up, T, xh, nullptr, w.h_shared, 0, w.ks_sgu, w.part_sgu,
+                                           w.cnt_sgu);
+        bq::QgemvParams sdn = dense_params(d->shared_down, T, w.h_shared, y, nullptr, H, w.ks_sd, w.part_sd, w.cnt_sd);
+        sgu.grid_groups = sdn.grid_groups = 1;   // more than 8 tokens: one CTA row per token group
+        bq::launch_qgemv(sgu, 1, ss);
+        bq::launch_qgemv(sdn, 1, ss);
         bq::stage_end(BQ_STAGE_SHARED, ss);
         if (side && cudaEventRecord(side->join, ss) != cudaSuccess)
             return bq::fail(BQ_ERR_CUDA, "bq_moe_gather_qmm: cudaEventRecord on the side stream failed");
