@@ -21,6 +21,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import shutil
 import statistics
 import subprocess
 import sys
@@ -47,7 +48,7 @@ def parse_args():
                     help="q2k: Q2_K experts + Q8_0 shared (default); int4: int4 experts, E=128, top-8")
     ap.add_argument("--decode-steps", type=int, default=200)
     ap.add_argument("--no-secondary", action="store_true", help="only the main step (faster)")
-    ap.add_argument("--only", choices=["decode", "int4", "mxfp4", "fp8_b128", "dense"], default=None,
+    ap.add_argument("--only", choices=["decode", "int4", "mxfp4", "fp8_b128", "dense", "dequant"], default=None,
                     help="run one secondary section alone and print it (no main step; for profiling)")
     ap.add_argument("--dense-case", default=None, help="with --only dense: run just this dense case")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -220,7 +221,7 @@ class L2Flush:
 #       python bench.py --steps 2 --warmup 1 --no-secondary --no-cpu-baseline
 # (689,870,848 read + 42,897,920 written at commit 668ac7f; the algorithmic bytes are
 # 740 MB).  Set to None whenever the GEMM kernel changes until it is captured again.
-GATE_UP_DRAM_BYTES = {"q2k": 689870848 + 42897920, "int4": None}
+GATE_UP_DRAM_BYTES = {"q2k": None, "int4": None}
 
 
 def time_steps(fn, k, flush, stage_events=None):
@@ -253,6 +254,63 @@ def time_steps(fn, k, flush, stage_events=None):
         bq.set_stage_events(sid, None, None)
         stage_ms[sid] = [a.elapsed_time(b) for a, b in stage_pairs[sid]]
     return [s.elapsed_time(e) for s, e in zip(starts, ends)], stage_ms
+
+
+def graph_time(calls, flush, reps=3):
+    """Back-to-back device time per call: captures `calls` (zero-argument
+    callables, each one library call) into one CUDA graph, replays it once,
+    then times `reps` replays with CUDA events on the current stream (L2
+    flushed before each replay, not between the calls inside it).  Returns
+    the median of the replay times divided by len(calls), in ms.  The calls
+    run one after another with no host launch gaps, so the figure separates
+    kernel time from launch and event latency; weights must rotate through
+    more than the L2 size inside the sequence for it to stay an HBM figure."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):   # lazy per-device set-up happens outside the capture
+        for c in calls[:2]:
+            c()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for c in calls:
+            c()
+    g.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    times = []
+    for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        g.replay()
+        b.record(st)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) / len(calls))
+    del g
+    return statistics.median(times)
+
+
+def weight_copies(bq, q, n):
+    """n device copies of a repacked weight (for rotating weights through more
+    than the L2 size in back-to-back timing)."""
+    out = []
+    for _ in range(n):
+        c = bq.QWeight(q.fmt, q.n_mats, q.n, q.k, bool(q.swiglu))
+        c.buf.copy_(q.buf)
+        out.append(c)
+    return out
+
+
+def l2_rotations(weight_bytes):
+    """ceil(3 * L2 / W): copies to rotate so that no weight is reread from L2."""
+    import math
+
+    import torch
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    return max(1, math.ceil(3 * l2 / weight_bytes))
 
 
 # ----------------------------------------------------------------------------- main arm
@@ -303,16 +361,19 @@ def run_main(args, world, rank, local):
     ms_per_step = total_ms / args.steps
     value = job_throughput(world, case.t, args.steps, total_ms)
 
-    # dominant kernel: the routed gate/up grouped GEMM (+ SwiGLU epilogue)
+    # dominant kernel: the routed gate/up grouped GEMM (+ SwiGLU epilogue); the stage
+    # events bracket that launch alone (the X_perm gather belongs to the permute stage)
     pairs = case.t * case.topk
     gu_flops = 2.0 * pairs * 2 * case.inter * case.hidden
     gu_ms = statistics.mean(stage_ms[1])
-    peak_tf = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    peak_tf = pk["bf16_tflops"]
     achieved_tf = gu_flops / (gu_ms / 1e3) / 1e12
-    roofline = {"kernel": "gate_up grouped GEMM + SwiGLU (stage timing)", "bound": "tensor",
+    roofline = {"kernel": "gate_up grouped GEMM + SwiGLU (events around its launch)", "bound": "tensor",
                 "achieved": round(achieved_tf, 2), "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": round(achieved_tf / peak_tf, 4), "traffic": GATE_UP_DRAM_BYTES.get(args.workload),
-                "peak_source": f"{pk_src} bf16 sustained (fp16 operands, same tensor rate)",
+                "flops_per_launch": gu_flops,
+                "peak_source": f"{pk_src} bf16 burst (a kernel timed alone; fp16 operands, same tensor rate)",
+                "frac_of_sustained": round(achieved_tf / pk.get("bf16_tflops_sustained", peak_tf), 4),
                 "stage_ms": {"gate_up": round(gu_ms, 4), "down": round(statistics.mean(stage_ms[2]), 4),
                              "shared": round(statistics.mean(stage_ms[3]), 4) if 3 in stage_ms else None}}
 
@@ -392,7 +453,50 @@ def decode_from_hidden(args, bq, flush, base, layer):
     return res
 
 
-def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "mxfp4", "fp8_b128", "dense")):
+def run_dequant(bq, flush, pk):
+    """Standalone dequantisation of a 4096 x 4096 weight in each format (GGUF
+    Q8_0 and Q2_K blocks, MXFP4 blocks, FP8 with 128 x 128 block scales) to
+    fp32; GB/s counts the bytes read plus the fp32 bytes written."""
+    import torch
+    dense = {}
+    for case in [c for c in synth.dense_sweep() if c.m == 1]:
+        _, w = synth.dense_inputs(case)
+        nb = w.size // (34 if case.fmt == "q8_0" else 84)
+        flat = upload(np.asarray(w).reshape(-1))
+        o = torch.empty(nb * (32 if case.fmt == "q8_0" else 256), dtype=torch.float32, device="cuda")
+        fn = bq.gguf_dequant_q8_0 if case.fmt == "q8_0" else bq.gguf_dequant_q2_k
+        for _ in range(3):
+            fn(flat, o)
+        ms, _ = time_steps(lambda: fn(flat, o), 20, flush)
+        t = statistics.median(ms) / 1e3
+        byt = flat.numel() + o.numel() * 4
+        dense[f"dequant_{case.fmt}_4096x4096"] = {"us": round(t * 1e6, 2), "GB_s": round(byt / t / 1e9, 1),
+                                                   "frac_hbm": round(byt / t / 1e9 / pk["hbm_gbs"], 4)}
+    # standalone MXFP4 dequantisation of a 4096 x 4096 weight
+    wm = upload(synth.mxfp4_blocks(synth.rng(4343), 4096, 4096).reshape(-1))
+    om = torch.empty(4096 * 4096, dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        bq.dequant_mxfp4(wm, om)
+    ms, _ = time_steps(lambda: bq.dequant_mxfp4(wm, om), 20, flush)
+    t = statistics.median(ms) / 1e3
+    byt = wm.numel() + om.numel() * 4
+    dense["dequant_mxfp4_4096x4096"] = {"us": round(t * 1e6, 2), "GB_s": round(byt / t / 1e9, 1),
+                                        "frac_hbm": round(byt / t / 1e9 / pk["hbm_gbs"], 4)}
+    # standalone FP8 block dequantisation of a 4096 x 4096 weight
+    w8 = synth.fp8_block_weight(synth.rng(4444), (), 4096, 4096)
+    wb8, sb8 = upload(w8.bytes), upload(w8.scales)
+    o8 = torch.empty((4096, 4096), dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        bq.dequant_fp8_b128(wb8, sb8, o8)
+    ms, _ = time_steps(lambda: bq.dequant_fp8_b128(wb8, sb8, o8), 20, flush)
+    t = statistics.median(ms) / 1e3
+    byt = wb8.numel() + sb8.numel() * 4 + o8.numel() * 4
+    dense["dequant_fp8_b128_4096x4096"] = {"us": round(t * 1e6, 2), "GB_s": round(byt / t / 1e9, 1),
+                                           "frac_hbm": round(byt / t / 1e9 / pk["hbm_gbs"], 4)}
+    return dense
+
+
+def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "mxfp4", "fp8_b128", "dense", "dequant")):
     import torch
     out = {}
     # the floor of this timing method: one trivial kernel (a one-element add) between
@@ -432,15 +536,52 @@ def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "mxfp4", "fp8
             for _ in range(3):
                 dstep()
             it = iter(range(10 ** 9))
-            ms, _ = time_steps(dstep, args.decode_steps, flush)
+            ms, stg = time_steps(dstep, args.decode_steps, flush,
+                                 stage_events=[bq.STAGE_GATE_UP, bq.STAGE_DOWN])
             eb = synth.expert_weight_bytes(case)
             shared_b = 3 * case.hidden * case.inter * synth.bytes_per_weight("q8_0") if case.shared_fmt else 0
             tot_bytes = sum(u * eb + shared_b for u in uniq)
             gbs = tot_bytes / (sum(ms) / 1e3) / 1e9
-            res[f"B{b}"] = {"GB_s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
-                            "us_per_step": round(1e3 * statistics.mean(ms), 2),
-                            "unique_experts_mean": round(statistics.mean(uniq), 2),
-                            "tok_s": round(b * len(ms) / (sum(ms) / 1e3), 1)}
+            # the routed gather-qgemv kernels alone: gate/up holds 2/3 of an expert's
+            # bytes, down 1/3 (same format, same density)
+            gu_b = sum(u * eb * 2 / 3 for u in uniq)
+            dn_b = sum(u * eb / 3 for u in uniq)
+            gu_ms, dn_ms = sum(stg[bq.STAGE_GATE_UP]), sum(stg[bq.STAGE_DOWN])
+            rec = {"GB_s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
+                   "us_per_step": round(1e3 * statistics.mean(ms), 2),
+                   "unique_experts_mean": round(statistics.mean(uniq), 2),
+                   "tok_s": round(b * len(ms) / (sum(ms) / 1e3), 1),
+                   "gate_up_gemv": {"us": round(1e3 * gu_ms / len(ms), 2),
+                                    "GB_s": round(gu_b / (gu_ms / 1e3) / 1e9, 1),
+                                    "frac_hbm": round(gu_b / (gu_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)},
+                   "down_gemv": {"us": round(1e3 * dn_ms / len(ms), 2),
+                                 "GB_s": round(dn_b / (dn_ms / 1e3) / 1e9, 1),
+                                 "frac_hbm": round(dn_b / (dn_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}}
+            # the same steps back to back in one CUDA graph; the shared expert rotates
+            # through ceil(3 L2 / W) copies (the routed experts change every step)
+            try:
+                layers = [layer]
+                if shared_b:
+                    n_rot = l2_rotations(shared_b)
+                    sgu, sdn = layer.weights[2], layer.weights[3]
+                    for cg, cd in zip(weight_copies(bq, sgu, n_rot - 1), weight_copies(bq, sdn, n_rot - 1)):
+                        ly = bq.MoELayer(b, base.hidden, base.inter, base.experts, base.topk, layer.weights[0],
+                                         layer.weights[1], cg, cd)
+                        layers.append(ly)
+                wss = [torch.empty(ly.workspace_bytes(), dtype=torch.uint8, device="cuda") for ly in layers]
+                calls = [(lambda i=i: bq.moe_gather_qmm(layers[i % len(layers)], x_all[i], l_all[i], None, y,
+                                                        wss[i % len(layers)]))
+                         for i in range(args.decode_steps)]
+                g_ms = graph_time(calls, flush)
+                g_gbs = (tot_bytes / len(uniq)) / (g_ms / 1e3) / 1e9
+                rec["back_to_back"] = {"us_per_step": round(1e3 * g_ms, 2), "GB_s": round(g_gbs, 1),
+                                       "frac_hbm": round(g_gbs / pk["hbm_gbs"], 4),
+                                       "shared_copies": len(layers),
+                                       "how": "200 steps in one CUDA graph replay, no flush between steps"}
+                del layers, wss
+            except Exception as ex:   # report, do not fail the bench line
+                rec["back_to_back"] = {"error": repr(ex)[:200]}
+            res[f"B{b}"] = rec
         if res:
             out[f"decode_{base.fmt}"] = res
         if base.fmt == "q2_k" and "decode" in sections:
@@ -464,10 +605,14 @@ def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "mxfp4", "fp8
                                    "gate_up_tflops": round(gu / (statistics.mean(stg[1]) / 1e3) / 1e12, 2)}
         del layer
         torch.cuda.empty_cache()
-    if "dense" not in sections:
-        return out
-    # dense qmm and dequant
     dense = {}
+    if "dequant" in sections:
+        dense.update(run_dequant(bq, flush, pk))
+    if "dense" not in sections:
+        if dense:
+            out["dense"] = dense
+        return out
+    # dense qmm
     for case in [synth.DENSE_Q8_0_M32] + synth.dense_sweep():
         if args.dense_case and case.name != args.dense_case:
             continue
@@ -484,40 +629,18 @@ def run_secondary(args, bq, flush, pk, sections=("decode", "int4", "mxfp4", "fp8
                "tflops": round(2.0 * case.m * case.n * case.k / t / 1e12, 3)}
         if case.m <= 32:
             rec["frac_hbm"] = round(wb / t / 1e9 / pk["hbm_gbs"], 4)
+        if case.m <= 8:
+            # back to back over ceil(3 L2 / W) rotated weight copies, no flush between calls
+            try:
+                qs = [q] + weight_copies(bq, q, l2_rotations(wb) - 1)
+                calls = [(lambda i=i: bq.qmm(x, qs[i % len(qs)], y)) for i in range(max(200, 4 * len(qs)))]
+                tb = graph_time(calls, flush) / 1e3
+                rec["back_to_back"] = {"us": round(tb * 1e6, 2), "weight_GB_s": round(wb / tb / 1e9, 1),
+                                       "frac_hbm": round(wb / tb / 1e9 / pk["hbm_gbs"], 4), "copies": len(qs)}
+                del qs
+            except Exception as ex:
+                rec["back_to_back"] = {"error": repr(ex)[:200]}
         dense[case.name] = rec
-        if case.m == 1:
-            nb = w.size // (34 if case.fmt == "q8_0" else 84)
-            flat = upload(np.asarray(w).reshape(-1))
-            o = torch.empty(nb * (32 if case.fmt == "q8_0" else 256), dtype=torch.float32, device="cuda")
-            fn = bq.gguf_dequant_q8_0 if case.fmt == "q8_0" else bq.gguf_dequant_q2_k
-            for _ in range(3):
-                fn(flat, o)
-            ms, _ = time_steps(lambda: fn(flat, o), 20, flush)
-            t = statistics.median(ms) / 1e3
-            byt = flat.numel() + o.numel() * 4
-            dense[f"dequant_{case.fmt}_4096x4096"] = {"us": round(t * 1e6, 2), "GB_s": round(byt / t / 1e9, 1),
-                                                       "frac_hbm": round(byt / t / 1e9 / pk["hbm_gbs"], 4)}
-    # standalone MXFP4 dequantisation of a 4096 x 4096 weight
-    wm = upload(synth.mxfp4_blocks(synth.rng(4343), 4096, 4096).reshape(-1))
-    om = torch.empty(4096 * 4096, dtype=torch.float32, device="cuda")
-    for _ in range(3):
-        bq.dequant_mxfp4(wm, om)
-    ms, _ = time_steps(lambda: bq.dequant_mxfp4(wm, om), 20, flush)
-    t = statistics.median(ms) / 1e3
-    byt = wm.numel() + om.numel() * 4
-    dense["dequant_mxfp4_4096x4096"] = {"us": round(t * 1e6, 2), "GB_s": round(byt / t / 1e9, 1),
-                                        "frac_hbm": round(byt / t / 1e9 / pk["hbm_gbs"], 4)}
-    # standalone FP8 block dequantisation of a 4096 x 4096 weight
-    w8 = synth.fp8_block_weight(synth.rng(4444), (), 4096, 4096)
-    wb8, sb8 = upload(w8.bytes), upload(w8.scales)
-    o8 = torch.empty((4096, 4096), dtype=torch.float32, device="cuda")
-    for _ in range(3):
-        bq.dequant_fp8_b128(wb8, sb8, o8)
-    ms, _ = time_steps(lambda: bq.dequant_fp8_b128(wb8, sb8, o8), 20, flush)
-    t = statistics.median(ms) / 1e3
-    byt = wb8.numel() + sb8.numel() * 4 + o8.numel() * 4
-    dense["dequant_fp8_b128_4096x4096"] = {"us": round(t * 1e6, 2), "GB_s": round(byt / t / 1e9, 1),
-                                           "frac_hbm": round(byt / t / 1e9 / pk["hbm_gbs"], 4)}
     out["dense"] = dense
     # router rules on the prefill router shape (T = 2048, E = 256, top-6, with a bias)
     route = {}
@@ -562,12 +685,68 @@ def oracle_sample(case, weights, xh, logits_h, bias_h, tokens):
 
 
 def _cores():
+    """Threads the oracle's BLAS uses (all available CPUs when it cannot be asked)."""
     try:
         from threadpoolctl import threadpool_info
         n = max((i.get("num_threads", 1) for i in threadpool_info()), default=1)
         return int(n)
     except Exception:
         return len(os.sched_getaffinity(0))
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+# The oracle on the dense Q8_0 32 x 256 x 2048 matmul and the M = 1 rows of the
+# 4096 x 4096 sweep: each call dequantises the weight (fp64) and multiplies.
+_DENSE_ORACLE = '''
+import json, sys, time
+sys.path.insert(0, {root!r})
+import oracle as O
+import synth
+res = {{}}
+for case in [synth.DENSE_Q8_0_M32] + [c for c in synth.dense_sweep() if c.m == 1]:
+    x, w = synth.dense_inputs(case)
+    deq = O.dequant_q8_0 if case.fmt == "q8_0" else O.dequant_q2_k
+    t0, n = time.perf_counter(), 0
+    while n < 2 or time.perf_counter() - t0 < 1.5:
+        O.qmm(x, deq(w).reshape(case.n, case.k))
+        n += 1
+    res[case.name] = round(1e3 * (time.perf_counter() - t0) / n, 2)
+print(json.dumps(res))
+'''
+
+
+def dense_oracle_times(one_core: bool):
+    """ms per oracle call on the dense C1 / C2-M1 workloads, in a child process
+    (one core: BLAS threads 1 and the process pinned to one CPU)."""
+    env = dict(os.environ)
+    cmd = [sys.executable, "-c", _DENSE_ORACLE.format(root=ROOT)]
+    if one_core:
+        for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+            env[v] = "1"
+        cpu = sorted(os.sched_getaffinity(0))[0]
+        if shutil.which("taskset"):
+            cmd = ["taskset", "-c", str(cpu)] + cmd
+    try:
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=120, env=env)
+        return json.loads(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else {"error": r.stderr[-200:]}
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError) as ex:
+        return {"error": repr(ex)[:200]}
 
 
 def cpu_baseline(case, weights, xh, logits_h, bias_h, budget_s=20.0):
@@ -580,8 +759,10 @@ def cpu_baseline(case, weights, xh, logits_h, bias_h, budget_s=20.0):
         tokens_all.extend(int(t) for t in tok)
     el = time.perf_counter() - t0
     return {"value": round(done / el, 3), "unit": "tok/s", "cores": _cores(), "kind": "oracle",
+            "cpu_model": cpu_model(), "cpus_available": len(os.sched_getaffinity(0)),
             "sample": f"{done} token rows of {case.name} (2 per call, each call dequantises the experts "
-                      f"its tokens route to plus the shared expert, fp64), {el:.1f} s"}
+                      f"its tokens route to plus the shared expert, fp64), {el:.1f} s",
+            "dense_ms_per_call": {"all_cores": dense_oracle_times(False), "one_core": dense_oracle_times(True)}}
 
 
 def run_reference(args, world, rank):

@@ -74,6 +74,7 @@ _SIGS = {
     "bq_moe_gather_qmm_hidden": (c_int32, [POINTER(MoEDescC), POINTER(QWeightC), c_void_p, c_void_p, c_float,
                                            c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "bq_launch_count": (c_uint64, []),
+    "bq_test_set_wait_probe": (c_int32, [c_int32, c_uint64]),
     "bq_moe_gather_qmm": (c_int32, [POINTER(MoEDescC), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                     c_size_t, c_void_p]),
 }
@@ -254,6 +255,14 @@ def set_stage_events(stage: int, start=None, stop=None):
 
 def launch_count() -> int:
     return int(_lib.bq_launch_count())
+
+
+def test_set_wait_probe(skip_weight_copies: bool, wait_limit_ns: int = 0):
+    """Test hook: GEMM launches that follow take `wait_limit_ns` as the bound of
+    their barrier waits and, with `skip_weight_copies`, issue no weight copies
+    (so those waits run out); (False, 0) restores the defaults."""
+    _check(_lib.bq_test_set_wait_probe(int(bool(skip_weight_copies)), int(wait_limit_ns)),
+           "bq_test_set_wait_probe")
 
 
 def moe_permute_noalloc(ids, n_experts: int, counts, offsets, perm_token, perm_slot, inv, stream=None):

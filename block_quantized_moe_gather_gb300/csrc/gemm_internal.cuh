@@ -11,7 +11,12 @@ bool gemm_supported(int fmt);
 size_t gemm_moe_workspace_bytes(const bq_moe_desc* d);
 // Y[m][n] = X[m][k] W^T for a dense weight (matrix 0).
 bq_status launch_gemm_dense(const bq_qweight* w, int m, const __half* x, float* y, cudaStream_t st);
-// Routed experts: gate/up + SwiGLU into h (permuted pair rows), down x gate into y_slot.
+// Routed experts, first part (the permute/gather step): the token-chunk
+// tile list and X_perm (the activation rows in permuted pair order).
+void launch_gemm_moe_prepare(const bq_moe_desc* d, const __half* x, const int32_t* perm_token,
+                             const int32_t* seg_count, const int32_t* n_segments, uint8_t* ws, cudaStream_t st);
+// Routed experts, second part: gate/up + SwiGLU into h (permuted pair rows),
+// down x gate into y_slot (after launch_gemm_moe_prepare on the same stream).
 bq_status launch_gemm_moe(const bq_moe_desc* d, const __half* x, const int32_t* perm_token, const float* perm_gate,
                      const int32_t* seg_expert, const int32_t* seg_start, const int32_t* seg_count,
                      const int32_t* n_segments, const int32_t* counts, __half* h, float* y_slot,

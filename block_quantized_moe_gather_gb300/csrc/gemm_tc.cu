@@ -37,6 +37,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "gemm_internal.cuh"
 #include "moe_internal.cuh"
@@ -65,7 +66,7 @@ constexpr int kEmptyRing = 16;
 static_assert(kMaxStagesA <= kEmptyRing && kMaxStagesB < kEmptyRing && kEmptyRing % 2 == 0, "empty ring");
 constexpr int kNumBars = kMaxStagesB + 2 * kMaxRawSlabs + kMaxStagesA + kEmptyRing + 1;
 constexpr int kSmemBytes = 1024 + kBBoxes * kBoxBytes + kRawBytes + 8 * kNumBars + 64;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s, unless a test sets another limit
 
 template <int FMT> struct G;
 // SK: K per slab, SB: slab bytes, SPS: stages per slab, NR: slabs in the raw ring.
@@ -97,6 +98,8 @@ struct GemmArgs {
     int ldy;
     const float* row_scale;       // EPI_SCALE
     int32_t* status;
+    unsigned long long wait_limit_ns;   // bound of every barrier wait (kWaitLimitNs unless a test sets it)
+    int skip_weight_copies;             // test only: the weight producer issues no copies (waits run out)
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -144,7 +147,7 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // Bounded wait: false if the CTA is aborting or the wait ran out (which
 // raises the abort flag and records BQ_DEV_WAIT_TIMEOUT).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                          int32_t* status) {
+                                          int32_t* status, unsigned long long limit_ns) {
     if (mbar_try(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
@@ -152,7 +155,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         for (int i = 0; i < 32; ++i)
             if (mbar_try_sleep(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             *abort_flag = 1u;
             bq::set_device_error(status, BQ_DEV_WAIT_TIMEOUT);
             return false;
@@ -184,17 +187,17 @@ __device__ __forceinline__ bool mbar_test4(const uint32_t (&bar)[4], const uint3
 // barriers waited on here cannot complete another phase of the same parity
 // before this warp itself moves on.
 __device__ __forceinline__ bool warp_wait_all(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                              int32_t* status) {
+                                              int32_t* status, unsigned long long limit_ns) {
     if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
-    const bool ok = mbar_wait(bar, parity, abort_flag, status);
+    const bool ok = mbar_wait(bar, parity, abort_flag, status, limit_ns);
     return __all_sync(0xffffffffu, ok);
 }
 
 // Warp-uniform bounded wait: lane 0 polls, every lane gets its verdict.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                          int32_t* status) {
+                                          int32_t* status, unsigned long long limit_ns) {
     int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, status);
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, status, limit_ns);
     ok = __shfl_sync(0xffffffffu, ok, 0);
     __syncwarp();
     return ok != 0;
@@ -596,7 +599,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
             const uint32_t stage_bytes = n_boxes * kBoxBytes;
             for (int ks = 0; ks < KS; ++ks) {
                 if (ks >= stages_b &&
-                    !(ok = mbar_wait(empty(ks - stages_b), empty_parity(ks - stages_b), abort_flag, a.status)))
+                    !(ok = mbar_wait(empty(ks - stages_b), empty_parity(ks - stages_b), abort_flag, a.status, a.wait_limit_ns)))
                     break;
                 mbar_expect_tx(b_full(s), stage_bytes);
                 const uint32_t dst = smem_u32(b_ring) + s * stage_bytes;
@@ -608,7 +611,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
             if (!ok) {   // let our own copies land before the CTA leaves (bounded)
                 volatile uint32_t no_abort = 0;
                 for (int u = max(0, issued - stages_b); u < issued; ++u)
-                    mbar_wait(b_full(u % stages_b), (u / stages_b) & 1, &no_abort, a.status);
+                    mbar_wait(b_full(u % stages_b), (u / stages_b) & 1, &no_abort, a.status, a.wait_limit_ns);
             }
         }
     } else if (warp == 2) {
@@ -617,8 +620,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
             int issued = 0, r = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int kt = 0; kt < k_slabs; ++kt) {
-                if (kt >= F::NR && !(ok = mbar_wait(raw_empty(r), ph ^ 1u, abort_flag, a.status))) break;
+            for (int kt = 0; kt < (a.skip_weight_copies ? 0 : k_slabs); ++kt) {
+                if (kt >= F::NR && !(ok = mbar_wait(raw_empty(r), ph ^ 1u, abort_flag, a.status, a.wait_limit_ns))) break;
                 mbar_expect_tx(raw_full(r), F::SB);
                 bulk_load(smem_u32(raw_ring + r * F::SB), wslab + (int64_t)kt * F::SB, F::SB, raw_full(r));
                 ++issued;
@@ -627,7 +630,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
             if (!ok) {
                 volatile uint32_t no_abort = 0;
                 for (int u = max(0, issued - F::NR); u < issued; ++u)
-                    mbar_wait(raw_full(u % F::NR), (u / F::NR) & 1, &no_abort, a.status);
+                    mbar_wait(raw_full(u % F::NR), (u / F::NR) & 1, &no_abort, a.status, a.wait_limit_ns);
             }
         }
     } else if (warp == 1) {
@@ -659,7 +662,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
                     bars[3] = b_full(sb1); pars[3] = sb1 == 0 ? pb ^ 1u : pb;
                 }
                 if (!mbar_test4(bars, pars)) {
-                    for (int q = 0; ok && q < 2 * nq; ++q) ok = mbar_wait(bars[q], pars[q], abort_flag, a.status);
+                    for (int q = 0; ok && q < 2 * nq; ++q) ok = mbar_wait(bars[q], pars[q], abort_flag, a.status, a.wait_limit_ns);
                     if (!ok) break;
                 }
                 tc_fence_after();
@@ -687,9 +690,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
             int sa = 0, sub = 0, r = 0;
             uint32_t pr = 0;
             for (int ks = 0; ks < KS; ++ks) {
-                if (sub == 0 && !(ok = warp_wait_all(raw_full(r), pr, abort_flag, a.status))) break;
+                if (sub == 0 && !(ok = warp_wait_all(raw_full(r), pr, abort_flag, a.status, a.wait_limit_ns))) break;
                 if (ks >= stages_a &&
-                    !(ok = warp_wait_all(empty(ks - stages_a), empty_parity(ks - stages_a), abort_flag, a.status)))
+                    !(ok = warp_wait_all(empty(ks - stages_a), empty_parity(ks - stages_a), abort_flag, a.status, a.wait_limit_ns)))
                     break;
                 uint32_t v[16];
                 dequant_half<FMT>(raw_ring + r * F::SB, p, sub, half, v);
@@ -714,9 +717,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
         for (int ks = half; !split_k && ks < KS; ks += 2) {
             const int sub = ks % F::SPS;
             // first stage of the slab this warp converts: wait for the slab
-            if ((F::SPS == 1 || sub == half) && !(ok = warp_wait_all(raw_full(r), pr, abort_flag, a.status))) break;
+            if ((F::SPS == 1 || sub == half) && !(ok = warp_wait_all(raw_full(r), pr, abort_flag, a.status, a.wait_limit_ns))) break;
             if (ks >= stages_a &&
-                !(ok = warp_wait_all(empty(ks - stages_a), empty_parity(ks - stages_a), abort_flag, a.status)))
+                !(ok = warp_wait_all(empty(ks - stages_a), empty_parity(ks - stages_a), abort_flag, a.status, a.wait_limit_ns)))
                 break;
             uint32_t v[32];
             dequant_stage<FMT>(raw_ring + r * F::SB, p, sub, v);
@@ -732,7 +735,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
             r += (ks + 2) / F::SPS - ks / F::SPS;   // slabs advanced: 0, 1 or 2 (< NR)
             if (r >= F::NR) { r -= F::NR; pr ^= 1u; }
         }
-        if (ok && warp_wait(acc_full, 0, abort_flag, a.status)) {
+        if (ok && warp_wait(acc_full, 0, abort_flag, a.status, a.wait_limit_ns)) {
             tc_fence_after();
             const int rt64 = 64 * rt + 16 * quarter + (lane & 15);   // SwiGLU feature
             const int frow = bq::kTileRows * rt + p;                  // plain output feature
@@ -883,12 +886,19 @@ void launch(int fmt, int epi, const CUtensorMap& map, const GemmArgs& a, dim3 gr
     else launch_epi<EPI_PLAIN>(fmt, map, a, grid, st);
 }
 
+// Test hook (bq_test_set_wait_probe): the wait bound and the "no weight
+// copies" switch of the GEMM launches that follow.
+std::atomic<unsigned long long> g_wait_limit_ns{kWaitLimitNs};
+std::atomic<int> g_skip_weight_copies{0};
+
 GemmArgs base_args(const bq_qweight* w) {
     GemmArgs a{};
     a.w = static_cast<const uint8_t*>(w->data);
     a.n = w->n;
     a.k = w->k;
     a.status = bq::device_status_ptr();
+    a.wait_limit_ns = g_wait_limit_ns.load();
+    a.skip_weight_copies = g_skip_weight_copies.load();
     return a;
 }
 
@@ -945,19 +955,24 @@ bq_status launch_gemm_dense(const bq_qweight* w, int m, const __half* x, float* 
     return dense_gemm(w, m, x, EPI_PLAIN, y, w->n, nullptr, 0, st);
 }
 
-bq_status launch_gemm_moe(const bq_moe_desc* d, const __half* x, const int32_t* perm_token, const float* perm_gate,
+void launch_gemm_moe_prepare(const bq_moe_desc* d, const __half* x, const int32_t* perm_token,
+                             const int32_t* seg_count, const int32_t* n_segments, uint8_t* ws, cudaStream_t st) {
+    const int P = d->T * d->topk, H = d->hidden;
+    GemmWs g = carve(d, ws);
+    tile_list_kernel<<<1, 1024, 0, st>>>(seg_count, n_segments, g.tiles, g.n_tiles);
+    gather_rows_kernel<<<(P + 7) / 8, 256, 0, st>>>(x, perm_token, P, H, g.x_perm);
+    note_launch(2);
+}
+
+bq_status launch_gemm_moe(const bq_moe_desc* d, const __half*, const int32_t*, const float* perm_gate,
                      const int32_t* seg_expert, const int32_t* seg_start, const int32_t* seg_count,
-                     const int32_t* n_segments, const int32_t*, __half* h, float* y_slot, uint8_t* ws,
+                     const int32_t*, const int32_t*, __half* h, float* y_slot, uint8_t* ws,
                      cudaStream_t st) {
     const int P = d->T * d->topk, H = d->hidden, I = d->inter;
     GemmWs g = carve(d, ws);
     const int max_tiles = std::min(d->n_experts, P) + (P + BN - 1) / BN;
-    tile_list_kernel<<<1, 1024, 0, st>>>(seg_count, n_segments, g.tiles, g.n_tiles);
-    note_launch();
 
     stage_begin(BQ_STAGE_GATE_UP, st);
-    gather_rows_kernel<<<(P + 7) / 8, 256, 0, st>>>(x, perm_token, P, H, g.x_perm);
-    note_launch();
     CUtensorMap map_x;
     if (!make_act_map(&map_x, g.x_perm, P, H)) return map_fail();
     GemmArgs a = base_args(&d->w_gate_up);
@@ -987,3 +1002,15 @@ bq_status launch_gemm_shared(const bq_qweight* gu, const bq_qweight* dn, int T, 
 }
 
 }  // namespace bq
+
+extern "C" bq_status bq_test_set_wait_probe(int32_t skip_weight_copies, uint64_t wait_limit_ns) {
+    if (skip_weight_copies < 0 || skip_weight_copies > 1)
+        return bq::fail(BQ_ERR_SHAPE, "bq_test_set_wait_probe: skip_weight_copies must be 0 or 1");
+    if (wait_limit_ns == 0) wait_limit_ns = kWaitLimitNs;
+    if (wait_limit_ns < 1000000ull || wait_limit_ns > kWaitLimitNs)
+        return bq::fail(BQ_ERR_SHAPE, "bq_test_set_wait_probe: wait limit %llu ns outside [1 ms, 2 s]",
+                        (unsigned long long)wait_limit_ns);
+    g_wait_limit_ns.store(wait_limit_ns);
+    g_skip_weight_copies.store(skip_weight_copies);
+    return BQ_OK;
+}

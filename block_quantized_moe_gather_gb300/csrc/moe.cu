@@ -217,13 +217,6 @@ SideStream* side_stream() {
     return &ss;
 }
 
-// Up to this many rows a dense qmm runs the GEMV (token groups as separate
-// CTAs) rather than the tensor-core GEMM, whose grid is only
-// (N / 128) x ceil(m / 160) CTAs walking all of K (measured on N = 256 and 4096:
-// the GEMV wins up to 32 rows for every format and up to 64 for the formats
-// below one byte per weight; every token group reads the weights again, from L2).
-int qmm_gemv_rows(int fmt) { return fmt == BQ_FMT_Q8_0 || fmt == BQ_FMT_FP8_B128 ? 32 : 64; }
-
 // Up to this many tokens a MoE layer runs its experts as GEMVs over their
 // segments (each expert's few tokens, 8 rows per pass) and routes with the
 // one-CTA front end; the grouped tensor-core GEMM would give every expert a
@@ -252,7 +245,7 @@ extern "C" bq_status bq_qmm(const uint16_t* x, int32_t m, const bq_qweight* w, f
     if (!bq::aligned(x, 16) || !bq::aligned(y, 16)) return bq::fail(BQ_ERR_ALIGN, "bq_qmm: x and y must be 16-byte aligned");
     if ((s = bq::check_arch()) != BQ_OK) return s;
     cudaStream_t st = (cudaStream_t)stream;
-    if (m <= qmm_gemv_rows(w->fmt) || !bq::gemm_supported(w->fmt)) {
+    if (m <= bq::qmm_gemv_rows(w->fmt) || !bq::gemm_supported(w->fmt)) {
         // small m: the GEMV, one CTA row of the grid per 8-row token group
         bq::QgemvParams p = dense_params(w, m, reinterpret_cast<const __half*>(x), y, nullptr, w->n);
         p.grid_groups = 1;
@@ -311,11 +304,13 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
                                             w.n_segments);
         bq::note_launch();
     }
-    bq::stage_end(BQ_STAGE_ROUTE_PERMUTE, st);
     const int max_segments = min(E, P);
     // up to kMoeGemvTokens tokens the experts run as GEMVs over their (short) segments;
     // above, the tensor-core grouped GEMM
     const bool decode = T <= kMoeGemvTokens || !bq::gemm_supported(d->w_gate_up.fmt);
+    // the GEMM path's gather of X_perm is the last part of the permute step
+    if (!decode) bq::launch_gemm_moe_prepare(d, xh, w.perm_token, w.seg_count, w.n_segments, base + w.bytes, st);
+    bq::stage_end(BQ_STAGE_ROUTE_PERMUTE, st);
 
     // Decode: the shared expert's two GEMVs run on a side stream, concurrently
     // with the routed experts (neither fills the GPU at these sizes); the

@@ -82,6 +82,13 @@ constexpr int kMaxKsplit = 16;
 int qgemv_ksplit(int fmt, int n, int k, int max_segments, int max_tokens);
 void launch_qgemv(const QgemvParams& p, int max_segments, cudaStream_t st, bool after_previous = false);
 
+// Up to this many rows a dense qmm runs the GEMV (token groups as separate
+// CTAs) rather than the tensor-core GEMM, whose grid is only
+// (N / 128) x ceil(m / 160) CTAs walking all of K (measured on N = 256 and 4096:
+// the GEMV wins up to 32 rows for every format and up to 64 for the formats
+// below one byte per weight; every token group reads the weights again, from L2).
+inline int qmm_gemv_rows(int fmt) { return fmt == BQ_FMT_Q8_0 || fmt == BQ_FMT_FP8_B128 ? 32 : 64; }
+
 // ---- RMSNorm (norm.cu)
 // x[r] = gamma * h[r] / sqrt(mean(h[r]^2) + eps) for rows r < T of length H.
 void launch_rmsnorm(const __half* h, int T, int H, const __half* gamma, float eps, __half* x, cudaStream_t st);

@@ -63,6 +63,7 @@ extern "C" bq_status bq_moe_permute_noalloc(const int32_t* ids, int32_t T, int32
     if (s != BQ_OK) return s;
     if (!counts || !offsets || (T > 0 && (!ids || !perm_token || !perm_slot || !inv)))
         return bq::fail(BQ_ERR_NULL, "bq_moe_permute_noalloc: NULL pointer");
+    // validate_route bounds T * k by INT32_MAX, so the int product below cannot wrap
     const size_t need = bq::permute_scratch_bytes(T * k, E) / sizeof(int32_t);
     if (need > (size_t)kNoAllocScratchInts)
         return bq::fail(BQ_ERR_SHAPE,

@@ -83,12 +83,16 @@ void launch_rmsnorm(const __half* h, int T, int H, const __half* gamma, float ep
 
 bq_status launch_rmsnorm_qmm(const __half* h, int m, const __half* gamma, float eps, const bq_qweight* w,
                              __half* x_out, float* y, cudaStream_t st, float* partial, int32_t* counters) {
-    if (m <= 8 || !gemm_supported(w->fmt)) {
-        if (m > 8) {   // no tensor-core path for this format: norm, then the plain GEMV
+    if (m <= qmm_gemv_rows(w->fmt) || !gemm_supported(w->fmt)) {
+        if (m > 8) {
+            // more rows than one norm-fused pass: the norm kernel, then the plain
+            // GEMV with one CTA row per 8-token group (faster than the tensor-core
+            // GEMM up to qmm_gemv_rows rows, as for bq_qmm)
             launch_rmsnorm(h, m, w->k, gamma, eps, x_out, st);
             QgemvParams p{};
             p.w = static_cast<const uint8_t*>(w->data);
             p.fmt = w->fmt; p.n = w->n; p.k = w->k; p.m = m; p.x = x_out; p.y = y; p.ldy = w->n; p.ksplit = 1;
+            p.grid_groups = 1;
             launch_qgemv(p, 1, st);
             return BQ_OK;
         }

@@ -519,6 +519,9 @@ void launch_qgemv(const QgemvParams& params, int max_segments, cudaStream_t st, 
     if (max_segments <= 0) return;
     QgemvParams p = params;
     if (p.ksplit < 1 || !p.partial || !p.counters) p.ksplit = 1;
+    // the split-K partials and counters are indexed by segment: one token group
+    // of at most 8 rows per segment, so a grid of token groups never splits K
+    if (p.grid_groups && !p.seg_expert && p.m > 8) p.ksplit = 1;
     note_launch();
     switch (p.fmt) {
         case BQ_FMT_Q8_0: launch_fmt<BQ_FMT_Q8_0>(p, max_segments, after_previous, st); break;

@@ -376,6 +376,9 @@ bq_status validate_route(const char* name, int T, int E, int k) {
     if (T < 0) return fail(BQ_ERR_SHAPE, "%s: T = %d < 0", name, T);
     if (E < 1 || E > 1024) return fail(BQ_ERR_SHAPE, "%s: E = %d outside [1, 1024]", name, E);
     if (k < 1 || k > 8 || k > E) return fail(BQ_ERR_SHAPE, "%s: k = %d outside [1, min(8, E)]", name, k);
+    // every pair count T * k below is an int
+    if ((int64_t)T * k > (int64_t)INT32_MAX)
+        return fail(BQ_ERR_SHAPE, "%s: T * k = %lld pairs exceeds %d", name, (long long)T * k, INT32_MAX);
     return BQ_OK;
 }
 
@@ -481,7 +484,7 @@ extern "C" bq_status bq_moe_route_scored(const float* logits, const float* bias,
 }
 
 extern "C" size_t bq_moe_permute_workspace_bytes(int32_t T, int32_t k, int32_t E) {
-    if (T < 0 || k < 1 || k > 8 || E < 1 || E > 1024) return 0;
+    if (T < 0 || k < 1 || k > 8 || E < 1 || E > 1024 || (int64_t)T * k > (int64_t)INT32_MAX) return 0;
     return bq::permute_scratch_bytes(T * k, E);
 }
 

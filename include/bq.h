@@ -244,9 +244,11 @@ bq_status bq_moe_route(const float* logits, const float* bias, int32_t T, int32_
 typedef enum {
     /* bq_moe_route above: bias added to the logits, softmax over the selected */
     BQ_SCORE_SOFTMAX = 0,
-    /* [slimserve] LFM2-MoE "softmax-then-bias": p = softmax(logits) over all
-     * E; select the k largest p[e] + bias[e]; weights = the selected p,
-     * renormalised to sum to 1 */
+    /* [butter] LFM2-MoE "softmax-then-bias" ("Everything Bagel 2", the LFM2
+     * family paragraph and the aura-port merge note): p = softmax(logits)
+     * over all E; select the k largest p[e] + bias[e]; weights = the
+     * selected unbiased p, renormalised to sum to 1 (the page does not say
+     * which probabilities the weights take; this is the reading used) */
     BQ_SCORE_SOFTMAX_THEN_BIAS = 1,
     /* [iron] DeepSeek V4 scoring: s = sqrt(softplus(logit)) with softplus(x) =
      * max(x, 0) + log1p(exp(-|x|)); select the k largest s[e] + bias[e]
@@ -409,8 +411,9 @@ bq_status bq_moe_gather_qmm_hidden(const bq_moe_desc* desc, const bq_qweight* ro
  * Errors: BQ_ERR_SHAPE (unknown stage).
  */
 typedef enum {
-    BQ_STAGE_ROUTE_PERMUTE = 0,  /* route, histogram, scan, placement, segment list */
-    BQ_STAGE_GATE_UP = 1,        /* routed gate/up GEMM with SwiGLU (+ activation gather) */
+    BQ_STAGE_ROUTE_PERMUTE = 0,  /* route, histogram, scan, placement, segment list, tile list and
+                                    the gather of the activation rows (tensor-core path) */
+    BQ_STAGE_GATE_UP = 1,        /* routed gate/up GEMM (or GEMV) with SwiGLU */
     BQ_STAGE_DOWN = 2,           /* routed down GEMM scaled by the gate weight */
     BQ_STAGE_SHARED = 3,         /* shared expert (gate/up + down) */
     BQ_STAGE_COMBINE = 4,        /* gate-weighted combine */
@@ -421,6 +424,22 @@ bq_status bq_set_stage_events(int32_t stage, void* start_event, void* stop_event
 
 /* Number of kernels this library has launched in this process (all threads). */
 uint64_t bq_launch_count(void);
+
+/*
+ * Test hook for the bounded waits of the tensor-core GEMM (the failure
+ * detection path; the pages have no counterpart).  Every barrier wait in
+ * that kernel gives up after a time limit, sets BQ_DEV_WAIT_TIMEOUT in the
+ * device status word, lets its own copies in flight land, frees its TMEM
+ * and returns.  Normally nothing makes a wait run out.  While set, GEMM
+ * launches (bq_qmm above the GEMV range, the prefill MoE layer) take
+ * `wait_limit_ns` as that limit (1 ms .. 2 s; 0 restores the 2 s default)
+ * and, if `skip_weight_copies` is 1, their weight producer issues no copies,
+ * so the waits for weights run out: the call then returns BQ_OK, its output
+ * is undefined and bq_device_status reports BQ_DEV_WAIT_TIMEOUT.  Process
+ * wide, for tests only; call bq_test_set_wait_probe(0, 0) to restore.
+ * Errors: BQ_ERR_SHAPE (argument outside the ranges above).
+ */
+bq_status bq_test_set_wait_probe(int32_t skip_weight_copies, uint64_t wait_limit_ns);
 
 #ifdef __cplusplus
 }

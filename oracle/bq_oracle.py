@@ -42,8 +42,10 @@ Readings taken where the pages are silent:
   selection and weighting.
 * Fused gate/up weight: rows [0, I) are the gate, rows [I, 2I) the up
   projection.
-* Scored routing: ``softmax_then_bias`` selects on softmax(logits) + bias
-  and weights the selected unbiased probabilities renormalised to 1;
+* Scored routing: ``softmax_then_bias`` (LFM2-MoE, *Everything Bagel 2*)
+  selects on softmax(logits) + bias and weights the selected unbiased
+  probabilities renormalised to 1 (the page leaves open which probabilities
+  the weights use);
   ``sqrtsoftplus`` selects on sqrt(softplus(logit)) + bias and weights the
   selected unbiased scores times the routed scaling factor, without
   renormalising (the pages name no renormalisation for it).
@@ -293,10 +295,15 @@ def route_scored(logits: np.ndarray, k: int, bias: np.ndarray | None = None, sco
 
     * ``softmax``: ``route`` (bias added to the logits, select on them,
       weights = softmax of the selected, renormalised).
-    * ``softmax_then_bias``: *SlimServe #2*, LFM2-MoE routing — the
-      softmax ``p`` over all experts, then the per-expert bias added only
-      for selection (select the k largest ``p + bias``); the weights are the
-      unbiased ``p`` of the selected experts, renormalised to sum to 1.
+    * ``softmax_then_bias``: *Everything Bagel 2* (butter #10), the LFM2
+      family paragraph and the aura-port merge note (``expertBias``):
+      LFM2-MoE routing — the softmax ``p`` over all experts, then the
+      per-expert bias added only for selection (select the k largest
+      ``p + bias``); the weights are the unbiased ``p`` of the selected
+      experts, renormalised to sum to 1.  The page does not say whether the
+      weights take the biased or the unbiased probabilities; the unbiased
+      reading is taken (the bias steers load, as in the aux-loss-free
+      DeepSeek rule).
     * ``sqrtsoftplus``: *iron #9*, DeepSeek V4 scoring
       ``s = sqrt(softplus(logit))``; selection on ``s + bias`` (aux-loss-free
       bias), weights = the unbiased ``s`` of the selected experts times the

@@ -138,6 +138,34 @@ def oracle_moe(inp: synth.MoEInputs, tokens=None, ids=None, wts=None):
     return O.moe_ffn_tokens(inp.x, ids, wts, tokens, gu, dn, shared)
 
 
+def oracle_moe_threaded(inp: synth.MoEInputs, workers: int = 8):
+    """The whole-output fp64 oracle of a MoE layer, as ``oracle.moe_ffn``
+    computes it (plain rule): every expert's SwiGLU FFN over its tokens with
+    the oracle's dequantisation, gate-weighted and summed, plus the shared
+    expert.  Experts are evaluated by a pool of threads (numpy releases the
+    GIL inside its array operations) and summed in ascending expert order, so
+    full-size layers finish in about a minute.  Test infrastructure only."""
+    from concurrent.futures import ThreadPoolExecutor
+    c = inp.case
+    ids, wts = O.route(inp.logits, c.topk, inp.bias)
+    experts = [int(e) for e in np.unique(ids)]
+
+    def expert_out(e):
+        tok, slot = np.nonzero(ids == e)
+        gu = dequant(c.fmt, expert_slice(c.fmt, inp.w_gu, e)).reshape(2 * c.inter, c.hidden)
+        dn = dequant(c.fmt, expert_slice(c.fmt, inp.w_d, e)).reshape(c.hidden, c.inter)
+        return tok, wts[tok, slot][:, None] * O.swiglu_ffn(inp.x[tok], gu, dn)
+
+    y = np.zeros((c.t, c.hidden), dtype=np.float64)
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        for tok, out in ex.map(expert_out, experts):
+            y[tok] += out
+    if inp.shared_gu is not None:
+        y += O.swiglu_ffn(inp.x, dequant("q8_0", inp.shared_gu).reshape(2 * c.inter, c.hidden),
+                          dequant("q8_0", inp.shared_d).reshape(c.hidden, c.inter))
+    return y
+
+
 def route_scored_dev(bq, logits, k, bias, scoring: str, scale: float = 1.0):
     """The GPU router under a scoring rule (ids, weights as numpy)."""
     import torch

@@ -162,3 +162,18 @@ def test_host_validation_of_the_layer_and_matmul_entry_points(bq):
     assert lib.bq_moe_gather_qmm(ctypes.byref(d), x, x, None, x, None, 0, None) == 5    # no workspace
     assert lib.bq_set_stage_events(6, None, None) == 2                                  # unknown stage
     assert lib.bq_set_stage_events(5, None, None) == 0                                  # norm + router stage
+
+
+def test_host_validation_of_pair_counts_and_the_wait_probe(bq):
+    lib = bq._lib
+    # T * k must fit an int: 2^29 + 1 tokens x top-8 is rejected before anything runs
+    big = (1 << 29) + 1
+    assert lib.bq_moe_route(None, None, big, 16, 8, None, None, None) == 2
+    assert lib.bq_moe_permute_workspace_bytes(big, 8, 16) == 0
+    assert lib.bq_moe_permute_noalloc(None, big, 8, 16, None, None, None, None, None, None) == 2
+    assert "pairs" in bq.last_error()
+    # the wait probe takes 0/1 and a limit in [1 ms, 2 s] (0 = default)
+    assert lib.bq_test_set_wait_probe(2, 0) == 2
+    assert lib.bq_test_set_wait_probe(0, 1000) == 2
+    assert lib.bq_test_set_wait_probe(0, 3_000_000_000) == 2
+    assert lib.bq_test_set_wait_probe(0, 0) == 0

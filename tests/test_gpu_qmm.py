@@ -55,8 +55,10 @@ def test_qmm_dense_sweep(lib, case):
     qw = make_qweight(lib, case.fmt, w, 1, case.n, case.k)
     got = _qmm(lib, qw, x)
     wd = dequant(case.fmt, w).reshape(case.n, case.k)
-    rows = np.arange(case.m) if case.m <= 32 else synth.rng(7).choice(case.m, 48, replace=False)
-    assert_close_matmul(got[rows], O.qmm(x[rows], wd), case.name)
+    ref = O.qmm(x, wd)   # every row, the 2048-row case included
+    assert_close_matmul(got, ref, case.name)
+    rel = np.linalg.norm(got - ref, axis=1) / np.linalg.norm(ref, axis=1)
+    assert rel.max() <= 4 * 2e-3, (int(rel.argmax()), float(rel.max()))
 
 
 def test_qmm_rejects_bad_shapes(lib):
