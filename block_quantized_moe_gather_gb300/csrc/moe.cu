@@ -249,7 +249,7 @@ extern "C" bq_status bq_qmm(const uint16_t* x, int32_t m, const bq_qweight* w, f
         // small m: the GEMV, one CTA row of the grid per 8-row token group
         bq::QgemvParams p = dense_params(w, m, reinterpret_cast<const __half*>(x), y, nullptr, w->n);
         p.grid_groups = 1;
-        bq::launch_qgemv(p, 1, st);
+        bq::launch_any_gemv(p, 1, m, st);
     } else if ((s = bq::launch_gemm_dense(w, m, reinterpret_cast<const __half*>(x), y, st)) != BQ_OK) {
         return s;
     }
@@ -332,8 +332,8 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
                                            w.cnt_sgu);
         bq::QgemvParams sdn = dense_params(d->shared_down, T, w.h_shared, y, nullptr, H, w.ks_sd, w.part_sd, w.cnt_sd);
         sgu.grid_groups = sdn.grid_groups = 1;   // more than 8 tokens: one CTA row per token group
-        bq::launch_qgemv(sgu, 1, ss);
-        bq::launch_qgemv(sdn, 1, ss);
+        bq::launch_any_gemv(sgu, 1, T, ss);
+        bq::launch_any_gemv(sdn, 1, T, ss, /*after_previous=*/true);
         bq::stage_end(BQ_STAGE_SHARED, ss);
         if (side && cudaEventRecord(side->join, ss) != cudaSuccess)
             return bq::fail(BQ_ERR_CUDA, "bq_moe_gather_qmm: cudaEventRecord on the side stream failed");
@@ -348,7 +348,7 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
         gu.n_segments = w.n_segments; gu.src_row = w.perm_token; gu.x = xh; gu.h = w.h;
         gu.ksplit = w.ks_gu; gu.partial = w.part_gu; gu.counters = w.cnt_gu;
         bq::stage_begin(BQ_STAGE_GATE_UP, st);
-        bq::launch_qgemv(gu, max_segments, st, /*after_previous=*/true);
+        bq::launch_any_gemv(gu, max_segments, T, st, /*after_previous=*/true);
         bq::stage_end(BQ_STAGE_GATE_UP, st);
 
         bq::QgemvParams dn = gu;
@@ -357,7 +357,7 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
         dn.src_row = nullptr; dn.x = w.h; dn.h = nullptr; dn.y = w.y_slot; dn.ldy = H; dn.row_scale = w.perm_gate;
         dn.ksplit = w.ks_d; dn.partial = w.part_d; dn.counters = w.cnt_d;
         bq::stage_begin(BQ_STAGE_DOWN, st);
-        bq::launch_qgemv(dn, max_segments, st, /*after_previous=*/true);
+        bq::launch_any_gemv(dn, max_segments, T, st, /*after_previous=*/true);
         bq::stage_end(BQ_STAGE_DOWN, st);
     } else {
         if ((s = bq::launch_gemm_moe(d, xh, w.perm_token, w.perm_gate, w.seg_expert, w.seg_start, w.seg_count,
@@ -369,10 +369,13 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
         const int Is = d->shared_gate_up->n / 2;
         bq::stage_begin(BQ_STAGE_SHARED, st);
         if (T <= 8 || !bq::gemm_supported(d->shared_gate_up->fmt)) {
-            bq::launch_qgemv(dense_params(d->shared_gate_up, T, xh, nullptr, w.h_shared, 0, w.ks_sgu, w.part_sgu,
-                                          w.cnt_sgu), 1, st);
-            bq::launch_qgemv(dense_params(d->shared_down, T, w.h_shared, y, nullptr, H, w.ks_sd, w.part_sd,
-                                          w.cnt_sd), 1, st);
+            bq::QgemvParams sgu = dense_params(d->shared_gate_up, T, xh, nullptr, w.h_shared, 0, w.ks_sgu, w.part_sgu,
+                                               w.cnt_sgu);
+            bq::QgemvParams sdn = dense_params(d->shared_down, T, w.h_shared, y, nullptr, H, w.ks_sd, w.part_sd,
+                                               w.cnt_sd);
+            sgu.grid_groups = sdn.grid_groups = 1;
+            bq::launch_any_gemv(sgu, 1, T, st);
+            bq::launch_any_gemv(sdn, 1, T, st);
         } else {
             if ((s = bq::launch_gemm_shared(d->shared_gate_up, d->shared_down, T, xh, w.h_shared, y, Is,
                                             base + w.bytes, st)) != BQ_OK)

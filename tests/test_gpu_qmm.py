@@ -174,3 +174,43 @@ def test_fp8_rejects_gate_up_halves_off_the_scale_grid(lib):
     import torch
     with pytest.raises(lib.BQError, match="SHAPE"):
         lib.repack_fp8_b128(torch.from_numpy(w.bytes).cuda(), torch.from_numpy(w.scales).cuda(), qw)
+
+
+@pytest.mark.parametrize("scale", [1e-4, 1.0, 300.0])
+@pytest.mark.parametrize("m", [1, 5, 8, 24])
+def test_qmm_q2_k_activation_range(lib, m, scale):
+    # The Q2_K GEMV multiplies fp16 code fields that are subnormal numbers and
+    # activations scaled by 2^-J (J up to 8); tiny activations (many already
+    # fp16 subnormals), unit ones and large ones must all match the oracle.
+    g = synth.rng(int(scale * 1000) + m)
+    n, k = 256, 1024
+    w = synth.q2_k_blocks(g, n, k)
+    qw = make_qweight(lib, "q2_k", w, 1, n, k)
+    x = (synth.fp16_normal(g, (m, k)).astype(np.float32) * scale).astype(np.float16)
+    ref = O.qmm(x, O.dequant_q2_k(w).reshape(n, k))
+    assert_close_matmul(_qmm(lib, qw, x), ref, f"q2_k m={m} scale={scale}")
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q2_k", "int4", "mxfp4", "fp8_b128"])
+@pytest.mark.parametrize("m", [1, 8, 9, 64])
+def test_qmm_long_k_split_across_a_cluster(lib, fmt, m):
+    # K long enough that the GEMV splits it over 8-16 CTAs of a cluster
+    # (partials summed in distributed shared memory), N = 2 row tiles
+    g = synth.rng(len(fmt) * 100 + m)
+    n, k = 256, {"q8_0": 4096, "q2_k": 8192, "int4": 4096, "mxfp4": 4096, "fp8_b128": 4096}[fmt]
+    if fmt == "q8_0":
+        w = synth.q8_0_blocks(g, n, k)
+    elif fmt == "q2_k":
+        w = synth.q2_k_blocks(g, n, k)
+    elif fmt == "mxfp4":
+        w = synth.mxfp4_blocks(g, n, k)
+    elif fmt == "fp8_b128":
+        w = synth.fp8_block_weight(g, (), n, k)
+    else:
+        w = synth.int4_weight(g, (n,), k)
+    qw = make_qweight(lib, fmt, w, 1, n, k)
+    x = synth.fp16_normal(g, (m, k))
+    ref = O.qmm(x, dequant(fmt, w).reshape(n, k))
+    got = _qmm(lib, qw, x)
+    assert_close_matmul(got, ref, f"{fmt} m={m} k={k}")
+    np.testing.assert_array_equal(got.view(np.uint32), _qmm(lib, qw, x).view(np.uint32))   # reproducible
