@@ -63,7 +63,7 @@ __host__ __device__ constexpr int up128(int v) { return (v + 127) & ~127; }
 // Shared-memory carve-up (bytes from a 128-byte aligned base) for a CTA
 // holding `ns` slabs and staging `ntk` activation rows.
 struct Carve {
-    int slabs, xs, ss, part, bars, total;
+    int slabs, xs, ss, part, bars, misc, total;
 };
 template <int FMT>
 __host__ __device__ Carve carve(int ns, int ntk) {
@@ -74,7 +74,8 @@ __host__ __device__ Carve carve(int ns, int ntk) {
     c.ss = c.xs + up128(ns * T::SK * ntk * 2);                 // staged activations (fp16)
     c.part = c.ss + up128(FMT == BQ_FMT_Q2_K ? ns * 32 * ntk : 0);   // Q2_K sub-block sums
     c.bars = c.part + 128 * 8 * 4;                              // fp32 partial [128 rows][8 rows of x]
-    c.total = c.bars + 8 * T::MAXS + 128;                       // + alignment slack
+    c.misc = c.bars + 8 * T::MAXS;                              // per x row: |x| max, unscale factor
+    c.total = c.misc + 64 + 128;                                // + alignment slack
     return c;
 }
 
@@ -174,15 +175,11 @@ __device__ __forceinline__ uint32_t q2_sub(uint32_t w, uint32_t wh) {
 __host__ __device__ constexpr int q2_step_j(int s, int e) { return q2_j(2 * (s & 3) + (e >> 1)); }
 
 // ---------------------------------------------------------------- staging
-// Activation rows [tok0, tok0 + ntk) of the share (slabs ks0 .. ks0 + ns - 1)
+// Activation rows [row0, row0 + ntk) of the share (slabs ks0 .. ks0 + ns - 1)
 // into xs: MMA step s of slab i, lane quarter t, row g at byte
-// ((i * STEPS + s) * 4 + t) * 8 * ntk + 8 * g (four fp16).  Q2_K: each value
-// scaled by 2^-J of its code field (exact), and the fp32 sums of the raw
-// values of each 16-value sub-block (fp16) into ss at ((i * 4 + t) * ntk +
-// g) * 8 (sub-blocks 4t .. 4t + 3 of the slab's super-block).
+// ((i * STEPS + s) * 4 + t) * 8 * ntk + 8 * g (four fp16).
 template <int FMT>
-__device__ __forceinline__ void stage_x(const bq::QgemvParams& p, int row0, int ntk, int ks0, int ns, uint8_t* xs,
-                                        uint8_t* ss) {
+__device__ __forceinline__ void stage_x(const bq::QgemvParams& p, int row0, int ntk, int ks0, int ns, uint8_t* xs) {
     using T = VT<FMT>;
     constexpr int STEPS = T::SK / 16, V = T::SK / 4;   // values per lane quarter
     const int units = ns * 4 * ntk;                    // (slab, quarter, row)
@@ -191,35 +188,73 @@ __device__ __forceinline__ void stage_x(const bq::QgemvParams& p, int row0, int 
         const int lr = row0 + g;
         const int src = p.src_row ? __ldg(p.src_row + lr) : lr;
         const uint4* xp = reinterpret_cast<const uint4*>(p.x + (int64_t)src * p.k + (int64_t)(ks0 + i) * T::SK + t * V);
-        float sums[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int v8 = 0; v8 < V / 8; ++v8) {   // 8 values = MMA steps 2 v8, 2 v8 + 1
-            uint4 q = __ldg(xp + v8);
-            if (FMT == BQ_FMT_Q2_K) {
-                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 f = __half22float2(bq::u32_as_h2(w[j]));
-                    sums[v8 >> 1] += f.x + f.y;
-                }
-                uint32_t o[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {   // word j: elements (2j, 2j+1) of the 8 -> step 2 v8 + j / 2
-                    const int s = 2 * v8 + (j >> 1), e = 2 * (j & 1);
-                    const int jj = q2_step_j(s, e);
-                    const __half sc = __ushort_as_half((uint16_t)((15 - jj) << 10));   // 2^-jj
-                    o[j] = bq::h2_as_u32(__hmul2(bq::u32_as_h2(w[j]), __halves2half2(sc, sc)));
-                }
-                q = make_uint4(o[0], o[1], o[2], o[3]);
-            }
+            const uint4 q = __ldg(xp + v8);
             const int s = 2 * v8;
             *reinterpret_cast<uint2*>(xs + ((i * STEPS + s) * 4 + t) * 8 * ntk + 8 * g) = make_uint2(q.x, q.y);
             *reinterpret_cast<uint2*>(xs + ((i * STEPS + s + 1) * 4 + t) * 8 * ntk + 8 * g) = make_uint2(q.z, q.w);
         }
-        if (FMT == BQ_FMT_Q2_K) {
-            const __half2 lo = __floats2half2_rn(sums[0], sums[1]), hi = __floats2half2_rn(sums[2], sums[3]);
-            *reinterpret_cast<uint2*>(ss + ((i * 4 + t) * ntk + g) * 8) = make_uint2(bq::h2_as_u32(lo), bq::h2_as_u32(hi));
+    }
+}
+
+// Q2_K staging (one (slab, quarter, row) unit per thread: ns * 4 * ntk <= 128).
+// Each value x is stored as fp16(x * 2^(S_g - J)), J the bit position of its
+// code field and 2^S_g a power of two per x row that brings the largest |x|
+// of this CTA's share to [256, 512): the scaled values are normal fp16
+// numbers (no bits lost to subnormals, no overflow) and exact where x * 2^S_g
+// is.  The fp32 sums of each 16-value sub-block, times 2^S_g, go to ss at
+// ((i * 4 + t) * ntk + g) * 8 (sub-blocks 4t .. 4t + 3 of the slab's
+// super-block); unscale[g] = 2^-S_g.  Contains __syncthreads.
+__device__ __forceinline__ void stage_x_q2k(const bq::QgemvParams& p, int row0, int ntk, int ks0, int ns, uint8_t* xs,
+                                            uint8_t* ss, unsigned* s_max, float* unscale) {
+    constexpr int STEPS = 16;
+    const int units = ns * 4 * ntk;
+    const int u = threadIdx.x;
+    const int g = u % ntk, t = (u / ntk) & 3, i = u / (4 * ntk);
+    float sums[4] = {0.f, 0.f, 0.f, 0.f}, mx = 0.f;
+    const uint4* xp = nullptr;
+    if (u < units) {
+        const int lr = row0 + g;
+        const int src = p.src_row ? __ldg(p.src_row + lr) : lr;
+        xp = reinterpret_cast<const uint4*>(p.x + (int64_t)src * p.k + (int64_t)(ks0 + i) * 256 + t * 64);
+#pragma unroll
+        for (int v8 = 0; v8 < 8; ++v8) {
+            const uint4 q = __ldg(xp + v8);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = __half22float2(bq::u32_as_h2(w[j]));
+                sums[v8 >> 1] += f.x + f.y;
+                mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
         }
+        atomicMax(s_max + g, __float_as_uint(mx));   // non-negative floats order as their bits
+    }
+    __syncthreads();
+    if (u < units) {
+        const float m = __uint_as_float(s_max[g]);
+        const int sh = (m > 0.f && m <= 65504.f) ? 8 - ilogbf(m) : 0;   // 2^sh * max in [256, 512)
+        const float fs = ldexpf(1.0f, sh);
+        if (i == 0 && t == 0) unscale[g] = ldexpf(1.0f, -sh);
+#pragma unroll
+        for (int v8 = 0; v8 < 8; ++v8) {   // the same 128 bytes again, from L1
+            const uint4 q = __ldg(xp + v8);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {   // word j: elements (2j, 2j+1) of the 8 -> step 2 v8 + j / 2
+                const int s = 2 * v8 + (j >> 1), e = 2 * (j & 1);
+                const float f = fs * __uint_as_float((uint32_t)(127 - q2_step_j(s, e)) << 23);   // 2^(S - J)
+                const float2 x2 = __half22float2(bq::u32_as_h2(w[j]));
+                o[j] = bq::h2_as_u32(__floats2half2_rn(x2.x * f, x2.y * f));
+            }
+            const int s = 2 * v8;
+            *reinterpret_cast<uint2*>(xs + ((i * STEPS + s) * 4 + t) * 8 * ntk + 8 * g) = make_uint2(o[0], o[1]);
+            *reinterpret_cast<uint2*>(xs + ((i * STEPS + s + 1) * 4 + t) * 8 * ntk + 8 * g) = make_uint2(o[2], o[3]);
+        }
+        const __half2 lo = __floats2half2_rn(sums[0] * fs, sums[1] * fs), hi = __floats2half2_rn(sums[2] * fs, sums[3] * fs);
+        *reinterpret_cast<uint2*>(ss + ((i * 4 + t) * ntk + g) * 8) = make_uint2(bq::h2_as_u32(lo), bq::h2_as_u32(hi));
     }
 }
 
@@ -379,6 +414,8 @@ gemv_kernel(const bq::QgemvParams p, int C, int ntk_max) {
     uint8_t* ss = smem + cv.ss;
     float* part = reinterpret_cast<float*>(smem + cv.part);
     const uint32_t bar0 = smem_u32(smem + cv.bars);
+    unsigned* s_max = reinterpret_cast<unsigned*>(smem + cv.misc);   // Q2_K: per x row
+    float* unscale = reinterpret_cast<float*>(smem + cv.misc + 32);
 
     // dense weights do not depend on the kernel before: their copies go out
     // before the dependency wait
@@ -394,6 +431,10 @@ gemv_kernel(const bq::QgemvParams p, int C, int ntk_max) {
     };
     const int gy = blockIdx.y;
     if (!routed && 8 * gy >= p.m) return;   // token group beyond m: the whole cluster leaves
+    if (FMT == BQ_FMT_Q2_K && threadIdx.x < 8) {
+        s_max[threadIdx.x] = 0u;
+        unscale[threadIdx.x] = 1.0f;
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < ns; ++i)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar0 + 8u * i), "r"(1u) : "memory");
@@ -413,7 +454,12 @@ gemv_kernel(const bq::QgemvParams p, int C, int ntk_max) {
         if (threadIdx.x == 0) issue(e);
     }
     const int tok0 = 8 * gy, ntok = min(8, count - tok0), row0 = start + tok0;
-    stage_x<FMT>(p, row0, ntok, ks0, ns, xs, ss);
+    if (FMT == BQ_FMT_Q2_K) {
+        __syncthreads();   // s_max cleared
+        stage_x_q2k(p, row0, ntok, ks0, ns, xs, ss, s_max, unscale);
+    } else {
+        stage_x<FMT>(p, row0, ntok, ks0, ns, xs);
+    }
     __syncthreads();   // staged activations and barrier inits visible to all warps
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -435,6 +481,13 @@ gemv_kernel(const bq::QgemvParams p, int C, int ntk_max) {
         for (int tile = 0; tile < 2; ++tile)
 #pragma unroll
             for (int j = 0; j < 4; ++j) acc[tile][j] *= 1.0f / bq::kFp8ScaleOffset;
+    }
+    if (FMT == BQ_FMT_Q2_K) {   // remove the power of two of each staged x row (exact)
+        const float u0 = unscale[2 * t], u1 = unscale[2 * t + 1];
+#pragma unroll
+        for (int tile = 0; tile < 2; ++tile) {
+            acc[tile][0] *= u0; acc[tile][1] *= u1; acc[tile][2] *= u0; acc[tile][3] *= u1;
+        }
     }
     // partial [128 rows][8 x rows] of this CTA: K half 1 stores, half 0 adds
     // in a fixed order (bit-reproducible)
