@@ -41,9 +41,11 @@
 // the same order, so the contraction is unchanged.
 #include <algorithm>
 
-#include "moe_internal.cuh"
+#include "gemv_common.cuh"
 
 namespace {
+
+using namespace bq::gemv;
 
 template <int FMT> struct VT;
 // SK: K per slab, SB: slab bytes, MAXS: most slabs one CTA holds.
@@ -56,7 +58,6 @@ template <> struct VT<BQ_FMT_FP8_B128> { static constexpr int SK = 64,  SB = 820
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kMaxCluster = 16;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s
 
 __host__ __device__ constexpr int up128(int v) { return (v + 127) & ~127; }
 
@@ -79,112 +80,18 @@ __host__ __device__ Carve carve(int ns, int ntk) {
     return c;
 }
 
-// ---------------------------------------------------------------- PTX helpers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok) : "r"(bar), "r"(parity), "r"(100000u) : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Bounded wait for phase `parity` of an mbarrier: false after the limit
-// (BQ_DEV_WAIT_TIMEOUT recorded).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status) {
-    if (mbar_try(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    while (!mbar_try(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) {
-            bq::set_device_error(status, BQ_DEV_WAIT_TIMEOUT);
-            return false;
-        }
-    }
-    return true;
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// 16 bytes at shared address `addr` of CTA `rank` of this cluster.
-__device__ __forceinline__ float4 ld_dsmem(uint32_t addr, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t comp(const uint4& v, int i) {
-    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
-// Exact small integers from bit fields: a field at bit J of each 16-bit lane
-// ORed into the mantissa of 2^(10-J) has weight 1; subtracting 2^(10-J)
-// leaves its value.
-template <int J>
-__device__ __forceinline__ __half2 field_h2(uint32_t w, uint32_t mask) {
-    constexpr uint32_t e = (uint32_t)(25 - J) << 10;   // biased exponent of 2^(10-J)
-    return __hsub2(bq::u32_as_h2((w & (mask << J)) | e | (e << 16)), bq::u32_as_h2(e | (e << 16)));
-}
-
-// ---- Q2_K code pairs as fp16 subnormals.  Sub-block word layout: value 2p
-// in bits 2p..2p+1 of the low 16-bit lane, value 2p+1 in the same bits of the
-// high lane (p = 0..7); pairs 5-7 are taken from the word shifted right by
-// 10.  Pair p sits at bit J(p) of its lane, where ANDing it out leaves the
-// fp16 bit pattern of q * 2^(J - 24) (exponent field 0).
-__host__ __device__ constexpr int q2_j(int p) { return p < 5 ? 2 * p : 2 * (p - 5); }
-
-template <int P>
-__device__ __forceinline__ uint32_t q2_sub(uint32_t w, uint32_t wh) {
-    return (P < 5 ? w : wh) & (0x00030003u << q2_j(P));
-}
-
-// The activation factor 2^-J of element e (0..3) of MMA step s: elements 0-1
-// meet pair 2(s % 4), elements 2-3 pair 2(s % 4) + 1 of the step's sub-block.
-__host__ __device__ constexpr int q2_step_j(int s, int e) { return q2_j(2 * (s & 3) + (e >> 1)); }
-
 // ---------------------------------------------------------------- staging
-// Activation rows [row0, row0 + ntk) of the share (slabs ks0 .. ks0 + ns - 1)
+// Activation rows [row0, row0 + ntok) of the share (slabs ks0 .. ks0 + ns - 1)
 // into xs: MMA step s of slab i, lane quarter t, row g at byte
-// ((i * STEPS + s) * 4 + t) * 8 * ntk + 8 * g (four fp16).
-template <int FMT>
-__device__ __forceinline__ void stage_x(const bq::QgemvParams& p, int row0, int ntk, int ks0, int ns, uint8_t* xs) {
+// ((i * STEPS + s) * 4 + t) * 8 * NTK + 8 * g (four fp16; NTK >= ntok row slots).
+template <int FMT, int NTK>
+__device__ __forceinline__ void stage_x(const bq::QgemvParams& p, int row0, int ntok, int ks0, int ns, uint8_t* xs) {
     using T = VT<FMT>;
     constexpr int STEPS = T::SK / 16, V = T::SK / 4;   // values per lane quarter
-    const int units = ns * 4 * ntk;                    // (slab, quarter, row)
+    const int units = ns * 4 * NTK;                    // (slab, quarter, row slot)
     for (int u = threadIdx.x; u < units; u += kThreads) {
-        const int g = u % ntk, t = (u / ntk) & 3, i = u / (4 * ntk);
+        const int g = u % NTK, t = (u / NTK) & 3, i = u / (4 * NTK);
+        if (g >= ntok) continue;
         const int lr = row0 + g;
         const int src = p.src_row ? __ldg(p.src_row + lr) : lr;
         const uint4* xp = reinterpret_cast<const uint4*>(p.x + (int64_t)src * p.k + (int64_t)(ks0 + i) * T::SK + t * V);
@@ -192,29 +99,31 @@ __device__ __forceinline__ void stage_x(const bq::QgemvParams& p, int row0, int 
         for (int v8 = 0; v8 < V / 8; ++v8) {   // 8 values = MMA steps 2 v8, 2 v8 + 1
             const uint4 q = __ldg(xp + v8);
             const int s = 2 * v8;
-            *reinterpret_cast<uint2*>(xs + ((i * STEPS + s) * 4 + t) * 8 * ntk + 8 * g) = make_uint2(q.x, q.y);
-            *reinterpret_cast<uint2*>(xs + ((i * STEPS + s + 1) * 4 + t) * 8 * ntk + 8 * g) = make_uint2(q.z, q.w);
+            *reinterpret_cast<uint2*>(xs + ((i * STEPS + s) * 4 + t) * 8 * NTK + 8 * g) = make_uint2(q.x, q.y);
+            *reinterpret_cast<uint2*>(xs + ((i * STEPS + s + 1) * 4 + t) * 8 * NTK + 8 * g) = make_uint2(q.z, q.w);
         }
     }
 }
 
-// Q2_K staging (one (slab, quarter, row) unit per thread: ns * 4 * ntk <= 128).
+// Q2_K staging (one (slab, quarter, row slot) unit per thread: ns * 4 * NTK <= 128).
 // Each value x is stored as fp16(x * 2^(S_g - J)), J the bit position of its
 // code field and 2^S_g a power of two per x row that brings the largest |x|
 // of this CTA's share to [256, 512): the scaled values are normal fp16
 // numbers (no bits lost to subnormals, no overflow) and exact where x * 2^S_g
 // is.  The fp32 sums of each 16-value sub-block, times 2^S_g, go to ss at
-// ((i * 4 + t) * ntk + g) * 8 (sub-blocks 4t .. 4t + 3 of the slab's
+// ((i * 4 + t) * NTK + g) * 8 (sub-blocks 4t .. 4t + 3 of the slab's
 // super-block); unscale[g] = 2^-S_g.  Contains __syncthreads.
-__device__ __forceinline__ void stage_x_q2k(const bq::QgemvParams& p, int row0, int ntk, int ks0, int ns, uint8_t* xs,
+template <int NTK>
+__device__ __forceinline__ void stage_x_q2k(const bq::QgemvParams& p, int row0, int ntok, int ks0, int ns, uint8_t* xs,
                                             uint8_t* ss, unsigned* s_max, float* unscale) {
     constexpr int STEPS = 16;
-    const int units = ns * 4 * ntk;
+    const int units = ns * 4 * NTK;
     const int u = threadIdx.x;
-    const int g = u % ntk, t = (u / ntk) & 3, i = u / (4 * ntk);
+    const int g = u % NTK, t = (u / NTK) & 3, i = u / (4 * NTK);
+    const bool live = u < units && g < ntok;
     float sums[4] = {0.f, 0.f, 0.f, 0.f}, mx = 0.f;
     const uint4* xp = nullptr;
-    if (u < units) {
+    if (live) {
         const int lr = row0 + g;
         const int src = p.src_row ? __ldg(p.src_row + lr) : lr;
         xp = reinterpret_cast<const uint4*>(p.x + (int64_t)src * p.k + (int64_t)(ks0 + i) * 256 + t * 64);
@@ -232,7 +141,7 @@ __device__ __forceinline__ void stage_x_q2k(const bq::QgemvParams& p, int row0, 
         atomicMax(s_max + g, __float_as_uint(mx));   // non-negative floats order as their bits
     }
     __syncthreads();
-    if (u < units) {
+    if (live) {
         const float m = __uint_as_float(s_max[g]);
         const int sh = (m > 0.f && m <= 65504.f) ? 8 - ilogbf(m) : 0;   // 2^sh * max in [256, 512)
         const float fs = ldexpf(1.0f, sh);
@@ -250,30 +159,30 @@ __device__ __forceinline__ void stage_x_q2k(const bq::QgemvParams& p, int row0, 
                 o[j] = bq::h2_as_u32(__floats2half2_rn(x2.x * f, x2.y * f));
             }
             const int s = 2 * v8;
-            *reinterpret_cast<uint2*>(xs + ((i * STEPS + s) * 4 + t) * 8 * ntk + 8 * g) = make_uint2(o[0], o[1]);
-            *reinterpret_cast<uint2*>(xs + ((i * STEPS + s + 1) * 4 + t) * 8 * ntk + 8 * g) = make_uint2(o[2], o[3]);
+            *reinterpret_cast<uint2*>(xs + ((i * STEPS + s) * 4 + t) * 8 * NTK + 8 * g) = make_uint2(o[0], o[1]);
+            *reinterpret_cast<uint2*>(xs + ((i * STEPS + s + 1) * 4 + t) * 8 * NTK + 8 * g) = make_uint2(o[2], o[3]);
         }
         const __half2 lo = __floats2half2_rn(sums[0] * fs, sums[1] * fs), hi = __floats2half2_rn(sums[2] * fs, sums[3] * fs);
-        *reinterpret_cast<uint2*>(ss + ((i * 4 + t) * ntk + g) * 8) = make_uint2(bq::h2_as_u32(lo), bq::h2_as_u32(hi));
+        *reinterpret_cast<uint2*>(ss + ((i * 4 + t) * NTK + g) * 8) = make_uint2(bq::h2_as_u32(lo), bq::h2_as_u32(hi));
     }
 }
 
 // ---------------------------------------------------------------- one slab
 // Warp rows 32 * quarter .. + 31: tile 0 = rows +0 .. +15, tile 1 = +16 .. +31;
 // lane (g, t) holds rows g and g + 8 of each tile.
-template <int FMT>
+template <int FMT, int NTK>
 __device__ __forceinline__ void slab_mma(const uint8_t* slab, const uint8_t* xs_slab, const uint8_t* ss_slab,
-                                         int rowbase, int g, int t, int ntk, float (&acc)[2][4]) {
+                                         int rowbase, int g, int t, int ntok, float (&acc)[2][4]) {
     using T = VT<FMT>;
     constexpr int STEPS = T::SK / 16;
-    const bool xv = g < ntk;
-    const uint8_t* xl = xs_slab + (t * ntk + g) * 8;
-    const int xstep = 32 * ntk;
+    constexpr int xstep = 32 * NTK;
+    const bool xv = g < ntok;
+    const uint8_t* xl = xs_slab + (t * NTK + g) * 8;
     if (FMT == BQ_FMT_Q2_K) {
         // one m16 tile at a time (its two rows per lane), so that the code
         // words, scales and the per-super-block sums fit the register budget
         uint2 bm = make_uint2(0u, 0u);   // sub-block sums of (4t, 4t+1), (4t+2, 4t+3) for x row g
-        if (xv) bm = *reinterpret_cast<const uint2*>(ss_slab + (t * ntk + g) * 8);
+        if (xv) bm = *reinterpret_cast<const uint2*>(ss_slab + (t * NTK + g) * 8);
 #pragma unroll
         for (int tile = 0; tile < 2; ++tile) {
             uint4 q[2];
@@ -397,10 +306,11 @@ __device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + _
 
 // ---------------------------------------------------------------- the kernel
 // grid (tiles * C, token groups, segments), cluster (C, 1, 1); C = CTAs
-// splitting K; ntk = activation rows staged per CTA (<= 8).
-template <int FMT, bool SWIGLU>
+// splitting K; NTK = activation row slots staged per CTA (>= the rows of any
+// token group, <= 8).
+template <int FMT, bool SWIGLU, int NTK>
 __global__ void __launch_bounds__(kThreads, 4)
-gemv_kernel(const bq::QgemvParams p, int C, int ntk_max) {
+gemv_kernel(const bq::QgemvParams p, int C) {
     using T = VT<FMT>;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 127) & ~uintptr_t(127));
@@ -409,7 +319,7 @@ gemv_kernel(const bq::QgemvParams p, int C, int ntk_max) {
     const int n_tiles = p.n / bq::kTileRows, k_slabs = p.k / T::SK;
     const int ks0 = (int)((int64_t)k_slabs * rank / C), ks1 = (int)((int64_t)k_slabs * (rank + 1) / C);
     const int ns = ks1 - ks0;
-    const Carve cv = carve<FMT>((k_slabs + C - 1) / C, ntk_max);
+    const Carve cv = carve<FMT>((k_slabs + C - 1) / C, NTK);
     uint8_t* xs = smem + cv.xs;
     uint8_t* ss = smem + cv.ss;
     float* part = reinterpret_cast<float*>(smem + cv.part);
@@ -453,12 +363,12 @@ gemv_kernel(const bq::QgemvParams p, int C, int ntk_max) {
         if (8 * gy >= count) return;
         if (threadIdx.x == 0) issue(e);
     }
-    const int tok0 = 8 * gy, ntok = min(8, count - tok0), row0 = start + tok0;
+    const int tok0 = 8 * gy, ntok = min(NTK, count - tok0), row0 = start + tok0;
     if (FMT == BQ_FMT_Q2_K) {
         __syncthreads();   // s_max cleared
-        stage_x_q2k(p, row0, ntok, ks0, ns, xs, ss, s_max, unscale);
+        stage_x_q2k<NTK>(p, row0, ntok, ks0, ns, xs, ss, s_max, unscale);
     } else {
-        stage_x<FMT>(p, row0, ntok, ks0, ns, xs);
+        stage_x<FMT, NTK>(p, row0, ntok, ks0, ns, xs);
     }
     __syncthreads();   // staged activations and barrier inits visible to all warps
 
@@ -468,8 +378,8 @@ gemv_kernel(const bq::QgemvParams p, int C, int ntk_max) {
     bool ok = true;
     for (int i = half; i < ns; i += 2) {
         if (!mbar_wait(bar0 + 8u * i, 0u, p.status)) { ok = false; break; }
-        slab_mma<FMT>(smem + i * up128(T::SB), xs + i * (T::SK / 16) * 32 * ntok,
-                      FMT == BQ_FMT_Q2_K ? ss + i * 32 * ntok : nullptr, rowbase, g, t, ntok, acc);
+        slab_mma<FMT, NTK>(smem + i * up128(T::SB), xs + i * (T::SK / 16) * 32 * NTK,
+                           FMT == BQ_FMT_Q2_K ? ss + i * 32 * NTK : nullptr, rowbase, g, t, ntok, acc);
     }
     if (!ok) {
         // let every copy this CTA issued land before it may leave (bounded)
@@ -591,17 +501,17 @@ int fmt_max_slabs(int fmt) {
     }
 }
 
-template <int FMT, bool SWIGLU>
-cudaError_t launch_fmt(const bq::QgemvParams& p, dim3 grid, int C, int ntk, bool after_previous, cudaStream_t st) {
+template <int FMT, bool SWIGLU, int NTK>
+cudaError_t launch_fmt(const bq::QgemvParams& p, dim3 grid, int C, bool after_previous, cudaStream_t st) {
     const int ks = p.k / VT<FMT>::SK;
-    const size_t smem = (size_t)carve<FMT>((ks + C - 1) / C, ntk).total;
-    auto kernel = gemv_kernel<FMT, SWIGLU>;
+    const size_t smem = (size_t)carve<FMT>((ks + C - 1) / C, NTK).total;
+    auto kernel = gemv_kernel<FMT, SWIGLU, NTK>;
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             carve<FMT>(VT<FMT>::MAXS, 8).total);
+                             carve<FMT>(VT<FMT>::MAXS, NTK).total);
         cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         attr_set[dev] = true;
     }
@@ -626,13 +536,21 @@ cudaError_t launch_fmt(const bq::QgemvParams& p, dim3 grid, int C, int ntk, bool
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kernel, p, C, ntk);
+    return cudaLaunchKernelEx(&cfg, kernel, p, C);
+}
+
+template <int FMT, int NTK>
+cudaError_t launch_ntk(const bq::QgemvParams& p, dim3 grid, int C, bool after_previous, cudaStream_t st) {
+    return p.swiglu ? launch_fmt<FMT, true, NTK>(p, grid, C, after_previous, st)
+                    : launch_fmt<FMT, false, NTK>(p, grid, C, after_previous, st);
 }
 
 template <int FMT>
 cudaError_t launch_swiglu(const bq::QgemvParams& p, dim3 grid, int C, int ntk, bool after_previous, cudaStream_t st) {
-    return p.swiglu ? launch_fmt<FMT, true>(p, grid, C, ntk, after_previous, st)
-                    : launch_fmt<FMT, false>(p, grid, C, ntk, after_previous, st);
+    if (ntk <= 1) return launch_ntk<FMT, 1>(p, grid, C, after_previous, st);
+    if (ntk <= 2) return launch_ntk<FMT, 2>(p, grid, C, after_previous, st);
+    if (ntk <= 4) return launch_ntk<FMT, 4>(p, grid, C, after_previous, st);
+    return launch_ntk<FMT, 8>(p, grid, C, after_previous, st);
 }
 
 }  // namespace

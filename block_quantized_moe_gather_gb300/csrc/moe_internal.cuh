@@ -91,6 +91,16 @@ void launch_qgemv(const QgemvParams& p, int max_segments, cudaStream_t st, bool 
 // norm-fused variant, or K too long for 16 CTAs; the caller then uses
 // launch_qgemv.
 bool launch_gemv(const QgemvParams& p, int max_segments, int max_tokens, cudaStream_t st, bool after_previous = false);
+// Stream-K GEMV over the routed experts of a step with at most 8 tokens, or a
+// dense weight over at most 8 rows (no segment arrays) (gemv_stream.cu): one
+// wave of gemv_stream_ctas(fmt) CTAs takes equal ranges of the (segment, row
+// tile, K slab) units.  partial: >= gemv_stream_partial_bytes() of
+// workspace; counters: one int per (segment, row tile), zero on entry and
+// left zero.
+int gemv_stream_ctas(int fmt);
+size_t gemv_stream_partial_bytes();
+void launch_gemv_stream(const QgemvParams& p, int max_segments, float* partial, int32_t* counters, cudaStream_t st,
+                        bool after_previous = false);
 // CTAs per cluster for a weight of n x k in this format with `jobs`
 // (segment, row tile, token group) units, or 0 when K is too long.
 int gemv_cluster(int fmt, int n, int k, int jobs);
