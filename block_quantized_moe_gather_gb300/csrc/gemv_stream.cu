@@ -259,7 +259,13 @@ gemv_stream_kernel(const bq::QgemvParams p, float* __restrict__ partial, int32_t
 
     const int tiles = p.n / bq::kTileRows, ks = p.k / T::SK;
     const bool routed = p.seg_expert != nullptr;   // else one dense segment of p.m rows
-    const int64_t G = gridDim.x, U = (int64_t)(routed ? __ldg(p.n_segments) : 1) * tiles * ks;
+    // the grid is sized for the most segments the call can have; with fewer
+    // units than CTAs only the first U CTAs take part, so that every
+    // participating CTA owns at least one unit (the split-tile counters count
+    // the CTAs between the first and the last holder of a tile)
+    const int64_t U = (int64_t)(routed ? __ldg(p.n_segments) : 1) * tiles * ks;
+    const int64_t G = std::min<int64_t>(gridDim.x, U);
+    if ((int64_t)blockIdx.x >= G) return;
     const int64_t u0 = range_begin(blockIdx.x, G, U), u1 = range_begin(blockIdx.x + 1, G, U);
     const int n = (int)(u1 - u0);
 
