@@ -89,10 +89,6 @@ struct MoeWs {
     int ks_gu, ks_d, ks_sgu, ks_sd;
     float *part_gu, *part_d, *part_sgu, *part_sd;
     int32_t *cnt_gu, *cnt_d, *cnt_sgu, *cnt_sd;
-    // decode (T <= 8) stream-K GEMVs: partials and tile counters of the routed
-    // experts (gate/up, then down) and of the shared expert (its own stream)
-    float *part_stream, *part_stream_s;
-    int32_t *cnt_stream, *cnt_stream_s;
     int n_counters;
     size_t bytes;
 };
@@ -125,8 +121,6 @@ MoeWs carve(const bq_moe_desc* d, uint8_t* base) {
     w.ks_gu = w.ks_d = w.ks_sgu = w.ks_sd = 1;
     w.part_gu = w.part_d = w.part_sgu = w.part_sd = nullptr;
     w.cnt_gu = w.cnt_d = w.cnt_sgu = w.cnt_sd = nullptr;
-    w.part_stream = w.part_stream_s = nullptr;
-    w.cnt_stream = w.cnt_stream_s = nullptr;
     w.n_counters = 0;
     if (d->T <= 8) {
         const int segs = (int)std::min(E, P);
@@ -144,11 +138,6 @@ MoeWs carve(const bq_moe_desc* d, uint8_t* base) {
             w.part_sd = (float*)take((size_t)t_d * w.ks_sd * 4096);
             nc += n_s / bq::kTileRows + t_d;
         }
-        const int nc_old = nc;
-        const int t_s = d->shared_gate_up ? std::max(d->shared_gate_up->n, (int)H) / bq::kTileRows : 0;
-        nc += segs * std::max(t_gu, t_d) + t_s;
-        w.part_stream = (float*)take(bq::gemv_stream_partial_bytes());
-        if (d->shared_gate_up) w.part_stream_s = (float*)take(bq::gemv_stream_partial_bytes());
         int32_t* cnt = (int32_t*)take((size_t)nc * 4);
         w.n_counters = nc;
         w.cnt_gu = cnt;
@@ -157,8 +146,6 @@ MoeWs carve(const bq_moe_desc* d, uint8_t* base) {
             w.cnt_sgu = cnt ? w.cnt_d + segs * t_d : nullptr;
             w.cnt_sd = cnt ? w.cnt_sgu + d->shared_gate_up->n / bq::kTileRows : nullptr;
         }
-        w.cnt_stream = cnt ? cnt + nc_old : nullptr;
-        if (d->shared_gate_up) w.cnt_stream_s = cnt ? w.cnt_stream + segs * std::max(t_gu, t_d) : nullptr;
     }
     w.bytes = off;
     return w;
@@ -262,7 +249,7 @@ extern "C" bq_status bq_qmm(const uint16_t* x, int32_t m, const bq_qweight* w, f
         // small m: the GEMV, one CTA row of the grid per 8-row token group
         bq::QgemvParams p = dense_params(w, m, reinterpret_cast<const __half*>(x), y, nullptr, w->n);
         p.grid_groups = 1;
-        bq::launch_any_gemv(p, 1, m, st);
+        bq::launch_qgemv(p, 1, st);
     } else if ((s = bq::launch_gemm_dense(w, m, reinterpret_cast<const __half*>(x), y, st)) != BQ_OK) {
         return s;
     }
@@ -345,13 +332,8 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
                                            w.cnt_sgu);
         bq::QgemvParams sdn = dense_params(d->shared_down, T, w.h_shared, y, nullptr, H, w.ks_sd, w.part_sd, w.cnt_sd);
         sgu.grid_groups = sdn.grid_groups = 1;   // more than 8 tokens: one CTA row per token group
-        if (T <= 8) {
-            bq::launch_gemv_stream(sgu, 1, w.part_stream_s, w.cnt_stream_s, ss);
-            bq::launch_gemv_stream(sdn, 1, w.part_stream_s, w.cnt_stream_s, ss, /*after_previous=*/true);
-        } else {
-            bq::launch_any_gemv(sgu, 1, T, ss);
-            bq::launch_any_gemv(sdn, 1, T, ss, /*after_previous=*/true);
-        }
+        bq::launch_qgemv(sgu, 1, ss);
+        bq::launch_qgemv(sdn, 1, ss);
         bq::stage_end(BQ_STAGE_SHARED, ss);
         if (side && cudaEventRecord(side->join, ss) != cudaSuccess)
             return bq::fail(BQ_ERR_CUDA, "bq_moe_gather_qmm: cudaEventRecord on the side stream failed");
@@ -366,8 +348,7 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
         gu.n_segments = w.n_segments; gu.src_row = w.perm_token; gu.x = xh; gu.h = w.h;
         gu.ksplit = w.ks_gu; gu.partial = w.part_gu; gu.counters = w.cnt_gu;
         bq::stage_begin(BQ_STAGE_GATE_UP, st);
-        if (T <= 8) bq::launch_gemv_stream(gu, max_segments, w.part_stream, w.cnt_stream, st, /*after_previous=*/true);
-        else bq::launch_any_gemv(gu, max_segments, T, st, /*after_previous=*/true);
+        bq::launch_qgemv(gu, max_segments, st, /*after_previous=*/true);
         bq::stage_end(BQ_STAGE_GATE_UP, st);
 
         bq::QgemvParams dn = gu;
@@ -376,8 +357,7 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
         dn.src_row = nullptr; dn.x = w.h; dn.h = nullptr; dn.y = w.y_slot; dn.ldy = H; dn.row_scale = w.perm_gate;
         dn.ksplit = w.ks_d; dn.partial = w.part_d; dn.counters = w.cnt_d;
         bq::stage_begin(BQ_STAGE_DOWN, st);
-        if (T <= 8) bq::launch_gemv_stream(dn, max_segments, w.part_stream, w.cnt_stream, st, /*after_previous=*/true);
-        else bq::launch_any_gemv(dn, max_segments, T, st, /*after_previous=*/true);
+        bq::launch_qgemv(dn, max_segments, st, /*after_previous=*/true);
         bq::stage_end(BQ_STAGE_DOWN, st);
     } else {
         if ((s = bq::launch_gemm_moe(d, xh, w.perm_token, w.perm_gate, w.seg_expert, w.seg_start, w.seg_count,
@@ -389,13 +369,10 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
         const int Is = d->shared_gate_up->n / 2;
         bq::stage_begin(BQ_STAGE_SHARED, st);
         if (T <= 8 || !bq::gemm_supported(d->shared_gate_up->fmt)) {
-            bq::QgemvParams sgu = dense_params(d->shared_gate_up, T, xh, nullptr, w.h_shared, 0, w.ks_sgu, w.part_sgu,
-                                               w.cnt_sgu);
-            bq::QgemvParams sdn = dense_params(d->shared_down, T, w.h_shared, y, nullptr, H, w.ks_sd, w.part_sd,
-                                               w.cnt_sd);
-            sgu.grid_groups = sdn.grid_groups = 1;
-            bq::launch_any_gemv(sgu, 1, T, st);
-            bq::launch_any_gemv(sdn, 1, T, st);
+            bq::launch_qgemv(dense_params(d->shared_gate_up, T, xh, nullptr, w.h_shared, 0, w.ks_sgu, w.part_sgu,
+                                          w.cnt_sgu), 1, st);
+            bq::launch_qgemv(dense_params(d->shared_down, T, w.h_shared, y, nullptr, H, w.ks_sd, w.part_sd,
+                                          w.cnt_sd), 1, st);
         } else {
             if ((s = bq::launch_gemm_shared(d->shared_gate_up, d->shared_down, T, xh, w.h_shared, y, Is,
                                             base + w.bytes, st)) != BQ_OK)

@@ -76,39 +76,11 @@ struct QgemvParams {
     // the m rows is its own CTA row of the grid (grid.y = ceil(m / 8)) instead
     // of a loop inside every CTA.
     int grid_groups;
-    // device status word (set by the launchers)
-    int32_t* status;
 };
 constexpr int kMaxKsplit = 16;
 // Split factor that gives the GPU enough CTAs for this shape.
 int qgemv_ksplit(int fmt, int n, int k, int max_segments, int max_tokens);
 void launch_qgemv(const QgemvParams& p, int max_segments, cudaStream_t st, bool after_previous = false);
-
-// The cluster GEMV (gemv.cu): weights staged by bulk copies, K split across
-// the CTAs of a thread-block cluster and summed in distributed shared memory,
-// token groups of 8 as grid rows.  max_tokens bounds the rows of any segment.
-// Returns false (and launches nothing) for shapes it does not take: the
-// norm-fused variant, or K too long for 16 CTAs; the caller then uses
-// launch_qgemv.
-bool launch_gemv(const QgemvParams& p, int max_segments, int max_tokens, cudaStream_t st, bool after_previous = false);
-// Stream-K GEMV over the routed experts of a step with at most 8 tokens, or a
-// dense weight over at most 8 rows (no segment arrays) (gemv_stream.cu): one
-// wave of gemv_stream_ctas(fmt) CTAs takes equal ranges of the (segment, row
-// tile, K slab) units.  partial: >= gemv_stream_partial_bytes() of
-// workspace; counters: one int per (segment, row tile), zero on entry and
-// left zero.
-int gemv_stream_ctas(int fmt);
-size_t gemv_stream_partial_bytes();
-void launch_gemv_stream(const QgemvParams& p, int max_segments, float* partial, int32_t* counters, cudaStream_t st,
-                        bool after_previous = false);
-// CTAs per cluster for a weight of n x k in this format with `jobs`
-// (segment, row tile, token group) units, or 0 when K is too long.
-int gemv_cluster(int fmt, int n, int k, int jobs);
-// The cluster GEMV when it takes the shape, else the split-K GEMV.
-inline void launch_any_gemv(const QgemvParams& p, int max_segments, int max_tokens, cudaStream_t st,
-                            bool after_previous = false) {
-    if (!launch_gemv(p, max_segments, max_tokens, st, after_previous)) launch_qgemv(p, max_segments, st, after_previous);
-}
 
 // Up to this many rows a dense qmm runs the GEMV (token groups as separate
 // CTAs) rather than the tensor-core GEMM, whose grid is only

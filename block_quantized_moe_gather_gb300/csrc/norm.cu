@@ -93,7 +93,7 @@ bq_status launch_rmsnorm_qmm(const __half* h, int m, const __half* gamma, float 
             p.w = static_cast<const uint8_t*>(w->data);
             p.fmt = w->fmt; p.n = w->n; p.k = w->k; p.m = m; p.x = x_out; p.y = y; p.ldy = w->n; p.ksplit = 1;
             p.grid_groups = 1;
-            launch_any_gemv(p, 1, m, st);
+            launch_qgemv(p, 1, st);
             return BQ_OK;
         }
         QgemvParams p{};
