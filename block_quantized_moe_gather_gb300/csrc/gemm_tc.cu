@@ -54,30 +54,21 @@ constexpr int kMaxStagesB = 15;    // activation ring: at most 15 stages in flig
 //  - CFG 1 (expert segments of more than 160 tokens): tiles of up to 256
 //    token rows, one CTA per SM with all 512 TMEM columns (256-column
 //    accumulator, 6 A slots), 32 activation boxes (6 stages of 160 rows .. 4
-//    of 256).  One MMA of N = 256 per K step, and 16 converter warps (four
-//    per TMEM lane quarter, each converting every fourth stage) into an 8-slot
-//    A ring: the dequantisation of a stage serves 1.6x the FLOPs.
-// NPH: converter warps per TMEM lane quarter; MAXA: most A-ring slots.
+//    of 256).  One MMA of N = 256 per K step: the dequantisation and the ring
+//    bookkeeping of a stage serve 1.6x the FLOPs.
 template <int CFG> struct Cfg;
-template <> struct Cfg<0> {
-    static constexpr int BN = 160, kBBoxes = 15, kMinBlocks = 2, NPH = 2, MAXA = 6;
-    static constexpr uint32_t kTmemCols = 256;
-};
-template <> struct Cfg<1> {
-    static constexpr int BN = 256, kBBoxes = 32, kMinBlocks = 1, NPH = 4, MAXA = 8;
-    static constexpr uint32_t kTmemCols = 512;
-};
+template <> struct Cfg<0> { static constexpr int BN = 160, kBBoxes = 15, kMinBlocks = 2; static constexpr uint32_t kTmemCols = 256; };
+template <> struct Cfg<1> { static constexpr int BN = 256, kBBoxes = 32, kMinBlocks = 1; static constexpr uint32_t kTmemCols = 512; };
 constexpr int BN = Cfg<0>::BN;           // the work queue's chunk of a segment for CFG 0
 constexpr int kBigBN = Cfg<1>::BN;
 constexpr int kBigMinRows = 161;         // segments with at least this many rows go to CFG 1
 // TMEM A ring: whatever the accumulator leaves of 256 columns, rounded down to
 // an even count so that every slot is always written by the same converter warps
-constexpr int kMaxStagesA = 8;
+constexpr int kMaxStagesA = 6;
 constexpr int kMaxRawSlabs = 4;    // raw quantised slabs in shared memory (per format below)
+constexpr int kConvWarps = 8;      // two per TMEM lane quarter, alternating stages
 constexpr int kFirstConvWarp = 3;  // warp 0: activation producer, 1: MMA, 2: weight producer
-// converters: 4 * Cfg::NPH warps (NPH per TMEM lane quarter, taking stages in turn)
-template <int CFG>
-constexpr int threads() { return 32 * (kFirstConvWarp + 4 * Cfg<CFG>::NPH); }
+constexpr int kThreads = 32 * (kFirstConvWarp + kConvWarps);
 constexpr int kBoxBytes = kBoxRows * 128;
 constexpr int kRawBytes = 34816;   // raw slab ring: 4 Q8_0 / 3 Q2_K / 3 int4 slabs
 // One "stage consumed" barrier per K stage, in a ring of 16 (a commit of the
@@ -530,14 +521,11 @@ __device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + _
 
 // ---------------------------------------------------------------- the kernel
 template <int FMT, int EPI, int CFG>
-__global__ void __launch_bounds__(threads<CFG>(), Cfg<CFG>::kMinBlocks)
+__global__ void __launch_bounds__(kThreads, Cfg<CFG>::kMinBlocks)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
     using F = G<FMT>;
-    constexpr int BN = Cfg<CFG>::BN, kBBoxes = Cfg<CFG>::kBBoxes, NPH = Cfg<CFG>::NPH;
+    constexpr int BN = Cfg<CFG>::BN, kBBoxes = Cfg<CFG>::kBBoxes;
     constexpr uint32_t kTmemCols = Cfg<CFG>::kTmemCols;
-    // a converter warp skips NPH / SPS slabs between its stages: at most one ring cycle
-    static_assert(NPH / F::SPS <= F::NR, "raw ring too short for the converter rotation");
-    static_assert(F::SPS > 1 || F::NR % NPH == 0, "one-stage slabs: each ring slot read by one phase");
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
     uint8_t* b_ring = smem;
@@ -577,14 +565,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
     // ring depths for this tile
     const int stages_b = min(kMaxStagesB, kBBoxes / n_boxes);
     const uint32_t acc_cols = (uint32_t)((n_mma + 31) & ~31);
-    // A ring: the columns the accumulator leaves.  With three slots (CFG 0,
-    // tiles of 129-160 tokens) every converter warp works on every stage, each
-    // on half of its K range, so the ring keeps all three slots; otherwise the
-    // NPH warps of a lane quarter take stages in turn and the ring is rounded
-    // down to a multiple of NPH (so a slot always belongs to the same warps).
+    // A ring: the columns the accumulator leaves.  With three slots (tiles of
+    // 129-160 tokens) every converter warp works on every stage, each on half
+    // of its K range, so the ring keeps all three slots; otherwise the two
+    // warps of a lane quarter take alternate stages and the ring is rounded
+    // down to an even count (so a slot always belongs to the same warps).
     const int free_slots = (int)((kTmemCols - acc_cols) / 32);                 // 3 .. 7 (CFG 1: 8 .. 11)
     const bool split_k = free_slots == 3;
-    const int stages_a = split_k ? 3 : min(Cfg<CFG>::MAXA, free_slots) & ~(NPH - 1);   // >= 4 otherwise
+    const int stages_a = split_k ? 3 : min(kMaxStagesA, free_slots) & ~1;   // >= 4 otherwise
     const int rt = blockIdx.x;
     const int n_tiles_w = a.n / bq::kTileRows, k_slabs = a.k / F::SK;
     const uint8_t* wslab = a.w + bq::slab_index(expert, rt, 0, n_tiles_w, k_slabs) * F::SB;
@@ -594,14 +582,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
     if (threadIdx.x == 0) {
         for (int i = 0; i < kMaxStagesB; ++i) mbar_init(b_full(i), 1);
         for (int j = 0; j < kEmptyRing; ++j) mbar_init(empty(j), 1);
-        // split K: all converter warps read every slab and write every stage;
-        // in turn: a slab is read by the warps of the min(SPS, NPH) phases
-        // whose stages fall in it (4 quarters each), a stage written by 4 warps
+        // a slab of one stage is read by the 4 warps of that stage's parity, longer slabs by all 8
+        // split K: all 8 converter warps read every slab and write every stage;
+        // alternating: a slab of one stage is read by the 4 warps of that stage's parity
         for (int i = 0; i < F::NR; ++i) {
             mbar_init(raw_full(i), 1);
-            mbar_init(raw_empty(i), 32 * (split_k ? 4 * NPH : 4 * min(F::SPS, NPH)));   // every converter lane arrives
+            mbar_init(raw_empty(i), 32 * (split_k || F::SPS > 1 ? 8 : 4));   // every converter lane arrives
         }
-        for (int i = 0; i < kMaxStagesA; ++i) mbar_init(a_full(i), 32 * (split_k ? 4 * NPH : 4));
+        for (int i = 0; i < kMaxStagesA; ++i) mbar_init(a_full(i), 32 * (split_k ? 8 : 4));
         mbar_init(acc_full, 1);
         *abort_flag = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -707,12 +695,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
         }
     } else {
         // ------------------------------------------------ converters, then epilogue
-        const int quarter = warp & 3, phase = (warp - kFirstConvWarp) >> 2;   // phase < NPH
+        const int quarter = warp & 3, half = (warp - kFirstConvWarp) >> 2;
         const int p = 32 * quarter + lane;                       // weight row = TMEM lane
         const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
         bool ok = true;
         if (split_k) {
-            // every stage: this warp converts K values 32*phase .. +31 of it (NPH = 2);
+            // every stage: this warp converts K values 32*half .. +31 of it;
             // r / pr: raw-ring slot and phase of the stage's slab
             int sa = 0, sub = 0, r = 0;
             uint32_t pr = 0;
@@ -722,8 +710,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
                     !(ok = warp_wait_all(empty(ks - stages_a), empty_parity(ks - stages_a), abort_flag, a.status, a.wait_limit_ns)))
                     break;
                 uint32_t v[16];
-                dequant_half<FMT>(raw_ring + r * F::SB, p, sub, phase, v);
-                tmem_st16(tmem + lane_base + a_col0 + 32u * sa + 16u * phase, v);
+                dequant_half<FMT>(raw_ring + r * F::SB, p, sub, half, v);
+                tmem_st16(tmem + lane_base + a_col0 + 32u * sa + 16u * half, v);
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
                 // every lane arrives (after its own fence): no warp barrier needed
@@ -736,15 +724,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
                 }
             }
         }
-        // otherwise this warp converts stages ks = phase, phase + NPH, ...; sa = A-ring slot of ks
-        int sa = phase;
+        // otherwise this warp converts stages ks = half, half + 2, ...; sa = A-ring slot of ks
+        int sa = half;
         // r / pr: raw-ring slot and phase of slab ks / SPS, advanced with ks
-        int r = (phase / F::SPS) % F::NR;
+        int r = (half / F::SPS) % F::NR;
         uint32_t pr = 0;
-        for (int ks = phase; !split_k && ks < KS; ks += NPH) {
+        for (int ks = half; !split_k && ks < KS; ks += 2) {
             const int sub = ks % F::SPS;
             // first stage of the slab this warp converts: wait for the slab
-            if (sub == phase % F::SPS && !(ok = warp_wait_all(raw_full(r), pr, abort_flag, a.status, a.wait_limit_ns))) break;
+            if ((F::SPS == 1 || sub == half) && !(ok = warp_wait_all(raw_full(r), pr, abort_flag, a.status, a.wait_limit_ns))) break;
             if (ks >= stages_a &&
                 !(ok = warp_wait_all(empty(ks - stages_a), empty_parity(ks - stages_a), abort_flag, a.status, a.wait_limit_ns)))
                 break;
@@ -755,19 +743,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
             tc_fence_before();
             // every lane arrives (after its own fence); last stage of the slab
             // this warp converts: release the slab
-            if (sub + NPH >= F::SPS) mbar_arrive(raw_empty(r));
+            if (F::SPS == 1 || sub >= F::SPS - 2) mbar_arrive(raw_empty(r));
             mbar_arrive(a_full(sa));
-            sa += NPH;
+            sa += 2;
             if (sa >= stages_a) sa -= stages_a;
-            r += (ks + NPH) / F::SPS - ks / F::SPS;   // slabs advanced: 0 .. NPH (<= NR)
+            r += (ks + 2) / F::SPS - ks / F::SPS;   // slabs advanced: 0, 1 or 2 (< NR)
             if (r >= F::NR) { r -= F::NR; pr ^= 1u; }
         }
         if (ok && warp_wait(acc_full, 0, abort_flag, a.status, a.wait_limit_ns)) {
             tc_fence_after();
             const int rt64 = 64 * rt + 16 * quarter + (lane & 15);   // SwiGLU feature
             const int frow = bq::kTileRows * rt + p;                  // plain output feature
-            // the NPH warps of a lane quarter take 32-column chunks in turn
-            for (int c0 = 32 * phase; c0 < nvalid; c0 += 32 * NPH) {
+            // the two warps of a lane quarter take alternate 32-column chunks
+            for (int c0 = 32 * half; c0 < nvalid; c0 += 64) {
                 uint32_t v[32];
                 tmem_ld32(tmem + lane_base + (uint32_t)c0, v);
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -894,7 +882,7 @@ void launch_one(const CUtensorMap& map, const GemmArgs& a, dim3 grid, cudaStream
         cudaFuncSetAttribute(gemm_kernel<FMT, EPI, CFG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<CFG>());
         attr_set[dev] = true;
     }
-    gemm_kernel<FMT, EPI, CFG><<<grid, threads<CFG>(), smem_bytes<CFG>(), st>>>(map, a);
+    gemm_kernel<FMT, EPI, CFG><<<grid, kThreads, smem_bytes<CFG>(), st>>>(map, a);
     bq::note_launch();
 }
 
