@@ -44,24 +44,11 @@
 
 namespace {
 
+constexpr int BN = 160;            // max token rows per tile (MMA N)
 constexpr int BK = 64;             // K per stage (one 128-byte swizzle row of fp16)
 constexpr int kBoxRows = 32;       // activation rows per TMA box (4 KB)
-constexpr int kMaxStagesB = 15;    // activation ring: at most 15 stages in flight
-// Two tile shapes:
-//  - CFG 0: tiles of up to 160 token rows, two CTAs per SM (256 TMEM columns
-//    each: a <= 160-column accumulator and a 3-6 slot A ring), 15 activation
-//    boxes (15 stages of 32 rows .. 3 of 160);
-//  - CFG 1 (expert segments of more than 160 tokens): tiles of up to 256
-//    token rows, one CTA per SM with all 512 TMEM columns (256-column
-//    accumulator, 6 A slots), 32 activation boxes (6 stages of 160 rows .. 4
-//    of 256).  One MMA of N = 256 per K step: the dequantisation and the ring
-//    bookkeeping of a stage serve 1.6x the FLOPs.
-template <int CFG> struct Cfg;
-template <> struct Cfg<0> { static constexpr int BN = 160, kBBoxes = 15, kMinBlocks = 2; static constexpr uint32_t kTmemCols = 256; };
-template <> struct Cfg<1> { static constexpr int BN = 256, kBBoxes = 32, kMinBlocks = 1; static constexpr uint32_t kTmemCols = 512; };
-constexpr int BN = Cfg<0>::BN;           // the work queue's chunk of a segment for CFG 0
-constexpr int kBigBN = Cfg<1>::BN;
-constexpr int kBigMinRows = 161;         // segments with at least this many rows go to CFG 1
+constexpr int kBBoxes = 15;        // activation ring capacity in boxes: 15 stages of 32 rows .. 3 of 160
+constexpr int kMaxStagesB = kBBoxes;
 // TMEM A ring: whatever the accumulator leaves of 256 columns, rounded down to
 // an even count so that every slot is always written by the same converter warps
 constexpr int kMaxStagesA = 6;
@@ -69,6 +56,7 @@ constexpr int kMaxRawSlabs = 4;    // raw quantised slabs in shared memory (per 
 constexpr int kConvWarps = 8;      // two per TMEM lane quarter, alternating stages
 constexpr int kFirstConvWarp = 3;  // warp 0: activation producer, 1: MMA, 2: weight producer
 constexpr int kThreads = 32 * (kFirstConvWarp + kConvWarps);
+constexpr uint32_t kTmemCols = 256;
 constexpr int kBoxBytes = kBoxRows * 128;
 constexpr int kRawBytes = 34816;   // raw slab ring: 4 Q8_0 / 3 Q2_K / 3 int4 slabs
 // One "stage consumed" barrier per K stage, in a ring of 16 (a commit of the
@@ -77,8 +65,7 @@ constexpr int kRawBytes = 34816;   // raw slab ring: 4 Q8_0 / 3 Q2_K / 3 int4 sl
 constexpr int kEmptyRing = 16;
 static_assert(kMaxStagesA <= kEmptyRing && kMaxStagesB < kEmptyRing && kEmptyRing % 2 == 0, "empty ring");
 constexpr int kNumBars = kMaxStagesB + 2 * kMaxRawSlabs + kMaxStagesA + kEmptyRing + 1;
-template <int CFG>
-constexpr int smem_bytes() { return 1024 + Cfg<CFG>::kBBoxes * kBoxBytes + kRawBytes + 8 * kNumBars + 64; }
+constexpr int kSmemBytes = 1024 + kBBoxes * kBoxBytes + kRawBytes + 8 * kNumBars + 64;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s, unless a test sets another limit
 
 template <int FMT> struct G;
@@ -520,12 +507,10 @@ __device__ __forceinline__ void dequant_half<BQ_FMT_FP8_B128>(const uint8_t* raw
 __device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
 // ---------------------------------------------------------------- the kernel
-template <int FMT, int EPI, int CFG>
-__global__ void __launch_bounds__(kThreads, Cfg<CFG>::kMinBlocks)
+template <int FMT, int EPI>
+__global__ void __launch_bounds__(kThreads, 2)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
     using F = G<FMT>;
-    constexpr int BN = Cfg<CFG>::BN, kBBoxes = Cfg<CFG>::kBBoxes;
-    constexpr uint32_t kTmemCols = Cfg<CFG>::kTmemCols;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
     uint8_t* b_ring = smem;
@@ -570,7 +555,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
     // of its K range, so the ring keeps all three slots; otherwise the two
     // warps of a lane quarter take alternate stages and the ring is rounded
     // down to an even count (so a slot always belongs to the same warps).
-    const int free_slots = (int)((kTmemCols - acc_cols) / 32);                 // 3 .. 7 (CFG 1: 8 .. 11)
+    const int free_slots = (int)((kTmemCols - acc_cols) / 32);                 // 3 .. 7
     const bool split_k = free_slots == 3;
     const int stages_a = split_k ? 3 : min(kMaxStagesA, free_slots) & ~1;   // >= 4 otherwise
     const int rt = blockIdx.x;
@@ -808,19 +793,17 @@ __global__ void gather_rows_kernel(const __half* __restrict__ x, const int32_t* 
     for (int i = lane; i < cols / 8; i += 32) d[i] = __ldg(s + i);
 }
 
-// Token-chunk tiles of the active segments with lo <= count <= hi, in
-// segment order (the per-expert work queue): a segment of c rows becomes
-// ceil(c/bn) chunks of near-equal size.  One CTA of 1024 threads; <= 1024
-// segments.
+// Token-chunk tiles of every active segment, in segment order (the
+// per-expert work queue): a segment of c rows becomes ceil(c/BN) chunks of
+// near-equal size.  One CTA of 1024 threads; <= 1024 segments.
 __global__ void __launch_bounds__(1024)
-tile_list_kernel(const int32_t* __restrict__ seg_count, const int32_t* __restrict__ n_segments, int lo, int hi,
-                 int bn, int4* __restrict__ tiles, int32_t* __restrict__ n_tiles) {
+tile_list_kernel(const int32_t* __restrict__ seg_count, const int32_t* __restrict__ n_segments,
+                 int4* __restrict__ tiles, int32_t* __restrict__ n_tiles) {
     __shared__ int32_t warp_sums[32];
     const int s = threadIdx.x;
     const int ns = *n_segments;
-    int cnt = s < ns ? seg_count[s] : 0;
-    if (cnt < lo || cnt > hi) cnt = 0;
-    const int c = (cnt + bn - 1) / bn;
+    const int cnt = s < ns ? seg_count[s] : 0;
+    const int c = (cnt + BN - 1) / BN;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = c;
 #pragma unroll
@@ -872,41 +855,35 @@ bool make_act_map(CUtensorMap* map, const __half* base, int rows, int cols) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int FMT, int EPI, int CFG>
+template <int FMT, int EPI>
 void launch_one(const CUtensorMap& map, const GemmArgs& a, dim3 grid, cudaStream_t st) {
     // per device: the attribute is a property of the function on the current device
     static bool attr_set[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        cudaFuncSetAttribute(gemm_kernel<FMT, EPI, CFG>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<CFG>());
+        cudaFuncSetAttribute(gemm_kernel<FMT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         attr_set[dev] = true;
     }
-    gemm_kernel<FMT, EPI, CFG><<<grid, kThreads, smem_bytes<CFG>(), st>>>(map, a);
+    gemm_kernel<FMT, EPI><<<grid, kThreads, kSmemBytes, st>>>(map, a);
     bq::note_launch();
 }
 
-template <int EPI, int CFG>
+template <int EPI>
 void launch_epi(int fmt, const CUtensorMap& map, const GemmArgs& a, dim3 grid, cudaStream_t st) {
     switch (fmt) {
-        case BQ_FMT_Q8_0: launch_one<BQ_FMT_Q8_0, EPI, CFG>(map, a, grid, st); break;
-        case BQ_FMT_Q2_K: launch_one<BQ_FMT_Q2_K, EPI, CFG>(map, a, grid, st); break;
-        case BQ_FMT_MXFP4: launch_one<BQ_FMT_MXFP4, EPI, CFG>(map, a, grid, st); break;
-        case BQ_FMT_FP8_B128: launch_one<BQ_FMT_FP8_B128, EPI, CFG>(map, a, grid, st); break;
-        default: launch_one<BQ_FMT_INT4_G64, EPI, CFG>(map, a, grid, st); break;
+        case BQ_FMT_Q8_0: launch_one<BQ_FMT_Q8_0, EPI>(map, a, grid, st); break;
+        case BQ_FMT_Q2_K: launch_one<BQ_FMT_Q2_K, EPI>(map, a, grid, st); break;
+        case BQ_FMT_MXFP4: launch_one<BQ_FMT_MXFP4, EPI>(map, a, grid, st); break;
+        case BQ_FMT_FP8_B128: launch_one<BQ_FMT_FP8_B128, EPI>(map, a, grid, st); break;
+        default: launch_one<BQ_FMT_INT4_G64, EPI>(map, a, grid, st); break;
     }
 }
 
-template <int CFG>
-void launch_cfg(int fmt, int epi, const CUtensorMap& map, const GemmArgs& a, dim3 grid, cudaStream_t st) {
-    if (epi == EPI_SWIGLU) launch_epi<EPI_SWIGLU, CFG>(fmt, map, a, grid, st);
-    else if (epi == EPI_SCALE) launch_epi<EPI_SCALE, CFG>(fmt, map, a, grid, st);
-    else launch_epi<EPI_PLAIN, CFG>(fmt, map, a, grid, st);
-}
-
-void launch(int fmt, int epi, const CUtensorMap& map, const GemmArgs& a, dim3 grid, cudaStream_t st, int cfg = 0) {
-    if (cfg) launch_cfg<1>(fmt, epi, map, a, grid, st);
-    else launch_cfg<0>(fmt, epi, map, a, grid, st);
+void launch(int fmt, int epi, const CUtensorMap& map, const GemmArgs& a, dim3 grid, cudaStream_t st) {
+    if (epi == EPI_SWIGLU) launch_epi<EPI_SWIGLU>(fmt, map, a, grid, st);
+    else if (epi == EPI_SCALE) launch_epi<EPI_SCALE>(fmt, map, a, grid, st);
+    else launch_epi<EPI_PLAIN>(fmt, map, a, grid, st);
 }
 
 // Test hook (bq_test_set_wait_probe): the wait bound and the "no weight
@@ -939,35 +916,24 @@ bq_status dense_gemm(const bq_qweight* w, int m, const __half* x, int epi, float
     return BQ_OK;
 }
 
-// Workspace the routed GEMMs add to the MoE carve-up: the two tile lists
-// (segments of at most 160 rows; longer segments in chunks of at most 256)
-// and X_perm.
+// Workspace the routed GEMMs add to the MoE carve-up.
 struct GemmWs {
-    int4 *tiles, *tiles_big;
-    int32_t *n_tiles, *n_tiles_big;
+    int4* tiles;
+    int32_t* n_tiles;
     __half* x_perm;
     size_t bytes;
 };
 
 size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
 
-// Tiles the two lists can hold: each segment of <= 160 rows is one tile; a
-// longer segment of c rows is ceil(c / 256) < c / 160 + 1 chunks.
-int max_tiles_small(const bq_moe_desc* d) { return std::min(d->n_experts, d->T * d->topk); }
-int max_tiles_big(const bq_moe_desc* d) {
-    const int P = d->T * d->topk;
-    return std::min(d->n_experts, P / kBigMinRows) + (P + kBigBN - 1) / kBigBN;
-}
-
 GemmWs carve(const bq_moe_desc* d, uint8_t* base) {
     const size_t P = (size_t)d->T * d->topk;
+    const size_t max_tiles = std::min<size_t>(d->n_experts, P) + (P + BN - 1) / BN;
     GemmWs g;
     size_t off = 0;
     auto take = [&](size_t bytes) { uint8_t* p = base ? base + off : nullptr; off += up256(bytes); return p; };
-    g.tiles = (int4*)take((size_t)max_tiles_small(d) * sizeof(int4));
+    g.tiles = (int4*)take(max_tiles * sizeof(int4));
     g.n_tiles = (int32_t*)take(4);
-    g.tiles_big = (int4*)take((size_t)std::max(1, max_tiles_big(d)) * sizeof(int4));
-    g.n_tiles_big = (int32_t*)take(4);
     g.x_perm = (__half*)take(P * (size_t)d->hidden * 2);
     g.bytes = off;
     return g;
@@ -993,11 +959,9 @@ void launch_gemm_moe_prepare(const bq_moe_desc* d, const __half* x, const int32_
                              const int32_t* seg_count, const int32_t* n_segments, uint8_t* ws, cudaStream_t st) {
     const int P = d->T * d->topk, H = d->hidden;
     GemmWs g = carve(d, ws);
-    tile_list_kernel<<<1, 1024, 0, st>>>(seg_count, n_segments, 1, kBigMinRows - 1, BN, g.tiles, g.n_tiles);
-    tile_list_kernel<<<1, 1024, 0, st>>>(seg_count, n_segments, kBigMinRows, 0x7fffffff, kBigBN, g.tiles_big,
-                                         g.n_tiles_big);
+    tile_list_kernel<<<1, 1024, 0, st>>>(seg_count, n_segments, g.tiles, g.n_tiles);
     gather_rows_kernel<<<(P + 7) / 8, 256, 0, st>>>(x, perm_token, P, H, g.x_perm);
-    note_launch(3);
+    note_launch(2);
 }
 
 bq_status launch_gemm_moe(const bq_moe_desc* d, const __half*, const int32_t*, const float* perm_gate,
@@ -1006,35 +970,26 @@ bq_status launch_gemm_moe(const bq_moe_desc* d, const __half*, const int32_t*, c
                      cudaStream_t st) {
     const int P = d->T * d->topk, H = d->hidden, I = d->inter;
     GemmWs g = carve(d, ws);
-    const int mts = max_tiles_small(d), mtb = max_tiles_big(d);
+    const int max_tiles = std::min(d->n_experts, P) + (P + BN - 1) / BN;
 
-    // long segments first (one CTA per SM, 256-row tiles), then the rest
     stage_begin(BQ_STAGE_GATE_UP, st);
     CUtensorMap map_x;
     if (!make_act_map(&map_x, g.x_perm, P, H)) return map_fail();
     GemmArgs a = base_args(&d->w_gate_up);
+    a.tiles = g.tiles; a.n_tiles = g.n_tiles;
     a.seg_expert = seg_expert; a.seg_start = seg_start; a.seg_count = seg_count;
     a.h = h; a.ldh = I;
-    if (mtb > 0) {
-        a.tiles = g.tiles_big; a.n_tiles = g.n_tiles_big;
-        launch(d->w_gate_up.fmt, EPI_SWIGLU, map_x, a, dim3(2 * I / kTileRows, mtb), st, 1);
-    }
-    a.tiles = g.tiles; a.n_tiles = g.n_tiles;
-    launch(d->w_gate_up.fmt, EPI_SWIGLU, map_x, a, dim3(2 * I / kTileRows, mts), st);
+    launch(d->w_gate_up.fmt, EPI_SWIGLU, map_x, a, dim3(2 * I / kTileRows, max_tiles), st);
     stage_end(BQ_STAGE_GATE_UP, st);
 
     stage_begin(BQ_STAGE_DOWN, st);
     CUtensorMap map_h;
     if (!make_act_map(&map_h, h, P, I)) return map_fail();
     GemmArgs b = base_args(&d->w_down);
+    b.tiles = g.tiles; b.n_tiles = g.n_tiles;
     b.seg_expert = seg_expert; b.seg_start = seg_start; b.seg_count = seg_count;
     b.y = y_slot; b.ldy = H; b.row_scale = perm_gate;
-    if (mtb > 0) {
-        b.tiles = g.tiles_big; b.n_tiles = g.n_tiles_big;
-        launch(d->w_down.fmt, EPI_SCALE, map_h, b, dim3(H / kTileRows, mtb), st, 1);
-    }
-    b.tiles = g.tiles; b.n_tiles = g.n_tiles;
-    launch(d->w_down.fmt, EPI_SCALE, map_h, b, dim3(H / kTileRows, mts), st);
+    launch(d->w_down.fmt, EPI_SCALE, map_h, b, dim3(H / kTileRows, max_tiles), st);
     stage_end(BQ_STAGE_DOWN, st);
     return BQ_OK;
 }
