@@ -32,6 +32,12 @@ SMALL = [
     _case("q2k_t32_shared", "q2_k", 32, 512, 256, 8, 3, shared="q8_0"),
     # first size on the tensor-core path
     _case("mxfp4_t33", "mxfp4", 33, 256, 128, 4, 4),
+    # segments cut into several token chunks by the work queue: one expert of
+    # 600 rows (4 chunks of 150), long and short experts side by side with a
+    # shared expert, ~267-row FP8 segments (2 chunks each)
+    _case("int4_e1_600", "int4", 600, 256, 128, 1, 1),
+    _case("q2k_long_and_short", "q2_k", 260, 512, 256, 3, 2, zipf=True, shared="q8_0"),
+    _case("fp8_long_segments", "fp8_b128", 400, 256, 256, 3, 2),
 ]
 
 
