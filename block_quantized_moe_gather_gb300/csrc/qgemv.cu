@@ -20,6 +20,11 @@
 // publishes a partial, and the last one to finish sums them in split order,
 // so results stay bit-reproducible.
 //
+// Q2_K routed-expert GEMVs (the decode MoE path) take a split-scale variant
+// (see "Q2_K with split scales" below): codes ANDed into fp16 subnormals,
+// times the sub-block scale in one exact packed multiply, the activations
+// staged once per CTA in shared memory; 27% fewer instructions per weight.
+//
 // K ordering inside a slab: lane t of a quad owns the contiguous quarter
 // [t*SK/4, (t+1)*SK/4) of the slab's K range; MMA step s takes the four
 // values [4s, 4s+4) of every lane's quarter.  The activation fragment is
@@ -152,6 +157,188 @@ __device__ __forceinline__ Q2Scales q2_scales(uint32_t sc4, uint32_t dm) {
         r.nm[j] = __hmul2_rn(nmin2, field_h2<4>(b, 0x000F000Fu));
     }
     return r;
+}
+
+// ---- Q2_K with split scales (activations staged in shared memory).
+//
+// A 2-bit code q at bit J of its 16-bit lane, ANDed out, is the fp16
+// subnormal q * 2^(J - 24); one packed multiply by the sub-block scale sc
+// (0..15) gives q * sc * 2^(J - 24) exactly.  The activations are staged per
+// (slab, token) as fp16(x * 2^(S - J)), where 2^S brings the largest |x| of
+// the slab's 256 values to [256, 512) (normal fp16 numbers, exact wherever
+// x * 2^S is), so every MMA product is q * sc * x * 2^(S - 24).  Each slab (one
+// 256-value super-block per row) is accumulated on its own and added as
+// 2^-S (d * 2^24 * cm - dmin * cmin), cmin being two more MMAs of the sub-block
+// minima m with the staged sub-block sums 2^S * sum(x), each held as an fp16
+// pair hi + lo (about 22 significant bits: the minimum term largely cancels
+// against the main one, and sums rounded once to fp16 would cost 3-7x the
+// error of the rest).  This takes two instructions per pair of weights instead
+// of three, and the weight is never rounded.
+//
+// Stage layout per slab of the CTA's K share (kQ2sSlabBytes):
+//   [0, 4096)     x:   [8 step pairs][4 quarters t][8 token slots] x 16 B
+//                      (steps 2j, 2j + 1 of quarter t: one 16-byte B load)
+//   [4096, 4352)  sums, hi: [4 quarters t][8 token slots] x 4 fp16 (sub-blocks 4t .. 4t + 3)
+//   [4352, 4608)  sums, lo: the same layout, fp16(sum - hi)
+//   [4608, 4640)  2^-S per token slot (fp32)
+// Token slots >= the group's token count are never written: they only feed
+// MMA columns that no epilogue stores.
+constexpr int kQ2sXsBytes = 4096;
+constexpr int kQ2sSsBytes = 256;   // one of the hi / lo halves
+constexpr int kQ2sSlabBytes = kQ2sXsBytes + 2 * kQ2sSsBytes + 32;
+constexpr int kQ2sMaxSlabs = 22;   // 100 KB: two CTAs still fit on an SM
+
+// Bit position of pair p (values 2p, 2p + 1) of a Q2_K sub-block word.
+__host__ __device__ constexpr int q2_j(int p) { return p < 5 ? 2 * p : 2 * (p - 5); }
+
+// Pair p as fp16 subnormals q * 2^(J(p) - 24) (wh = the word shifted right by 10).
+__device__ __forceinline__ uint32_t q2_code(uint32_t w, uint32_t wh, int p) {
+    switch (p) {
+        case 0: return w & 0x00030003u;
+        case 1: return w & 0x000C000Cu;
+        case 2: return w & 0x00300030u;
+        case 3: return w & 0x00C000C0u;
+        case 4: return w & 0x03000300u;
+        case 5: return wh & 0x00030003u;
+        case 6: return wh & 0x000C000Cu;
+        default: return wh & 0x00300030u;
+    }
+}
+
+// Stages the rows of one token group (list rows row0 .. row0 + ntok - 1,
+// gathered through src_row) for the slabs [ks_lo, ks_lo + share).  A unit is
+// (slab i, token g, quarter t): 64 values, one thread; the four quarters of a
+// (slab, token) sit in adjacent lanes and combine their maxima by shuffles.
+// The values are read twice (the second time from L1), one sub-block at a
+// time, so that few of them are live at once.
+__device__ __forceinline__ void q2s_stage(const bq::QgemvParams& p, int row0, int ntok, int ks_lo, int share,
+                                          uint8_t* stage) {
+    const int units = share * ntok * 4;
+    const int lane = threadIdx.x & 31;
+    for (int ub = threadIdx.x & ~31; ub < units; ub += kThreads) {   // warp-uniform bound (shuffles below)
+        const int u = ub + lane;
+        const bool live = u < units;
+        const int t = u & 3, gi = u >> 2, g = gi % ntok, i = gi / ntok;
+        const uint4* xp = nullptr;
+        __half2 m2 = __float2half2_rn(0.f);
+        if (live) {
+            const int lr = row0 + g;
+            const int src = p.src_row ? __ldg(p.src_row + lr) : lr;
+            xp = reinterpret_cast<const uint4*>(p.x + (int64_t)src * p.k + (int64_t)(ks_lo + i) * 256 + 64 * t);
+#pragma unroll
+            for (int v8 = 0; v8 < 8; ++v8) {
+                const uint4 q = __ldg(xp + v8);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) m2 = __hmax2(m2, __habs2(bq::u32_as_h2(comp(q, j))));
+            }
+        }
+        float mx = fmaxf(__low2float(m2), __high2float(m2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        if (!live) continue;
+        // 2^S * max in [256, 512); max is an fp16 value, a normal fp32 number
+        const int S = (mx > 0.f && mx <= 65504.f) ? 8 - ((__float_as_int(mx) >> 23) - 127) : 0;
+        const float fs = __int_as_float((127 + S) << 23);
+        uint8_t* sl = stage + i * kQ2sSlabBytes;
+#pragma unroll 1
+        for (int sb = 0; sb < 4; ++sb) {   // values 16 sb .. + 15 of the quarter = steps 4 sb .. 4 sb + 3
+            float sum = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {   // 16 bytes: steps 4 sb + 2h, + 1 (step pair 2 sb + h)
+                const uint4 q = __ldg(xp + 2 * sb + h);
+                uint32_t o[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {   // word j: elements 2 (j & 1), + 1 of step 4 sb + 2h + j / 2
+                    const int J = q2_j(2 * (2 * h + (j >> 1)) + (j & 1));
+                    const float f = __int_as_float((127 + S - J) << 23);   // 2^(S - J), exact
+                    const float2 xf = __half22float2(bq::u32_as_h2(comp(q, j)));
+                    sum += xf.x + xf.y;
+                    o[j] = bq::h2_as_u32(__floats2half2_rn(xf.x * f, xf.y * f));
+                }
+                *reinterpret_cast<uint4*>(sl + (((2 * sb + h) * 4 + t) * 8 + g) * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            const float ss = sum * fs;
+            const __half hi = __float2half_rn(ss);
+            reinterpret_cast<__half*>(sl + kQ2sXsBytes + (t * 8 + g) * 8)[sb] = hi;
+            reinterpret_cast<__half*>(sl + kQ2sXsBytes + kQ2sSsBytes + (t * 8 + g) * 8)[sb] =
+                __float2half_rn(ss - __half2float(hi));
+        }
+        if (t == 0) reinterpret_cast<float*>(sl + kQ2sXsBytes + 2 * kQ2sSsBytes)[g] = __int_as_float((127 - S) << 23);
+    }
+}
+
+// Shared-memory reads at 32-bit shared addresses, issued where written:
+// the second tile's reads of the same B fragments must not be merged with
+// the first's (that would keep all of them live in registers).
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a));
+    return r;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 r;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(a));
+    return r;
+}
+
+// One slab on the split-scale path: B fragments from the stage at shared
+// address `sl`.  One m16 tile at a time (its code words, scales and slab
+// accumulator), so that the three-slab register ring still fits; the tile's
+// B fragments are read from shared memory again for the second tile.
+__device__ __forceinline__ void mma_slab_q2s(const Frag<BQ_FMT_Q2_K>& f, uint32_t sl, int g, int t,
+                                             float (&acc)[2][4]) {
+    const uint32_t xl = sl + (t * 8 + g) * 16;   // + step pair * 512
+#pragma unroll
+    for (int tile = 0; tile < 2; ++tile) {
+        float cm[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int sb = 0; sb < 4; ++sb) {
+            __half2 sc[2];
+            uint32_t w[2], wh[2];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                // byte sb of the scale word (sub-block 4t + sb) in both lanes; its low nibble is sc
+                sc[hh] = field_h2<0>(__byte_perm(f.sc[tile][hh], 0u, (uint32_t)(sb | (sb << 8))), 0x000F000Fu);
+                w[hh] = comp(f.q[tile][hh], sb);
+                wh[hh] = w[hh] >> 10;
+            }
+#pragma unroll
+            for (int s2h = 0; s2h < 2; ++s2h) {
+                const uint4 bv = lds128(xl + (2 * sb + s2h) * 512);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int s4 = 2 * s2h + e;
+                    uint32_t a[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {   // r = hh + 2 * lohi
+                        const int hh = r & 1, pr = 2 * s4 + (r >> 1);
+                        a[r] = bq::h2_as_u32(__hmul2_rn(bq::u32_as_h2(q2_code(w[hh], wh[hh], pr)), sc[hh]));
+                    }
+                    mma16816(cm, a, e ? bv.z : bv.x, e ? bv.w : bv.y);
+                }
+            }
+        }
+        // minimum term: A = m of sub-blocks (4t, 4t + 1) and (4t + 2, 4t + 3), B = their staged sums
+        uint32_t am[4];
+        am[0] = bq::h2_as_u32(field_h2<4>(__byte_perm(f.sc[tile][0], 0u, 0x4140u), 0x000F000Fu));
+        am[1] = bq::h2_as_u32(field_h2<4>(__byte_perm(f.sc[tile][1], 0u, 0x4140u), 0x000F000Fu));
+        am[2] = bq::h2_as_u32(field_h2<4>(__byte_perm(f.sc[tile][0], 0u, 0x4342u), 0x000F000Fu));
+        am[3] = bq::h2_as_u32(field_h2<4>(__byte_perm(f.sc[tile][1], 0u, 0x4342u), 0x000F000Fu));
+        const uint2 bh = lds64(sl + kQ2sXsBytes + (t * 8 + g) * 8);
+        const uint2 bl = lds64(sl + kQ2sXsBytes + kQ2sSsBytes + (t * 8 + g) * 8);
+        float cmin[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816(cmin, am, bl.x, bl.y);
+        mma16816(cmin, am, bh.x, bh.y);
+        const uint2 usb = lds64(sl + kQ2sXsBytes + 2 * kQ2sSsBytes + 8 * t);   // 2^-S of tokens 2t, 2t + 1
+        const float u0 = __uint_as_float(usb.x), u1 = __uint_as_float(usb.y);
+        const float2 f0 = __half22float2(bq::u32_as_h2(f.dm[tile][0]));   // (d, dmin) of row g
+        const float2 f1 = __half22float2(bq::u32_as_h2(f.dm[tile][1]));   // row g + 8
+        const float d0 = f0.x * 16777216.0f, d1 = f1.x * 16777216.0f;     // d * 2^24 (exact)
+        acc[tile][0] = fmaf(u0, fmaf(d0, cm[0], -f0.y * cmin[0]), acc[tile][0]);
+        acc[tile][1] = fmaf(u1, fmaf(d0, cm[1], -f0.y * cmin[1]), acc[tile][1]);
+        acc[tile][2] = fmaf(u0, fmaf(d1, cm[2], -f1.y * cmin[2]), acc[tile][2]);
+        acc[tile][3] = fmaf(u1, fmaf(d1, cm[3], -f1.y * cmin[3]), acc[tile][3]);
+    }
 }
 
 // Multiplies one slab; the lane's activation values of the slab (token g,
@@ -317,12 +504,18 @@ __device__ __forceinline__ void qgemv_epilogue(const bq::QgemvParams& p, const f
 // then normalises its activation fragments as it loads them; the CTAs of
 // row tile 0, row quarter 0 also store the normalised rows of their K share
 // to x_out, so each value is written once.
-template <int FMT, bool SWIGLU, int KW, bool NORM>
+//
+// Q2S (Q2_K only, no norm): the split-scale path above; the CTA's K share of
+// each token group's activations is staged in dynamic shared memory first.
+template <int FMT, bool SWIGLU, int KW, bool NORM, bool Q2S = false>
 __global__ void __launch_bounds__(kThreads, NORM ? 1 : 2)   // the norm-fused GEMV needs more registers
 qgemv_kernel(const bq::QgemvParams p) {
     using T = Traits<FMT>;
     static_assert(KW == 2 || KW == 8, "K ways per CTA");
     static_assert(!(NORM && SWIGLU), "the norm-fused GEMV has a plain epilogue");
+    static_assert(!Q2S || (FMT == BQ_FMT_Q2_K && !NORM), "the split-scale path is Q2_K without the norm");
+    extern __shared__ __align__(16) uint8_t q2s_stage_smem[];
+    const uint32_t stage_addr = static_cast<uint32_t>(__cvta_generic_to_shared(q2s_stage_smem));
     // partials of the warps with K piece > 0: [quarter (KW 2) or piece - 1 (KW 8)][tile][lane][row half]
     __shared__ float2 red[KW == 8 ? 7 : 4][2][32][2];
     __shared__ int s_last;
@@ -364,7 +557,8 @@ qgemv_kernel(const bq::QgemvParams p) {
         }
         // register ring of D slabs in flight (D - 1 ahead of the one being multiplied);
         // the first loads go out before the norm prologue below
-        constexpr int D = T::DEPTH;
+        // (the split-scale path keeps two slabs in flight: a third would not fit the registers)
+        constexpr int D = Q2S ? 2 : T::DEPTH;
         Frag<FMT> f[D];
         const int n = kt_end - kt_begin;
 #pragma unroll
@@ -372,6 +566,10 @@ qgemv_kernel(const bq::QgemvParams p) {
             if (d < n) load_frag<FMT>(f[d], wbase + (int64_t)(kt_begin + d) * T::SB, rowbase, g, t);
         float inv = 0.f;
         __half* xo = nullptr;
+        if constexpr (Q2S) {   // the previous token group's readers of the stage are past the reduction barriers
+            q2s_stage(p, start + tok0, ntok, ks_lo, ks_hi - ks_lo, q2s_stage_smem);
+            __syncthreads();
+        }
         if (NORM) {
             __syncthreads();   // the previous token group is done with s_inv
             bq::rows_inv_rms(p.x + (int64_t)(start + tok0) * p.k, p.k, ntok, p.k, p.eps, s_part, s_inv);
@@ -389,7 +587,9 @@ qgemv_kernel(const bq::QgemvParams p) {
                 if (nxt < n)
                     load_frag<FMT>(f[(d + D - 1) % D], wbase + (int64_t)(kt_begin + nxt) * T::SB, rowbase, g, t);
                 const int kc = (kt_begin + i + d) * T::SK;
-                if (NORM)
+                if constexpr (Q2S)
+                    mma_slab_q2s(f[d], stage_addr + (kt_begin + i + d - ks_lo) * kQ2sSlabBytes, g, t, acc);
+                else if (NORM)
                     mma_frag<FMT, true>(f[d], xrow + kc, xvalid, t, acc, p.gamma + kc, inv, xo ? xo + kc : nullptr);
                 else
                     mma_frag<FMT, false>(f[d], xrow + kc, xvalid, t, acc);
@@ -487,11 +687,29 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
     const int ny = p.grid_groups && !p.seg_expert ? (p.m + 7) / 8 : max_segments;
     const bool quarters = p.ksplit == 1 && !p.seg_expert && tiles * ny < sm_count();
     dim3 grid(tiles * (quarters ? 4 : 1), ny, p.ksplit);
+    // The routed-expert GEMVs of a Q2_K MoE step take the split-scale path when
+    // the CTA's K share fits the stage.  A dense matrix does not: its few CTAs
+    // (K split over the SMs, or 32-row quarters) pay the staging latency, or
+    // stage the same rows four times, for less than they save (measured on
+    // N = K = 4096, m = 1, 8 and 32: 20-120% slower).
+    const int share = (p.k / Traits<FMT>::SK + p.ksplit - 1) / p.ksplit;
+    const bool q2s = FMT == BQ_FMT_Q2_K && p.seg_expert && !p.gamma && share <= kQ2sMaxSlabs;
+    constexpr bool kQ2 = FMT == BQ_FMT_Q2_K;
     auto kernel = p.gamma ? (quarters ? qgemv_kernel<FMT, false, 8, true> : qgemv_kernel<FMT, false, 2, true>)
+                : q2s ? (p.swiglu ? qgemv_kernel<FMT, true, 2, false, kQ2> : qgemv_kernel<FMT, false, 2, false, kQ2>)
                 : quarters ? (p.swiglu ? qgemv_kernel<FMT, true, 8, false> : qgemv_kernel<FMT, false, 8, false>)
                            : (p.swiglu ? qgemv_kernel<FMT, true, 2, false> : qgemv_kernel<FMT, false, 2, false>);
-    if (after_previous) bq::launch_after(kernel, grid, dim3(kThreads), 0, st, p);
-    else kernel<<<grid, kThreads, 0, st>>>(p);
+    const size_t smem = q2s ? (size_t)share * kQ2sSlabBytes : 0;
+    if (q2s) {   // (expert segments: never the quarter CTAs, which serve a dense matrix)
+        static bool attr_set[2] = {false, false};   // per instantiation (swiglu)
+        bool& done = attr_set[p.swiglu ? 1 : 0];
+        if (!done) {
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQ2sMaxSlabs * kQ2sSlabBytes);
+            done = true;
+        }
+    }
+    if (after_previous) bq::launch_after(kernel, grid, dim3(kThreads), smem, st, p);
+    else kernel<<<grid, kThreads, smem, st>>>(p);
 }
 
 }  // namespace

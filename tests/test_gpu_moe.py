@@ -62,6 +62,53 @@ def test_moe_decode_small(lib, base, t):
     assert_close_matmul(run_moe(lib, layer, inp), oracle_moe(inp), f"{case.name} t={t}")
 
 
+@pytest.mark.parametrize("case", [
+    # Q2_K expert GEMVs on the split-scale path: K split over two CTAs per tile
+    # (few CTAs: 4 gate/up row tiles x 2-6 segments, K = 4096)
+    _case("dec_q2k_ksplit_t1", "q2_k", 1, 4096, 256, 16, 2),
+    _case("dec_q2k_ksplit_t3", "q2_k", 3, 4096, 256, 16, 2),
+    # the largest activation stage (22 slabs of K = 5632 in one CTA), and one
+    # slab over it (K = 6144: the register-ring GEMV)
+    _case("dec_q2k_stage_22", "q2_k", 4, 5632, 1024, 12, 4),
+    _case("dec_q2k_stage_24", "q2_k", 4, 6144, 1024, 12, 4),
+], ids=lambda c: c.name)
+def test_moe_decode_q2k_k_shares(lib, case):
+    from helpers import oracle_moe_threaded
+    inp = synth.moe_inputs(case)
+    layer = build_layer(lib, inp)
+    assert_close_matmul(run_moe(lib, layer, inp), oracle_moe_threaded(inp), case.name)
+
+
+@pytest.mark.parametrize("mode", ["tiny", "large", "mixed_rows", "zero_slab"])
+def test_moe_decode_q2k_activation_range(lib, mode):
+    # The split-scale Q2_K GEMV stages each (slab, token) of the activations
+    # with its own power of two: small rows (fp16 subnormals among them), large
+    # rows, rows of very different size side by side, and an all-zero slab
+    # must all match the oracle.  The scales keep the SwiGLU output h, which the
+    # layer holds in fp16, inside fp16's normal range (x * 1e-4 would put h at
+    # ~1e-8, x * 300 past 65504), so that the GEMVs are what is measured.
+    case = _case("dec_q2k_range", "q2_k", 6, 1024, 256, 4, 2)   # 4 experts: segments of several tokens
+    inp = synth.moe_inputs(case)
+    x = inp.x.astype(np.float32)
+    if mode == "tiny":
+        x *= 1e-2
+    elif mode == "large":
+        x *= 10.0
+    elif mode == "mixed_rows":
+        x *= np.array([1e-2, 1.0, 10.0, 3e-2, 5.0, 1.0], dtype=np.float32)[:, None]
+    else:
+        x[:, 256:512] = 0.0   # the second slab of every token
+        x[2, :] = 0.0         # and all of one token
+    inp.x = x.astype(np.float16)
+    layer = build_layer(lib, inp)
+    got = run_moe(lib, layer, inp)
+    ref = oracle_moe(inp)
+    assert_close_matmul(got, ref, mode)
+    live = np.linalg.norm(ref, axis=1) > 0
+    rel = np.linalg.norm(got - ref, axis=1)[live] / np.linalg.norm(ref, axis=1)[live]
+    assert rel.max() <= 4 * 2e-3, (mode, float(rel.max()))   # each token, not just the whole
+
+
 @pytest.mark.parametrize("idx", [2, 6, 8], ids=lambda i: SMALL[i].name)   # Q2_K, MXFP4, FP8 experts
 def test_moe_bit_reproducible(lib, idx):
     case = SMALL[idx]
