@@ -215,7 +215,7 @@ __device__ __forceinline__ void q2s_stage(const bq::QgemvParams& p, int row0, in
                                           uint8_t* stage) {
     const int units = share * ntok * 4;
     const int lane = threadIdx.x & 31;
-    for (int ub = threadIdx.x & ~31; ub < units; ub += kThreads) {   // warp-uniform bound (shuffles below)
+    for (int ub = threadIdx.x & ~31; ub < units; ub += blockDim.x) {   // warp-uniform bound (shuffles below)
         const int u = ub + lane;
         const bool live = u < units;
         const int t = u & 3, gi = u >> 2, g = gi % ntok, i = gi / ntok;
@@ -498,6 +498,9 @@ __device__ __forceinline__ void qgemv_epilogue(const bq::QgemvParams& p, const f
 // fill the GPU, without a K split across CTAs): a CTA covers one 32-row
 // quarter of a tile and its 8 warps take 8 contiguous K pieces; the partials
 // are summed in warp order, so results stay bit-reproducible either way.
+// KW = 1 (the split-scale path): 128 threads, warp w takes row quarter w over
+// the CTA's whole K share; four CTAs fit on an SM, so a grid of a few hundred
+// CTAs is spread over the SMs in steps of a quarter of the old CTA size.
 //
 // NORM (single segment, no SwiGLU): RMSNorm in front of the GEMV.  Every CTA
 // first computes 1/rms of its token rows over the whole K (bq::rows_inv_rms),
@@ -508,20 +511,20 @@ __device__ __forceinline__ void qgemv_epilogue(const bq::QgemvParams& p, const f
 // Q2S (Q2_K only, no norm): the split-scale path above; the CTA's K share of
 // each token group's activations is staged in dynamic shared memory first.
 template <int FMT, bool SWIGLU, int KW, bool NORM, bool Q2S = false>
-__global__ void __launch_bounds__(kThreads, NORM ? 1 : 2)   // the norm-fused GEMV needs more registers
+__global__ void __launch_bounds__(KW == 1 ? 128 : kThreads, NORM ? 1 : (KW == 1 ? 4 : 2))   // (the norm-fused GEMV needs more registers)
 qgemv_kernel(const bq::QgemvParams p) {
     using T = Traits<FMT>;
-    static_assert(KW == 2 || KW == 8, "K ways per CTA");
+    static_assert(KW == 1 || KW == 2 || KW == 8, "K ways per CTA");
     static_assert(!(NORM && SWIGLU), "the norm-fused GEMV has a plain epilogue");
     static_assert(!Q2S || (FMT == BQ_FMT_Q2_K && !NORM), "the split-scale path is Q2_K without the norm");
     extern __shared__ __align__(16) uint8_t q2s_stage_smem[];
     const uint32_t stage_addr = static_cast<uint32_t>(__cvta_generic_to_shared(q2s_stage_smem));
     // partials of the warps with K piece > 0: [quarter (KW 2) or piece - 1 (KW 8)][tile][lane][row half]
-    __shared__ float2 red[KW == 8 ? 7 : 4][2][32][2];
+    __shared__ float2 red[KW == 8 ? 7 : KW == 2 ? 4 : 1][2][32][2];
     __shared__ int s_last;
     __shared__ float s_inv[NORM ? 8 : 1];
     __shared__ float s_part[NORM ? 8 : 1][8];
-    static_assert(!NORM || kThreads == bq::kNormThreads, "the norm prologue is written for 256 threads");
+    static_assert(!NORM || (KW != 1 && kThreads == bq::kNormThreads), "the norm prologue is written for 256 threads");
 
     // launched right behind the kernel that produced the routing / activations
     bq::grid_dependency_wait();
@@ -540,7 +543,7 @@ qgemv_kernel(const bq::QgemvParams p) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int quarter = KW == 8 ? (int)(blockIdx.x & 3) : (warp & 3), rowbase = 32 * quarter;
-    const int kw = KW == 8 ? warp : (warp >> 2);   // this warp's K piece
+    const int kw = KW == 8 ? warp : KW == 2 ? (warp >> 2) : 0;   // this warp's K piece
     // this CTA's share of the slabs (split K), then KW contiguous pieces of it
     const int ks_lo = (int)((int64_t)k_slabs * kp / p.ksplit), ks_hi = (int)((int64_t)k_slabs * (kp + 1) / p.ksplit);
     const int kt_begin = ks_lo + ((ks_hi - ks_lo) * kw + KW - 1) / KW;
@@ -696,7 +699,7 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
     const bool q2s = FMT == BQ_FMT_Q2_K && p.seg_expert && !p.gamma && share <= kQ2sMaxSlabs;
     constexpr bool kQ2 = FMT == BQ_FMT_Q2_K;
     auto kernel = p.gamma ? (quarters ? qgemv_kernel<FMT, false, 8, true> : qgemv_kernel<FMT, false, 2, true>)
-                : q2s ? (p.swiglu ? qgemv_kernel<FMT, true, 2, false, kQ2> : qgemv_kernel<FMT, false, 2, false, kQ2>)
+                : q2s ? (p.swiglu ? qgemv_kernel<FMT, true, 1, false, kQ2> : qgemv_kernel<FMT, false, 1, false, kQ2>)
                 : quarters ? (p.swiglu ? qgemv_kernel<FMT, true, 8, false> : qgemv_kernel<FMT, false, 8, false>)
                            : (p.swiglu ? qgemv_kernel<FMT, true, 2, false> : qgemv_kernel<FMT, false, 2, false>);
     const size_t smem = q2s ? (size_t)share * kQ2sSlabBytes : 0;
@@ -708,19 +711,30 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
             done = true;
         }
     }
-    if (after_previous) bq::launch_after(kernel, grid, dim3(kThreads), smem, st, p);
-    else kernel<<<grid, kThreads, smem, st>>>(p);
+    const int threads = q2s ? 128 : kThreads;
+    if (after_previous) bq::launch_after(kernel, grid, dim3(threads), smem, st, p);
+    else kernel<<<grid, threads, smem, st>>>(p);
 }
 
 }  // namespace
 
 namespace bq {
 
-int qgemv_ksplit(int fmt, int n, int k, int max_segments, int max_tokens) {
+int qgemv_ksplit(int fmt, int n, int k, int max_segments, int max_tokens, bool experts) {
     if (max_tokens > 8 || max_segments <= 0) return 1;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (experts && fmt == BQ_FMT_Q2_K) {
+        // Split-scale expert GEMV (128-thread CTAs, up to four per SM): K is
+        // split until the grid holds about 2.5 CTAs per SM, keeping at least
+        // 4 slabs per CTA, so that all CTAs are resident at once and no SM
+        // gets more than about 1.2x the mean load.
+        const int ctas = (n / kTileRows) * max_segments;
+        const int want = (5 * sms + 2 * ctas - 1) / (2 * ctas);
+        const int k_slabs = k / fmt_info(fmt).slab_k;
+        return std::max(1, std::min(want, std::min(kMaxKsplit, k_slabs / 4)));
+    }
     // About one CTA per SM: a split adds a partial round trip and a last-CTA
     // reduction, and short K shares never fill the register prefetch ring,
     // so K is split only as far as needed to reach the SM count, keeping at
