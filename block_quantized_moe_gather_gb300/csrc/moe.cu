@@ -290,6 +290,41 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
     const int T = d->T, k = d->topk, E = d->n_experts, H = d->hidden, I = d->inter, P = T * k;
     const __half* xh = reinterpret_cast<const __half*>(x);
 
+    // up to kMoeGemvTokens tokens the experts run as GEMVs over their (short) segments;
+    // above, the tensor-core grouped GEMM
+    const bool decode = T <= kMoeGemvTokens || !bq::gemm_supported(d->w_gate_up.fmt);
+
+    // The shared expert runs on a side stream, concurrently with the routed
+    // experts; the combine waits for both.  Prefill (tensor-core GEMMs, which
+    // need only x and keep no counters) forks here, so that the shared GEMMs
+    // also fill the SMs that the routing front end leaves idle.  Decode forks
+    // after the routing kernel, which clears the split-K counters of every
+    // GEMV of the layer, the shared expert's included.
+    int accumulate = 0;
+    std::unique_lock<std::mutex> side_lock;
+    SideStream* side = nullptr;
+    auto fork_side = [&]() -> cudaStream_t {
+        side_lock = std::unique_lock<std::mutex>(g_side_mutex);
+        side = side_stream();
+        if (side && cudaEventRecord(side->fork, st) == cudaSuccess &&
+            cudaStreamWaitEvent(side->stream, side->fork, 0) == cudaSuccess)
+            return side->stream;
+        side = nullptr;
+        return st;
+    };
+    const bool shared_gemm = d->shared_gate_up && T > kMoeGemvTokens && bq::gemm_supported(d->shared_gate_up->fmt);
+    if (shared_gemm) {
+        const cudaStream_t ss = fork_side();
+        bq::stage_begin(BQ_STAGE_SHARED, ss);
+        if ((s = bq::launch_gemm_shared(d->shared_gate_up, d->shared_down, T, xh, w.h_shared, y,
+                                        d->shared_gate_up->n / 2, base + w.bytes, ss)) != BQ_OK)
+            return s;
+        bq::stage_end(BQ_STAGE_SHARED, ss);
+        if (side && cudaEventRecord(side->join, ss) != cudaSuccess)
+            return bq::fail(BQ_ERR_CUDA, "bq_moe_gather_qmm: cudaEventRecord on the side stream failed");
+        accumulate = 1;
+    }
+
     bq::stage_begin(BQ_STAGE_ROUTE_PERMUTE, st);
     if (bq::route_permute_small_ok(T, k)) {
         const bq::MoeRouting r{w.ids, w.gate, w.counts, w.offsets, w.perm_token, w.perm_slot, w.perm_gate,
@@ -305,28 +340,14 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
         bq::note_launch();
     }
     const int max_segments = min(E, P);
-    // up to kMoeGemvTokens tokens the experts run as GEMVs over their (short) segments;
-    // above, the tensor-core grouped GEMM
-    const bool decode = T <= kMoeGemvTokens || !bq::gemm_supported(d->w_gate_up.fmt);
     // the GEMM path's gather of X_perm is the last part of the permute step
     if (!decode) bq::launch_gemm_moe_prepare(d, xh, w.perm_token, w.seg_count, w.n_segments, base + w.bytes, st);
     bq::stage_end(BQ_STAGE_ROUTE_PERMUTE, st);
 
-    // Decode: the shared expert's two GEMVs run on a side stream, concurrently
-    // with the routed experts (neither fills the GPU at these sizes); the
-    // combine waits for both.
-    int accumulate = 0;
-    std::unique_lock<std::mutex> side_lock;
-    SideStream* side = nullptr;
+    // Decode: the shared expert's two GEMVs (neither they nor the routed
+    // experts fill the GPU at these sizes).
     if (d->shared_gate_up && T <= kMoeGemvTokens) {
-        side_lock = std::unique_lock<std::mutex>(g_side_mutex);
-        side = side_stream();
-        cudaStream_t ss = st;
-        if (side && cudaEventRecord(side->fork, st) == cudaSuccess &&
-            cudaStreamWaitEvent(side->stream, side->fork, 0) == cudaSuccess)
-            ss = side->stream;
-        else
-            side = nullptr;
+        const cudaStream_t ss = fork_side();
         bq::stage_begin(BQ_STAGE_SHARED, ss);
         bq::QgemvParams sgu = dense_params(d->shared_gate_up, T, xh, nullptr, w.h_shared, 0, w.ks_sgu, w.part_sgu,
                                            w.cnt_sgu);
@@ -365,19 +386,12 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
             return s;
     }
 
-    if (d->shared_gate_up && !accumulate) {
-        const int Is = d->shared_gate_up->n / 2;
+    if (d->shared_gate_up && !accumulate) {   // a shared expert the GEMM cannot take: GEMVs on this stream
         bq::stage_begin(BQ_STAGE_SHARED, st);
-        if (T <= 8 || !bq::gemm_supported(d->shared_gate_up->fmt)) {
-            bq::launch_qgemv(dense_params(d->shared_gate_up, T, xh, nullptr, w.h_shared, 0, w.ks_sgu, w.part_sgu,
-                                          w.cnt_sgu), 1, st);
-            bq::launch_qgemv(dense_params(d->shared_down, T, w.h_shared, y, nullptr, H, w.ks_sd, w.part_sd,
-                                          w.cnt_sd), 1, st);
-        } else {
-            if ((s = bq::launch_gemm_shared(d->shared_gate_up, d->shared_down, T, xh, w.h_shared, y, Is,
-                                            base + w.bytes, st)) != BQ_OK)
-                return s;
-        }
+        bq::launch_qgemv(dense_params(d->shared_gate_up, T, xh, nullptr, w.h_shared, 0, w.ks_sgu, w.part_sgu,
+                                      w.cnt_sgu), 1, st);
+        bq::launch_qgemv(dense_params(d->shared_down, T, w.h_shared, y, nullptr, H, w.ks_sd, w.part_sd,
+                                      w.cnt_sd), 1, st);
         bq::stage_end(BQ_STAGE_SHARED, st);
         accumulate = 1;
     }

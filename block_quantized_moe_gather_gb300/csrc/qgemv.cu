@@ -685,8 +685,10 @@ template <int FMT>
 void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous, cudaStream_t st) {
     const int tiles = p.n / bq::kTileRows;
     // one CTA per 32-row quarter when a dense weight's whole-tile CTAs would
-    // leave SMs idle and K is not split across CTAs (no workspace for partials);
-    // the expert GEMVs of a MoE step are left whole-tile (measured no better)
+    // leave SMs idle and K is not split across CTAs (no workspace for partials).
+    // The expert GEMVs of a MoE step keep whole tiles, in 128-thread CTAs on the
+    // Q2_K split-scale path below; the other formats stay on 256-thread CTAs
+    // (128-thread ones measured 5-16% slower on their decode steps at B = 1, 2, 8)
     const int ny = p.grid_groups && !p.seg_expert ? (p.m + 7) / 8 : max_segments;
     const bool quarters = p.ksplit == 1 && !p.seg_expert && tiles * ny < sm_count();
     dim3 grid(tiles * (quarters ? 4 : 1), ny, p.ksplit);
