@@ -89,7 +89,7 @@ __device__ __forceinline__ void load_frag(Frag<FMT>& f, const uint8_t* slab, int
                 f.sc[tile][hh] = __ldg(slab + 8192 + 4 * row + t);   // the lane's quarter = block t
             } else if (FMT == BQ_FMT_FP8_B128) {
                 // rows 16 * tile .. + 15 of the quarter share one block scale
-                f.sc[tile][hh] = __ldg(reinterpret_cast<const uint16_t*>(slab + 8192) + tile);
+                if (hh == 0) f.sc[tile][0] = __ldg(reinterpret_cast<const uint16_t*>(slab + 8192) + tile);
             } else {
                 f.sc[tile][hh] = __ldg(reinterpret_cast<const uint32_t*>(slab + 8192 + 512 * (t >> 1) + 4 * row));
             }
@@ -406,6 +406,33 @@ __device__ __forceinline__ void mma_frag(const Frag<FMT>& f, const __half* xq, b
                 }
             }
         }
+    } else if constexpr (FMT == BQ_FMT_FP8_B128) {
+        // One block scale per 16-row tile of the slab: the MMAs take the exact
+        // e4m3 values (fp16 holds every e4m3 value) and the slab's sums are
+        // scaled once, in fp32, by the stored fp16(256 s).
+        float cm[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int s = 0; s < Traits<FMT>::STEPS; ++s) {
+            const uint4 xv = x[s >> 1];
+            const uint32_t b0 = (s & 1) ? xv.z : xv.x;
+            const uint32_t b1 = (s & 1) ? xv.w : xv.y;
+#pragma unroll
+            for (int tile = 0; tile < 2; ++tile) {
+                uint32_t a[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {   // r = hh + 2 * lohi
+                    const uint32_t w = comp(f.q[tile][r & 1], s);
+                    a[r] = bq::h2_as_u32(bq::e4m3x2_to_half2((r >> 1) ? w >> 16 : w));
+                }
+                mma16816(cm[tile], a, b0, b1);
+            }
+        }
+#pragma unroll
+        for (int tile = 0; tile < 2; ++tile) {
+            const float sc = __half2float(__ushort_as_half((uint16_t)f.sc[tile][0]));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[tile][j] = fmaf(sc, cm[tile][j], acc[tile][j]);
+        }
     } else {
         __half2 sc2[2][2], bi2[2][2], d2[2][2];
 #pragma unroll
@@ -418,8 +445,6 @@ __device__ __forceinline__ void mma_frag(const Frag<FMT>& f, const __half* xq, b
                     bi2[tile][hh] = __high2half2(sbh);
                 } else if (FMT == BQ_FMT_MXFP4) {
                     sc2[tile][hh] = bq::mx_scale_h2(f.sc[tile][hh]);
-                } else if (FMT == BQ_FMT_FP8_B128) {
-                    sc2[tile][hh] = bq::u32_as_h2(f.sc[tile][hh] | (f.sc[tile][hh] << 16));
                 } else {
                     const __half d = __ushort_as_half((uint16_t)f.sc[tile][hh]);
                     d2[tile][hh] = __halves2half2(d, d);
@@ -439,10 +464,6 @@ __device__ __forceinline__ void mma_frag(const Frag<FMT>& f, const __half* xq, b
                     if (FMT == BQ_FMT_Q8_0) {
                         const uint32_t wx = comp(f.q[tile][hh], s) ^ 0x80808080u;
                         a[r] = bq::h2_as_u32(__hmul2(bq::s8pair_to_half2(wx, lohi ? 0x4342u : 0x4140u), d2[tile][hh]));
-                    } else if (FMT == BQ_FMT_FP8_B128) {
-                        // exact e4m3 -> fp16, times the stored fp16(256 s), rounded once
-                        const uint32_t w = comp(f.q[tile][hh], s);
-                        a[r] = bq::h2_as_u32(__hmul2_rn(bq::e4m3x2_to_half2(lohi ? w >> 16 : w), sc2[tile][hh]));
                     } else if (FMT == BQ_FMT_MXFP4) {
                         // exact fp16 operands: the product is the scaled value rounded once
                         const uint32_t w = comp(f.q[tile][hh], s >> 1);
@@ -699,11 +720,14 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
     // N = K = 4096, m = 1, 8 and 32: 20-120% slower).
     const int share = (p.k / Traits<FMT>::SK + p.ksplit - 1) / p.ksplit;
     const bool q2s = FMT == BQ_FMT_Q2_K && p.seg_expert && !p.gamma && share <= kQ2sMaxSlabs;
-    constexpr bool kQ2 = FMT == BQ_FMT_Q2_K;
-    auto kernel = p.gamma ? (quarters ? qgemv_kernel<FMT, false, 8, true> : qgemv_kernel<FMT, false, 2, true>)
-                : q2s ? (p.swiglu ? qgemv_kernel<FMT, true, 1, false, kQ2> : qgemv_kernel<FMT, false, 1, false, kQ2>)
-                : quarters ? (p.swiglu ? qgemv_kernel<FMT, true, 8, false> : qgemv_kernel<FMT, false, 8, false>)
-                           : (p.swiglu ? qgemv_kernel<FMT, true, 2, false> : qgemv_kernel<FMT, false, 2, false>);
+    using Kernel = void (*)(const bq::QgemvParams);
+    Kernel split_scale = nullptr;   // instantiated for Q2_K only
+    if constexpr (FMT == BQ_FMT_Q2_K)
+        split_scale = p.swiglu ? qgemv_kernel<FMT, true, 1, false, true> : qgemv_kernel<FMT, false, 1, false, true>;
+    const Kernel kernel = p.gamma ? (quarters ? qgemv_kernel<FMT, false, 8, true> : qgemv_kernel<FMT, false, 2, true>)
+                        : q2s ? split_scale
+                        : quarters ? (p.swiglu ? qgemv_kernel<FMT, true, 8, false> : qgemv_kernel<FMT, false, 8, false>)
+                                   : (p.swiglu ? qgemv_kernel<FMT, true, 2, false> : qgemv_kernel<FMT, false, 2, false>);
     const size_t smem = q2s ? (size_t)share * kQ2sSlabBytes : 0;
     if (q2s) {   // (expert segments: never the quarter CTAs, which serve a dense matrix)
         static bool attr_set[2] = {false, false};   // per instantiation (swiglu)
