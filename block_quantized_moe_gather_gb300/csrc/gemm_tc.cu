@@ -858,12 +858,12 @@ bool make_act_map(CUtensorMap* map, const __half* base, int rows, int cols) {
 template <int FMT, int EPI>
 void launch_one(const CUtensorMap& map, const GemmArgs& a, dim3 grid, cudaStream_t st) {
     // per device: the attribute is a property of the function on the current device
-    static bool attr_set[64] = {};
+    static std::atomic<bool> attr_set[64];
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (dev >= 0 && dev < 64 && !attr_set[dev].load(std::memory_order_acquire)) {
         cudaFuncSetAttribute(gemm_kernel<FMT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     gemm_kernel<FMT, EPI><<<grid, kThreads, kSmemBytes, st>>>(map, a);
     bq::note_launch();

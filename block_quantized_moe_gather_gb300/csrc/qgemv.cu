@@ -30,6 +30,7 @@
 // values [4s, 4s+4) of every lane's quarter.  The activation fragment is
 // read in the same order, so the contraction is unchanged.
 #include <algorithm>
+#include <atomic>
 
 #include "moe_internal.cuh"
 
@@ -730,11 +731,14 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
                                    : (p.swiglu ? qgemv_kernel<FMT, true, 2, false> : qgemv_kernel<FMT, false, 2, false>);
     const size_t smem = q2s ? (size_t)share * kQ2sSlabBytes : 0;
     if (q2s) {   // (expert segments: never the quarter CTAs, which serve a dense matrix)
-        static bool attr_set[2] = {false, false};   // per instantiation (swiglu)
-        bool& done = attr_set[p.swiglu ? 1 : 0];
-        if (!done) {
+        // per instantiation (swiglu) and device: the attribute belongs to the
+        // function on the current device
+        static std::atomic<bool> attr_set[2][64];
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev >= 0 && dev < 64 && !attr_set[p.swiglu ? 1 : 0][dev].load(std::memory_order_acquire)) {
             cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQ2sMaxSlabs * kQ2sSlabBytes);
-            done = true;
+            attr_set[p.swiglu ? 1 : 0][dev].store(true, std::memory_order_release);
         }
     }
     const int threads = q2s ? 128 : kThreads;
