@@ -793,17 +793,21 @@ __global__ void gather_rows_kernel(const __half* __restrict__ x, const int32_t* 
     for (int i = lane; i < cols / 8; i += 32) d[i] = __ldg(s + i);
 }
 
-// Token-chunk tiles of every active segment, in segment order (the
-// per-expert work queue): a segment of c rows becomes ceil(c/BN) chunks of
-// near-equal size.  One CTA of 1024 threads; <= 1024 segments.
+// Token-chunk tiles of every active segment of more than `small_max` rows,
+// in segment order (the per-expert work queue): a segment of c rows becomes
+// ceil(c/BN) chunks of near-equal size.  The other active segments (1 to
+// small_max rows) are listed in `small` (segment indices, ascending; count in
+// n_small).  One CTA of 1024 threads; <= 1024 segments.
 __global__ void __launch_bounds__(1024)
-tile_list_kernel(const int32_t* __restrict__ seg_count, const int32_t* __restrict__ n_segments,
-                 int4* __restrict__ tiles, int32_t* __restrict__ n_tiles) {
+tile_list_kernel(const int32_t* __restrict__ seg_count, const int32_t* __restrict__ n_segments, int small_max,
+                 int4* __restrict__ tiles, int32_t* __restrict__ n_tiles, int32_t* __restrict__ small,
+                 int32_t* __restrict__ n_small) {
+    __shared__ int32_t warp_small[32];
     __shared__ int32_t warp_sums[32];
     const int s = threadIdx.x;
     const int ns = *n_segments;
     const int cnt = s < ns ? seg_count[s] : 0;
-    const int c = (cnt + BN - 1) / BN;
+    const int c = cnt > small_max ? (cnt + BN - 1) / BN : 0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = c;
 #pragma unroll
@@ -827,6 +831,23 @@ tile_list_kernel(const int32_t* __restrict__ seg_count, const int32_t* __restric
     const int size = c ? (cnt + c - 1) / c : 0;
     for (int i = 0; i < c; ++i) tiles[base + i] = make_int4(s, i * size, min(size, cnt - i * size), 0);
     if (threadIdx.x == 0) *n_tiles = warp_sums[31];
+    // the small segments, compacted in order
+    const bool is_small = cnt > 0 && cnt <= small_max;
+    const uint32_t bal = __ballot_sync(0xffffffffu, is_small);
+    if (lane == 0) warp_small[warp] = __popc(bal);
+    __syncthreads();
+    if (warp == 0) {
+        int v = warp_small[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += u;
+        }
+        warp_small[lane] = v;
+    }
+    __syncthreads();
+    if (is_small) small[(warp ? warp_small[warp - 1] : 0) + __popc(bal & ((1u << lane) - 1u))] = s;
+    if (threadIdx.x == 0) *n_small = warp_small[31];
 }
 
 // ---------------------------------------------------------------- host side
@@ -920,6 +941,8 @@ bq_status dense_gemm(const bq_qweight* w, int m, const __half* x, int epi, float
 struct GemmWs {
     int4* tiles;
     int32_t* n_tiles;
+    int32_t* small;     // segments left to the expert GEMVs
+    int32_t* n_small;
     __half* x_perm;
     size_t bytes;
 };
@@ -934,6 +957,8 @@ GemmWs carve(const bq_moe_desc* d, uint8_t* base) {
     auto take = [&](size_t bytes) { uint8_t* p = base ? base + off : nullptr; off += up256(bytes); return p; };
     g.tiles = (int4*)take(max_tiles * sizeof(int4));
     g.n_tiles = (int32_t*)take(4);
+    g.small = (int32_t*)take(std::min<size_t>(d->n_experts, P) * 4);
+    g.n_small = (int32_t*)take(4);
     g.x_perm = (__half*)take(P * (size_t)d->hidden * 2);
     g.bytes = off;
     return g;
@@ -956,10 +981,11 @@ bq_status launch_gemm_dense(const bq_qweight* w, int m, const __half* x, float* 
 }
 
 void launch_gemm_moe_prepare(const bq_moe_desc* d, const __half* x, const int32_t* perm_token,
-                             const int32_t* seg_count, const int32_t* n_segments, uint8_t* ws, cudaStream_t st) {
+                             const int32_t* seg_count, const int32_t* n_segments, int small_max, uint8_t* ws,
+                             cudaStream_t st) {
     const int P = d->T * d->topk, H = d->hidden;
     GemmWs g = carve(d, ws);
-    tile_list_kernel<<<1, 1024, 0, st>>>(seg_count, n_segments, g.tiles, g.n_tiles);
+    tile_list_kernel<<<1, 1024, 0, st>>>(seg_count, n_segments, small_max, g.tiles, g.n_tiles, g.small, g.n_small);
     gather_rows_kernel<<<(P + 7) / 8, 256, 0, st>>>(x, perm_token, P, H, g.x_perm);
     note_launch(2);
 }
@@ -967,6 +993,7 @@ void launch_gemm_moe_prepare(const bq_moe_desc* d, const __half* x, const int32_
 bq_status launch_gemm_moe(const bq_moe_desc* d, const __half*, const int32_t*, const float* perm_gate,
                      const int32_t* seg_expert, const int32_t* seg_start, const int32_t* seg_count,
                      const int32_t*, const int32_t*, __half* h, float* y_slot, uint8_t* ws,
+                     const QgemvParams* small_gu, const QgemvParams* small_dn, int max_segments,
                      cudaStream_t st) {
     const int P = d->T * d->topk, H = d->hidden, I = d->inter;
     GemmWs g = carve(d, ws);
@@ -980,6 +1007,11 @@ bq_status launch_gemm_moe(const bq_moe_desc* d, const __half*, const int32_t*, c
     a.seg_expert = seg_expert; a.seg_start = seg_start; a.seg_count = seg_count;
     a.h = h; a.ldh = I;
     launch(d->w_gate_up.fmt, EPI_SWIGLU, map_x, a, dim3(2 * I / kTileRows, max_tiles), st);
+    if (small_gu) {
+        QgemvParams q = *small_gu;
+        q.seg_list = g.small; q.n_list = g.n_small;
+        launch_qgemv(q, max_segments, st);
+    }
     stage_end(BQ_STAGE_GATE_UP, st);
 
     stage_begin(BQ_STAGE_DOWN, st);
@@ -990,6 +1022,11 @@ bq_status launch_gemm_moe(const bq_moe_desc* d, const __half*, const int32_t*, c
     b.seg_expert = seg_expert; b.seg_start = seg_start; b.seg_count = seg_count;
     b.y = y_slot; b.ldy = H; b.row_scale = perm_gate;
     launch(d->w_down.fmt, EPI_SCALE, map_h, b, dim3(H / kTileRows, max_tiles), st);
+    if (small_dn) {
+        QgemvParams q = *small_dn;
+        q.seg_list = g.small; q.n_list = g.n_small;
+        launch_qgemv(q, max_segments, st);
+    }
     stage_end(BQ_STAGE_DOWN, st);
     return BQ_OK;
 }

@@ -222,6 +222,11 @@ SideStream* side_stream() {
 // one-CTA front end; the grouped tensor-core GEMM would give every expert a
 // tile of a handful of tokens that still dequantises all of its weights.
 constexpr int kMoeGemvTokens = 32;
+// Prefill experts of at most this many tokens run as expert GEMVs, in layers
+// whose experts average fewer than kSmallMean tokens (measured on the Q2_K
+// layer, E = 256, top-6, Zipf bias: 8 beat 4 and 16).
+constexpr int kSmallSegment = 8;
+constexpr int kSmallMean = 64;
 
 // One dense weight over `m` rows of x (single segment).
 bq::QgemvParams dense_params(const bq_qweight* w, int m, const __half* x, float* y, __half* h, int ldy,
@@ -341,7 +346,15 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
     }
     const int max_segments = min(E, P);
     // the GEMM path's gather of X_perm is the last part of the permute step
-    if (!decode) bq::launch_gemm_moe_prepare(d, xh, w.perm_token, w.seg_count, w.n_segments, base + w.bytes, st);
+    // Prefill: experts holding at most kSmallSegment tokens run as expert GEMVs
+    // (one pass of 8 token rows dequantises the weight once, like a GEMM tile,
+    // at a third of the GEMM's fixed per-chunk cost); the tile list skips them.
+    // Only where experts average fewer than kSmallMean tokens, i.e. where a
+    // skewed routing leaves many with a handful: elsewhere the two extra
+    // launches would cost more than they save.
+    const int small_max = !decode && P < kSmallMean * E ? kSmallSegment : 0;
+    if (!decode)
+        bq::launch_gemm_moe_prepare(d, xh, w.perm_token, w.seg_count, w.n_segments, small_max, base + w.bytes, st);
     bq::stage_end(BQ_STAGE_ROUTE_PERMUTE, st);
 
     // Decode: the shared expert's two GEMVs (neither they nor the routed
@@ -381,8 +394,20 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
         bq::launch_qgemv(dn, max_segments, st, /*after_previous=*/true);
         bq::stage_end(BQ_STAGE_DOWN, st);
     } else {
+        bq::QgemvParams sgu{}, sdn{};
+        sgu.w = static_cast<const uint8_t*>(d->w_gate_up.data);
+        sgu.fmt = d->w_gate_up.fmt; sgu.n = 2 * I; sgu.k = H; sgu.swiglu = 1;
+        sgu.seg_expert = w.seg_expert; sgu.seg_start = w.seg_start; sgu.seg_count = w.seg_count;
+        sgu.n_segments = w.n_segments; sgu.src_row = w.perm_token; sgu.x = xh; sgu.h = w.h;
+        sgu.ksplit = 1;
+        sdn = sgu;
+        sdn.w = static_cast<const uint8_t*>(d->w_down.data);
+        sdn.fmt = d->w_down.fmt; sdn.n = H; sdn.k = I; sdn.swiglu = 0;
+        sdn.src_row = nullptr; sdn.x = w.h; sdn.h = nullptr; sdn.y = w.y_slot; sdn.ldy = H; sdn.row_scale = w.perm_gate;
         if ((s = bq::launch_gemm_moe(d, xh, w.perm_token, w.perm_gate, w.seg_expert, w.seg_start, w.seg_count,
-                                     w.n_segments, w.counts, w.h, w.y_slot, base + w.bytes, st)) != BQ_OK)
+                                     w.n_segments, w.counts, w.h, w.y_slot, base + w.bytes,
+                                     small_max ? &sgu : nullptr, small_max ? &sdn : nullptr, max_segments,
+                                     st)) != BQ_OK)
             return s;
     }
 

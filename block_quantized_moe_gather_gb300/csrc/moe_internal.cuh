@@ -76,6 +76,11 @@ struct QgemvParams {
     // the m rows is its own CTA row of the grid (grid.y = ceil(m / 8)) instead
     // of a loop inside every CTA.
     int grid_groups;
+    // Optional, with segment arrays: only the segments listed in seg_list
+    // (n_list of them, a device count) are multiplied; CTA row y of the grid
+    // takes entry y (no K split).
+    const int32_t* seg_list;
+    const int32_t* n_list;
 };
 constexpr int kMaxKsplit = 16;
 // Split factor that gives the GPU enough CTAs for this shape (experts: the

@@ -532,7 +532,11 @@ __device__ __forceinline__ void qgemv_epilogue(const bq::QgemvParams& p, const f
 //
 // Q2S (Q2_K only, no norm): the split-scale path above; the CTA's K share of
 // each token group's activations is staged in dynamic shared memory first.
-template <int FMT, bool SWIGLU, int KW, bool NORM, bool Q2S = false>
+//
+// LIST (expert GEMVs with a segment list, no K split): grid row y takes list
+// entry y; the grid has a row per possible entry, and rows past the list's
+// end return at once.
+template <int FMT, bool SWIGLU, int KW, bool NORM, bool Q2S = false, bool LIST = false>
 __global__ void __launch_bounds__(KW == 1 ? 128 : kThreads, NORM ? 1 : (KW == 1 ? 4 : 2))   // (the norm-fused GEMV needs more registers)
 qgemv_kernel(const bq::QgemvParams p) {
     using T = Traits<FMT>;
@@ -552,12 +556,15 @@ qgemv_kernel(const bq::QgemvParams p) {
     bq::grid_dependency_wait();
     bq::allow_dependents();
     const bool gg = p.grid_groups && !p.seg_expert;   // grid.y = token groups of one segment
-    const int seg = gg ? 0 : (int)blockIdx.y;
+
+    // One segment (y: the grid row, the token group of a grid of token groups);
+    // a return ends this segment's work.
+    auto run_segment = [&](const int seg, const int y) {
     if (p.n_segments && seg >= __ldg(p.n_segments)) return;
     const int e = p.seg_expert ? __ldg(p.seg_expert + seg) : 0;
     const int start = p.seg_start ? __ldg(p.seg_start + seg) : 0;
     const int count = p.seg_count ? __ldg(p.seg_count + seg) : p.m;
-    const int tok_lo = gg ? 8 * (int)blockIdx.y : 0, tok_hi = gg ? min(count, tok_lo + 8) : count;
+    const int tok_lo = gg ? 8 * y : 0, tok_hi = gg ? min(count, tok_lo + 8) : count;
 
     const int rt = KW == 8 ? (int)(blockIdx.x >> 2) : (int)blockIdx.x, kp = blockIdx.z;
     const int n_tiles = p.n / bq::kTileRows, k_slabs = p.k / T::SK;
@@ -688,6 +695,14 @@ qgemv_kernel(const bq::QgemvParams p) {
         if (threadIdx.x == 0) p.counters[seg * n_tiles + rt] = 0;   // ready for the next call
         return;
     }
+    };
+
+    if constexpr (LIST) {
+        const int j = (int)blockIdx.y;
+        if (j < __ldg(p.n_list)) run_segment(__ldg(p.seg_list + j), j);
+    } else {
+        run_segment(gg ? 0 : (int)blockIdx.y, (int)blockIdx.y);
+    }
 }
 
 int sm_count() {
@@ -713,7 +728,6 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
     // (128-thread ones measured 5-16% slower on their decode steps at B = 1, 2, 8)
     const int ny = p.grid_groups && !p.seg_expert ? (p.m + 7) / 8 : max_segments;
     const bool quarters = p.ksplit == 1 && !p.seg_expert && tiles * ny < sm_count();
-    dim3 grid(tiles * (quarters ? 4 : 1), ny, p.ksplit);
     // The routed-expert GEMVs of a Q2_K MoE step take the split-scale path when
     // the CTA's K share fits the stage.  A dense matrix does not: its few CTAs
     // (K split over the SMs, or 32-row quarters) pay the staging latency, or
@@ -721,24 +735,35 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
     // N = K = 4096, m = 1, 8 and 32: 20-120% slower).
     const int share = (p.k / Traits<FMT>::SK + p.ksplit - 1) / p.ksplit;
     const bool q2s = FMT == BQ_FMT_Q2_K && p.seg_expert && !p.gamma && share <= kQ2sMaxSlabs;
+    // (a segment list keeps one grid row per possible entry; fewer rows, each
+    // walking several entries in turn, left the SMs underfilled: measured 7% slower)
+    dim3 grid(tiles * (quarters ? 4 : 1), ny, p.ksplit);
     using Kernel = void (*)(const bq::QgemvParams);
-    Kernel split_scale = nullptr;   // instantiated for Q2_K only
-    if constexpr (FMT == BQ_FMT_Q2_K)
+    Kernel split_scale = nullptr, split_scale_list = nullptr;   // instantiated for Q2_K only
+    if constexpr (FMT == BQ_FMT_Q2_K) {
         split_scale = p.swiglu ? qgemv_kernel<FMT, true, 1, false, true> : qgemv_kernel<FMT, false, 1, false, true>;
-    const Kernel kernel = p.gamma ? (quarters ? qgemv_kernel<FMT, false, 8, true> : qgemv_kernel<FMT, false, 2, true>)
-                        : q2s ? split_scale
-                        : quarters ? (p.swiglu ? qgemv_kernel<FMT, true, 8, false> : qgemv_kernel<FMT, false, 8, false>)
-                                   : (p.swiglu ? qgemv_kernel<FMT, true, 2, false> : qgemv_kernel<FMT, false, 2, false>);
+        split_scale_list = p.swiglu ? qgemv_kernel<FMT, true, 1, false, true, true>
+                                    : qgemv_kernel<FMT, false, 1, false, true, true>;
+    }
+    const bool list = p.seg_list && p.seg_expert;
+    const Kernel kernel =
+        p.gamma ? (quarters ? qgemv_kernel<FMT, false, 8, true> : qgemv_kernel<FMT, false, 2, true>)
+        : list ? (q2s ? split_scale_list
+                      : p.swiglu ? qgemv_kernel<FMT, true, 2, false, false, true> : qgemv_kernel<FMT, false, 2, false, false, true>)
+        : q2s ? split_scale
+        : quarters ? (p.swiglu ? qgemv_kernel<FMT, true, 8, false> : qgemv_kernel<FMT, false, 8, false>)
+                   : (p.swiglu ? qgemv_kernel<FMT, true, 2, false> : qgemv_kernel<FMT, false, 2, false>);
     const size_t smem = q2s ? (size_t)share * kQ2sSlabBytes : 0;
     if (q2s) {   // (expert segments: never the quarter CTAs, which serve a dense matrix)
-        // per instantiation (swiglu) and device: the attribute belongs to the
+        // per instantiation (list, swiglu) and device: the attribute belongs to the
         // function on the current device
-        static std::atomic<bool> attr_set[2][64];
+        static std::atomic<bool> attr_set[4][64];
+        const int which = 2 * (list ? 1 : 0) + (p.swiglu ? 1 : 0);
         int dev = 0;
         cudaGetDevice(&dev);
-        if (dev >= 0 && dev < 64 && !attr_set[p.swiglu ? 1 : 0][dev].load(std::memory_order_acquire)) {
+        if (dev >= 0 && dev < 64 && !attr_set[which][dev].load(std::memory_order_acquire)) {
             cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQ2sMaxSlabs * kQ2sSlabBytes);
-            attr_set[p.swiglu ? 1 : 0][dev].store(true, std::memory_order_release);
+            attr_set[which][dev].store(true, std::memory_order_release);
         }
     }
     const int threads = q2s ? 128 : kThreads;
@@ -784,6 +809,7 @@ void launch_qgemv(const QgemvParams& params, int max_segments, cudaStream_t st, 
     // the split-K partials and counters are indexed by segment: one token group
     // of at most 8 rows per segment, so a grid of token groups never splits K
     if (p.grid_groups && !p.seg_expert && p.m > 8) p.ksplit = 1;
+    if (p.seg_list) p.ksplit = 1;   // no partials are kept for listed segments
     note_launch();
     switch (p.fmt) {
         case BQ_FMT_Q8_0: launch_fmt<BQ_FMT_Q8_0>(p, max_segments, after_previous, st); break;

@@ -79,6 +79,21 @@ def test_moe_decode_q2k_k_shares(lib, case):
     assert_close_matmul(run_moe(lib, layer, inp), oracle_moe_threaded(inp), case.name)
 
 
+@pytest.mark.parametrize("case", [
+    # prefill layers whose experts average fewer than 64 tokens: experts of at
+    # most 8 tokens run as expert GEMVs, the others as the tensor-core GEMM
+    _case("pre_q2k_mixed", "q2_k", 64, 512, 256, 64, 6, zipf=True, shared="q8_0"),
+    _case("pre_int4_mixed", "int4", 96, 256, 128, 32, 4, zipf=True),
+    # no expert small enough (an empty GEMV list), and every expert small (no GEMM tile)
+    _case("pre_q2k_none_small", "q2_k", 40, 256, 256, 4, 2),
+    _case("pre_q2k_all_small", "q2_k", 40, 256, 256, 64, 2, shared="q8_0"),
+], ids=lambda c: c.name)
+def test_moe_prefill_small_experts(lib, case):
+    inp = synth.moe_inputs(case)
+    layer = build_layer(lib, inp)
+    assert_close_matmul(run_moe(lib, layer, inp), oracle_moe(inp), case.name)
+
+
 @pytest.mark.parametrize("mode", ["tiny", "large", "mixed_rows", "zero_slab"])
 def test_moe_decode_q2k_activation_range(lib, mode):
     # The split-scale Q2_K GEMV stages each (slab, token) of the activations
