@@ -215,14 +215,18 @@ class L2Flush:
         torch.sum(self.rbuf, dim=0, out=self.sink)
 
 
-# DRAM bytes (read + write) of one routed gate/up GEMM launch, per workload, from one
-# capture of the current kernel:
-#   ncu --set full --clock-control none --kernel-name-base demangled \
-#       -k regex:"gemm_kernel<.int.2, .int.0>" -c 1 -o gemm_q2k_gu \
+# DRAM bytes (read + write) of one routed gate/up stage, per workload: the
+# grouped GEMM (experts of more than 8 tokens) and the expert GEMV behind it
+# (the rest), from one capture of the current kernels:
+#   ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum \
+#       --clock-control none --kernel-name-base demangled \
+#       -k regex:"gemm_kernel<.int.2, .int.0>|qgemv_kernel<.int.2, .bool.1, .int.1, .bool.0, .bool.1, .bool.1>" \
+#       -c 2 --csv --log-file gu_traffic.csv \
 #       python bench.py --steps 2 --warmup 1 --no-secondary --no-cpu-baseline
-# (689,895,424 read + 42,246,144 written; the algorithmic bytes are 740 MB).  Set to
-# None whenever the GEMM kernel changes until it is captured again.
-GATE_UP_DRAM_BYTES = {"q2k": 689895424 + 42246144, "int4": None}
+# (GEMM 364,728,576 read + 37,929,984 written; GEMV 326,085,120 read + 84,992
+# written; the algorithmic bytes are 740 MB).  Set to None whenever either
+# kernel changes until they are captured again.
+GATE_UP_DRAM_BYTES = {"q2k": 364728576 + 37929984 + 326085120 + 84992, "int4": None}
 
 
 def time_steps(fn, k, flush, stage_events=None):
@@ -294,14 +298,15 @@ def graph_time(calls, flush, reps=3):
     return statistics.median(times)
 
 
-def e2e_pipelined(bq, layer, ws, xp, lp, bias, y_ref, steps):
+def e2e_pipelined(bq, layer, ws, xp, lp, bias, y_ref, steps, reps=3):
     """End-to-end steps as a serving loop runs them: k calls of the MoE layer,
     step i's inputs uploaded from pinned host memory on an upload stream and
     its output downloaded to pinned host memory on a download stream, with
     two device buffers of each, so that the copies of steps i + 1 and i - 1
-    run while step i computes.  One timed region from the first upload to the
-    last download (CUDA events, synchronized on both sides).  Returns (ms,
-    whether every downloaded output equals y_ref bit for bit)."""
+    run while step i computes.  Each of `reps` passes is one timed region
+    from the first upload to the last download (CUDA events, synchronized on
+    both sides).  Returns (median ms of a pass, whether every downloaded
+    output of every pass equals y_ref bit for bit)."""
     import torch
     comp = torch.cuda.current_stream()
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
@@ -309,37 +314,41 @@ def e2e_pipelined(bq, layer, ws, xp, lp, bias, y_ref, steps):
     ls = [torch.empty(lp.shape, dtype=lp.dtype, device="cuda") for _ in range(2)]
     ys = [torch.empty(y_ref.shape, dtype=y_ref.dtype, device="cuda") for _ in range(2)]
     yh = [torch.empty(y_ref.shape, dtype=y_ref.dtype).pin_memory() for _ in range(steps)]
-    ev = lambda: torch.cuda.Event()   # noqa: E731
-    uploaded = [ev() for _ in range(steps)]
-    computed = [ev() for _ in range(steps)]
-    downloaded = [ev() for _ in range(steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    start.record(comp)
-    up.wait_event(start)
-    for i in range(steps):
-        b = i % 2
-        with torch.cuda.stream(up):
-            if i >= 2:
-                up.wait_event(computed[i - 2])   # step i - 2 has read buffer b
-            xs[b].copy_(xp, non_blocking=True)
-            ls[b].copy_(lp, non_blocking=True)
-            uploaded[i].record(up)
-        comp.wait_event(uploaded[i])
-        if i >= 2:
-            comp.wait_event(downloaded[i - 2])   # y buffer b has been read back
-        bq.moe_gather_qmm(layer, xs[b], ls[b], bias, ys[b], ws)
-        computed[i].record(comp)
-        with torch.cuda.stream(down):
-            down.wait_event(computed[i])
-            yh[i].copy_(ys[b], non_blocking=True)
-            downloaded[i].record(down)
-    comp.wait_event(downloaded[steps - 1])
-    end.record(comp)
-    torch.cuda.synchronize()
     ref = y_ref.cpu().numpy().view(np.uint32)
-    ok = all(np.array_equal(h.numpy().view(np.uint32), ref) for h in yh)
-    return start.elapsed_time(end), bool(ok)
+    times, ok = [], True
+    for _ in range(reps):
+        uploaded = [torch.cuda.Event() for _ in range(steps)]
+        computed = [torch.cuda.Event() for _ in range(steps)]
+        downloaded = [torch.cuda.Event() for _ in range(steps)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for h in yh:
+            h.zero_()
+        torch.cuda.synchronize()
+        start.record(comp)
+        up.wait_event(start)
+        for i in range(steps):
+            b = i % 2
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(computed[i - 2])   # step i - 2 has read buffer b
+                xs[b].copy_(xp, non_blocking=True)
+                ls[b].copy_(lp, non_blocking=True)
+                uploaded[i].record(up)
+            comp.wait_event(uploaded[i])
+            if i >= 2:
+                comp.wait_event(downloaded[i - 2])   # y buffer b has been read back
+            bq.moe_gather_qmm(layer, xs[b], ls[b], bias, ys[b], ws)
+            computed[i].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(computed[i])
+                yh[i].copy_(ys[b], non_blocking=True)
+                downloaded[i].record(down)
+        comp.wait_event(downloaded[steps - 1])
+        end.record(comp)
+        torch.cuda.synchronize()
+        times.append(start.elapsed_time(end))
+        ok = ok and all(np.array_equal(h.numpy().view(np.uint32), ref) for h in yh)
+    return statistics.median(times), bool(ok)
 
 
 def weight_copies(bq, q, n):
@@ -410,14 +419,17 @@ def run_main(args, world, rank, local):
     ms_per_step = total_ms / args.steps
     value = job_throughput(world, case.t, args.steps, total_ms)
 
-    # dominant kernel: the routed gate/up grouped GEMM (+ SwiGLU epilogue); the stage
-    # events bracket that launch alone (the X_perm gather belongs to the permute stage)
+    # dominant stage: the routed gate/up (+ SwiGLU): the grouped GEMM and, for
+    # experts of at most 8 tokens, the expert GEMV; the stage events bracket those
+    # two launches (the X_perm gather belongs to the permute stage)
     pairs = case.t * case.topk
     gu_flops = 2.0 * pairs * 2 * case.inter * case.hidden
     gu_ms = statistics.mean(stage_ms[1])
     peak_tf = pk["bf16_tflops"]
     achieved_tf = gu_flops / (gu_ms / 1e3) / 1e12
-    roofline = {"kernel": "gate_up grouped GEMM + SwiGLU (events around its launch)", "bound": "tensor",
+    roofline = {"kernel": ("routed gate/up + SwiGLU stage: the grouped GEMM for experts of more than 8 "
+                           "tokens and the expert GEMV behind it for the rest (events around both launches)"),
+                "bound": "tensor",
                 "achieved": round(achieved_tf, 2), "peak": peak_tf, "unit": "TFLOP/s",
                 "frac": round(achieved_tf / peak_tf, 4), "traffic": GATE_UP_DRAM_BYTES.get(args.workload),
                 "flops_per_launch": gu_flops,
@@ -449,8 +461,8 @@ def run_main(args, world, rank, local):
            "how": ("K steps back to back through bq.moe_gather_qmm: each step's x and logits copied from "
                    "pinned host memory on an upload stream and its y copied to pinned host memory on a "
                    "download stream, double-buffered, so that the copies of steps i+1 and i-1 overlap "
-                   "step i; one timed region from the first upload to the last download; no L2 flush "
-                   "(the weights one step reads are ~5x the L2)"),
+                   "step i; one timed region from the first upload to the last download (median of 3 "
+                   "such passes); no L2 flush (the weights one step reads are ~5x the L2)"),
            "outputs_match_device_run": pipe_ok,
            "serial": {"value": round(job_throughput(world, case.t, args.steps, serial_total), 1),
                       "how": "each step alone: upload, layer, download, L2 flushed before it"}}
