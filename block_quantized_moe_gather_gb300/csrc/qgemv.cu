@@ -560,141 +560,141 @@ qgemv_kernel(const bq::QgemvParams p) {
     // One segment (y: the grid row, the token group of a grid of token groups);
     // a return ends this segment's work.
     auto run_segment = [&](const int seg, const int y) {
-    if (p.n_segments && seg >= __ldg(p.n_segments)) return;
-    const int e = p.seg_expert ? __ldg(p.seg_expert + seg) : 0;
-    const int start = p.seg_start ? __ldg(p.seg_start + seg) : 0;
-    const int count = p.seg_count ? __ldg(p.seg_count + seg) : p.m;
-    const int tok_lo = gg ? 8 * y : 0, tok_hi = gg ? min(count, tok_lo + 8) : count;
+        if (p.n_segments && seg >= __ldg(p.n_segments)) return;
+        const int e = p.seg_expert ? __ldg(p.seg_expert + seg) : 0;
+        const int start = p.seg_start ? __ldg(p.seg_start + seg) : 0;
+        const int count = p.seg_count ? __ldg(p.seg_count + seg) : p.m;
+        const int tok_lo = gg ? 8 * y : 0, tok_hi = gg ? min(count, tok_lo + 8) : count;
 
-    const int rt = KW == 8 ? (int)(blockIdx.x >> 2) : (int)blockIdx.x, kp = blockIdx.z;
-    const int n_tiles = p.n / bq::kTileRows, k_slabs = p.k / T::SK;
-    const uint8_t* wbase = p.w + bq::slab_index(e, rt, 0, n_tiles, k_slabs) * T::SB;
+        const int rt = KW == 8 ? (int)(blockIdx.x >> 2) : (int)blockIdx.x, kp = blockIdx.z;
+        const int n_tiles = p.n / bq::kTileRows, k_slabs = p.k / T::SK;
+        const uint8_t* wbase = p.w + bq::slab_index(e, rt, 0, n_tiles, k_slabs) * T::SB;
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int quarter = KW == 8 ? (int)(blockIdx.x & 3) : (warp & 3), rowbase = 32 * quarter;
-    const int kw = KW == 8 ? warp : KW == 2 ? (warp >> 2) : 0;   // this warp's K piece
-    // this CTA's share of the slabs (split K), then KW contiguous pieces of it
-    const int ks_lo = (int)((int64_t)k_slabs * kp / p.ksplit), ks_hi = (int)((int64_t)k_slabs * (kp + 1) / p.ksplit);
-    const int kt_begin = ks_lo + ((ks_hi - ks_lo) * kw + KW - 1) / KW;
-    const int kt_end = ks_lo + ((ks_hi - ks_lo) * (kw + 1) + KW - 1) / KW;
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+        const int quarter = KW == 8 ? (int)(blockIdx.x & 3) : (warp & 3), rowbase = 32 * quarter;
+        const int kw = KW == 8 ? warp : KW == 2 ? (warp >> 2) : 0;   // this warp's K piece
+        // this CTA's share of the slabs (split K), then KW contiguous pieces of it
+        const int ks_lo = (int)((int64_t)k_slabs * kp / p.ksplit), ks_hi = (int)((int64_t)k_slabs * (kp + 1) / p.ksplit);
+        const int kt_begin = ks_lo + ((ks_hi - ks_lo) * kw + KW - 1) / KW;
+        const int kt_end = ks_lo + ((ks_hi - ks_lo) * (kw + 1) + KW - 1) / KW;
 
-    for (int tok0 = tok_lo; tok0 < tok_hi; tok0 += 8) {
-        const int ntok = min(8, count - tok0);
-        const bool xvalid = g < ntok;
-        const __half* xrow = p.x;
-        if (xvalid) {
-            const int lr = start + tok0 + g;
-            const int src = p.src_row ? __ldg(p.src_row + lr) : lr;
-            xrow = p.x + (int64_t)src * p.k;
-        }
-        // register ring of D slabs in flight (D - 1 ahead of the one being multiplied);
-        // the first loads go out before the norm prologue below
-        // (the split-scale path keeps two slabs in flight: a third would not fit the registers)
-        constexpr int D = Q2S ? 2 : T::DEPTH;
-        Frag<FMT> f[D];
-        const int n = kt_end - kt_begin;
-#pragma unroll
-        for (int d = 0; d < D - 1; ++d)
-            if (d < n) load_frag<FMT>(f[d], wbase + (int64_t)(kt_begin + d) * T::SB, rowbase, g, t);
-        float inv = 0.f;
-        __half* xo = nullptr;
-        if constexpr (Q2S) {   // the previous token group's readers of the stage are past the reduction barriers
-            q2s_stage(p, start + tok0, ntok, ks_lo, ks_hi - ks_lo, q2s_stage_smem);
-            __syncthreads();
-        }
-        if (NORM) {
-            __syncthreads();   // the previous token group is done with s_inv
-            bq::rows_inv_rms(p.x + (int64_t)(start + tok0) * p.k, p.k, ntok, p.k, p.eps, s_part, s_inv);
+        for (int tok0 = tok_lo; tok0 < tok_hi; tok0 += 8) {
+            const int ntok = min(8, count - tok0);
+            const bool xvalid = g < ntok;
+            const __half* xrow = p.x;
             if (xvalid) {
-                inv = s_inv[g];
-                if (p.x_out && rt == 0 && quarter == 0) xo = p.x_out + (int64_t)(start + tok0 + g) * p.k;
+                const int lr = start + tok0 + g;
+                const int src = p.src_row ? __ldg(p.src_row + lr) : lr;
+                xrow = p.x + (int64_t)src * p.k;
             }
-        }
-        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        for (int i = 0; i < n; i += D) {
+            // register ring of D slabs in flight (D - 1 ahead of the one being multiplied);
+            // the first loads go out before the norm prologue below
+            // (the split-scale path keeps two slabs in flight: a third would not fit the registers)
+            constexpr int D = Q2S ? 2 : T::DEPTH;
+            Frag<FMT> f[D];
+            const int n = kt_end - kt_begin;
 #pragma unroll
-            for (int d = 0; d < D; ++d) {
-                if (i + d >= n) break;
-                const int nxt = i + d + D - 1;
-                if (nxt < n)
-                    load_frag<FMT>(f[(d + D - 1) % D], wbase + (int64_t)(kt_begin + nxt) * T::SB, rowbase, g, t);
-                const int kc = (kt_begin + i + d) * T::SK;
-                if constexpr (Q2S)
-                    mma_slab_q2s(f[d], stage_addr + (kt_begin + i + d - ks_lo) * kQ2sSlabBytes, g, t, acc);
-                else if (NORM)
-                    mma_frag<FMT, true>(f[d], xrow + kc, xvalid, t, acc, p.gamma + kc, inv, xo ? xo + kc : nullptr);
-                else
-                    mma_frag<FMT, false>(f[d], xrow + kc, xvalid, t, acc);
+            for (int d = 0; d < D - 1; ++d)
+                if (d < n) load_frag<FMT>(f[d], wbase + (int64_t)(kt_begin + d) * T::SB, rowbase, g, t);
+            float inv = 0.f;
+            __half* xo = nullptr;
+            if constexpr (Q2S) {   // the previous token group's readers of the stage are past the reduction barriers
+                q2s_stage(p, start + tok0, ntok, ks_lo, ks_hi - ks_lo, q2s_stage_smem);
+                __syncthreads();
             }
-        }
-        if (FMT == BQ_FMT_FP8_B128) {   // the FP8 slab scales carry a factor 256 (exact to remove)
-#pragma unroll
-            for (int tile = 0; tile < 2; ++tile)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[tile][j] *= 1.0f / bq::kFp8ScaleOffset;
-        }
-        __syncthreads();   // previous token group's readers of `red` are done
-        if (kw) {
-            const int slot = KW == 8 ? kw - 1 : quarter;
-#pragma unroll
-            for (int tile = 0; tile < 2; ++tile) {
-                red[slot][tile][lane][0] = make_float2(acc[tile][0], acc[tile][1]);
-                red[slot][tile][lane][1] = make_float2(acc[tile][2], acc[tile][3]);
+            if (NORM) {
+                __syncthreads();   // the previous token group is done with s_inv
+                bq::rows_inv_rms(p.x + (int64_t)(start + tok0) * p.k, p.k, ntok, p.k, p.eps, s_part, s_inv);
+                if (xvalid) {
+                    inv = s_inv[g];
+                    if (p.x_out && rt == 0 && quarter == 0) xo = p.x_out + (int64_t)(start + tok0 + g) * p.k;
+                }
             }
-        }
-        __syncthreads();
-        if (!kw) {
-            // piece 0 adds the other pieces in a fixed order: bit-reproducible
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            for (int i = 0; i < n; i += D) {
 #pragma unroll
-            for (int j = 0; j < KW - 1; ++j) {
-                const int slot = KW == 8 ? j : quarter;
+                for (int d = 0; d < D; ++d) {
+                    if (i + d >= n) break;
+                    const int nxt = i + d + D - 1;
+                    if (nxt < n)
+                        load_frag<FMT>(f[(d + D - 1) % D], wbase + (int64_t)(kt_begin + nxt) * T::SB, rowbase, g, t);
+                    const int kc = (kt_begin + i + d) * T::SK;
+                    if constexpr (Q2S)
+                        mma_slab_q2s(f[d], stage_addr + (kt_begin + i + d - ks_lo) * kQ2sSlabBytes, g, t, acc);
+                    else if (NORM)
+                        mma_frag<FMT, true>(f[d], xrow + kc, xvalid, t, acc, p.gamma + kc, inv, xo ? xo + kc : nullptr);
+                    else
+                        mma_frag<FMT, false>(f[d], xrow + kc, xvalid, t, acc);
+                }
+            }
+            if (FMT == BQ_FMT_FP8_B128) {   // the FP8 slab scales carry a factor 256 (exact to remove)
+#pragma unroll
+                for (int tile = 0; tile < 2; ++tile)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[tile][j] *= 1.0f / bq::kFp8ScaleOffset;
+            }
+            __syncthreads();   // previous token group's readers of `red` are done
+            if (kw) {
+                const int slot = KW == 8 ? kw - 1 : quarter;
 #pragma unroll
                 for (int tile = 0; tile < 2; ++tile) {
-                    const float2 r0 = red[slot][tile][lane][0], r1 = red[slot][tile][lane][1];
-                    acc[tile][0] += r0.x; acc[tile][1] += r0.y; acc[tile][2] += r1.x; acc[tile][3] += r1.y;
+                    red[slot][tile][lane][0] = make_float2(acc[tile][0], acc[tile][1]);
+                    red[slot][tile][lane][1] = make_float2(acc[tile][2], acc[tile][3]);
                 }
             }
-        }
-        if (p.ksplit == 1) {
-            if (!kw) qgemv_epilogue<SWIGLU>(p, acc, rt, quarter, g, t, start + tok0, ntok);
-            continue;
-        }
-        // Split K (one token group only): publish this CTA's partial; the last
-        // CTA of the (segment, tile) sums all partials in split order.
-        float* part = p.partial + ((int64_t)(seg * n_tiles + rt) * p.ksplit) * 1024;
-        if (!kw) {
+            __syncthreads();
+            if (!kw) {
+                // piece 0 adds the other pieces in a fixed order: bit-reproducible
 #pragma unroll
-            for (int tile = 0; tile < 2; ++tile)
+                for (int j = 0; j < KW - 1; ++j) {
+                    const int slot = KW == 8 ? j : quarter;
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int row = rowbase + 16 * tile + 8 * hh + g;
-                    *reinterpret_cast<float2*>(part + (int64_t)kp * 1024 + row * 8 + 2 * t) =
-                        make_float2(acc[tile][2 * hh], acc[tile][2 * hh + 1]);
+                    for (int tile = 0; tile < 2; ++tile) {
+                        const float2 r0 = red[slot][tile][lane][0], r1 = red[slot][tile][lane][1];
+                        acc[tile][0] += r0.x; acc[tile][1] += r0.y; acc[tile][2] += r1.x; acc[tile][3] += r1.y;
+                    }
                 }
-        }
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) s_last = atomicAdd(p.counters + seg * n_tiles + rt, 1) == p.ksplit - 1;
-        __syncthreads();
-        if (!s_last) return;
-        __threadfence();
-        if (!kw) {
-            float sum[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            for (int q = 0; q < p.ksplit; ++q)
+            }
+            if (p.ksplit == 1) {
+                if (!kw) qgemv_epilogue<SWIGLU>(p, acc, rt, quarter, g, t, start + tok0, ntok);
+                continue;
+            }
+            // Split K (one token group only): publish this CTA's partial; the last
+            // CTA of the (segment, tile) sums all partials in split order.
+            float* part = p.partial + ((int64_t)(seg * n_tiles + rt) * p.ksplit) * 1024;
+            if (!kw) {
 #pragma unroll
                 for (int tile = 0; tile < 2; ++tile)
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const int row = rowbase + 16 * tile + 8 * hh + g;
-                        const float2 v = __ldcg(reinterpret_cast<const float2*>(part + (int64_t)q * 1024 + row * 8 + 2 * t));
-                        sum[tile][2 * hh] += v.x;
-                        sum[tile][2 * hh + 1] += v.y;
+                        *reinterpret_cast<float2*>(part + (int64_t)kp * 1024 + row * 8 + 2 * t) =
+                            make_float2(acc[tile][2 * hh], acc[tile][2 * hh + 1]);
                     }
-            qgemv_epilogue<SWIGLU>(p, sum, rt, quarter, g, t, start + tok0, ntok);
+            }
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) s_last = atomicAdd(p.counters + seg * n_tiles + rt, 1) == p.ksplit - 1;
+            __syncthreads();
+            if (!s_last) return;
+            __threadfence();
+            if (!kw) {
+                float sum[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                for (int q = 0; q < p.ksplit; ++q)
+#pragma unroll
+                    for (int tile = 0; tile < 2; ++tile)
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int row = rowbase + 16 * tile + 8 * hh + g;
+                            const float2 v = __ldcg(reinterpret_cast<const float2*>(part + (int64_t)q * 1024 + row * 8 + 2 * t));
+                            sum[tile][2 * hh] += v.x;
+                            sum[tile][2 * hh + 1] += v.y;
+                        }
+                qgemv_epilogue<SWIGLU>(p, sum, rt, quarter, g, t, start + tok0, ntok);
+            }
+            if (threadIdx.x == 0) p.counters[seg * n_tiles + rt] = 0;   // ready for the next call
+            return;
         }
-        if (threadIdx.x == 0) p.counters[seg * n_tiles + rt] = 0;   // ready for the next call
-        return;
-    }
     };
 
     if constexpr (LIST) {
