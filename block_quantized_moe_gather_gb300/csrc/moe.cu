@@ -86,9 +86,9 @@ struct MoeWs {
     float *gate, *perm_gate, *y_slot;
     __half *h, *h_shared;
     // decode (T <= 8) split-K: split factors, partials and counters per GEMV
-    int ks_gu, ks_d, ks_sgu, ks_sd;
-    float *part_gu, *part_d, *part_sgu, *part_sd;
-    int32_t *cnt_gu, *cnt_d, *cnt_sgu, *cnt_sd;
+    int ks_gu, ks_d;
+    float *part_gu, *part_d;
+    int32_t *cnt_gu, *cnt_d;
     int n_counters;
     size_t bytes;
 };
@@ -118,9 +118,9 @@ MoeWs carve(const bq_moe_desc* d, uint8_t* base) {
     w.h_shared = nullptr;
     if (d->shared_gate_up) w.h_shared = (__half*)take(T * (size_t)(d->shared_gate_up->n / 2) * 2);
     // decode split-K buffers
-    w.ks_gu = w.ks_d = w.ks_sgu = w.ks_sd = 1;
-    w.part_gu = w.part_d = w.part_sgu = w.part_sd = nullptr;
-    w.cnt_gu = w.cnt_d = w.cnt_sgu = w.cnt_sd = nullptr;
+    w.ks_gu = w.ks_d = 1;
+    w.part_gu = w.part_d = nullptr;
+    w.cnt_gu = w.cnt_d = nullptr;
     w.n_counters = 0;
     if (d->T <= 8) {
         const int segs = (int)std::min(E, P);
@@ -130,22 +130,15 @@ MoeWs carve(const bq_moe_desc* d, uint8_t* base) {
         w.part_gu = (float*)take((size_t)segs * t_gu * w.ks_gu * 4096);
         w.part_d = (float*)take((size_t)segs * t_d * w.ks_d * 4096);
         int nc = segs * t_gu + segs * t_d;
-        if (d->shared_gate_up) {
-            const int n_s = d->shared_gate_up->n, i_s = n_s / 2;
-            w.ks_sgu = bq::qgemv_ksplit(d->shared_gate_up->fmt, n_s, (int)H, 1, d->T);
-            w.ks_sd = bq::qgemv_ksplit(d->shared_down->fmt, (int)H, i_s, 1, d->T);
-            w.part_sgu = (float*)take((size_t)(n_s / bq::kTileRows) * w.ks_sgu * 4096);
-            w.part_sd = (float*)take((size_t)t_d * w.ks_sd * 4096);
-            nc += n_s / bq::kTileRows + t_d;
-        }
+        // The shared expert's GEMVs run beside the routed ones without a K split
+        // (no partials, no counters): they take the quarter-CTA form, the K pieces
+        // summed inside each CTA, which leaves the routed GEMVs more room than K
+        // split across CTAs (measured on the hidden-4096 Q2_K layer: B = 1 44.8 ->
+        // 43.0 us, B = 2-8 0.6-1.2% faster).
         int32_t* cnt = (int32_t*)take((size_t)nc * 4);
         w.n_counters = nc;
         w.cnt_gu = cnt;
         w.cnt_d = cnt ? cnt + segs * t_gu : nullptr;
-        if (d->shared_gate_up) {
-            w.cnt_sgu = cnt ? w.cnt_d + segs * t_d : nullptr;
-            w.cnt_sd = cnt ? w.cnt_sgu + d->shared_gate_up->n / bq::kTileRows : nullptr;
-        }
     }
     w.bytes = off;
     return w;
@@ -229,13 +222,12 @@ constexpr int kSmallSegment = 8;
 constexpr int kSmallMean = 64;
 
 // One dense weight over `m` rows of x (single segment).
-bq::QgemvParams dense_params(const bq_qweight* w, int m, const __half* x, float* y, __half* h, int ldy,
-                             int ksplit = 1, float* partial = nullptr, int32_t* counters = nullptr) {
+bq::QgemvParams dense_params(const bq_qweight* w, int m, const __half* x, float* y, __half* h, int ldy) {
     bq::QgemvParams p{};
     p.w = static_cast<const uint8_t*>(w->data);
     p.fmt = w->fmt; p.n = w->n; p.k = w->k; p.swiglu = w->swiglu;
     p.m = m; p.x = x; p.y = y; p.h = h; p.ldy = ldy;
-    p.ksplit = ksplit; p.partial = partial; p.counters = counters;
+    p.ksplit = 1;
     return p;
 }
 
@@ -300,11 +292,12 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
     const bool decode = T <= kMoeGemvTokens || !bq::gemm_supported(d->w_gate_up.fmt);
 
     // The shared expert runs on a side stream, concurrently with the routed
-    // experts; the combine waits for both.  Prefill (tensor-core GEMMs, which
-    // need only x and keep no counters) forks here, so that the shared GEMMs
-    // also fill the SMs that the routing front end leaves idle.  Decode forks
-    // after the routing kernel, which clears the split-K counters of every
-    // GEMV of the layer, the shared expert's included.
+    // experts; the combine waits for both.  It needs only x and keeps no split-K
+    // counters.  Prefill (tensor-core GEMMs) forks here, before the routing, so
+    // that the shared GEMMs also fill the SMs that the routing front end leaves
+    // idle.  Decode forks after the routing kernel: forked before it, the shared
+    // GEMVs took the SMs ahead of the routed gate/up GEMV, the critical path
+    // (measured on the hidden-4096 Q2_K layer: B = 1 43.0 -> 47.0 us).
     int accumulate = 0;
     std::unique_lock<std::mutex> side_lock;
     SideStream* side = nullptr;
@@ -318,17 +311,27 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
         return st;
     };
     const bool shared_gemm = d->shared_gate_up && T > kMoeGemvTokens && bq::gemm_supported(d->shared_gate_up->fmt);
-    if (shared_gemm) {
+    auto launch_shared = [&](bool gemm) -> bq_status {
         const cudaStream_t ss = fork_side();
         bq::stage_begin(BQ_STAGE_SHARED, ss);
-        if ((s = bq::launch_gemm_shared(d->shared_gate_up, d->shared_down, T, xh, w.h_shared, y,
-                                        d->shared_gate_up->n / 2, base + w.bytes, ss)) != BQ_OK)
-            return s;
+        if (gemm) {
+            const bq_status r = bq::launch_gemm_shared(d->shared_gate_up, d->shared_down, T, xh, w.h_shared, y,
+                                                       d->shared_gate_up->n / 2, base + w.bytes, ss);
+            if (r != BQ_OK) return r;
+        } else {
+            bq::QgemvParams sgu = dense_params(d->shared_gate_up, T, xh, nullptr, w.h_shared, 0);
+            bq::QgemvParams sdn = dense_params(d->shared_down, T, w.h_shared, y, nullptr, H);
+            sgu.grid_groups = sdn.grid_groups = 1;   // more than 8 tokens: one CTA row per token group
+            bq::launch_qgemv(sgu, 1, ss);
+            bq::launch_qgemv(sdn, 1, ss);
+        }
         bq::stage_end(BQ_STAGE_SHARED, ss);
         if (side && cudaEventRecord(side->join, ss) != cudaSuccess)
             return bq::fail(BQ_ERR_CUDA, "bq_moe_gather_qmm: cudaEventRecord on the side stream failed");
         accumulate = 1;
-    }
+        return BQ_OK;
+    };
+    if (shared_gemm && (s = launch_shared(true)) != BQ_OK) return s;
 
     bq::stage_begin(BQ_STAGE_ROUTE_PERMUTE, st);
     if (bq::route_permute_small_ok(T, k)) {
@@ -356,23 +359,7 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
     if (!decode)
         bq::launch_gemm_moe_prepare(d, xh, w.perm_token, w.seg_count, w.n_segments, small_max, base + w.bytes, st);
     bq::stage_end(BQ_STAGE_ROUTE_PERMUTE, st);
-
-    // Decode: the shared expert's two GEMVs (neither they nor the routed
-    // experts fill the GPU at these sizes).
-    if (d->shared_gate_up && T <= kMoeGemvTokens) {
-        const cudaStream_t ss = fork_side();
-        bq::stage_begin(BQ_STAGE_SHARED, ss);
-        bq::QgemvParams sgu = dense_params(d->shared_gate_up, T, xh, nullptr, w.h_shared, 0, w.ks_sgu, w.part_sgu,
-                                           w.cnt_sgu);
-        bq::QgemvParams sdn = dense_params(d->shared_down, T, w.h_shared, y, nullptr, H, w.ks_sd, w.part_sd, w.cnt_sd);
-        sgu.grid_groups = sdn.grid_groups = 1;   // more than 8 tokens: one CTA row per token group
-        bq::launch_qgemv(sgu, 1, ss);
-        bq::launch_qgemv(sdn, 1, ss);
-        bq::stage_end(BQ_STAGE_SHARED, ss);
-        if (side && cudaEventRecord(side->join, ss) != cudaSuccess)
-            return bq::fail(BQ_ERR_CUDA, "bq_moe_gather_qmm: cudaEventRecord on the side stream failed");
-        accumulate = 1;
-    }
+    if (d->shared_gate_up && T <= kMoeGemvTokens && (s = launch_shared(false)) != BQ_OK) return s;
 
     if (decode) {
         bq::QgemvParams gu{};
@@ -413,10 +400,8 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
 
     if (d->shared_gate_up && !accumulate) {   // a shared expert the GEMM cannot take: GEMVs on this stream
         bq::stage_begin(BQ_STAGE_SHARED, st);
-        bq::launch_qgemv(dense_params(d->shared_gate_up, T, xh, nullptr, w.h_shared, 0, w.ks_sgu, w.part_sgu,
-                                      w.cnt_sgu), 1, st);
-        bq::launch_qgemv(dense_params(d->shared_down, T, w.h_shared, y, nullptr, H, w.ks_sd, w.part_sd,
-                                      w.cnt_sd), 1, st);
+        bq::launch_qgemv(dense_params(d->shared_gate_up, T, xh, nullptr, w.h_shared, 0), 1, st);
+        bq::launch_qgemv(dense_params(d->shared_down, T, w.h_shared, y, nullptr, H), 1, st);
         bq::stage_end(BQ_STAGE_SHARED, st);
         accumulate = 1;
     }
