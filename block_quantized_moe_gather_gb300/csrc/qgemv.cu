@@ -208,63 +208,59 @@ __device__ __forceinline__ uint32_t q2_code(uint32_t w, uint32_t wh, int p) {
 
 // Stages the rows of one token group (list rows row0 .. row0 + ntok - 1,
 // gathered through src_row) for the slabs [ks_lo, ks_lo + share).  A unit is
-// (slab i, token g, quarter t): 64 values, one thread; the four quarters of a
-// (slab, token) sit in adjacent lanes and combine their maxima by shuffles.
-// The values are read twice (the second time from L1), one sub-block at a
-// time, so that few of them are live at once.
+// (slab i, token g, K quarter t, sub-block sb of the quarter): 16 values, one
+// thread, read once into registers.  The 16 units of a (slab, token) sit in
+// adjacent lanes and combine their maxima by shuffles, so a single token's
+// slabs already spread over all the CTA's warps.
 __device__ __forceinline__ void q2s_stage(const bq::QgemvParams& p, int row0, int ntok, int ks_lo, int share,
                                           uint8_t* stage) {
-    const int units = share * ntok * 4;
+    const int units = share * ntok * 16;
     const int lane = threadIdx.x & 31;
     for (int ub = threadIdx.x & ~31; ub < units; ub += blockDim.x) {   // warp-uniform bound (shuffles below)
         const int u = ub + lane;
-        const bool live = u < units;
-        const int t = u & 3, gi = u >> 2, g = gi % ntok, i = gi / ntok;
-        const uint4* xp = nullptr;
-        __half2 m2 = __float2half2_rn(0.f);
+        const bool live = u < units;   // a (slab, token) has all its 16 lanes live or none
+        const int sb = u & 3, t = (u >> 2) & 3, gi = u >> 4, g = gi % ntok, i = gi / ntok;
+        uint4 q[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
         if (live) {
             const int lr = row0 + g;
             const int src = p.src_row ? __ldg(p.src_row + lr) : lr;
-            xp = reinterpret_cast<const uint4*>(p.x + (int64_t)src * p.k + (int64_t)(ks_lo + i) * 256 + 64 * t);
-#pragma unroll
-            for (int v8 = 0; v8 < 8; ++v8) {
-                const uint4 q = __ldg(xp + v8);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) m2 = __hmax2(m2, __habs2(bq::u32_as_h2(comp(q, j))));
-            }
+            const uint4* xp =
+                reinterpret_cast<const uint4*>(p.x + (int64_t)src * p.k + (int64_t)(ks_lo + i) * 256 + 64 * t + 16 * sb);
+            q[0] = __ldg(xp);
+            q[1] = __ldg(xp + 1);
         }
+        __half2 m2 = __float2half2_rn(0.f);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) m2 = __hmax2(m2, __habs2(bq::u32_as_h2(comp(q[h], j))));
         float mx = fmaxf(__low2float(m2), __high2float(m2));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
         if (!live) continue;
         // 2^S * max in [256, 512); max is an fp16 value, a normal fp32 number
         const int S = (mx > 0.f && mx <= 65504.f) ? 8 - ((__float_as_int(mx) >> 23) - 127) : 0;
-        const float fs = __int_as_float((127 + S) << 23);
         uint8_t* sl = stage + i * kQ2sSlabBytes;
-#pragma unroll 1
-        for (int sb = 0; sb < 4; ++sb) {   // values 16 sb .. + 15 of the quarter = steps 4 sb .. 4 sb + 3
-            float sum = 0.f;
+        float sum = 0.f;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {   // 16 bytes: steps 4 sb + 2h, + 1 (step pair 2 sb + h)
-                const uint4 q = __ldg(xp + 2 * sb + h);
-                uint32_t o[4];
+        for (int h = 0; h < 2; ++h) {   // 16 bytes: steps 4 sb + 2h, + 1 (step pair 2 sb + h)
+            uint32_t o[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {   // word j: elements 2 (j & 1), + 1 of step 4 sb + 2h + j / 2
-                    const int J = q2_j(2 * (2 * h + (j >> 1)) + (j & 1));
-                    const float f = __int_as_float((127 + S - J) << 23);   // 2^(S - J), exact
-                    const float2 xf = __half22float2(bq::u32_as_h2(comp(q, j)));
-                    sum += xf.x + xf.y;
-                    o[j] = bq::h2_as_u32(__floats2half2_rn(xf.x * f, xf.y * f));
-                }
-                *reinterpret_cast<uint4*>(sl + (((2 * sb + h) * 4 + t) * 8 + g) * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+            for (int j = 0; j < 4; ++j) {   // word j: elements 2 (j & 1), + 1 of step 4 sb + 2h + j / 2
+                const int J = q2_j(2 * (2 * h + (j >> 1)) + (j & 1));
+                const float f = __int_as_float((127 + S - J) << 23);   // 2^(S - J), exact
+                const float2 xf = __half22float2(bq::u32_as_h2(comp(q[h], j)));
+                sum += xf.x + xf.y;
+                o[j] = bq::h2_as_u32(__floats2half2_rn(xf.x * f, xf.y * f));
             }
-            const float ss = sum * fs;
-            const __half hi = __float2half_rn(ss);
-            reinterpret_cast<__half*>(sl + kQ2sXsBytes + (t * 8 + g) * 8)[sb] = hi;
-            reinterpret_cast<__half*>(sl + kQ2sXsBytes + kQ2sSsBytes + (t * 8 + g) * 8)[sb] =
-                __float2half_rn(ss - __half2float(hi));
+            *reinterpret_cast<uint4*>(sl + (((2 * sb + h) * 4 + t) * 8 + g) * 16) = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        if (t == 0) reinterpret_cast<float*>(sl + kQ2sXsBytes + 2 * kQ2sSsBytes)[g] = __int_as_float((127 - S) << 23);
+        const float ss = sum * __int_as_float((127 + S) << 23);
+        const __half hi = __float2half_rn(ss);
+        reinterpret_cast<__half*>(sl + kQ2sXsBytes + (t * 8 + g) * 8)[sb] = hi;
+        reinterpret_cast<__half*>(sl + kQ2sXsBytes + kQ2sSsBytes + (t * 8 + g) * 8)[sb] =
+            __float2half_rn(ss - __half2float(hi));
+        if ((u & 15) == 0) reinterpret_cast<float*>(sl + kQ2sXsBytes + 2 * kQ2sSsBytes)[g] = __int_as_float((127 - S) << 23);
     }
 }
 
@@ -521,8 +517,12 @@ __device__ __forceinline__ void qgemv_epilogue(const bq::QgemvParams& p, const f
 // quarter of a tile and its 8 warps take 8 contiguous K pieces; the partials
 // are summed in warp order, so results stay bit-reproducible either way.
 // KW = 1 (the split-scale path): 128 threads, warp w takes row quarter w over
-// the CTA's whole K share; four CTAs fit on an SM, so a grid of a few hundred
-// CTAs is spread over the SMs in steps of a quarter of the old CTA size.
+// the CTA's whole K share; a grid of a few hundred CTAs is spread over the
+// SMs in steps of a quarter of the old CTA size.  The register bound is set
+// for three CTAs per SM (up to 168 registers a thread): the K split targets
+// about 2.5 CTAs per SM, and the extra registers schedule better than a
+// fourth resident CTA would help (decode B = 2 58.7 -> 54.1 us together with
+// the sub-block staging below).
 //
 // NORM (single segment, no SwiGLU): RMSNorm in front of the GEMV.  Every CTA
 // first computes 1/rms of its token rows over the whole K (bq::rows_inv_rms),
@@ -537,7 +537,7 @@ __device__ __forceinline__ void qgemv_epilogue(const bq::QgemvParams& p, const f
 // entry y; the grid has a row per possible entry, and rows past the list's
 // end return at once.
 template <int FMT, bool SWIGLU, int KW, bool NORM, bool Q2S = false, bool LIST = false>
-__global__ void __launch_bounds__(KW == 1 ? 128 : kThreads, NORM ? 1 : (KW == 1 ? 4 : 2))   // (the norm-fused GEMV needs more registers)
+__global__ void __launch_bounds__(KW == 1 ? 128 : kThreads, NORM ? 1 : (KW == 1 ? 3 : 2))   // (the norm-fused GEMV needs more registers)
 qgemv_kernel(const bq::QgemvParams p) {
     using T = Traits<FMT>;
     static_assert(KW == 1 || KW == 2 || KW == 8, "K ways per CTA");
