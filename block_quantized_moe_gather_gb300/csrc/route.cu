@@ -89,42 +89,47 @@ __device__ __forceinline__ void route_row(const float* __restrict__ row, const f
             }
         }
     }
+    // Order-preserving 32-bit keys: a larger float gives a larger key, every NaN
+    // the smallest (it loses to any number), -0 and +0 the same.  Each round
+    // takes the largest key of the warp, ties to the lower expert id, with two
+    // warp reductions: the largest key, then the smallest id holding it.
+    uint32_t ok[NPER];
+#pragma unroll
+    for (int i = 0; i < NPER; ++i) {
+        const float kx = key[i] + 0.f;   // -0 -> +0
+        const uint32_t u = __float_as_uint(kx);
+        ok[i] = kx == kx ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+    }
     uint32_t taken = 0;
     float exsel = 0.f, z0 = 0.f, denom = 0.f;
     esel = 0;
     for (int j = 0; j < k; ++j) {
         // lane-local best among untaken entries; "none" is e = INT_MAX
+        uint32_t bk = 0u;
         float bz = 0.f, bs = 0.f;
         int be = 0x7fffffff;
 #pragma unroll
         for (int i = 0; i < NPER; ++i) {
             const int e = lane + 32 * i;
-            if (e < E && !(taken >> i & 1u)) {
-                // e ascends within a lane, so ties keep the lower id; a NaN loses to any number
-                const bool better = be == 0x7fffffff || key[i] > bz || (!(bz == bz) && key[i] == key[i]);
-                if (better) { bz = key[i]; bs = score[i]; be = e; }
+            // e ascends within a lane, so ties keep the lower id
+            if (e < E && !(taken >> i & 1u) && (be == 0x7fffffff || ok[i] > bk)) {
+                bk = ok[i]; bz = key[i]; bs = score[i]; be = e;
             }
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float oz = __shfl_xor_sync(0xffffffffu, bz, off);
-            const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-            const bool take = oe != 0x7fffffff &&
-                              (be == 0x7fffffff || oz > bz || (oz == bz && oe < be) ||
-                               (!(bz == bz) && oz == oz));
-            if (take) { bz = oz; bs = os; be = oe; }
-        }
-        if ((be & 31) == lane && be != 0x7fffffff) taken |= 1u << (be >> 5);
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, be == 0x7fffffff ? 0u : bk);
+        const int win = __reduce_min_sync(0xffffffffu, (be != 0x7fffffff && bk == kmax) ? be : 0x7fffffff);
+        const int wl = win & 31;   // expert e sits in lane e % 32
+        if (lane == wl && win != 0x7fffffff) taken |= 1u << (win >> 5);
+        const float wz = __shfl_sync(0xffffffffu, bz, wl), ws = __shfl_sync(0xffffffffu, bs, wl);
         float part;
         if (RULE == RULE_SOFTMAX) {
-            if (j == 0) z0 = bz;
-            part = expf(bz - z0);
+            if (j == 0) z0 = wz;
+            part = expf(wz - z0);
         } else {
-            part = bs;
+            part = ws;
         }
         denom += part;
-        if (lane == j) { exsel = part; esel = be; }
+        if (lane == j) { exsel = part; esel = win; }
     }
     if (RULE == RULE_SQRTSOFTPLUS) wsel = exsel * scale;
     else wsel = exsel / denom;
@@ -166,7 +171,9 @@ route_permute_small_kernel(const float* __restrict__ logits, const float* __rest
     __shared__ int32_t s_rank[256];    // rank among the earlier pairs of its expert
     __shared__ int32_t s_off[1024];    // per expert: pairs with a smaller expert id
     __shared__ int32_t s_cnt[1024];
+    __shared__ int32_t s_nseg;         // active experts
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) s_nseg = 0;
     const int P = T * k;
     bq::allow_dependents();   // the GEMV that follows may be scheduled now; it waits for this grid
     for (int i = threadIdx.x; i < out.n_zero; i += kSmallThreads) out.zero[i] = 0;
@@ -208,6 +215,7 @@ route_permute_small_kernel(const float* __restrict__ logits, const float* __rest
         for (int i = 0; i < f; ++i) rank += s_ids[i] == e;
         s_rank[f] = rank;
         s_first[f] = e >= 0 && rank == 0;
+        if (s_first[f]) atomicAdd(&s_nseg, 1);
     }
     __syncthreads();
     if (threadIdx.x < P) {
@@ -230,11 +238,7 @@ route_permute_small_kernel(const float* __restrict__ logits, const float* __rest
             }
         }
     }
-    if (threadIdx.x == 0) {
-        int n = 0;
-        for (int i = 0; i < P; ++i) n += s_first[i];
-        *out.n_segments = n;
-    }
+    if (threadIdx.x == 0) *out.n_segments = s_nseg;
 }
 
 // chunk_hist is stored expert-major: chunk_hist[e * n_chunks + c].
