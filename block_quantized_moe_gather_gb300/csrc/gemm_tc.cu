@@ -510,6 +510,10 @@ __device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + _
 template <int FMT, int EPI>
 __global__ void __launch_bounds__(kThreads, 2)
 gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a) {
+    // a kernel launched behind this one as a programmatic dependent (the
+    // small-expert GEMV of the same stage) starts once every CTA of this grid
+    // has started: its CTAs then take the SMs that this grid's last wave frees
+    bq::allow_dependents();
     using F = G<FMT>;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -1007,10 +1011,10 @@ bq_status launch_gemm_moe(const bq_moe_desc* d, const __half*, const int32_t*, c
     a.seg_expert = seg_expert; a.seg_start = seg_start; a.seg_count = seg_count;
     a.h = h; a.ldh = I;
     launch(d->w_gate_up.fmt, EPI_SWIGLU, map_x, a, dim3(2 * I / kTileRows, max_tiles), st);
-    if (small_gu) {
+    if (small_gu) {   // a programmatic dependent of the GEMM: it fills the SMs of the GEMM's last wave
         QgemvParams q = *small_gu;
         q.seg_list = g.small; q.n_list = g.n_small;
-        launch_qgemv(q, max_segments, st);
+        launch_qgemv(q, max_segments, st, /*after_previous=*/true);
     }
     stage_end(BQ_STAGE_GATE_UP, st);
 
@@ -1025,7 +1029,7 @@ bq_status launch_gemm_moe(const bq_moe_desc* d, const __half*, const int32_t*, c
     if (small_dn) {
         QgemvParams q = *small_dn;
         q.seg_list = g.small; q.n_list = g.n_small;
-        launch_qgemv(q, max_segments, st);
+        launch_qgemv(q, max_segments, st, /*after_previous=*/true);
     }
     stage_end(BQ_STAGE_DOWN, st);
     return BQ_OK;

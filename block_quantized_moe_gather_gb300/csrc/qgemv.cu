@@ -552,8 +552,13 @@ qgemv_kernel(const bq::QgemvParams p) {
     __shared__ float s_part[NORM ? 8 : 1][8];
     static_assert(!NORM || (KW != 1 && kThreads == bq::kNormThreads), "the norm prologue is written for 256 threads");
 
-    // launched right behind the kernel that produced the routing / activations
-    bq::grid_dependency_wait();
+    // Launched right behind the kernel that produced the routing / activations.
+    // The list-driven GEMV of small experts is launched behind the grouped GEMM
+    // of the same stage instead, whose output it does not read (its list,
+    // source rows and activations come from kernels that completed before
+    // that GEMM started, and its output rows are not the GEMM's): it does not
+    // wait for the GEMM, so its CTAs fill the SMs of the GEMM's last wave.
+    if constexpr (!LIST) bq::grid_dependency_wait();
     bq::allow_dependents();
     const bool gg = p.grid_groups && !p.seg_expert;   // grid.y = token groups of one segment
 
