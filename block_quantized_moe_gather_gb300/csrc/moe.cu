@@ -322,6 +322,7 @@ extern "C" bq_status bq_moe_gather_qmm(const bq_moe_desc* d, const uint16_t* x, 
             bq::QgemvParams sgu = dense_params(d->shared_gate_up, T, xh, nullptr, w.h_shared, 0);
             bq::QgemvParams sdn = dense_params(d->shared_down, T, w.h_shared, y, nullptr, H);
             sgu.grid_groups = sdn.grid_groups = 1;   // more than 8 tokens: one CTA row per token group
+            sgu.beside = sdn.beside = 1;
             bq::launch_qgemv(sgu, 1, ss);
             bq::launch_qgemv(sdn, 1, ss);
         }

@@ -81,6 +81,9 @@ struct QgemvParams {
     // takes entry y (no K split).
     const int32_t* seg_list;
     const int32_t* n_list;
+    // 1: the GEMV runs beside other kernels (a MoE layer's shared expert):
+    // keep the 8-warp quarter CTAs rather than taking whole SMs with 16 warps.
+    int beside;
 };
 constexpr int kMaxKsplit = 16;
 // Split factor that gives the GPU enough CTAs for this shape (experts: the

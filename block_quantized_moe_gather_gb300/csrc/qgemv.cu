@@ -516,6 +516,8 @@ __device__ __forceinline__ void qgemv_epilogue(const bq::QgemvParams& p, const f
 // fill the GPU, without a K split across CTAs): a CTA covers one 32-row
 // quarter of a tile and its 8 warps take 8 contiguous K pieces; the partials
 // are summed in warp order, so results stay bit-reproducible either way.
+// KW = 16: the same with 16 warps (512 threads, one CTA per SM) and 16 K
+// pieces, for quarters whose K holds at least 4 slabs per warp.
 // KW = 1 (the split-scale path): 128 threads, warp w takes row quarter w over
 // the CTA's whole K share; a grid of a few hundred CTAs is spread over the
 // SMs in steps of a quarter of the old CTA size.  The register bound is set
@@ -537,20 +539,21 @@ __device__ __forceinline__ void qgemv_epilogue(const bq::QgemvParams& p, const f
 // entry y; the grid has a row per possible entry, and rows past the list's
 // end return at once.
 template <int FMT, bool SWIGLU, int KW, bool NORM, bool Q2S = false, bool LIST = false>
-__global__ void __launch_bounds__(KW == 1 ? 128 : kThreads, NORM ? 1 : (KW == 1 ? 3 : 2))   // (the norm-fused GEMV needs more registers)
+__global__ void __launch_bounds__(KW == 1 ? 128 : KW == 16 ? 2 * kThreads : kThreads,
+                                   NORM || KW == 16 ? 1 : (KW == 1 ? 3 : 2))   // (the norm-fused GEMV needs more registers)
 qgemv_kernel(const bq::QgemvParams p) {
     using T = Traits<FMT>;
-    static_assert(KW == 1 || KW == 2 || KW == 8, "K ways per CTA");
+    static_assert(KW == 1 || KW == 2 || KW == 8 || KW == 16, "K ways per CTA");
     static_assert(!(NORM && SWIGLU), "the norm-fused GEMV has a plain epilogue");
     static_assert(!Q2S || (FMT == BQ_FMT_Q2_K && !NORM), "the split-scale path is Q2_K without the norm");
     extern __shared__ __align__(16) uint8_t q2s_stage_smem[];
     const uint32_t stage_addr = static_cast<uint32_t>(__cvta_generic_to_shared(q2s_stage_smem));
     // partials of the warps with K piece > 0: [quarter (KW 2) or piece - 1 (KW 8)][tile][lane][row half]
-    __shared__ float2 red[KW == 8 ? 7 : KW == 2 ? 4 : 1][2][32][2];
+    __shared__ float2 red[KW >= 8 ? KW - 1 : KW == 2 ? 4 : 1][2][32][2];
     __shared__ int s_last;
     __shared__ float s_inv[NORM ? 8 : 1];
     __shared__ float s_part[NORM ? 8 : 1][8];
-    static_assert(!NORM || (KW != 1 && kThreads == bq::kNormThreads), "the norm prologue is written for 256 threads");
+    static_assert(!NORM || (KW != 1 && KW != 16 && kThreads == bq::kNormThreads), "the norm prologue is written for 256 threads");
 
     // Launched right behind the kernel that produced the routing / activations.
     // The list-driven GEMV of small experts is launched behind the grouped GEMM
@@ -571,13 +574,13 @@ qgemv_kernel(const bq::QgemvParams p) {
         const int count = p.seg_count ? __ldg(p.seg_count + seg) : p.m;
         const int tok_lo = gg ? 8 * y : 0, tok_hi = gg ? min(count, tok_lo + 8) : count;
 
-        const int rt = KW == 8 ? (int)(blockIdx.x >> 2) : (int)blockIdx.x, kp = blockIdx.z;
+        const int rt = KW >= 8 ? (int)(blockIdx.x >> 2) : (int)blockIdx.x, kp = blockIdx.z;
         const int n_tiles = p.n / bq::kTileRows, k_slabs = p.k / T::SK;
         const uint8_t* wbase = p.w + bq::slab_index(e, rt, 0, n_tiles, k_slabs) * T::SB;
 
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-        const int quarter = KW == 8 ? (int)(blockIdx.x & 3) : (warp & 3), rowbase = 32 * quarter;
-        const int kw = KW == 8 ? warp : KW == 2 ? (warp >> 2) : 0;   // this warp's K piece
+        const int quarter = KW >= 8 ? (int)(blockIdx.x & 3) : (warp & 3), rowbase = 32 * quarter;
+        const int kw = KW >= 8 ? warp : KW == 2 ? (warp >> 2) : 0;   // this warp's K piece
         // this CTA's share of the slabs (split K), then KW contiguous pieces of it
         const int ks_lo = (int)((int64_t)k_slabs * kp / p.ksplit), ks_hi = (int)((int64_t)k_slabs * (kp + 1) / p.ksplit);
         const int kt_begin = ks_lo + ((ks_hi - ks_lo) * kw + KW - 1) / KW;
@@ -640,7 +643,7 @@ qgemv_kernel(const bq::QgemvParams p) {
             }
             __syncthreads();   // previous token group's readers of `red` are done
             if (kw) {
-                const int slot = KW == 8 ? kw - 1 : quarter;
+                const int slot = KW >= 8 ? kw - 1 : quarter;
 #pragma unroll
                 for (int tile = 0; tile < 2; ++tile) {
                     red[slot][tile][lane][0] = make_float2(acc[tile][0], acc[tile][1]);
@@ -652,7 +655,7 @@ qgemv_kernel(const bq::QgemvParams p) {
                 // piece 0 adds the other pieces in a fixed order: bit-reproducible
 #pragma unroll
                 for (int j = 0; j < KW - 1; ++j) {
-                    const int slot = KW == 8 ? j : quarter;
+                    const int slot = KW >= 8 ? j : quarter;
 #pragma unroll
                     for (int tile = 0; tile < 2; ++tile) {
                         const float2 r0 = red[slot][tile][lane][0], r1 = red[slot][tile][lane][1];
@@ -751,11 +754,18 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
                                     : qgemv_kernel<FMT, false, 1, false, true, true>;
     }
     const bool list = p.seg_list && p.seg_expert;
+    // Quarter CTAs of 16 warps (16 K pieces, one CTA per SM) for one token
+    // group where K holds at least 4 slabs per warp: twice the loads in flight
+    // of 8 warps on an SM (dense Q8_0 N = K = 4096, m = 1: 9.0 -> 7.4 us).  Not
+    // for several token groups (m = 32: 17.2 -> 21.4 us), nor beside the routed
+    // GEMVs of a MoE step (0.5-0.9 us slower per step).
+    const bool wide = quarters && ny == 1 && !p.gamma && !p.beside && p.k / Traits<FMT>::SK >= 64;
     const Kernel kernel =
         p.gamma ? (quarters ? qgemv_kernel<FMT, false, 8, true> : qgemv_kernel<FMT, false, 2, true>)
         : list ? (q2s ? split_scale_list
                       : p.swiglu ? qgemv_kernel<FMT, true, 2, false, false, true> : qgemv_kernel<FMT, false, 2, false, false, true>)
         : q2s ? split_scale
+        : wide ? (p.swiglu ? qgemv_kernel<FMT, true, 16, false> : qgemv_kernel<FMT, false, 16, false>)
         : quarters ? (p.swiglu ? qgemv_kernel<FMT, true, 8, false> : qgemv_kernel<FMT, false, 8, false>)
                    : (p.swiglu ? qgemv_kernel<FMT, true, 2, false> : qgemv_kernel<FMT, false, 2, false>);
     const size_t smem = q2s ? (size_t)share * kQ2sSlabBytes : 0;
@@ -771,7 +781,7 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
             attr_set[which][dev].store(true, std::memory_order_release);
         }
     }
-    const int threads = q2s ? 128 : kThreads;
+    const int threads = q2s ? 128 : wide ? 2 * kThreads : kThreads;
     if (after_previous) bq::launch_after(kernel, grid, dim3(threads), smem, st, p);
     else kernel<<<grid, threads, smem, st>>>(p);
 }
