@@ -517,7 +517,7 @@ __device__ __forceinline__ void qgemv_epilogue(const bq::QgemvParams& p, const f
 // quarter of a tile and its 8 warps take 8 contiguous K pieces; the partials
 // are summed in warp order, so results stay bit-reproducible either way.
 // KW = 16: the same with 16 warps (512 threads, one CTA per SM) and 16 K
-// pieces, for quarters whose K holds at least 4 slabs per warp.
+// pieces, for quarters whose K holds at least one slab per warp.
 // KW = 1 (the split-scale path): 128 threads, warp w takes row quarter w over
 // the CTA's whole K share; a grid of a few hundred CTAs is spread over the
 // SMs in steps of a quarter of the old CTA size.  The register bound is set
@@ -755,11 +755,11 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
     }
     const bool list = p.seg_list && p.seg_expert;
     // Quarter CTAs of 16 warps (16 K pieces, one CTA per SM) for one token
-    // group where K holds at least 4 slabs per warp: twice the loads in flight
-    // of 8 warps on an SM (dense Q8_0 N = K = 4096, m = 1: 9.0 -> 7.4 us).  Not
-    // for several token groups (m = 32: 17.2 -> 21.4 us), nor beside the routed
-    // GEMVs of a MoE step (0.5-0.9 us slower per step).
-    const bool wide = quarters && ny == 1 && !p.gamma && !p.beside && p.k / Traits<FMT>::SK >= 64;
+    // group where K holds at least one slab per warp: twice the loads in flight
+    // of 8 warps on an SM (N = K = 4096, m = 1: Q8_0 9.0 -> 7.3 us, Q2_K 5.95 ->
+    // 5.69 us).  Not for several token groups (Q8_0 m = 32: 17.2 -> 21.4 us),
+    // nor beside the routed GEMVs of a MoE step (0.5-0.9 us slower per step).
+    const bool wide = quarters && ny == 1 && !p.gamma && !p.beside && p.k / Traits<FMT>::SK >= 16;
     const Kernel kernel =
         p.gamma ? (quarters ? qgemv_kernel<FMT, false, 8, true> : qgemv_kernel<FMT, false, 2, true>)
         : list ? (q2s ? split_scale_list
