@@ -197,8 +197,9 @@ def test_qmm_q2_k_activation_range(lib, m, scale):
 @pytest.mark.parametrize("fmt", ["q8_0", "q2_k", "int4", "mxfp4", "fp8_b128"])
 @pytest.mark.parametrize("m", [1, 8, 9, 64])
 def test_qmm_long_k(lib, fmt, m):
-    # long K and few row tiles: the GEMV splits K over the 8 warps of each
-    # CTA (summed in warp order), N = 2 row tiles
+    # long K and few row tiles: the GEMV splits K over the warps of each CTA
+    # (16 for one token group, m <= 8; 8 otherwise; summed in warp order),
+    # N = 2 row tiles
     g = synth.rng(len(fmt) * 100 + m)
     n, k = 256, {"q8_0": 4096, "q2_k": 8192, "int4": 4096, "mxfp4": 4096, "fp8_b128": 4096}[fmt]
     if fmt == "q8_0":
