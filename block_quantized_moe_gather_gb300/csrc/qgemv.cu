@@ -264,6 +264,28 @@ __device__ __forceinline__ void q2s_stage(const bq::QgemvParams& p, int row0, in
     }
 }
 
+// Thread-block cluster helpers (the split-scale GEMV's K split over a cluster).
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// The shared address `a` of this CTA, mapped to the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t a, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f4(uint32_t a, float x, float y, float z, float w) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(x), "f"(y), "f"(z), "f"(w)
+                 : "memory");
+}
+// Every thread of every CTA of the cluster; the stores before it are seen after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+constexpr int kClusterMaxSplit = 4;
+
 // Shared-memory reads at 32-bit shared addresses, issued where written:
 // the second tile's reads of the same B fragments must not be merged with
 // the first's (that would keep all of them live in registers).
@@ -538,7 +560,7 @@ __device__ __forceinline__ void qgemv_epilogue(const bq::QgemvParams& p, const f
 // LIST (expert GEMVs with a segment list, no K split): grid row y takes list
 // entry y; the grid has a row per possible entry, and rows past the list's
 // end return at once.
-template <int FMT, bool SWIGLU, int KW, bool NORM, bool Q2S = false, bool LIST = false>
+template <int FMT, bool SWIGLU, int KW, bool NORM, bool Q2S = false, bool LIST = false, bool CLUSTER = false>
 __global__ void __launch_bounds__(KW == 1 ? 128 : KW == 16 ? 2 * kThreads : kThreads,
                                    NORM || KW == 16 ? 1 : (KW == 1 ? 3 : 2))   // (the norm-fused GEMV needs more registers)
 qgemv_kernel(const bq::QgemvParams p) {
@@ -546,6 +568,9 @@ qgemv_kernel(const bq::QgemvParams p) {
     static_assert(KW == 1 || KW == 2 || KW == 8 || KW == 16, "K ways per CTA");
     static_assert(!(NORM && SWIGLU), "the norm-fused GEMV has a plain epilogue");
     static_assert(!Q2S || (FMT == BQ_FMT_Q2_K && !NORM), "the split-scale path is Q2_K without the norm");
+    static_assert(!CLUSTER || (Q2S && !LIST && KW == 1), "the cluster K split is the split-scale expert GEMV's");
+    // CLUSTER: the partials of K parts 1 .. ksplit-1, written here by those CTAs
+    __shared__ __align__(16) float cl_part[CLUSTER ? kClusterMaxSplit - 1 : 1][CLUSTER ? 4 : 1][32][8];
     extern __shared__ __align__(16) uint8_t q2s_stage_smem[];
     const uint32_t stage_addr = static_cast<uint32_t>(__cvta_generic_to_shared(q2s_stage_smem));
     // partials of the warps with K piece > 0: [quarter (KW 2) or piece - 1 (KW 8)][tile][lane][row half]
@@ -667,6 +692,35 @@ qgemv_kernel(const bq::QgemvParams p) {
                 if (!kw) qgemv_epilogue<SWIGLU>(p, acc, rt, quarter, g, t, start + tok0, ntok);
                 continue;
             }
+            if constexpr (CLUSTER) {
+                // Split K over the CTAs of one cluster (rank = K part, one token
+                // group): parts 1.. write their accumulators into part 0's shared
+                // memory, one cluster barrier (every CTA of the cluster reaches it:
+                // they share the segment, so they return or continue together),
+                // then part 0 sums them in part order and runs the epilogue.
+                const uint32_t rank = cluster_rank();
+                if (rank > 0) {
+                    const uint32_t dst = cluster_map(
+                        static_cast<uint32_t>(__cvta_generic_to_shared(&cl_part[rank - 1][warp][lane][0])), 0);
+                    st_cluster_f4(dst, acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+                    st_cluster_f4(dst + 16, acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
+                }
+                cluster_sync();
+                if (rank == 0) {
+                    float sum[2][4];
+#pragma unroll
+                    for (int tile = 0; tile < 2; ++tile)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) sum[tile][j] = 0.f + acc[tile][j];
+                    for (int q = 1; q < p.ksplit; ++q)
+#pragma unroll
+                        for (int tile = 0; tile < 2; ++tile)
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) sum[tile][j] += cl_part[q - 1][warp][lane][4 * tile + j];
+                    qgemv_epilogue<SWIGLU>(p, sum, rt, quarter, g, t, start + tok0, ntok);
+                }
+                return;
+            }
             // Split K (one token group only): publish this CTA's partial; the last
             // CTA of the (segment, tile) sums all partials in split order.
             float* part = p.partial + ((int64_t)(seg * n_tiles + rt) * p.ksplit) * 1024;
@@ -747,13 +801,19 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
     // walking several entries in turn, left the SMs underfilled: measured 7% slower)
     dim3 grid(tiles * (quarters ? 4 : 1), ny, p.ksplit);
     using Kernel = void (*)(const bq::QgemvParams);
-    Kernel split_scale = nullptr, split_scale_list = nullptr;   // instantiated for Q2_K only
+    Kernel split_scale = nullptr, split_scale_list = nullptr, split_scale_cluster = nullptr;   // Q2_K only
     if constexpr (FMT == BQ_FMT_Q2_K) {
         split_scale = p.swiglu ? qgemv_kernel<FMT, true, 1, false, true> : qgemv_kernel<FMT, false, 1, false, true>;
         split_scale_list = p.swiglu ? qgemv_kernel<FMT, true, 1, false, true, true>
                                     : qgemv_kernel<FMT, false, 1, false, true, true>;
+        split_scale_cluster = p.swiglu ? qgemv_kernel<FMT, true, 1, false, true, false, true>
+                                       : qgemv_kernel<FMT, false, 1, false, true, false, true>;
     }
     const bool list = p.seg_list && p.seg_expert;
+    // A K split of the split-scale expert GEMV (a one-token-group decode step)
+    // runs over a thread-block cluster of ksplit CTAs, summed in shared memory,
+    // instead of partials in global memory and a last-CTA count.
+    const bool cluster = q2s && !list && p.ksplit > 1 && p.ksplit <= kClusterMaxSplit;
     // Quarter CTAs of 16 warps (16 K pieces, one CTA per SM) for one token
     // group where K holds at least one slab per warp: twice the loads in flight
     // of 8 warps on an SM (N = K = 4096, m = 1: Q8_0 9.0 -> 7.3 us, Q2_K 5.95 ->
@@ -764,6 +824,7 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
         p.gamma ? (quarters ? qgemv_kernel<FMT, false, 8, true> : qgemv_kernel<FMT, false, 2, true>)
         : list ? (q2s ? split_scale_list
                       : p.swiglu ? qgemv_kernel<FMT, true, 2, false, false, true> : qgemv_kernel<FMT, false, 2, false, false, true>)
+        : cluster ? split_scale_cluster
         : q2s ? split_scale
         : wide ? (p.swiglu ? qgemv_kernel<FMT, true, 16, false> : qgemv_kernel<FMT, false, 16, false>)
         : quarters ? (p.swiglu ? qgemv_kernel<FMT, true, 8, false> : qgemv_kernel<FMT, false, 8, false>)
@@ -772,8 +833,8 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
     if (q2s) {   // (expert segments: never the quarter CTAs, which serve a dense matrix)
         // per instantiation (list, swiglu) and device: the attribute belongs to the
         // function on the current device
-        static std::atomic<bool> attr_set[4][64];
-        const int which = 2 * (list ? 1 : 0) + (p.swiglu ? 1 : 0);
+        static std::atomic<bool> attr_set[6][64];
+        const int which = 2 * (list ? 1 : cluster ? 2 : 0) + (p.swiglu ? 1 : 0);
         int dev = 0;
         cudaGetDevice(&dev);
         if (dev >= 0 && dev < 64 && !attr_set[which][dev].load(std::memory_order_acquire)) {
@@ -782,8 +843,27 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
         }
     }
     const int threads = q2s ? 128 : wide ? 2 * kThreads : kThreads;
-    if (after_previous) bq::launch_after(kernel, grid, dim3(threads), smem, st, p);
-    else kernel<<<grid, threads, smem, st>>>(p);
+    if (cluster) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(threads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = (unsigned)p.ksplit;   // grid.z = ksplit: one cluster per (tile, segment)
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = after_previous ? 2 : 1;
+        cudaLaunchKernelEx(&cfg, kernel, p);
+    } else if (after_previous) {
+        bq::launch_after(kernel, grid, dim3(threads), smem, st, p);
+    } else {
+        kernel<<<grid, threads, smem, st>>>(p);
+    }
 }
 
 }  // namespace
