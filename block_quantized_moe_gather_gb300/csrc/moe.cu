@@ -63,6 +63,7 @@ segments_kernel(const int32_t* __restrict__ counts, const int32_t* __restrict__ 
 __global__ void combine_kernel(const float* __restrict__ y_slot, const int32_t* __restrict__ inv, int T,
                                int k, int H, int accumulate, float* __restrict__ y) {
     bq::grid_dependency_wait();   // may be launched behind the down projection
+    bq::allow_dependents();       // the next layer call's routing kernel may be scheduled (it waits for this grid)
     const int h4 = H / 4;
     const int64_t total = (int64_t)T * h4;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;

@@ -175,6 +175,11 @@ route_permute_small_kernel(const float* __restrict__ logits, const float* __rest
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) s_nseg = 0;
     const int P = T * k;
+    // Launched as a programmatic dependent of whatever kernel precedes it on the
+    // stream (the previous layer's last kernel, a router GEMV): it waits for that
+    // grid before touching memory, which it may have written (the logits) or
+    // still read (this workspace), so only the launch latency is hidden.
+    bq::grid_dependency_wait();
     bq::allow_dependents();   // the GEMV that follows may be scheduled now; it waits for this grid
     for (int i = threadIdx.x; i < out.n_zero; i += kSmallThreads) out.zero[i] = 0;
     for (int t = warp; t < T; t += kSmallThreads / 32) {
@@ -416,12 +421,13 @@ template <int RULE>
 void launch_small_rule(const float* logits, const float* bias, int T, int E, int k, float scale,
                        const MoeRouting& out, int32_t* status, cudaStream_t st) {
     const dim3 g(1), b(kSmallThreads);
-    if (E <= 32) route_permute_small_kernel<1, RULE><<<g, b, 0, st>>>(logits, bias, T, E, k, scale, out, status);
-    else if (E <= 64) route_permute_small_kernel<2, RULE><<<g, b, 0, st>>>(logits, bias, T, E, k, scale, out, status);
-    else if (E <= 128) route_permute_small_kernel<4, RULE><<<g, b, 0, st>>>(logits, bias, T, E, k, scale, out, status);
-    else if (E <= 256) route_permute_small_kernel<8, RULE><<<g, b, 0, st>>>(logits, bias, T, E, k, scale, out, status);
-    else if (E <= 512) route_permute_small_kernel<16, RULE><<<g, b, 0, st>>>(logits, bias, T, E, k, scale, out, status);
-    else route_permute_small_kernel<32, RULE><<<g, b, 0, st>>>(logits, bias, T, E, k, scale, out, status);
+    auto go = [&](auto kernel) { bq::launch_after(kernel, g, b, 0, st, logits, bias, T, E, k, scale, out, status); };
+    if (E <= 32) go(route_permute_small_kernel<1, RULE>);
+    else if (E <= 64) go(route_permute_small_kernel<2, RULE>);
+    else if (E <= 128) go(route_permute_small_kernel<4, RULE>);
+    else if (E <= 256) go(route_permute_small_kernel<8, RULE>);
+    else if (E <= 512) go(route_permute_small_kernel<16, RULE>);
+    else go(route_permute_small_kernel<32, RULE>);
 }
 
 void launch_route_permute_small(const float* logits, const float* bias, int T, int E, int k, const MoeRouting& out,
