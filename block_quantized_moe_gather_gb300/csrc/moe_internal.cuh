@@ -63,6 +63,9 @@ struct QgemvParams {
     // publishes a [128][8] fp32 partial to `partial` ([segment][tile][split]);
     // the last CTA of a (segment, tile), counted in `counters`
     // ([segment][tile], zero on entry, left zero), sums them in split order.
+    // (The Q2_K split-scale expert GEMV sums a split of up to 4 inside a
+    // thread-block cluster instead, in the same order; partial and counters
+    // must still be given, as for any split.)
     int ksplit;
     float* partial;
     int32_t* counters;
