@@ -24,6 +24,8 @@
 // (see "Q2_K with split scales" below): codes ANDed into fp16 subnormals,
 // times the sub-block scale in one exact packed multiply, the activations
 // staged once per CTA in shared memory; 27% fewer instructions per weight.
+// Where it splits K (a one-token step), the parts of a tile form a
+// thread-block cluster and are summed in part 0's shared memory.
 //
 // K ordering inside a slab: lane t of a quad owns the contiguous quarter
 // [t*SK/4, (t+1)*SK/4) of the slab's K range; MMA step s takes the four
