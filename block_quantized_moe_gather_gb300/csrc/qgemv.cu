@@ -570,7 +570,7 @@ qgemv_kernel(const bq::QgemvParams p) {
     static_assert(KW == 1 || KW == 2 || KW == 8 || KW == 16, "K ways per CTA");
     static_assert(!(NORM && SWIGLU), "the norm-fused GEMV has a plain epilogue");
     static_assert(!Q2S || (FMT == BQ_FMT_Q2_K && !NORM), "the split-scale path is Q2_K without the norm");
-    static_assert(!CLUSTER || (Q2S && !LIST && KW == 1), "the cluster K split is the split-scale expert GEMV's");
+    static_assert(!CLUSTER || (!LIST && !NORM && (KW == 1 || KW == 2)), "the cluster K split: whole-tile expert GEMVs");
     // CLUSTER: the partials of K parts 1 .. ksplit-1, written here by those CTAs
     __shared__ __align__(16) float cl_part[CLUSTER ? kClusterMaxSplit - 1 : 1][CLUSTER ? 4 : 1][32][8];
     extern __shared__ __align__(16) uint8_t q2s_stage_smem[];
@@ -700,15 +700,17 @@ qgemv_kernel(const bq::QgemvParams p) {
                 // memory, one cluster barrier (every CTA of the cluster reaches it:
                 // they share the segment, so they return or continue together),
                 // then part 0 sums them in part order and runs the epilogue.
+                // (KW = 2: the warps of K half 0 hold the CTA's sums after the
+                // reduction above; the others only take part in the barrier)
                 const uint32_t rank = cluster_rank();
-                if (rank > 0) {
+                if (rank > 0 && !kw) {
                     const uint32_t dst = cluster_map(
                         static_cast<uint32_t>(__cvta_generic_to_shared(&cl_part[rank - 1][warp][lane][0])), 0);
                     st_cluster_f4(dst, acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
                     st_cluster_f4(dst + 16, acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
                 }
                 cluster_sync();
-                if (rank == 0) {
+                if (rank == 0 && !kw) {
                     float sum[2][4];
 #pragma unroll
                     for (int tile = 0; tile < 2; ++tile)
@@ -812,10 +814,11 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
                                        : qgemv_kernel<FMT, false, 1, false, true, false, true>;
     }
     const bool list = p.seg_list && p.seg_expert;
-    // A K split of the split-scale expert GEMV (a one-token-group decode step)
-    // runs over a thread-block cluster of ksplit CTAs, summed in shared memory,
-    // instead of partials in global memory and a last-CTA count.
-    const bool cluster = q2s && !list && p.ksplit > 1 && p.ksplit <= kClusterMaxSplit;
+    // A K split of an expert GEMV over whole tiles (a one-token-group decode
+    // step) runs over a thread-block cluster of ksplit CTAs, summed in shared
+    // memory, instead of partials in global memory and a last-CTA count.
+    const bool cluster = p.seg_expert && !list && !p.gamma && !quarters && p.ksplit > 1 &&
+                         p.ksplit <= kClusterMaxSplit;
     // Quarter CTAs of 16 warps (16 K pieces, one CTA per SM) for one token
     // group where K holds at least one slab per warp: twice the loads in flight
     // of 8 warps on an SM (N = K = 4096, m = 1: Q8_0 9.0 -> 7.3 us, Q2_K 5.95 ->
@@ -826,7 +829,9 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
         p.gamma ? (quarters ? qgemv_kernel<FMT, false, 8, true> : qgemv_kernel<FMT, false, 2, true>)
         : list ? (q2s ? split_scale_list
                       : p.swiglu ? qgemv_kernel<FMT, true, 2, false, false, true> : qgemv_kernel<FMT, false, 2, false, false, true>)
-        : cluster ? split_scale_cluster
+        : cluster ? (q2s ? split_scale_cluster
+                         : p.swiglu ? qgemv_kernel<FMT, true, 2, false, false, false, true>
+                                    : qgemv_kernel<FMT, false, 2, false, false, false, true>)
         : q2s ? split_scale
         : wide ? (p.swiglu ? qgemv_kernel<FMT, true, 16, false> : qgemv_kernel<FMT, false, 16, false>)
         : quarters ? (p.swiglu ? qgemv_kernel<FMT, true, 8, false> : qgemv_kernel<FMT, false, 8, false>)
