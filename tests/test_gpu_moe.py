@@ -30,6 +30,10 @@ SMALL = [
     _case("fp8_t9", "fp8_b128", 9, 256, 128, 4, 4),
     _case("fp8_t32_shared", "fp8_b128", 32, 256, 256, 4, 2, shared="q8_0"),
     _case("q2k_t32_shared", "q2_k", 32, 512, 256, 8, 3, shared="q8_0"),
+    # one token, long K over few tiles: the gate/up GEMV splits K four ways and
+    # sums the parts inside a thread-block cluster (split-scale and 256-thread kernels)
+    _case("q2k_t1_split4_shared", "q2_k", 1, 4096, 256, 8, 2, shared="q8_0"),
+    _case("int4_t1_split4", "int4", 1, 4096, 128, 8, 2),
     # first size on the tensor-core path
     _case("mxfp4_t33", "mxfp4", 33, 256, 128, 4, 4),
     # segments cut into several token chunks by the work queue: one expert of
