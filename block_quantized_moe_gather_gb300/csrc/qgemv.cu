@@ -892,6 +892,17 @@ int qgemv_ksplit(int fmt, int n, int k, int max_segments, int max_tokens, bool e
         const int k_slabs = k / fmt_info(fmt).slab_k;
         return std::max(1, std::min(want, std::min(kMaxKsplit, k_slabs / 4)));
     }
+    if (experts) {
+        // The other formats' expert GEMVs (256-thread CTAs, two per SM): their K
+        // split is summed inside a cluster (up to kClusterMaxSplit parts), so K is
+        // split until the grid holds just under two CTAs per SM, one wave, keeping
+        // at least 4 slabs (2 per K-half warp) per CTA.
+        const int ctas = (n / kTileRows) * max_segments;
+        const int want = (2 * sms - 1) / ctas;
+        const int slab_k = fmt_info(fmt).slab_k;
+        if (slab_k <= 0) return 1;
+        return std::max(1, std::min(want, std::min(kClusterMaxSplit, k / slab_k / 4)));
+    }
     // About one CTA per SM: a split adds a partial round trip and a last-CTA
     // reduction, and short K shares never fill the register prefetch ring,
     // so K is split only as far as needed to reach the SM count, keeping at
