@@ -118,7 +118,9 @@ MoeWs carve(const bq_moe_desc* d, uint8_t* base) {
     w.y_slot = (float*)take(P * H * 4);
     w.h_shared = nullptr;
     if (d->shared_gate_up) w.h_shared = (__half*)take(T * (size_t)(d->shared_gate_up->n / 2) * 2);
-    // decode split-K buffers
+    // decode split-K buffers. K is split only when the whole call holds at most
+    // 8 tokens: the split-K sums (through partials or inside a cluster) cover one
+    // 8-token group per segment, and a larger call leaves ks_gu = ks_d = 1.
     w.ks_gu = w.ks_d = 1;
     w.part_gu = w.part_d = nullptr;
     w.cnt_gu = w.cnt_d = nullptr;
