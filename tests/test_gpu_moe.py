@@ -42,6 +42,10 @@ SMALL = [
     _case("int4_e1_600", "int4", 600, 256, 128, 1, 1),
     _case("q2k_long_and_short", "q2_k", 260, 512, 256, 3, 2, zipf=True, shared="q8_0"),
     _case("fp8_long_segments", "fp8_b128", 400, 256, 256, 3, 2),
+    # one token, top-8 of 8 experts, inter 1024: the down GEMV of the 256-thread
+    # formats also splits K (8 slabs) in two inside a cluster
+    _case("int4_t1_down_cluster", "int4", 1, 2048, 1024, 8, 8),
+    _case("mxfp4_t1_down_cluster", "mxfp4", 1, 2048, 1024, 8, 8),
 ]
 
 
@@ -67,14 +71,26 @@ def test_moe_decode_small(lib, base, t):
 
 
 @pytest.mark.parametrize("case", [
-    # Q2_K expert GEMVs on the split-scale path: K split over two CTAs per tile
-    # (few CTAs: 4 gate/up row tiles x 2-6 segments, K = 4096)
+    # Q2_K expert GEMVs of a decode step, by the K share each CTA takes. The K
+    # split is chosen for about 2.5 CTAs per SM (152 SMs), at least 4 slabs of
+    # K = 256 per part; split-scale CTAs stage at most 22 slabs, longer shares
+    # take the register-ring GEMV.
+    # few CTAs (4 gate/up row tiles x 2-6 segments, K = 4096): K split four ways
+    # in a cluster
     _case("dec_q2k_ksplit_t1", "q2_k", 1, 4096, 256, 16, 2),
     _case("dec_q2k_ksplit_t3", "q2_k", 3, 4096, 256, 16, 2),
-    # the largest activation stage (22 slabs of K = 5632 in one CTA), and one
-    # slab over it (K = 6144: the register-ring GEMV)
-    _case("dec_q2k_stage_22", "q2_k", 4, 5632, 1024, 12, 4),
-    _case("dec_q2k_stage_24", "q2_k", 4, 6144, 1024, 12, 4),
+    # 32 gate/up tiles x 12 segments = 384 CTAs, no split: the largest stage,
+    # 22 slabs (K = 5632) in one CTA
+    _case("dec_q2k_stage_22", "q2_k", 3, 5632, 2048, 12, 4),
+    # 96 gate/up and 48 down tiles x 8 segments, no split, 24 slabs per CTA
+    # (hidden = inter = 6144): both GEMVs on the register ring
+    _case("dec_q2k_ring", "q2_k", 2, 6144, 6144, 8, 4),
+    # 16 gate/up tiles x 12 segments = 192 CTAs: K = 11776 split in two inside a
+    # cluster, 23 slabs per part: the register ring with the cluster sum
+    _case("dec_q2k_ring_cluster", "q2_k", 3, 11776, 1024, 12, 4),
+    # 4 gate/up tiles x 2 segments: K = 8192 split eight ways, more parts than a
+    # cluster takes: split-scale parts summed through global partials
+    _case("dec_q2k_split8_partials", "q2_k", 1, 8192, 256, 8, 2),
 ], ids=lambda c: c.name)
 def test_moe_decode_q2k_k_shares(lib, case):
     from helpers import oracle_moe_threaded
@@ -91,6 +107,9 @@ def test_moe_decode_q2k_k_shares(lib, case):
     # no expert small enough (an empty GEMV list), and every expert small (no GEMM tile)
     _case("pre_q2k_none_small", "q2_k", 40, 256, 256, 4, 2),
     _case("pre_q2k_all_small", "q2_k", 40, 256, 256, 64, 2, shared="q8_0"),
+    # hidden 6144 (24 slabs): the listed experts' gate/up takes the register-ring
+    # list GEMV, longer than a split-scale stage
+    _case("pre_q2k_list_ring", "q2_k", 40, 6144, 256, 64, 2, zipf=True),
 ], ids=lambda c: c.name)
 def test_moe_prefill_small_experts(lib, case):
     inp = synth.moe_inputs(case)
