@@ -18,6 +18,18 @@ def _qmm(lib, qw, x):
     return y.cpu().numpy()
 
 
+def _draw_weight(g, fmt, n, k):
+    if fmt == "q8_0":
+        return synth.q8_0_blocks(g, n, k)
+    if fmt == "q2_k":
+        return synth.q2_k_blocks(g, n, k)
+    if fmt == "mxfp4":
+        return synth.mxfp4_blocks(g, n, k)
+    if fmt == "fp8_b128":
+        return synth.fp8_block_weight(g, (), n, k)
+    return synth.int4_weight(g, (n,), k)
+
+
 @pytest.mark.parametrize("fmt,n,k", [("q8_0", 128, 64), ("q8_0", 384, 576), ("q2_k", 256, 512),
                                      ("q2_k", 128, 256), ("int4", 256, 384), ("int4", 128, 128),
                                      ("mxfp4", 256, 384), ("mxfp4", 128, 128),
@@ -25,20 +37,31 @@ def _qmm(lib, qw, x):
 @pytest.mark.parametrize("m", [1, 3, 8, 13, 40, 70, 130])
 def test_qmm_small_shapes(lib, fmt, n, k, m):
     g = synth.rng(n + k + m)
-    if fmt == "q8_0":
-        w = synth.q8_0_blocks(g, n, k)
-    elif fmt == "q2_k":
-        w = synth.q2_k_blocks(g, n, k)
-    elif fmt == "mxfp4":
-        w = synth.mxfp4_blocks(g, n, k)
-    elif fmt == "fp8_b128":
-        w = synth.fp8_block_weight(g, (), n, k)
-    else:
-        w = synth.int4_weight(g, (n,), k)
+    w = _draw_weight(g, fmt, n, k)
     qw = make_qweight(lib, fmt, w, 1, n, k)
     x = synth.fp16_normal(g, (m, k))
     ref = O.qmm(x, dequant(fmt, w).reshape(n, k))
     assert_close_matmul(_qmm(lib, qw, x), ref, f"{fmt} m={m} n={n} k={k}")
+
+
+@pytest.mark.parametrize("fmt,n,k,m", [("q8_0", 5120, 1024, 32), ("q8_0", 5120, 1024, 29),
+                                       ("fp8_b128", 5120, 1024, 32), ("q2_k", 4096, 2048, 64),
+                                       ("q2_k", 4096, 2048, 61), ("int4", 4096, 1024, 64),
+                                       ("mxfp4", 4096, 1024, 61)])
+def test_qmm_gemv_whole_tile_grid(lib, fmt, n, k, m):
+    # Up to the GEMV row limit (32 rows for Q8_0 / FP8, 64 for the others) with
+    # at least 152 (row tile, 8-row token group) pairs: the GEMV runs whole-tile
+    # CTAs over a grid of token groups instead of 32-row quarter CTAs
+    # (40 tiles x 4 groups, 32 tiles x 8 groups; a ragged last group at m = 29, 61)
+    g = synth.rng(n + k + m + 17)
+    w = _draw_weight(g, fmt, n, k)
+    qw = make_qweight(lib, fmt, w, 1, n, k)
+    x = synth.fp16_normal(g, (m, k))
+    got = _qmm(lib, qw, x)
+    ref = O.qmm(x, dequant(fmt, w).reshape(n, k))
+    assert_close_matmul(got, ref, f"{fmt} m={m} n={n} k={k}")
+    rel = np.linalg.norm(got - ref, axis=1) / np.linalg.norm(ref, axis=1)
+    assert rel.max() <= 4 * 2e-3, (int(rel.argmax()), float(rel.max()))   # every token group
 
 
 def test_qmm_dense_q8_0_m32_with_dequant(lib):
@@ -202,16 +225,7 @@ def test_qmm_long_k(lib, fmt, m):
     # N = 2 row tiles
     g = synth.rng(len(fmt) * 100 + m)
     n, k = 256, {"q8_0": 4096, "q2_k": 8192, "int4": 4096, "mxfp4": 4096, "fp8_b128": 4096}[fmt]
-    if fmt == "q8_0":
-        w = synth.q8_0_blocks(g, n, k)
-    elif fmt == "q2_k":
-        w = synth.q2_k_blocks(g, n, k)
-    elif fmt == "mxfp4":
-        w = synth.mxfp4_blocks(g, n, k)
-    elif fmt == "fp8_b128":
-        w = synth.fp8_block_weight(g, (), n, k)
-    else:
-        w = synth.int4_weight(g, (n,), k)
+    w = _draw_weight(g, fmt, n, k)
     qw = make_qweight(lib, fmt, w, 1, n, k)
     x = synth.fp16_normal(g, (m, k))
     ref = O.qmm(x, dequant(fmt, w).reshape(n, k))
