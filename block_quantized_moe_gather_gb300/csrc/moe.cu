@@ -128,8 +128,8 @@ MoeWs carve(const bq_moe_desc* d, uint8_t* base) {
     if (d->T <= 8) {
         const int segs = (int)std::min(E, P);
         const int t_gu = 2 * (int)I / bq::kTileRows, t_d = (int)H / bq::kTileRows;
-        w.ks_gu = bq::qgemv_ksplit(d->w_gate_up.fmt, 2 * (int)I, (int)H, segs, d->T, true);
-        w.ks_d = bq::qgemv_ksplit(d->w_down.fmt, (int)H, (int)I, segs, d->T, true);
+        w.ks_gu = bq::qgemv_ksplit(d->w_gate_up.fmt, 2 * (int)I, (int)H, segs, d->T);
+        w.ks_d = bq::qgemv_ksplit(d->w_down.fmt, (int)H, (int)I, segs, d->T);
         w.part_gu = (float*)take((size_t)segs * t_gu * w.ks_gu * 4096);
         w.part_d = (float*)take((size_t)segs * t_d * w.ks_d * 4096);
         int nc = segs * t_gu + segs * t_d;

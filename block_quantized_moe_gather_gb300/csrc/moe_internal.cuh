@@ -89,9 +89,9 @@ struct QgemvParams {
     int beside;
 };
 constexpr int kMaxKsplit = 16;
-// Split factor that gives the GPU enough CTAs for this shape (experts: the
-// routed-expert GEMVs of a MoE step, which for Q2_K use smaller CTAs).
-int qgemv_ksplit(int fmt, int n, int k, int max_segments, int max_tokens, bool experts = false);
+// K split of the routed-expert GEMVs of a MoE decode step (at most 8 tokens):
+// enough CTAs to fill the GPU for this shape (Q2_K experts use smaller CTAs).
+int qgemv_ksplit(int fmt, int n, int k, int max_segments, int max_tokens);
 void launch_qgemv(const QgemvParams& p, int max_segments, cudaStream_t st, bool after_previous = false);
 
 // Up to this many rows a dense qmm runs the GEMV (token groups as separate

@@ -877,12 +877,12 @@ void launch_fmt(const bq::QgemvParams& p, int max_segments, bool after_previous,
 
 namespace bq {
 
-int qgemv_ksplit(int fmt, int n, int k, int max_segments, int max_tokens, bool experts) {
+int qgemv_ksplit(int fmt, int n, int k, int max_segments, int max_tokens) {
     if (max_tokens > 8 || max_segments <= 0) return 1;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (experts && fmt == BQ_FMT_Q2_K) {
+    if (fmt == BQ_FMT_Q2_K) {
         // Split-scale expert GEMV (128-thread CTAs, up to four per SM): K is
         // split until the grid holds about 2.5 CTAs per SM, keeping at least
         // 4 slabs per CTA, so that all CTAs are resident at once and no SM
@@ -892,27 +892,15 @@ int qgemv_ksplit(int fmt, int n, int k, int max_segments, int max_tokens, bool e
         const int k_slabs = k / fmt_info(fmt).slab_k;
         return std::max(1, std::min(want, std::min(kMaxKsplit, k_slabs / 4)));
     }
-    if (experts) {
-        // The other formats' expert GEMVs (256-thread CTAs, two per SM): their K
-        // split is summed inside a cluster (up to kClusterMaxSplit parts), so K is
-        // split until the grid holds just under two CTAs per SM, one wave, keeping
-        // at least 4 slabs (2 per K-half warp) per CTA.
-        const int ctas = (n / kTileRows) * max_segments;
-        const int want = (2 * sms - 1) / ctas;
-        const int slab_k = fmt_info(fmt).slab_k;
-        if (slab_k <= 0) return 1;
-        return std::max(1, std::min(want, std::min(kClusterMaxSplit, k / slab_k / 4)));
-    }
-    // About one CTA per SM: a split adds a partial round trip and a last-CTA
-    // reduction, and short K shares never fill the register prefetch ring,
-    // so K is split only as far as needed to reach the SM count, keeping at
-    // least 8 slabs (4 per K-half warp) per CTA.
+    // The other formats' expert GEMVs (256-thread CTAs, two per SM): their K
+    // split is summed inside a cluster (up to kClusterMaxSplit parts), so K is
+    // split until the grid holds just under two CTAs per SM, one wave, keeping
+    // at least 4 slabs (2 per K-half warp) per CTA.
     const int ctas = (n / kTileRows) * max_segments;
-    const int want = (sms + ctas - 1) / ctas;
+    const int want = (2 * sms - 1) / ctas;
     const int slab_k = fmt_info(fmt).slab_k;
     if (slab_k <= 0) return 1;   // unknown format: callers reject it before any launch
-    const int k_slabs = k / slab_k;
-    return std::max(1, std::min(want, std::min(kMaxKsplit, k_slabs / 8)));
+    return std::max(1, std::min(want, std::min(kClusterMaxSplit, k / slab_k / 4)));
 }
 
 void launch_qgemv(const QgemvParams& params, int max_segments, cudaStream_t st, bool after_previous) {
