@@ -134,15 +134,6 @@ __device__ __forceinline__ void set_device_error(int32_t* status, int32_t code) 
     atomicCAS(status, 0, code);
 }
 
-// fp16 pair from two 16-bit codes c0 (low lane) and c1 (high lane) that
-// already sit in the low 10 bits of each lane: 1024 + c exactly, then
-// subtract 1024 exactly.
-__device__ __forceinline__ __half2 codes_to_half2(uint32_t lanes) {
-    uint32_t h = lanes | 0x64006400u;
-    __half2 v = *reinterpret_cast<__half2*>(&h);
-    return __hsub2(v, __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400)));
-}
-
 __device__ __forceinline__ uint32_t h2_as_u32(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
 
