@@ -325,8 +325,10 @@ bq_status bq_moe_permute_noalloc(const int32_t* ids, int32_t T, int32_t k, int32
  * prefill GEMM and sum-folded q2_K down projection; [butter]: GPU router,
  * expert-indexed gemv with no host readback, swiglu, scalarFMA combine.)
  * Token counts up to 32 take the GEMV path (gather-qgemv over each
- * expert's tokens, 8 rows per pass); larger ones the tensor-core grouped GEMM.  Intermediates: gathered activations and
- * the SwiGLU output are fp16, expert outputs fp32.
+ * expert's tokens, 8 rows per pass); larger ones the tensor-core grouped
+ * GEMM, except that where the experts average fewer than 64 tokens the
+ * experts holding at most 8 take the GEMV beside it.  Intermediates:
+ * gathered activations and the SwiGLU output are fp16, expert outputs fp32.
  *
  * desc: host struct.  w_gate_up: n_mats = E, n = 2*inter, k = hidden,
  *   swiglu = 1.  w_down: n_mats = E, n = hidden, k = inter, swiglu = 0.
