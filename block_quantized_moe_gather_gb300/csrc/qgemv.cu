@@ -1,5 +1,8 @@
-// Grouped split-K quantised GEMV for up to 8 activation rows per pass
-// (dense qmm with m <= 8, and the decode MoE path).
+// Grouped split-K quantised GEMV for up to 8 activation rows per pass: dense
+// qmm up to 32 rows (Q8_0, FP8) or 64 rows (the other formats), one CTA row of
+// the grid per 8-row token group; the expert GEMVs of a MoE step of up to 32
+// tokens; and, in prefill layers with many small experts, the experts of at
+// most 8 tokens (a list-driven form launched beside the grouped GEMM).
 //
 // "metal: DSV4 M1 Ultra prefill/decode campaign" (QuixiAI/SlimServe PR
 // #2): qc_mmvq batch 2-8 "mb" fast path for q8_0 / q2_K; sum-folded q2_K
@@ -15,17 +18,19 @@
 // dequantises them in registers straight into mma.sync m16n8k16 A
 // fragments (fp16, scale applied), and multiplies with up to 8 activation
 // rows (the n = 8 side of the MMA) with fp32 accumulation.  The two K
-// halves are summed in a fixed order through shared memory.  When the GPU
-// would otherwise get too few CTAs, K is also split across CTAs: each
-// publishes a partial, and the last one to finish sums them in split order,
-// so results stay bit-reproducible.
+// halves are summed in a fixed order through shared memory.  A dense weight
+// whose whole-tile CTAs would leave SMs idle runs one CTA per 32-row quarter
+// instead, its 8 (or 16) warps on K pieces summed in warp order.  The expert
+// GEMVs of a step of at most 8 tokens also split K across CTAs: the parts of
+// a tile form a thread-block cluster and part 0 sums them in part order from
+// its shared memory.  Q2_K splits of more than four parts, and the norm-fused
+// router GEMV, publish partials that the last CTA sums in split order.  Every
+// sum has a fixed order, so results are bit-reproducible.
 //
-// Q2_K routed-expert GEMVs (the decode MoE path) take a split-scale variant
-// (see "Q2_K with split scales" below): codes ANDed into fp16 subnormals,
-// times the sub-block scale in one exact packed multiply, the activations
-// staged once per CTA in shared memory; 27% fewer instructions per weight.
-// Where it splits K (a one-token step), the parts of a tile form a
-// thread-block cluster and are summed in part 0's shared memory.
+// Q2_K routed-expert GEMVs take a split-scale variant (see "Q2_K with split
+// scales" below): codes ANDed into fp16 subnormals, times the sub-block scale
+// in one exact packed multiply, the activations staged once per CTA in shared
+// memory; 27% fewer instructions per weight.
 //
 // K ordering inside a slab: lane t of a quad owns the contiguous quarter
 // [t*SK/4, (t+1)*SK/4) of the slab's K range; MMA step s takes the four
