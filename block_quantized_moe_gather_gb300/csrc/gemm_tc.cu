@@ -1,6 +1,7 @@
 // Tensor-core (tcgen05) grouped GEMM with in-register dequantisation, for
-// the dense qmm (m > 8), the routed experts' gate/up (+ SwiGLU) and down
-// projections, and the shared expert.
+// the dense qmm above the GEMV's row limit (32 rows for Q8_0 and FP8, 64 for
+// the other formats), the routed experts' gate/up (+ SwiGLU) and down
+// projections of a prefill layer, and its shared expert.
 //
 // "metal: DSV4 M1 Ultra prefill/decode campaign" (QuixiAI/SlimServe PR
 // #2): a work queue (qc_moe_mm_map0) feeds a per-expert tiled prefill GEMM

@@ -7,9 +7,10 @@
 // states, x = gamma * h / sqrt(mean(h^2) + eps), logits = W_router x.
 //
 // Decode (<= 8 rows): one kernel, the norm-fused qgemv (qgemv.cu, NORM).
-// Larger row counts: this file's norm kernel writes x, then the tcgen05 GEMM
-// multiplies it (the GEMM reads its activations by TMA straight into shared
-// memory, so there is no register stage to fold the norm into).
+// Larger row counts: this file's norm kernel writes x, then the plain qgemv
+// (up to the GEMV row limit of bq_qmm) or the tcgen05 GEMM multiplies it (the
+// GEMM reads its activations by TMA straight into shared memory, so there is
+// no register stage to fold the norm into).
 #include <algorithm>
 
 #include "gemm_internal.cuh"
