@@ -1,4 +1,5 @@
-// Standalone block dequantisation to fp32: GGUF Q8_0 and Q2_K, and MXFP4.
+// Standalone block dequantisation to fp32: GGUF Q8_0 and Q2_K, MXFP4, and FP8
+// e4m3 with 128 x 128 block scales.
 //
 // "feat(gguf,dsv4): GGUF block-dequant + DSv4 kernel surface (WIP)"
 // (thewafflehaus/iron PR #9), kernels 1 and 2: Q8_0 out[i] = qs[i] *
@@ -8,7 +9,7 @@
 // Each CTA stages a chunk of whole blocks into shared memory with 16-byte
 // loads (the chunk sizes keep every chunk start 16-byte aligned), then
 // writes the decoded values with 16-byte float4 stores.  The path is bound
-// by the fp32 writes (4 bytes out per 1.06, 0.33 or 0.53 bytes in).
+// by the fp32 writes (4 bytes out per 1.06, 0.33, 0.53 or 1 byte in).
 //
 // Same page, MXFP4 section (DeepSeek V4-Flash MoE experts, OCP MX v1.0):
 // 17-byte blocks of one E8M0 exponent and 16 bytes of e2m1 codes, low
