@@ -11,8 +11,11 @@ resident in HBM; `e2e` is the same through the public API with the
 inputs copied from pinned host memory and the output read back every
 step, the copies of neighbouring steps overlapping the layer as a serving
 loop runs them (`e2e.serial`: each step alone).  `secondary` holds the
-other workloads: decode MoE steps (unique expert weight GB/s), the int4
-MoE prefill, dense qmm and the standalone dequant kernels.
+other workloads: decode MoE steps of 1-8 tokens for the four expert formats
+(unique expert weight GB/s, per step after an L2 flush and back to back in a
+CUDA graph; the routed GEMVs alone; decode from hidden states), the int4,
+MXFP4 and FP8 MoE prefill layers, dense qmm and the standalone dequant
+kernels.
 
 `--impl reference` times the CPU oracle (test infrastructure) on a bounded
 sample of the same workload instead.
