@@ -1,6 +1,8 @@
-"""GPU parity: standalone GGUF dequant kernels against the oracle, bit-exact
-(every value in the tested ranges is exactly representable in fp32, so the
-fp64 oracle value cast to fp32 is the only correct fp32 answer)."""
+"""GPU parity: the standalone dequant kernels (GGUF Q8_0 and Q2_K, MXFP4, FP8
+e4m3 with 128 x 128 block scales) against the oracle, bit-exact: the fp64
+oracle value cast to fp32 is the only correct fp32 answer (every value in the
+tested ranges is exact in fp32; MXFP4 magnitudes of 2^128 and above overflow
+to inf as that cast does; NaN positions are compared, not payloads)."""
 import numpy as np
 import pytest
 
